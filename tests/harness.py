@@ -1,0 +1,80 @@
+"""Test-side helpers: workload inputs with routing margins, and bf16 decoding.
+
+Routing indices and the permutation are compared bit for bit, so a token
+whose top-(k+1) logits lie closer together than the float32 rounding of
+either side could be ordered differently by the two.  The workloads are
+therefore conditioned: tokens whose smallest gap between consecutive logits
+among the k+1 largest is below ``REL_GAP`` times the token's logit RMS are
+redrawn (``inputs.redraw_token_rows``) until none is left.  The logits used
+for that decision are the oracle's (fp64); the CUDA path plays no part.
+"""
+from __future__ import annotations
+
+import functools
+import math
+
+import numpy as np
+
+from oracle import moe_oracle as orc
+from routing_expert_ffn_gb300 import inputs as gen
+
+REL_GAP = 1e-4
+
+
+def routing_gaps(logits: np.ndarray, k: int) -> np.ndarray:
+    """Per token: smallest gap between consecutive sorted logits among the k+1 largest."""
+    E = logits.shape[1]
+    top = -np.sort(-logits, axis=1)[:, : min(k + 1, E)]
+    if top.shape[1] < 2:
+        return np.full(logits.shape[0], np.inf)
+    return np.min(top[:, :-1] - top[:, 1:], axis=1)
+
+
+def near_tie_tokens(inp: dict, k: int) -> np.ndarray:
+    l = orc.router_logits(inp["x"], inp["W_r"], inp["bias"])
+    rms = np.sqrt(np.mean(l * l, axis=1))
+    return np.nonzero(routing_gaps(l, k) < REL_GAP * rms)[0]
+
+
+def condition(cfg: gen.MoEConfig, inp: dict, max_rounds: int = 50) -> dict:
+    for attempt in range(max_rounds):
+        bad = near_tie_tokens(inp, cfg.k)
+        if len(bad) == 0:
+            return inp
+        gen.redraw_token_rows(cfg, inp["x"], inp["labels"], bad, attempt)
+    raise RuntimeError(f"{cfg.name}: routing ties remain after {max_rounds} redraws")
+
+
+@functools.lru_cache(maxsize=4)
+def workload(name: str, T: int | None = None, x_kind: str | None = None) -> tuple:
+    """(cfg, conditioned inputs) for a named workload, optionally with fewer tokens."""
+    cfg = gen.CONFIGS[name]
+    if T is not None:
+        cfg = cfg.with_tokens(T)
+    if x_kind is not None:
+        from dataclasses import replace
+        cfg = replace(cfg, x_kind=x_kind)
+    inp = condition(cfg, gen.make_inputs(cfg))
+    return cfg, inp
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def max_rel_err(got: np.ndarray, ref: np.ndarray) -> float:
+    ref = np.asarray(ref, dtype=np.float64)
+    scale = float(np.max(np.abs(ref))) if ref.size else 0.0
+    if scale == 0.0:
+        return float(np.max(np.abs(got))) if got.size else 0.0
+    return float(np.max(np.abs(np.asarray(got, np.float64) - ref))) / scale
+
+
+def tolerance(cfg: gen.MoEConfig) -> float:
+    """Output tolerance relative to max|oracle|: 1e-4 for fp32 layers, 1e-2 for bf16 layers."""
+    return 1e-4 if cfg.dtype == "f32" else 1e-2
+
+
+def angle_rows(angles_deg, norms) -> np.ndarray:
+    return np.array([[n * math.cos(math.radians(a)), n * math.sin(math.radians(a))]
+                     for a, n in zip(angles_deg, norms)])
