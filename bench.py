@@ -1,0 +1,455 @@
+#!/usr/bin/env python
+"""Throughput of the routed-expert MoE layer on GB300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+A step is one moe_layer_forward call (router -> dispatch -> [condensation] ->
+expert FFN -> combine) over one batch of T synthetic tokens already resident
+in HBM.  Default workload: the DeepSeek-V2-Lite-shaped bf16 layer (T=4096,
+d=2048, 64 experts top-6, hidden 1408, 2 shared experts).  Inputs and weights
+are seeded synthetic draws (routing_expert_ffn_gb300.inputs); the weights
+(1.1 GB) exceed L2 and L2 is additionally flushed (a 256 MB write) between
+timed steps, outside the timed events.
+
+Under torchrun each rank runs an independent replica on its own GPU (weak
+scaling, no data-path collective); the reported time is the max over ranks.
+`--impl reference` times the fp64 CPU oracle on a bounded token sample of the
+same workload instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s on 1 GB300; expert-GEMM % of BF16 peak; dispatch GB/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks() -> tuple[dict, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ clocks (NVML, read only)
+class ClockSampler:
+    """Polls SM clock and clock-event reasons through NVML while the timed region runs."""
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+    def __init__(self, device_index: int):
+        self.samples: list[tuple[int, int]] = []
+        self.max_mhz = None
+        self.ok = False
+        self._stop = threading.Event()
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            uuid = os.environ.get("BENCH_GPU_UUID")
+            if uuid:
+                r = self.nvml.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h))
+            else:
+                r = self.nvml.nvmlDeviceGetHandleByIndex_v2(device_index, ctypes.byref(self.h))
+            if r != 0:
+                return
+            mx = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0:  # 1 = SM
+                self.max_mhz = int(mx.value)
+            self.ok = True
+        except OSError:
+            pass
+
+    def _sample(self):
+        c = ctypes.c_uint()
+        reasons = ctypes.c_ulonglong()
+        if self.nvml.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c)) != 0:
+            return
+        self.nvml.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(reasons))
+        self.samples.append((int(c.value), int(reasons.value)))
+
+    def _run(self):
+        while not self._stop.is_set():
+            self._sample()
+            time.sleep(0.002)
+
+    def start(self):
+        if self.ok:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+
+    def stop(self) -> dict:
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
+        self._stop.set()
+        self._t.join()
+        if not self.samples:
+            self._sample()
+        mhz = [s for s, _ in self.samples]
+        mask = 0
+        for _, r in self.samples:
+            mask |= r
+        reasons = [n for b, n in self.REASONS.items() if mask & b and n != "gpu_idle"]
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(mhz)}
+
+
+# ------------------------------------------------------------------ work accounting
+def work(cfg, n_condensed: int = 0) -> dict:
+    """Algorithmic FLOPs and bytes of one layer call (no padding rows, no re-reads)."""
+    b = 2 if cfg.dtype == "bf16" else 4
+    P = cfg.T * cfg.k
+    routed_flops = 6.0 * cfg.d * cfg.H * (P - n_condensed)
+    shared_flops = 6.0 * cfg.d * cfg.H_shared * cfg.T * cfg.n_shared
+    idx_bytes = P * 4
+    dispatch_bytes = cfg.T * cfg.d * b + P * cfg.d * b + idx_bytes * 3  # x in, x_perm out, idx/perm/slot_of
+    res_reads = {"none": 0, "input": 1, "external": 1, "input_plus_external": 2}[cfg.residual]
+    combine_bytes = (P * cfg.d * b + cfg.T * cfg.d * b * (1 + res_reads + (1 if cfg.n_shared else 0))
+                     + idx_bytes * 2)
+    return dict(routed_flops=routed_flops, shared_flops=shared_flops,
+                ffn_flops=routed_flops + shared_flops, dispatch_bytes=dispatch_bytes,
+                combine_bytes=combine_bytes, router_flops=2.0 * cfg.T * cfg.d * cfg.E)
+
+
+def launches_per_step(cfg, condense: bool) -> int:
+    n = 2 + 4  # router (logits, top-k) + dispatch (hist, scan, scatter, gather)
+    if condense:
+        n += 6  # row stats, m-tiles, tile list, similarity GEMM, greedy scan, count
+        n += 3  # compact reps, m-tiles over representatives, gather representative rows
+    else:
+        n += 1  # m-tiles
+    n += 2      # routed gate/up + down GEMMs
+    if cfg.n_shared:
+        n += 3  # shared m-tiles + gate/up + down GEMMs
+    n += 1      # combine
+    return n
+
+
+# ------------------------------------------------------------------ ours
+def run_ours(args, rank: int, world: int, local_rank: int) -> None:
+    import torch
+    from routing_expert_ffn_gb300 import build as moe_build
+    from routing_expert_ffn_gb300 import inputs as gen
+    from routing_expert_ffn_gb300 import moe
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    moe_build.build()
+    moe.lib()
+    cfg = gen.CONFIGS[args.workload]
+    inp = gen.make_inputs(cfg)
+    C = moe.Config.from_workload(cfg)
+    w, x, r = moe.upload(C, inp, device=dev)
+    tau = cfg.taus[0] if cfg.taus else math.nan
+    condense = tau <= 1.0
+    layer = moe.Layer(C, w, condense=condense, device=dev)
+    out = torch.empty((C.T, C.d), dtype=C.torch_dtype, device=dev)
+    ncond = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        layer(x, r, tau, out=out, n_condensed_out=ncond)
+    torch.cuda.synchronize()
+    st = moe.get_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {moe.status_string(st)}")
+    n_condensed = int(ncond.item())
+
+    sampler = ClockSampler(local_rank)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        layer(x, r, tau, out=out, n_condensed_out=ncond)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    barrier()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = sum(step_ms) / len(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # per-phase breakdown (FarSkip Eq. 9 terms): the same step as separate ABI calls
+    phases = phase_breakdown(args, moe, C, w, x, r, tau, flush, stream, torch)
+    # end to end: pinned host input -> device -> layer -> pinned host output, every step
+    e2e = end_to_end(args, moe, C, layer, x, r, tau, stream, torch)
+    st = moe.get_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status after timing: {moe.status_string(st)}")
+
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    wk = work(C, n_condensed)
+    ffn_s = phases["T_routed_ms"] / 1e3
+    achieved = wk["ffn_flops"] / ffn_s / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    disp_gbs = wk["dispatch_bytes"] / (phases["T_dispatch_ms"] / 1e3) / 1e9
+    comb_gbs = wk["combine_bytes"] / (phases["T_combine_ms"] / 1e3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": world * C.T / (ms / 1e3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": C.dtype,
+        "data": "synthetic (seeded N(0,1) tokens, N(0,0.02^2) weights, router N(0,1/d)); no dataset",
+        "config": {"workload": f"{cfg.name}: T={C.T} d={C.d} E={C.E} top-{C.k} {C.gating} "
+                               f"H={C.H} shared={C.n_shared}x{C.H_shared} residual={C.residual}"
+                               + (f" tau={tau:.6f}" if condense else ""),
+                   "tokens_per_gpu": C.T, "parallelism": f"replicas x{world}",
+                   "l2": "256 MB write between timed steps (outside the timed events); weights "
+                         f"{(C.E * 3 * C.H + C.n_shared * 3 * C.H_shared) * C.d * 2 / 1e9:.2f} GB > L2"},
+        "roofline": {"bound": "tensor", "kernel": "grouped expert GEMM (moe_expert_ffn)",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_src} bf16 burst",
+                     "traffic": None},
+        "dispatch": {"GB/s": disp_gbs, "frac_of_hbm": disp_gbs / hbm,
+                     "bytes": wk["dispatch_bytes"]},
+        "combine": {"GB/s": comb_gbs, "frac_of_hbm": comb_gbs / hbm, "bytes": wk["combine_bytes"]},
+        "phases_ms": phases,
+        "condensed": n_condensed,
+        "gpu_launches": launches_per_step(C, condense) * args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, inp, target_s=args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def phase_breakdown(args, moe, C, w, x, r, tau, flush, stream, torch) -> dict:
+    """Per-phase device time of the step, each phase its own ABI call, events between them."""
+    L = moe.lib()
+    c = C.c()
+    dev = x.device
+    P = C.T * C.k
+    i32, f32 = torch.int32, torch.float32
+    logits = torch.empty((C.T, C.E), dtype=f32, device=dev)
+    idx = torch.empty((C.T, C.k), dtype=i32, device=dev)
+    gate = torch.empty((C.T, C.k), dtype=f32, device=dev)
+    counts = torch.empty((C.E,), dtype=i32, device=dev)
+    offsets = torch.empty((C.E + 1,), dtype=i32, device=dev)
+    perm = torch.empty((P,), dtype=i32, device=dev)
+    slot_of = torch.empty((C.T, C.k), dtype=i32, device=dev)
+    x_perm = torch.empty((P, C.d), dtype=C.torch_dtype, device=dev)
+    y_perm = torch.empty((P, C.d), dtype=C.torch_dtype, device=dev)
+    so = torch.empty((C.T, C.d), dtype=C.torch_dtype, device=dev) if C.n_shared else None
+    rep_of = torch.empty((P,), dtype=i32, device=dev)
+    n_rep = torch.empty((C.E,), dtype=i32, device=dev)
+    ncond = torch.empty((1,), dtype=i32, device=dev)
+    out = torch.empty((C.T, C.d), dtype=C.torch_dtype, device=dev)
+    condense = tau <= 1.0
+    nd = L.moe_dispatch_workspace_size(ctypes.byref(c))
+    nc = L.moe_condense_workspace_size(ctypes.byref(c)) if condense else 0
+    nf = L.moe_expert_ffn_workspace_size(ctypes.byref(c), int(condense))
+    ws_d = torch.empty(max(nd, 1), dtype=torch.uint8, device=dev)
+    ws_c = torch.empty(max(nc, 1), dtype=torch.uint8, device=dev)
+    ws_f = torch.empty(max(nf, 1), dtype=torch.uint8, device=dev)
+    wc = w.c()
+    p = lambda t: None if t is None else t.data_ptr()
+    s = stream.cuda_stream
+
+    def step(evs):
+        evs[0].record(stream)
+        moe._check(L.moe_route(ctypes.byref(c), p(x), p(w.W_r), p(w.router_bias), p(logits), p(idx),
+                               p(gate), s), "route")
+        evs[1].record(stream)
+        moe._check(L.moe_dispatch(ctypes.byref(c), p(x), p(idx), p(counts), p(offsets), p(perm),
+                                  p(slot_of), p(x_perm), p(ws_d), nd, s), "dispatch")
+        evs[2].record(stream)
+        if condense:
+            moe._check(L.moe_condense(ctypes.byref(c), p(x_perm), p(offsets), tau, p(rep_of),
+                                      p(n_rep), p(ncond), p(ws_c), nc, s), "condense")
+        evs[3].record(stream)
+        moe._check(L.moe_expert_ffn(ctypes.byref(c), ctypes.byref(wc), p(x_perm), p(offsets),
+                                    p(rep_of) if condense else None, p(x), p(y_perm), p(so),
+                                    p(ws_f), nf, s), "expert_ffn")
+        evs[4].record(stream)
+        moe._check(L.moe_combine(ctypes.byref(c), p(y_perm), p(so), p(slot_of),
+                                 p(rep_of) if condense else None, p(gate), p(x), p(r), p(out), s),
+                   "combine")
+        evs[5].record(stream)
+
+    for _ in range(max(1, args.warmup)):
+        step([torch.cuda.Event(enable_timing=True) for _ in range(6)])
+    torch.cuda.synchronize()
+    all_evs = []
+    for _ in range(args.steps):
+        flush.zero_()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        step(evs)
+        all_evs.append(evs)
+    torch.cuda.synchronize()
+    names = ["T_gate_ms", "T_dispatch_ms", "T_condense_ms", "T_routed_ms", "T_combine_ms"]
+    res = {n: 0.0 for n in names}
+    for evs in all_evs:
+        for i, n in enumerate(names):
+            res[n] += evs[i].elapsed_time(evs[i + 1]) / len(all_evs)
+    res["note"] = ("T_routed = moe_expert_ffn: routed + shared grouped GEMMs (tcgen05) and their "
+                   "m-tile table kernels")
+    return res
+
+
+def end_to_end(args, moe, C, layer, x, r, tau, stream, torch) -> dict:
+    """Host pinned x (and residual) -> device -> layer -> host pinned out, every step."""
+    xh = x.cpu().pin_memory()
+    rh = r.cpu().pin_memory() if r is not None else None
+    xd = torch.empty_like(x)
+    rd = torch.empty_like(r) if r is not None else None
+    outd = torch.empty((C.T, C.d), dtype=C.torch_dtype, device=x.device)
+    outh = torch.empty((C.T, C.d), dtype=C.torch_dtype).pin_memory()
+
+    def step():
+        xd.copy_(xh, non_blocking=True)
+        if rh is not None:
+            rd.copy_(rh, non_blocking=True)
+        layer(xd, rd, tau, out=outd)
+        outh.copy_(outd, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    h2d = xh.numel() * xh.element_size() + (rh.numel() * rh.element_size() if rh is not None else 0)
+    d2h = outh.numel() * outh.element_size()
+    return {"value": C.T / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ------------------------------------------------------------------ oracle (CPU) timing
+def _oracle_call(orc, cfg, inp64, T_s):
+    return orc.layer_forward(inp64["x"][:T_s], inp64["W_r"], inp64["bias"], inp64["W_gu"],
+                             inp64["W_down"], inp64["Ws_gu"], inp64["Ws_down"], cfg.k, cfg.gating,
+                             residual_mode=cfg.residual,
+                             residual=None if inp64["residual"] is None else inp64["residual"][:T_s],
+                             tau=cfg.taus[0] if cfg.taus else None)
+
+
+def _as_f64(inp):
+    import numpy as np
+    return {k: (None if v is None else np.asarray(v, dtype=np.float64)) for k, v in inp.items()
+            if k != "labels"}
+
+
+def cpu_baseline(cfg, inp, target_s: float = 12.0) -> dict:
+    """The oracle as it stands on this host's cores, on a prefix of the workload's tokens."""
+    from oracle import moe_oracle as orc
+    inp64 = _as_f64(inp)
+    T_s = min(cfg.T, 128)
+    t0 = time.perf_counter()
+    _oracle_call(orc, cfg, inp64, T_s)
+    dt = time.perf_counter() - t0
+    if dt < target_s / 3 and T_s < cfg.T:
+        T_s = min(cfg.T, max(T_s, int(T_s * target_s / max(dt, 1e-3))))
+        t0 = time.perf_counter()
+        _oracle_call(orc, cfg, inp64, T_s)
+        dt = time.perf_counter() - t0
+    return {"value": T_s / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"first {T_s} of {cfg.T} tokens as one fp64 layer call ({dt:.1f} s); "
+                      "weights pre-cast to float64"}
+
+
+def run_reference(args, rank: int) -> None:
+    if rank != 0:
+        return
+    from oracle import moe_oracle as orc
+    from routing_expert_ffn_gb300 import inputs as gen
+    cfg = gen.CONFIGS[args.workload]
+    inp64 = _as_f64(gen.make_inputs(cfg))
+    T_s = min(cfg.T, args.reference_tokens)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        _oracle_call(orc, cfg, inp64, T_s)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = T_s / (ms / 1e3)
+    sample = f"first {T_s} of {cfg.T} tokens per step, fp64 oracle, weights pre-cast to float64"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": cfg.name, "tokens_per_step": T_s},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="dsv2_lite")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--reference-tokens", type=int, default=96)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,217 @@
+/*
+ * moe.h -- C ABI of libmoe.so, the routed-expert path of a Mixture-of-Experts
+ * layer on one GB300 (sm_103a).
+ *
+ * The path, as the FarSkip-Collective and Luffy pages describe the layer:
+ *   router (top-k gating) -> Dispatch (expert-contiguous permutation)
+ *   -> [optional Luffy token condensation inside each expert bucket]
+ *   -> per-expert SwiGLU FFN (+ shared experts on every token)
+ *   -> gated Combine, adding the FarSkip-Collective residual base.
+ * Sources (page title, section):
+ *   "FarSkip-Collective: Unhobbling Blocking Communication in Mixture of
+ *    Experts Models" (Pith review of arXiv 2511.11505): "Core claim" (the MoE
+ *    sub-block reads the previous layer's full output; the attention input is
+ *    the partial activation including the shared expert), ledger axiom Eq. 9
+ *    (T_gate, T_Dispatch, T_routed, T_Combine), referee minor comment 1 (Eq. 6
+ *    needs the base residual o_0).
+ *   "Communication-Efficient Sparsely-Activated Model Training via Sequence
+ *    Migration and Token Condensation" (Luffy, Pith review of arXiv
+ *    2411.15419): "What carries the argument" (similar tokens routed to the
+ *    same expert reuse one representative's expert output; adaptive threshold
+ *    h_t = 1/(1+exp(l_norm))), referee major comment 1 (a condensed token's
+ *    forward uses the representative's output).
+ *
+ * Conventions for every entry point below:
+ *   - Every data pointer is a DEVICE pointer on the current CUDA device,
+ *     allocated and owned by the caller.  The library allocates no device
+ *     memory and never frees caller memory.  Scratch comes from the caller's
+ *     workspace `ws` of `ws_bytes` bytes (sizes from the *_workspace_size
+ *     functions).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream).  The library never synchronises the stream, except
+ *     moe_get_device_status, which says so.
+ *   - Tensors are dense, row-major, with no strides.  Every pointer must be
+ *     16-byte aligned.  "act" below means the activation/weight dtype of the
+ *     config (fp32 or bf16, raw IEEE / bfloat16 bits).
+ *   - Errors found on the host are returned before anything is launched:
+ *     MOE_ERR_INVALID_ARG (null or misaligned pointer, non-positive size,
+ *     k > E, bad enum), MOE_ERR_UNSUPPORTED (a shape the kernels do not
+ *     tile), MOE_ERR_WORKSPACE (ws_bytes too small).  A failed launch returns
+ *     MOE_ERR_CUDA.  Conditions found on the device (an expert index out of
+ *     range, a bounded wait that gave up) are recorded in a per-device status
+ *     word that moe_get_device_status reads; the kernels then skip the bad
+ *     access and return instead of faulting or hanging.
+ *   - Outputs may not alias inputs, except that `out` may alias `residual`.
+ *   - Sizes: T >= 0 tokens (T == 0 is a no-op), d model dim, E <= 256 routed
+ *     experts, 1 <= k <= E, H expert hidden, n_shared shared experts of
+ *     hidden H_shared.  bf16 layers need d % 256 == 0, H % 128 == 0 and
+ *     H_shared % 128 == 0 (tensor-core tiles); fp32 layers need d % 4 == 0
+ *     and H % 4 == 0.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,
+  MOE_ERR_UNSUPPORTED = 2,
+  MOE_ERR_WORKSPACE = 3,
+  MOE_ERR_CUDA = 4,
+  MOE_ERR_TIMEOUT = 5,      /* device: a bounded wait gave up */
+  MOE_ERR_DEVICE_INDEX = 6  /* device: an index was out of range and was skipped */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+/* Gating (router page readings; the pages print no router):
+ *   SOFTMAX_TOPK        g = softmax over all E logits, at the k selected experts
+ *   SOFTMAX_TOPK_RENORM g = softmax over the k selected logits
+ *   SIGMOID_TOPK        g = 1/(1+exp(-l_e)) of each selected expert          */
+typedef enum {
+  MOE_GATE_SOFTMAX_TOPK = 0,
+  MOE_GATE_SOFTMAX_TOPK_RENORM = 1,
+  MOE_GATE_SIGMOID_TOPK = 2
+} moe_gating;
+
+/* Residual base added by the combine (FarSkip-Collective "Core claim": the
+ * MoE input x is the previous layer's full output h_{l-1}; the residual base
+ * can be a separately given stream such as the attention-partial a_l):
+ *   NONE 0; INPUT r = x; EXTERNAL r = residual; INPUT_PLUS_EXTERNAL r = x + residual */
+typedef enum {
+  MOE_RES_NONE = 0,
+  MOE_RES_INPUT = 1,
+  MOE_RES_EXTERNAL = 2,
+  MOE_RES_INPUT_PLUS_EXTERNAL = 3
+} moe_residual;
+
+typedef struct {
+  int32_t T, d, E, k, H, n_shared, H_shared;
+  int32_t act_dtype; /* moe_dtype */
+  int32_t gating;    /* moe_gating */
+  int32_t residual;  /* moe_residual */
+} moe_config;
+
+typedef struct {
+  const float* W_r;         /* [d, E] fp32 router weight                              */
+  const float* router_bias; /* [E] fp32, added to the logits before selection; NULL = none */
+  const void* W_gu;         /* [E, 2H, d] act: rows 0..H-1 gate proj, rows H..2H-1 up proj */
+  const void* W_down;       /* [E, d, H] act                                           */
+  const void* Ws_gu;        /* [n_shared, 2H_shared, d] act; NULL when n_shared == 0   */
+  const void* Ws_down;      /* [n_shared, d, H_shared] act; NULL when n_shared == 0    */
+} moe_weights;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* moe_status_string(moe_status s);
+
+/* Luffy's adaptive condensation threshold h_t = 1/(1+exp(l_norm)), computed
+ * on the host in float64 and rounded to float (Luffy review, "What carries the
+ * argument", Eq. 2).  l_norm is the normalised loss decrease of the previous
+ * iteration; larger l_norm gives a lower threshold (more condensation). */
+float moe_adaptive_tau(float l_norm);
+
+/* Reads and clears this device's status word.  SYNCHRONISES `stream` first.
+ * Returns MOE_OK, or the first device-side condition recorded since the last
+ * read (MOE_ERR_TIMEOUT / MOE_ERR_DEVICE_INDEX), or MOE_ERR_CUDA. */
+moe_status moe_get_device_status(moe_stream_t stream);
+
+/* ---------------------------------------------------------------- router
+ * T_gate of FarSkip Eq. 9.  logits[t,e] = sum_i x[t,i] W_r[i,e] (+ bias[e]) in
+ * fp32 FMA (no TF32); the k experts with the largest logits, largest first,
+ * a tie going to the lower index; gates per cfg->gating from the fp32 logits.
+ *   x        [T, d] act           (in)
+ *   W_r      [d, E] fp32          (in)
+ *   bias     [E] fp32 or NULL     (in)
+ *   logits   [T, E] fp32          (out, scratch the caller may read)
+ *   topk_idx [T, k] int32         (out)
+ *   topk_gate[T, k] fp32          (out)                                     */
+moe_status moe_route(const moe_config* cfg, const void* x, const float* W_r, const float* bias,
+                     float* logits, int32_t* topk_idx, float* topk_gate, moe_stream_t stream);
+
+/* ---------------------------------------------------------------- dispatch
+ * T_Dispatch of FarSkip Eq. 9, on one GPU: the permutation that the
+ * expert-parallel Dispatch all-to-all performs.  Bucket e holds the tokens
+ * routed to e in ascending token order; buckets are laid end to end.
+ *   topk_idx [T, k] int32   (in)   entries outside [0, E) are skipped and flagged
+ *   counts   [E] int32      (out)  tokens per expert
+ *   offsets  [E+1] int32    (out)  exclusive prefix of counts; offsets[E] = T*k
+ *   perm     [T*k] int32    (out)  slot -> token
+ *   slot_of  [T, k] int32   (out)  (token, j) -> slot
+ *   x_perm   [T*k, d] act   (out)  x_perm[s] = x[perm[s]]
+ *   ws       moe_dispatch_workspace_size(cfg) bytes of scratch              */
+size_t moe_dispatch_workspace_size(const moe_config* cfg);
+moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                        int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* slot_of,
+                        void* x_perm, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------- condensation
+ * Luffy token condensation inside each expert bucket (bf16 layers).  Walking a
+ * bucket in slot order with the set R of representatives, slot j is condensed
+ * onto the earliest r in R with cos(x_perm[j], x_perm[r]) >= tau, else j joins
+ * R.  Bitwise-identical rows have similarity 1; a zero row is otherwise
+ * dissimilar to everything.  tau > 1 or NaN: no slot is condensed.
+ *   x_perm      [T*k, d] bf16 (in)   offsets [E+1] int32 (in, from moe_dispatch)
+ *   rep_of      [T*k] int32   (out)  representative slot of every slot (itself if a representative)
+ *   n_rep       [E] int32     (out)  representatives per bucket
+ *   n_condensed [1] int32     (out)  number of condensed slots                 */
+size_t moe_condense_workspace_size(const moe_config* cfg);
+moe_status moe_condense(const moe_config* cfg, const void* x_perm, const int32_t* offsets, float tau,
+                        int32_t* rep_of, int32_t* n_rep, int32_t* n_condensed,
+                        void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------- expert FFN
+ * T_routed of FarSkip Eq. 9: y[s] = W_down,e (SiLU(W_gate,e x_perm[s]) * (W_up,e x_perm[s]))
+ * for every slot s of bucket e.  bf16 layers run on tcgen05 tensor cores
+ * (bf16 in, fp32 accumulate, the hidden h rounded to bf16, y stored bf16);
+ * fp32 layers run fp32 FMA.  With rep_of non-NULL only representative slots
+ * are computed and y is written at those slots only (a condensed slot reads
+ * its representative's row).  With n_shared > 0 the shared experts run on all
+ * T rows of x and shared_out[t] = sum over shared experts.
+ *   x_perm [T*k, d] act (in)  offsets [E+1] (in)  rep_of [T*k] or NULL (in)
+ *   x [T, d] act (in, used when n_shared > 0)
+ *   y_perm [T*k, d] act (out)  shared_out [T, d] act (out, NULL when n_shared == 0) */
+size_t moe_expert_ffn_workspace_size(const moe_config* cfg, int with_condensation);
+moe_status moe_expert_ffn(const moe_config* cfg, const moe_weights* w, const void* x_perm,
+                          const int32_t* offsets, const int32_t* rep_of, const void* x,
+                          void* y_perm, void* shared_out, void* ws, size_t ws_bytes,
+                          moe_stream_t stream);
+
+/* ---------------------------------------------------------------- combine
+ * T_Combine of FarSkip Eq. 9 plus the residual add (FarSkip Eq. 6 with its
+ * base term): out[t] = r[t] + shared_out[t] + sum_j gate[t,j] * y_perm[rep(slot_of[t,j])],
+ * accumulated in fp32 (j in order), one rounding to act.  rep(s) = rep_of[s],
+ * or s when rep_of is NULL.  r per cfg->residual.
+ *   y_perm [T*k, d] act (in)  shared_out [T, d] act or NULL (in)
+ *   slot_of [T, k] (in)  rep_of [T*k] or NULL (in)  topk_gate [T, k] fp32 (in)
+ *   x [T, d] act (in, for MOE_RES_INPUT*)  residual [T, d] act (in, for *EXTERNAL)
+ *   out [T, d] act (out; may alias residual)                                   */
+moe_status moe_combine(const moe_config* cfg, const void* y_perm, const void* shared_out,
+                       const int32_t* slot_of, const int32_t* rep_of, const float* topk_gate,
+                       const void* x, const void* residual, void* out, moe_stream_t stream);
+
+/* ---------------------------------------------------------------- whole layer
+ * route -> dispatch -> [condense if tau <= 1] -> expert FFN -> combine, all on
+ * `stream`, no host synchronisation, intermediates in `ws`.
+ *   x [T, d] act (in)  residual [T, d] act or NULL (in)  tau: <= 1 condenses, > 1 or NaN does not
+ *   out [T, d] act (out)
+ *   topk_idx_out [T, k] int32 or NULL (out)  n_condensed_out [1] int32 or NULL (out)
+ *   ws: moe_workspace_size(cfg, tau <= 1) bytes                                 */
+size_t moe_workspace_size(const moe_config* cfg, int with_condensation);
+moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const void* x,
+                             const void* residual, float tau, void* out, int32_t* topk_idx_out,
+                             int32_t* n_condensed_out, void* ws, size_t ws_bytes,
+                             moe_stream_t stream);
+
+#ifdef __cplusplus
+} /* extern "C" */
+#endif
+
+#endif /* MOE_H_ */

@@ -1,0 +1,467 @@
+// Persistent grouped GEMM on tcgen05 tensor cores (sm_103a), bf16 in, fp32
+// accumulate in TMEM, for the routed-expert FFN and the condensation
+// similarity tiles.
+//
+//   D[m, n] = sum_k A[row0 + m, k] * B[slice, n0 + n, k]     (both operands K-major)
+//
+// One CTA per SM.  Warp 0 issues TMA loads into a 4-stage shared-memory ring,
+// warp 1 allocates TMEM and has one thread issue tcgen05.mma (M=128, N=256,
+// K=16) into one of two 256-column fp32 accumulators, warps 2-5 drain the
+// other accumulator through tcgen05.ld and run the epilogue, so the epilogue of
+// tile i overlaps the main loop of tile i+1.
+//
+// Epilogues:
+//   kSwiGLU  B rows are loaded as 128 gate rows then 128 up rows of the same
+//            hidden units, so one accumulator holds gate|up; the epilogue writes
+//            h = SiLU(gate) * up (bf16) -- the gate/up half of a SwiGLU expert.
+//   kStore   writes D (bf16), optionally to a remapped output row.
+//   kSimBits condensation: D is a tile of the bucket's Gram matrix; the
+//            epilogue turns cos(x_i, x_j) >= tau, j < i, into bits.
+//
+// Tiles.  Rows are grouped (one group per expert / bucket); a group's rows are
+// cut into 128-row m-tiles (the last one ragged; rows past the group are
+// computed but never stored).  For kSwiGLU/kStore, the linear tile index walks
+// groups in order; inside a group it walks blocks of up to 16 m-tiles, and
+// inside a block the N tiles with the m-tiles fastest, so CTAs running at the
+// same time share B tiles (weights) and A tiles (tokens) through L2.
+// kSimBits reads an explicit (m-tile, column tile) list.
+//
+// Every wait is bounded; on timeout the CTA records MOE_ERR_TIMEOUT, stops
+// issuing work, drains what it issued, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace tc {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_THREADS = 192;
+constexpr int TMEM_COLS = 512;
+constexpr int M_GROUP = 16;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align slack*/ + 256 /*barriers*/;
+
+enum Mode { kSwiGLU = 0, kStore = 1, kSimBits = 2 };
+
+struct Shared {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  volatile int abort_flag;
+};
+
+// Bounded mbarrier wait.  Returns false if the CTA is aborting or the limit passed.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Shared* sh,
+                                         unsigned* status) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (sh->abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        sh->abort_flag = 1;
+        record_status(status, MOE_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+struct TileInfo {
+  int slice;  // B slice (expert) of the m-tile
+  int row0;   // first A row
+  int nrows;  // valid rows (<= 128)
+  int gbase;  // first row of the group (bucket offset)
+  int nt;     // N tile (or column tile for kSimBits)
+};
+
+template <int MODE>
+__device__ __forceinline__ TileInfo tile_info(const TcGemmArgs& a, int tile) {
+  int mt, nt;
+  if (MODE == kSimBits) {
+    int2 e = a.tile_list[tile];
+    mt = e.x;
+    nt = e.y;
+  } else {
+    const int NT = a.n_ntiles;
+    int lo = 0, hi = a.n_groups;  // largest g with begin[g] * NT <= tile
+    while (hi - lo > 1) {
+      int mid = (lo + hi) >> 1;
+      if (a.group_mt_begin[mid] * NT <= tile) lo = mid; else hi = mid;
+    }
+    const int beg = a.group_mt_begin[lo];
+    const int cnt = a.group_mt_begin[lo + 1] - beg;
+    const int local = tile - beg * NT;
+    const int blk = local / (M_GROUP * NT);
+    const int within = local - blk * M_GROUP * NT;
+    const int bs = min(M_GROUP, cnt - blk * M_GROUP);
+    nt = within / bs;
+    mt = beg + blk * M_GROUP + (within - nt * bs);
+  }
+  int4 m = a.mt_info[mt];
+  TileInfo t;
+  t.slice = m.x;
+  t.row0 = m.y;
+  t.nrows = m.z;
+  t.gbase = m.w;
+  t.nt = nt;
+  return t;
+}
+
+template <int MODE>
+__device__ __forceinline__ int total_tiles(const TcGemmArgs& a) {
+  if (MODE == kSimBits) return *a.n_list;
+  return a.group_mt_begin[a.n_groups] * a.n_ntiles;
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ bool rows_identical(const __nv_bfloat16* rows, int d, int i, int j) {
+  const uint4* a = reinterpret_cast<const uint4*>(rows + static_cast<long long>(i) * d);
+  const uint4* b = reinterpret_cast<const uint4*>(rows + static_cast<long long>(j) * d);
+  for (int v = 0; v < d / 8; ++v) {
+    uint4 x = a[v], y = b[v];
+    if (x.x != y.x || x.y != y.y || x.z != y.z || x.w != y.w) return false;
+  }
+  return true;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const TcGemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  Shared* sh = reinterpret_cast<Shared*>(smem + STAGES * STAGE_BYTES);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t smem0 = ptx::smem_u32(smem);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&sh->full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&sh->empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(ptx::smem_u32(&sh->tmem_full[a]), 1);
+      ptx::mbar_init(ptx::smem_u32(&sh->tmem_empty[a]), 4);
+    }
+    ptx::mbar_init(ptx::smem_u32(&sh->drain), 1);
+    sh->abort_flag = 0;
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(&sh->tmem_base), TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = sh->tmem_base;
+  const int n_tiles = total_tiles<MODE>(args);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    int stage = 0;
+    uint32_t phase = 0;
+    int issued[STAGES];
+    uint32_t issued_phase[STAGES];
+    for (int s = 0; s < STAGES; ++s) issued[s] = 0, issued_phase[s] = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+      const TileInfo t = tile_info<MODE>(args, tile);
+      for (int kb = 0; kb < args.n_kblocks; ++kb) {
+        if (!wait_bar(ptx::smem_u32(&sh->empty[stage]), phase ^ 1u, sh, args.status)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t full = ptx::smem_u32(&sh->full[stage]);
+          const uint32_t sa = smem0 + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+          const int kslice = kb / args.kb_per_slice;
+          const int kin = (kb - kslice * args.kb_per_slice) * BK;
+          ptx::mbar_arrive_expect_tx(full, STAGE_BYTES);
+          ptx::tma_load_2d(sa, &tmA, full, kb * BK, t.row0);
+          if (MODE == kSwiGLU) {
+            const int nslice = t.nt / args.nt_per_slice;
+            const int n0 = (t.nt - nslice * args.nt_per_slice) * (BN / 2);
+            const int z = t.slice + nslice + kslice;
+            ptx::tma_load_3d(sb, &tmB, full, kin, n0, z);
+            ptx::tma_load_3d(sb + B_BYTES / 2, &tmB, full, kin, args.b_up_offset + n0, z);
+          } else if (MODE == kStore) {
+            const int nslice = t.nt / args.nt_per_slice;
+            const int n0 = (t.nt - nslice * args.nt_per_slice) * BN;
+            ptx::tma_load_3d(sb, &tmB, full, kin, n0, t.slice + nslice + kslice);
+          } else {
+            ptx::tma_load_3d(sb, &tmB, full, kb * BK, t.gbase + t.nt * BN, 0);
+          }
+        }
+        __syncwarp();
+        issued[stage] = 1;
+        issued_phase[stage] = phase;
+        if (++stage == STAGES) stage = 0, phase ^= 1u;
+      }
+    }
+    if (!ok) {
+      // Let the loads already in flight land before the CTA exits.
+      for (int s = 0; s < STAGES; ++s) {
+        if (!issued[s]) continue;
+        uint64_t t0 = globaltimer_ns();
+        while (!ptx::mbar_try_wait(ptx::smem_u32(&sh->full[s]), issued_phase[s]) &&
+               globaltimer_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int local = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++local) {
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      if (!wait_bar(ptx::smem_u32(&sh->tmem_empty[acc]), acc_phase ^ 1u, sh, args.status)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      for (int kb = 0; kb < args.n_kblocks; ++kb) {
+        if (!wait_bar(ptx::smem_u32(&sh->full[stage]), phase, sh, args.status)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        if (lane == 0) {
+          const uint32_t sa = smem0 + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+          const uint64_t adesc = ptx::sw128_kmajor_desc(sa);
+          const uint64_t bdesc = ptx::sw128_kmajor_desc(sb);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            // +32 bytes per K step of 16 elements = +2 in the encoded start address
+            ptx::umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc,
+                           (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          ptx::umma_commit(ptx::smem_u32(&sh->empty[stage]));
+        }
+        __syncwarp();
+        if (++stage == STAGES) stage = 0, phase ^= 1u;
+      }
+      if (!ok) break;
+      if (lane == 0) ptx::umma_commit(ptx::smem_u32(&sh->tmem_full[acc]));
+      __syncwarp();
+    }
+    if (!ok) {
+      // Wait for the MMAs already issued before TMEM is released.
+      if (lane == 0) ptx::umma_commit(ptx::smem_u32(&sh->drain));
+      __syncwarp();
+      uint64_t t0 = globaltimer_ns();
+      while (!ptx::mbar_try_wait(ptx::smem_u32(&sh->drain), 0) &&
+             globaltimer_ns() - t0 < kWaitLimitNs) {
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    int local = 0;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++local) {
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      if (!wait_bar(ptx::smem_u32(&sh->tmem_full[acc]), acc_phase, sh, args.status)) break;
+      ptx::tc_fence_after();
+      const TileInfo t = tile_info<MODE>(args, tile);
+      const uint32_t col0 = lane_addr + acc * BN;
+      const bool valid = r < t.nrows;
+      if (MODE == kSwiGLU) {
+        __nv_bfloat16* orow = args.out + (static_cast<long long>(t.row0) + r) * args.ld_out +
+                              static_cast<long long>(t.nt) * (BN / 2);
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t g[32], u[32];
+          ptx::tmem_ld_32x32b_x32(col0 + c * 32, g);
+          ptx::tmem_ld_32x32b_x32(col0 + BN / 2 + c * 32, u);
+          ptx::tmem_ld_wait();
+          if (valid) {
+            uint32_t p[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float h0 = silu_f(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
+              const float h1 =
+                  silu_f(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
+              p[i] = pack_bf16x2(h0, h1);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(p[4 * v], p[4 * v + 1], p[4 * v + 2], p[4 * v + 3]);
+          }
+        }
+      } else if (MODE == kStore) {
+        long long orow_idx = static_cast<long long>(t.row0) + r;
+        if (valid && args.out_rowmap) orow_idx = args.out_rowmap[orow_idx];
+        __nv_bfloat16* orow =
+            args.out + orow_idx * args.ld_out + static_cast<long long>(t.nt) * BN;
+#pragma unroll 1
+        for (int c = 0; c < 8; c += 2) {
+          uint32_t v0[32], v1[32];
+          ptx::tmem_ld_32x32b_x32(col0 + c * 32, v0);
+          ptx::tmem_ld_32x32b_x32(col0 + (c + 1) * 32, v1);
+          ptx::tmem_ld_wait();
+          if (valid) {
+            uint32_t p[32];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              p[i] = pack_bf16x2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
+              p[16 + i] = pack_bf16x2(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1]));
+            }
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[v] = make_uint4(p[4 * v], p[4 * v + 1], p[4 * v + 2], p[4 * v + 3]);
+          }
+        }
+      } else {
+        // Gram tile of bucket `slice`: row slot i = row0 + r, column slot j = gbase + nt*256 + c.
+        const int e = t.slice;
+        const int n_e = args.bucket_off[e + 1] - args.bucket_off[e];
+        const int W = (n_e + 31) >> 5;
+        const int i = t.row0 + r;
+        const int li = i - t.gbase;
+        const float ni = valid ? args.norm[i] : 0.f;
+        const unsigned long long hi = valid ? args.row_hash[i] : 0ull;
+        unsigned* brow = args.bits + args.bits_base[e] + static_cast<long long>(li) * W;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t v[32];
+          ptx::tmem_ld_32x32b_x32(col0 + c * 32, v);
+          ptx::tmem_ld_wait();
+          const int lj0 = t.nt * BN + c * 32;
+          if (valid && lj0 < li) {
+            uint32_t word = 0;
+#pragma unroll 4
+            for (int b = 0; b < 32; ++b) {
+              const int lj = lj0 + b;
+              if (lj >= li) break;
+              const int j = t.gbase + lj;
+              const float nj = args.norm[j];
+              bool similar;
+              if (args.row_hash[j] == hi && rows_identical(args.rows, args.d, i, j)) {
+                similar = true;  // identical rows: similarity exactly 1
+              } else if (ni == 0.f || nj == 0.f) {
+                similar = false;
+              } else {
+                float s = __uint_as_float(v[b]) / (ni * nj);
+                s = fminf(fmaxf(s, -1.f), 1.f);
+                similar = s >= args.tau;
+              }
+              word |= static_cast<uint32_t>(similar) << b;
+            }
+            brow[lj0 >> 5] = word;
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sh->tmem_empty[acc]));
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// ---------------------------------------------------------------- host side
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// bf16 tensor map with 128-byte swizzle and a box of 64 (K) x box_rows.
+// rank 2: [rows][inner]; rank 3: [outer][rows][inner].
+static bool make_map(CUtensorMap* m, int rank, const void* base, uint64_t inner, uint64_t rows,
+                     uint64_t outer, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {inner, rows, outer};
+  cuuint64_t strides[2] = {inner * 2, inner * rows * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
+                  strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int MODE>
+static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const TcGemmArgs& args,
+                          int grid, cudaStream_t stream) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  grouped_gemm_kernel<MODE><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(a, b, args);
+  return cudaGetLastError();
+}
+
+}  // namespace tc
+
+cudaError_t tc_gemm(int mode, const void* A, long long a_rows, int K, const void* B,
+                    int b_slices, int b_rows, int b_cols, const TcGemmArgs& args, int grid,
+                    cudaStream_t stream) {
+  CUtensorMap ma, mb;
+  if (!tc::make_map(&ma, 2, A, K, a_rows, 1, tc::BM)) return cudaErrorInvalidValue;
+  const uint32_t box_rows = mode == tc::kSwiGLU ? tc::BN / 2 : tc::BN;
+  if (!tc::make_map(&mb, 3, B, b_cols, b_rows, b_slices, box_rows)) return cudaErrorInvalidValue;
+  switch (mode) {
+    case tc::kSwiGLU: return tc::launch<tc::kSwiGLU>(ma, mb, args, grid, stream);
+    case tc::kStore: return tc::launch<tc::kStore>(ma, mb, args, grid, stream);
+    case tc::kSimBits: return tc::launch<tc::kSimBits>(ma, mb, args, grid, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

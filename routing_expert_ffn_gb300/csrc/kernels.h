@@ -1,0 +1,105 @@
+// Internal (C++) launch interface between the C-ABI layer (moe_api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// ------------------------------------------------------------------ router
+// logits = x W_r (+bias), fp32 FMA; then per-token top-k and gates.
+cudaError_t launch_router_logits(int act_dtype, const void* x, const float* W_r, const float* bias,
+                                 float* logits, int T, int d, int E, cudaStream_t stream);
+cudaError_t launch_router_topk(const float* logits, int32_t* topk_idx, float* topk_gate, int T,
+                               int E, int k, int gating, cudaStream_t stream);
+
+// ------------------------------------------------------------------ dispatch / combine
+constexpr int kDispatchChunk = 128;  // tokens per dispatch chunk
+size_t dispatch_scratch_bytes(int T, int E);
+cudaError_t launch_dispatch(int act_dtype, const void* x, const int32_t* topk_idx, int T, int d,
+                            int E, int k, int32_t* counts, int32_t* offsets, int32_t* perm,
+                            int32_t* slot_of, void* x_perm, void* scratch, unsigned* status,
+                            cudaStream_t stream);
+// dst[r] = src[rows[r]] for r < *n_rows_dev (<= max_rows); rows outside [0, src_rows) are flagged.
+cudaError_t launch_gather_rows(int act_dtype, const void* src, int src_rows, const int32_t* rows,
+                               const int* n_rows_dev, int max_rows, int d, void* dst,
+                               unsigned* status, cudaStream_t stream);
+cudaError_t launch_combine(int act_dtype, const void* y_perm, const void* shared_out,
+                           const int32_t* slot_of, const int32_t* rep_of, const float* topk_gate,
+                           const void* x, const void* residual, int residual_mode, void* out, int T,
+                           int d, int k, int P, unsigned* status, cudaStream_t stream);
+
+// ------------------------------------------------------------------ m-tile tables
+// Groups of rows (experts, buckets, or one group of fixed_rows rows when counts
+// is NULL) are cut into 128-row m-tiles.  mt_info[m] = {group, row0, nrows,
+// group first row}; group_mt_begin[g] = first m-tile of group g (n_groups + 1
+// entries, the last being the total).  offsets_out (nullable) receives the
+// exclusive prefix of the group row counts.
+constexpr int kMTile = 128;
+inline int max_mtiles(long long rows, int n_groups) {
+  return static_cast<int>((rows + kMTile - 1) / kMTile) + n_groups;
+}
+// Row counts per group come from `counts`, else from `offsets_in` (n_groups+1
+// entries), else each group has fixed_rows rows.
+cudaError_t launch_build_mtiles(const int32_t* counts, const int32_t* offsets_in, int fixed_rows,
+                                int n_groups, int32_t* offsets_out, int4* mt_info,
+                                int32_t* group_mt_begin, cudaStream_t stream);
+
+// ------------------------------------------------------------------ tcgen05 grouped GEMM
+struct TcGemmArgs {
+  const int4* mt_info;
+  const int32_t* group_mt_begin;
+  int n_groups;
+  const int2* tile_list;  // kSimBits only
+  const int32_t* n_list;  // kSimBits only
+  int n_ntiles;
+  int n_kblocks;
+  int kb_per_slice;  // K blocks per B slice (the shared down projection spans slices along K)
+  int nt_per_slice;  // N tiles per B slice (the shared gate/up projection spans slices along N)
+  int b_up_offset;   // kSwiGLU: row of the first up-projection row inside a B slice (= H)
+  __nv_bfloat16* out;
+  long long ld_out;
+  const int32_t* out_rowmap;  // kStore: output row = out_rowmap[row], or row when NULL
+  // kSimBits
+  const float* norm;                   // [rows] L2 norm of each row (fp32)
+  const unsigned long long* row_hash;  // [rows] hash of each row's bits
+  const __nv_bfloat16* rows;           // the rows themselves (exact-duplicate check)
+  int d;
+  const int32_t* bucket_off;  // [E+1]
+  const long long* bits_base;  // [E] first word of bucket e's bit matrix
+  unsigned* bits;
+  float tau;
+  unsigned* status;
+};
+enum TcMode { kTcSwiGLU = 0, kTcStore = 1, kTcSimBits = 2 };
+// A: [a_rows, K] bf16 row-major.  B: [b_slices, b_rows, b_cols] bf16 (b_cols = K per slice).
+cudaError_t tc_gemm(int mode, const void* A, long long a_rows, int K, const void* B, int b_slices,
+                    int b_rows, int b_cols, const TcGemmArgs& args, int grid, cudaStream_t stream);
+constexpr int kTcTileN = 256;
+constexpr int kTcTileK = 64;
+
+// ------------------------------------------------------------------ fp32 SIMT grouped GEMM
+// Same tables and tile semantics as the tensor-core path, fp32 FMA throughout.
+cudaError_t simt_gemm_swiglu(const float* A, const float* B, int b_slices, int b_rows, int K,
+                             int kb_per_slice_k, int nt_per_slice, int H_total, int b_up_offset,
+                             const int4* mt_info, const int32_t* group_mt_begin, int n_groups,
+                             int max_mt, float* out, cudaStream_t stream);
+cudaError_t simt_gemm_store(const float* A, const float* B, int b_slices, int b_rows, int K,
+                            int k_per_slice, int N, const int4* mt_info,
+                            const int32_t* group_mt_begin, int n_groups, int max_mt,
+                            const int32_t* out_rowmap, float* out, cudaStream_t stream);
+
+// ------------------------------------------------------------------ condensation
+size_t condense_scratch_bytes(int T, int k, int E);
+cudaError_t launch_condense(const __nv_bfloat16* x_perm, const int32_t* offsets, int P, int d,
+                            int E, float tau, int num_sms, int32_t* rep_of, int32_t* n_rep,
+                            int32_t* n_condensed, void* scratch, unsigned* status,
+                            cudaStream_t stream);
+// Representative rows compacted bucket by bucket: rep_rows[c] = slot of the c-th
+// representative, rep_counts[e] = representatives of bucket e.
+cudaError_t launch_compact_reps(const int32_t* rep_of, const int32_t* offsets, int P, int E,
+                                int32_t* rep_rows, int32_t* rep_counts, cudaStream_t stream);
+
+}  // namespace moe

@@ -1,0 +1,513 @@
+// C ABI of libmoe.so: argument checks, workspace layout, and the launch
+// sequence of the routed-expert MoE path.  See include/moe.h for the contract.
+#include <math.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+// One status word per device, shared by every call on that device.
+static __device__ unsigned g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  int num_sms = 0;
+  unsigned* status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+// Per-device set-up, done on the first call made with that device current.
+DeviceInfo* device_info() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return nullptr;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    d.status = static_cast<unsigned*>(p);
+    d.ready = true;
+  }
+  return &d;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+inline size_t act_bytes(const moe_config* c) { return c->act_dtype == MOE_BF16 ? 2 : 4; }
+
+moe_status check_cfg(const moe_config* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->T < 0 || c->d <= 0 || c->E <= 0 || c->E > 256 || c->k < 1 || c->k > c->E || c->k > 32 ||
+      c->H <= 0 || c->n_shared < 0 || (c->n_shared > 0 && c->H_shared <= 0))
+    return MOE_ERR_INVALID_ARG;
+  if (c->act_dtype != MOE_F32 && c->act_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (c->gating < MOE_GATE_SOFTMAX_TOPK || c->gating > MOE_GATE_SIGMOID_TOPK)
+    return MOE_ERR_INVALID_ARG;
+  if (c->residual < MOE_RES_NONE || c->residual > MOE_RES_INPUT_PLUS_EXTERNAL)
+    return MOE_ERR_INVALID_ARG;
+  if (static_cast<long long>(c->T) * c->k > (1ll << 30)) return MOE_ERR_UNSUPPORTED;
+  if (c->act_dtype == MOE_BF16) {
+    if (c->d % 256 || c->H % 128 || (c->n_shared > 0 && c->H_shared % 128))
+      return MOE_ERR_UNSUPPORTED;
+  } else {
+    if (c->d % 64 || c->H % 64 || (c->n_shared > 0 && c->H_shared % 64)) return MOE_ERR_UNSUPPORTED;
+  }
+  return MOE_OK;
+}
+
+#define MOE_REQUIRE(cond, code) \
+  do {                          \
+    if (!(cond)) return (code); \
+  } while (0)
+#define MOE_PTR(p) MOE_REQUIRE((p) != nullptr && aligned16(p), MOE_ERR_INVALID_ARG)
+#define MOE_OPT_PTR(p) MOE_REQUIRE((p) == nullptr || aligned16(p), MOE_ERR_INVALID_ARG)
+#define MOE_CUDA(expr)                                   \
+  do {                                                   \
+    if ((expr) != cudaSuccess) return MOE_ERR_CUDA;      \
+  } while (0)
+
+// Bump allocator over a caller workspace.
+struct Carver {
+  char* base;
+  size_t off = 0;
+  explicit Carver(void* b) : base(static_cast<char*>(b)) {}
+  template <typename T>
+  T* take(size_t count) {
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off = align256(off + count * sizeof(T));
+    return p;
+  }
+};
+
+// ------------------------------------------------------------------ expert FFN scratch
+struct FfnScratch {
+  int4* mt_routed;
+  int32_t* gmb_routed;
+  int4* mt_shared;
+  int32_t* gmb_shared;
+  void* h;
+  void* h_shared;
+  int32_t* rep_rows;
+  int32_t* rep_counts;
+  int32_t* rep_off;
+  void* x_rep;
+};
+
+size_t carve_ffn(const moe_config* c, bool condense, void* ws, FfnScratch* s) {
+  const long long P = static_cast<long long>(c->T) * c->k;
+  const size_t ab = act_bytes(c);
+  Carver cv(ws);
+  FfnScratch t;
+  t.mt_routed = cv.take<int4>(max_mtiles(P, c->E));
+  t.gmb_routed = cv.take<int32_t>(c->E + 1);
+  t.mt_shared = cv.take<int4>(max_mtiles(c->T, 1));
+  t.gmb_shared = cv.take<int32_t>(2);
+  t.h = cv.take<char>(static_cast<size_t>(P) * c->H * ab);
+  t.h_shared = cv.take<char>(static_cast<size_t>(c->T) * c->n_shared * c->H_shared * ab);
+  t.rep_rows = t.rep_counts = t.rep_off = nullptr;
+  t.x_rep = nullptr;
+  if (condense) {
+    t.rep_rows = cv.take<int32_t>(P);
+    t.rep_counts = cv.take<int32_t>(c->E);
+    t.rep_off = cv.take<int32_t>(c->E + 1);
+    t.x_rep = cv.take<char>(static_cast<size_t>(P) * c->d * ab);
+  }
+  if (s) *s = t;
+  return cv.off;
+}
+
+moe_status run_expert_ffn(const moe_config* c, const moe_weights* w, const void* x_perm,
+                          const int32_t* offsets, const int32_t* rep_of, const void* x,
+                          void* y_perm, void* shared_out, const FfnScratch& s, DeviceInfo* di,
+                          cudaStream_t st) {
+  const int T = c->T, d = c->d, E = c->E, H = c->H, S = c->n_shared, Hs = c->H_shared;
+  const long long P = static_cast<long long>(T) * c->k;
+  if (T == 0) return MOE_OK;
+  const bool bf16 = c->act_dtype == MOE_BF16;
+  // Rows the routed experts run on: every slot, or the representatives only.
+  const void* A1 = x_perm;
+  const int32_t* rowmap = nullptr;
+  if (rep_of) {
+    MOE_CUDA(launch_compact_reps(rep_of, offsets, static_cast<int>(P), E, s.rep_rows,
+                                 s.rep_counts, st));
+    MOE_CUDA(launch_build_mtiles(s.rep_counts, nullptr, 0, E, s.rep_off, s.mt_routed,
+                                 s.gmb_routed, st));
+    MOE_CUDA(launch_gather_rows(c->act_dtype, x_perm, static_cast<int>(P), s.rep_rows,
+                                s.rep_off + E, static_cast<int>(P), d, s.x_rep, di->status, st));
+    A1 = s.x_rep;
+    rowmap = s.rep_rows;
+  } else {
+    MOE_CUDA(launch_build_mtiles(nullptr, offsets, 0, E, nullptr, s.mt_routed, s.gmb_routed, st));
+  }
+  if (S > 0) MOE_CUDA(launch_build_mtiles(nullptr, nullptr, T, 1, nullptr, s.mt_shared, s.gmb_shared, st));
+  const int mt_routed_max = max_mtiles(P, E);
+  const int mt_shared_max = max_mtiles(T, 1);
+
+  if (bf16) {
+    TcGemmArgs a = {};
+    a.status = di->status;
+    // routed gate/up + SwiGLU
+    a.mt_info = s.mt_routed;
+    a.group_mt_begin = s.gmb_routed;
+    a.n_groups = E;
+    a.n_ntiles = H / 128;
+    a.nt_per_slice = H / 128;
+    a.n_kblocks = d / kTcTileK;
+    a.kb_per_slice = a.n_kblocks;
+    a.b_up_offset = H;
+    a.out = static_cast<__nv_bfloat16*>(s.h);
+    a.ld_out = H;
+    MOE_CUDA(tc_gemm(kTcSwiGLU, A1, P, d, w->W_gu, E, 2 * H, d, a, di->num_sms, st));
+    // routed down projection
+    a.n_ntiles = d / kTcTileN;
+    a.nt_per_slice = a.n_ntiles;
+    a.n_kblocks = H / kTcTileK;
+    a.kb_per_slice = a.n_kblocks;
+    a.b_up_offset = 0;
+    a.out = static_cast<__nv_bfloat16*>(y_perm);
+    a.ld_out = d;
+    a.out_rowmap = rowmap;
+    MOE_CUDA(tc_gemm(kTcStore, s.h, P, H, w->W_down, E, d, H, a, di->num_sms, st));
+    if (S > 0) {
+      TcGemmArgs b = {};
+      b.status = di->status;
+      b.mt_info = s.mt_shared;
+      b.group_mt_begin = s.gmb_shared;
+      b.n_groups = 1;
+      b.n_ntiles = S * Hs / 128;
+      b.nt_per_slice = Hs / 128;
+      b.n_kblocks = d / kTcTileK;
+      b.kb_per_slice = b.n_kblocks;
+      b.b_up_offset = Hs;
+      b.out = static_cast<__nv_bfloat16*>(s.h_shared);
+      b.ld_out = static_cast<long long>(S) * Hs;
+      MOE_CUDA(tc_gemm(kTcSwiGLU, x, T, d, w->Ws_gu, S, 2 * Hs, d, b, di->num_sms, st));
+      b.n_ntiles = d / kTcTileN;
+      b.nt_per_slice = b.n_ntiles;
+      b.n_kblocks = S * Hs / kTcTileK;
+      b.kb_per_slice = Hs / kTcTileK;
+      b.b_up_offset = 0;
+      b.out = static_cast<__nv_bfloat16*>(shared_out);
+      b.ld_out = d;
+      MOE_CUDA(tc_gemm(kTcStore, s.h_shared, T, S * Hs, w->Ws_down, S, d, Hs, b, di->num_sms,
+                       st));
+    }
+  } else {
+    const float* Wgu = static_cast<const float*>(w->W_gu);
+    const float* Wdn = static_cast<const float*>(w->W_down);
+    MOE_CUDA(simt_gemm_swiglu(static_cast<const float*>(A1), Wgu, E, 2 * H, d, 0, H / 64, H, H,
+                              s.mt_routed, s.gmb_routed, E, mt_routed_max,
+                              static_cast<float*>(s.h), st));
+    MOE_CUDA(simt_gemm_store(static_cast<const float*>(s.h), Wdn, E, d, H, H, d, s.mt_routed,
+                             s.gmb_routed, E, mt_routed_max, rowmap, static_cast<float*>(y_perm),
+                             st));
+    if (S > 0) {
+      MOE_CUDA(simt_gemm_swiglu(static_cast<const float*>(x), static_cast<const float*>(w->Ws_gu),
+                                S, 2 * Hs, d, 0, Hs / 64, S * Hs, Hs, s.mt_shared, s.gmb_shared, 1,
+                                mt_shared_max, static_cast<float*>(s.h_shared), st));
+      MOE_CUDA(simt_gemm_store(static_cast<const float*>(s.h_shared),
+                               static_cast<const float*>(w->Ws_down), S, d, S * Hs, Hs, d,
+                               s.mt_shared, s.gmb_shared, 1, mt_shared_max, nullptr,
+                               static_cast<float*>(shared_out), st));
+    }
+  }
+  return MOE_OK;
+}
+
+moe_status check_weights(const moe_config* c, const moe_weights* w) {
+  MOE_REQUIRE(w != nullptr, MOE_ERR_INVALID_ARG);
+  MOE_PTR(w->W_gu);
+  MOE_PTR(w->W_down);
+  if (c->n_shared > 0) {
+    MOE_PTR(w->Ws_gu);
+    MOE_PTR(w->Ws_down);
+  }
+  return MOE_OK;
+}
+
+// ------------------------------------------------------------------ layer workspace
+struct LayerScratch {
+  float* logits;
+  int32_t* topk_idx;
+  float* gate;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* perm;
+  int32_t* slot_of;
+  void* x_perm;
+  void* dispatch_ws;
+  int32_t* rep_of;
+  int32_t* n_rep;
+  int32_t* n_condensed;
+  void* condense_ws;
+  void* y_perm;
+  void* shared_out;
+  void* ffn_ws;
+};
+
+size_t carve_layer(const moe_config* c, bool condense, void* ws, LayerScratch* s) {
+  const long long P = static_cast<long long>(c->T) * c->k;
+  const size_t ab = act_bytes(c);
+  Carver cv(ws);
+  LayerScratch t;
+  t.logits = cv.take<float>(static_cast<size_t>(c->T) * c->E);
+  t.topk_idx = cv.take<int32_t>(P);
+  t.gate = cv.take<float>(P);
+  t.counts = cv.take<int32_t>(c->E);
+  t.offsets = cv.take<int32_t>(c->E + 1);
+  t.perm = cv.take<int32_t>(P);
+  t.slot_of = cv.take<int32_t>(P);
+  t.x_perm = cv.take<char>(static_cast<size_t>(P) * c->d * ab);
+  t.dispatch_ws = cv.take<char>(dispatch_scratch_bytes(c->T, c->E));
+  t.rep_of = cv.take<int32_t>(P);
+  t.n_rep = cv.take<int32_t>(c->E);
+  t.n_condensed = cv.take<int32_t>(1);
+  t.condense_ws = condense ? cv.take<char>(condense_scratch_bytes(c->T, c->k, c->E)) : nullptr;
+  t.y_perm = cv.take<char>(static_cast<size_t>(P) * c->d * ab);
+  t.shared_out = cv.take<char>(c->n_shared > 0 ? static_cast<size_t>(c->T) * c->d * ab : 0);
+  t.ffn_ws = cv.take<char>(carve_ffn(c, condense, nullptr, nullptr));
+  if (s) *s = t;
+  return cv.off;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_DEVICE_INDEX: return "device index out of range";
+  }
+  return "unknown status";
+}
+
+float moe_adaptive_tau(float l_norm) {
+  return static_cast<float>(1.0 / (1.0 + exp(static_cast<double>(l_norm))));
+}
+
+moe_status moe_get_device_status(moe_stream_t stream) {
+  DeviceInfo* di = device_info();
+  if (!di) return MOE_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  unsigned v = 0;
+  MOE_CUDA(cudaStreamSynchronize(st));
+  MOE_CUDA(cudaMemcpyAsync(&v, di->status, sizeof(v), cudaMemcpyDeviceToHost, st));
+  MOE_CUDA(cudaMemsetAsync(di->status, 0, sizeof(unsigned), st));
+  MOE_CUDA(cudaStreamSynchronize(st));
+  return static_cast<moe_status>(v);
+}
+
+moe_status moe_route(const moe_config* cfg, const void* x, const float* W_r, const float* bias,
+                     float* logits, int32_t* topk_idx, float* topk_gate, moe_stream_t stream) {
+  moe_status s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (cfg->T == 0) return MOE_OK;
+  MOE_PTR(x);
+  MOE_PTR(W_r);
+  MOE_OPT_PTR(bias);
+  MOE_PTR(logits);
+  MOE_PTR(topk_idx);
+  MOE_PTR(topk_gate);
+  if (!device_info()) return MOE_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  MOE_CUDA(launch_router_logits(cfg->act_dtype, x, W_r, bias, logits, cfg->T, cfg->d, cfg->E, st));
+  MOE_CUDA(launch_router_topk(logits, topk_idx, topk_gate, cfg->T, cfg->E, cfg->k, cfg->gating, st));
+  return MOE_OK;
+}
+
+size_t moe_dispatch_workspace_size(const moe_config* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return 0;
+  return align256(dispatch_scratch_bytes(cfg->T, cfg->E));
+}
+
+moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                        int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* slot_of,
+                        void* x_perm, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  moe_status s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  MOE_PTR(counts);
+  MOE_PTR(offsets);
+  if (cfg->T > 0) {
+    MOE_PTR(x);
+    MOE_PTR(topk_idx);
+    MOE_PTR(perm);
+    MOE_PTR(slot_of);
+    MOE_PTR(x_perm);
+  }
+  MOE_OPT_PTR(ws);
+  MOE_REQUIRE(ws_bytes >= moe_dispatch_workspace_size(cfg), MOE_ERR_WORKSPACE);
+  MOE_REQUIRE(ws != nullptr || moe_dispatch_workspace_size(cfg) == 0, MOE_ERR_WORKSPACE);
+  DeviceInfo* di = device_info();
+  if (!di) return MOE_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  MOE_CUDA(launch_dispatch(cfg->act_dtype, x, topk_idx, cfg->T, cfg->d, cfg->E, cfg->k, counts,
+                           offsets, perm, slot_of, x_perm, ws, di->status, st));
+  return MOE_OK;
+}
+
+size_t moe_condense_workspace_size(const moe_config* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return 0;
+  return align256(condense_scratch_bytes(cfg->T, cfg->k, cfg->E));
+}
+
+moe_status moe_condense(const moe_config* cfg, const void* x_perm, const int32_t* offsets, float tau,
+                        int32_t* rep_of, int32_t* n_rep, int32_t* n_condensed, void* ws,
+                        size_t ws_bytes, moe_stream_t stream) {
+  moe_status s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  MOE_PTR(offsets);
+  MOE_PTR(n_rep);
+  MOE_PTR(n_condensed);
+  const long long P = static_cast<long long>(cfg->T) * cfg->k;
+  if (P > 0) {
+    MOE_PTR(x_perm);
+    MOE_PTR(rep_of);
+  }
+  const bool active = tau <= 1.0f;
+  if (active) {
+    if (cfg->act_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    if (P > 65536) return MOE_ERR_UNSUPPORTED;
+    MOE_PTR(ws);
+    MOE_REQUIRE(ws_bytes >= moe_condense_workspace_size(cfg), MOE_ERR_WORKSPACE);
+  }
+  DeviceInfo* di = device_info();
+  if (!di) return MOE_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  MOE_CUDA(launch_condense(static_cast<const __nv_bfloat16*>(x_perm), offsets, static_cast<int>(P),
+                           cfg->d, cfg->E, tau, di->num_sms, rep_of, n_rep, n_condensed, ws,
+                           di->status, st));
+  return MOE_OK;
+}
+
+size_t moe_expert_ffn_workspace_size(const moe_config* cfg, int with_condensation) {
+  if (check_cfg(cfg) != MOE_OK) return 0;
+  return carve_ffn(cfg, with_condensation != 0, nullptr, nullptr);
+}
+
+moe_status moe_expert_ffn(const moe_config* cfg, const moe_weights* w, const void* x_perm,
+                          const int32_t* offsets, const int32_t* rep_of, const void* x,
+                          void* y_perm, void* shared_out, void* ws, size_t ws_bytes,
+                          moe_stream_t stream) {
+  moe_status s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (cfg->T == 0) return MOE_OK;
+  s = check_weights(cfg, w);
+  if (s != MOE_OK) return s;
+  MOE_PTR(x_perm);
+  MOE_PTR(offsets);
+  MOE_OPT_PTR(rep_of);
+  MOE_PTR(y_perm);
+  if (cfg->n_shared > 0) {
+    MOE_PTR(x);
+    MOE_PTR(shared_out);
+  }
+  MOE_PTR(ws);
+  MOE_REQUIRE(ws_bytes >= moe_expert_ffn_workspace_size(cfg, rep_of != nullptr), MOE_ERR_WORKSPACE);
+  DeviceInfo* di = device_info();
+  if (!di) return MOE_ERR_CUDA;
+  FfnScratch fs;
+  carve_ffn(cfg, rep_of != nullptr, ws, &fs);
+  return run_expert_ffn(cfg, w, x_perm, offsets, rep_of, x, y_perm, shared_out, fs, di,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_combine(const moe_config* cfg, const void* y_perm, const void* shared_out,
+                       const int32_t* slot_of, const int32_t* rep_of, const float* topk_gate,
+                       const void* x, const void* residual, void* out, moe_stream_t stream) {
+  moe_status s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (cfg->T == 0) return MOE_OK;
+  MOE_PTR(y_perm);
+  MOE_OPT_PTR(shared_out);
+  MOE_REQUIRE(cfg->n_shared == 0 || shared_out != nullptr, MOE_ERR_INVALID_ARG);
+  MOE_PTR(slot_of);
+  MOE_OPT_PTR(rep_of);
+  MOE_PTR(topk_gate);
+  MOE_PTR(out);
+  if (cfg->residual == MOE_RES_INPUT || cfg->residual == MOE_RES_INPUT_PLUS_EXTERNAL) MOE_PTR(x);
+  if (cfg->residual == MOE_RES_EXTERNAL || cfg->residual == MOE_RES_INPUT_PLUS_EXTERNAL)
+    MOE_PTR(residual);
+  DeviceInfo* di = device_info();
+  if (!di) return MOE_ERR_CUDA;
+  MOE_CUDA(launch_combine(cfg->act_dtype, y_perm, cfg->n_shared > 0 ? shared_out : nullptr, slot_of,
+                          rep_of, topk_gate, x, residual, cfg->residual, out, cfg->T, cfg->d,
+                          cfg->k, cfg->T * cfg->k, di->status,
+                          reinterpret_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+size_t moe_workspace_size(const moe_config* cfg, int with_condensation) {
+  if (check_cfg(cfg) != MOE_OK) return 0;
+  return carve_layer(cfg, with_condensation != 0, nullptr, nullptr);
+}
+
+moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const void* x,
+                             const void* residual, float tau, void* out, int32_t* topk_idx_out,
+                             int32_t* n_condensed_out, void* ws, size_t ws_bytes,
+                             moe_stream_t stream) {
+  moe_status s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (cfg->T == 0) return MOE_OK;
+  s = check_weights(cfg, w);
+  if (s != MOE_OK) return s;
+  MOE_PTR(w->W_r);
+  MOE_OPT_PTR(w->router_bias);
+  MOE_PTR(x);
+  MOE_PTR(out);
+  MOE_OPT_PTR(topk_idx_out);
+  MOE_OPT_PTR(n_condensed_out);
+  if (cfg->residual == MOE_RES_EXTERNAL || cfg->residual == MOE_RES_INPUT_PLUS_EXTERNAL)
+    MOE_PTR(residual);
+  const bool condense = tau <= 1.0f;
+  const long long P = static_cast<long long>(cfg->T) * cfg->k;
+  if (condense && (cfg->act_dtype != MOE_BF16 || P > 65536)) return MOE_ERR_UNSUPPORTED;
+  MOE_PTR(ws);
+  MOE_REQUIRE(ws_bytes >= moe_workspace_size(cfg, condense), MOE_ERR_WORKSPACE);
+  DeviceInfo* di = device_info();
+  if (!di) return MOE_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  LayerScratch L;
+  carve_layer(cfg, condense, ws, &L);
+  int32_t* idx = topk_idx_out ? topk_idx_out : L.topk_idx;
+  MOE_CUDA(launch_router_logits(cfg->act_dtype, x, w->W_r, w->router_bias, L.logits, cfg->T,
+                                cfg->d, cfg->E, st));
+  MOE_CUDA(launch_router_topk(L.logits, idx, L.gate, cfg->T, cfg->E, cfg->k, cfg->gating, st));
+  MOE_CUDA(launch_dispatch(cfg->act_dtype, x, idx, cfg->T, cfg->d, cfg->E, cfg->k, L.counts,
+                           L.offsets, L.perm, L.slot_of, L.x_perm, L.dispatch_ws, di->status, st));
+  const int32_t* rep_of = nullptr;
+  if (condense) {
+    MOE_CUDA(launch_condense(static_cast<const __nv_bfloat16*>(L.x_perm), L.offsets,
+                             static_cast<int>(P), cfg->d, cfg->E, tau, di->num_sms, L.rep_of,
+                             L.n_rep, n_condensed_out ? n_condensed_out : L.n_condensed,
+                             L.condense_ws, di->status, st));
+    rep_of = L.rep_of;
+  } else if (n_condensed_out) {
+    MOE_CUDA(cudaMemsetAsync(n_condensed_out, 0, sizeof(int32_t), st));
+  }
+  FfnScratch fs;
+  carve_ffn(cfg, condense, L.ffn_ws, &fs);
+  s = run_expert_ffn(cfg, w, L.x_perm, L.offsets, rep_of, x, L.y_perm, L.shared_out, fs, di, st);
+  if (s != MOE_OK) return s;
+  MOE_CUDA(launch_combine(cfg->act_dtype, L.y_perm, cfg->n_shared > 0 ? L.shared_out : nullptr,
+                          L.slot_of, rep_of, L.gate, x, residual, cfg->residual, out, cfg->T,
+                          cfg->d, cfg->k, static_cast<int>(P), di->status, st));
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -45,7 +45,7 @@ def condition(cfg: gen.MoEConfig, inp: dict, max_rounds: int = 50) -> dict:
     raise RuntimeError(f"{cfg.name}: routing ties remain after {max_rounds} redraws")
 
 
-@functools.lru_cache(maxsize=4)
+@functools.lru_cache(maxsize=16)
 def workload(name: str, T: int | None = None, x_kind: str | None = None) -> tuple:
     """(cfg, conditioned inputs) for a named workload, optionally with fewer tokens."""
     cfg = gen.CONFIGS[name]

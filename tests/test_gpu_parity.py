@@ -1,0 +1,276 @@
+"""CUDA path vs the fp64 oracle, through the C ABI (libmoe.so) on one GPU.
+
+Bit-exact: routing indices, counts, offsets, permutation, slot map, x_perm,
+condensation assignment.  Within max|gpu - oracle| <= tol * max|oracle|
+(1e-4 fp32 layers, 1e-2 bf16 layers): gates, expert outputs, layer outputs.
+Small cases run every token; the full-size workloads compare sampled tokens
+(their routing and permutation are still compared in full).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+
+from oracle import moe_oracle as orc
+from routing_expert_ffn_gb300 import inputs as gen
+from tests import harness
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+NAMES = gen.CONFIG_ORDER
+# Token counts the oracle runs whole layers on in seconds, spanning several m-tiles and a ragged tail.
+SMALL_T = {"tiny_fp32": 256, "dsv2_lite": 600, "qwen3_30b_a3b": 700, "llama4_scout_farskip": 300,
+           "luffy_condense": 1000}
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from routing_expert_ffn_gb300 import build
+    build.build()
+    from routing_expert_ffn_gb300 import moe as m
+    m.lib()
+    return m
+
+
+def _np(t):
+    return t.detach().float().cpu().numpy() if t.dtype in (torch.bfloat16, torch.float16) else t.detach().cpu().numpy()
+
+
+def _setup(moe, name, T=None, x_kind=None, **over):
+    cfg, inp = harness.workload(name, T, x_kind)
+    C = moe.Config.from_workload(cfg)
+    for k_, v in over.items():
+        setattr(C, k_, v)
+    w, x, r = moe.upload(C, inp)
+    return cfg, inp, C, w, x, r
+
+
+def _sample_tokens(T, n=48, seed=0):
+    rng = np.random.default_rng(seed)
+    s = set(rng.choice(T, size=min(n, T), replace=False).tolist()) | {0, T - 1}
+    return np.array(sorted(s))
+
+
+def _status_ok(moe):
+    assert moe.get_device_status() == 0
+
+
+# ------------------------------------------------------------------ router
+@pytest.mark.parametrize("name", NAMES)
+def test_router_full_size(moe, name):
+    cfg, inp, C, w, x, r = _setup(moe, name)
+    logits, idx, gate = moe.route(C, x, w.W_r, w.router_bias)
+    torch.cuda.synchronize()
+    l_ref, idx_ref, g_ref = orc.route(inp["x"], inp["W_r"], inp["bias"], cfg.k, cfg.gating)
+    np.testing.assert_array_equal(_np(idx), idx_ref)
+    assert harness.max_rel_err(_np(logits), l_ref) < 1e-5
+    np.testing.assert_allclose(_np(gate), g_ref, rtol=2e-5, atol=1e-7)
+    _status_ok(moe)
+
+
+# ------------------------------------------------------------------ dispatch
+@pytest.mark.parametrize("name", NAMES)
+def test_dispatch_full_size(moe, name):
+    cfg, inp, C, w, x, r = _setup(moe, name)
+    _, idx, _ = moe.route(C, x, w.W_r, w.router_bias)
+    out = moe.dispatch(C, x, idx)
+    torch.cuda.synchronize()
+    counts, offsets, perm, slot_of = orc.dispatch(_np(idx), cfg.E)
+    np.testing.assert_array_equal(_np(out["counts"]), counts)
+    np.testing.assert_array_equal(_np(out["offsets"]), offsets)
+    np.testing.assert_array_equal(_np(out["perm"])[: cfg.P], perm)
+    np.testing.assert_array_equal(_np(out["slot_of"]), slot_of)
+    # rows moved bit for bit
+    ref = x.index_select(0, out["perm"][: cfg.P].long())
+    assert torch.equal(out["x_perm"][: cfg.P], ref)
+    _status_ok(moe)
+
+
+def test_dispatch_empty_buckets_and_skew(moe):
+    cfg, inp, C, w, x, r = _setup(moe, "qwen3_30b_a3b")
+    _, idx, _ = moe.route(C, x, w.W_r, w.router_bias)
+    out = moe.dispatch(C, x, idx)
+    counts = _np(out["counts"])
+    assert (counts == 0).any() and counts.max() > 4 * cfg.P / cfg.E
+    assert counts.sum() == cfg.P
+
+
+# ------------------------------------------------------------------ expert FFN
+def _ffn_check(moe, name, T):
+    cfg, inp, C, w, x, r = _setup(moe, name, T=T)
+    _, idx, _ = moe.route(C, x, w.W_r, w.router_bias)
+    d = moe.dispatch(C, x, idx)
+    y, so = moe.expert_ffn(C, w, d["x_perm"], d["offsets"], None, x)
+    torch.cuda.synchronize()
+    perm = _np(d["perm"])[: cfg.P]
+    offsets = _np(d["offsets"])
+    rng = np.random.default_rng(1)
+    slots = np.unique(np.concatenate([rng.choice(cfg.P, size=min(256, cfg.P), replace=False),
+                                      offsets[1:-1] - 1, offsets[:-1][offsets[:-1] < cfg.P],
+                                      [cfg.P - 1]]))
+    expert_of_slot = np.searchsorted(offsets, slots, side="right") - 1
+    yg = _np(y)[slots]
+    yr = np.zeros_like(yg, dtype=np.float64)
+    for e in np.unique(expert_of_slot):
+        m = expert_of_slot == e
+        yr[m] = orc.swiglu_expert(inp["x"][perm[slots[m]]], inp["W_gu"][e], inp["W_down"][e])
+    assert harness.max_rel_err(yg, yr) <= harness.tolerance(cfg), name
+    if cfg.n_shared:
+        toks = _sample_tokens(cfg.T, 64)
+        sr = orc.shared_experts(inp["x"][toks], inp["Ws_gu"], inp["Ws_down"])
+        assert harness.max_rel_err(_np(so)[toks], sr) <= harness.tolerance(cfg), name
+    _status_ok(moe)
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_expert_ffn_small(moe, name):
+    _ffn_check(moe, name, SMALL_T[name])
+
+
+@pytest.mark.parametrize("name", ["dsv2_lite", "qwen3_30b_a3b", "llama4_scout_farskip"])
+def test_expert_ffn_full_size(moe, name):
+    _ffn_check(moe, name, None)
+
+
+# ------------------------------------------------------------------ combine / round trip
+def test_round_trip_identity_experts(moe):
+    """dispatch -> identity experts (y = x_perm) -> combine with gates summing to 1 == x."""
+    cfg, inp, C, w, x, r = _setup(moe, "qwen3_30b_a3b", T=1000)
+    C.residual = "none"
+    _, idx, gate = moe.route(C, x, w.W_r, w.router_bias)  # renormalised gates
+    d = moe.dispatch(C, x, idx)
+    out = moe.combine(C, d["x_perm"], None, d["slot_of"], None, gate, x)
+    torch.cuda.synchronize()
+    assert torch.equal(out, x)
+
+
+# ------------------------------------------------------------------ whole layer
+def _layer_check(moe, name, T=None, tau=math.nan, residual=None, tokens=None):
+    cfg, inp, C, w, x, r = _setup(moe, name, T=T)
+    if residual is not None:
+        C.residual = residual
+    lay = moe.Layer(C, w, condense=tau <= 1.0)
+    idx = torch.empty((C.T, C.k), dtype=torch.int32, device=x.device)
+    ncond = torch.zeros(1, dtype=torch.int32, device=x.device)
+    out = lay(x, r, tau, topk_idx_out=idx, n_condensed_out=ncond)
+    torch.cuda.synchronize()
+    toks = np.arange(C.T) if tokens is None else tokens
+    ref = orc.layer_forward(inp["x"], inp["W_r"], inp["bias"], inp["W_gu"], inp["W_down"],
+                            inp["Ws_gu"], inp["Ws_down"], cfg.k, cfg.gating,
+                            residual_mode=C.residual, residual=inp["residual"],
+                            tau=None if not tau <= 1.0 else tau, tokens=toks)
+    np.testing.assert_array_equal(_np(idx), ref["idx"])
+    err = harness.max_rel_err(_np(out)[toks], ref["out"])
+    assert err <= harness.tolerance(cfg), (name, err)
+    expected_cond = int((ref["rep_of"] != np.arange(len(ref["rep_of"]))).sum())
+    assert int(ncond.item()) == expected_cond
+    _status_ok(moe)
+    return out, ref
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_layer_small(moe, name):
+    _layer_check(moe, name, T=SMALL_T[name])
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_layer_small_moe_part_only(moe, name):
+    """The residual dominates max|out|; the routed + shared part alone meets the same bound."""
+    _layer_check(moe, name, T=SMALL_T[name], residual="none")
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_layer_full_size_sampled(moe, name):
+    cfg = gen.CONFIGS[name]
+    tau = cfg.taus[0] if cfg.taus else math.nan
+    _layer_check(moe, name, tau=tau, tokens=_sample_tokens(cfg.T, 48))
+
+
+@pytest.mark.parametrize("T", [1, 2, 127, 129, 777])
+def test_layer_ragged_token_counts(moe, T):
+    _layer_check(moe, "dsv2_lite", T=T)
+    _layer_check(moe, "tiny_fp32", T=min(T, 256))
+
+
+def test_layer_k_equals_E_identical_experts(moe):
+    """k = E, identical experts, renormalised gates: the layer is one dense SwiGLU FFN."""
+    cfg, inp = harness.workload("tiny_fp32")
+    from dataclasses import replace
+    E = 4
+    cfgk = replace(cfg, E=E, k=E, gating="softmax_topk_renorm", residual="none", n_shared=0)
+    C = moe.Config.from_workload(cfgk)
+    inp2 = dict(inp)
+    inp2["W_r"] = inp["W_r"][:, :E].copy()
+    inp2["W_gu"] = np.repeat(inp["W_gu"][:1], E, axis=0)
+    inp2["W_down"] = np.repeat(inp["W_down"][:1], E, axis=0)
+    inp2["Ws_gu"] = inp["Ws_gu"][:0]
+    inp2["Ws_down"] = inp["Ws_down"][:0]
+    w, x, _ = moe.upload(C, inp2)
+    out = moe.Layer(C, w)(x)
+    torch.cuda.synchronize()
+    dense = orc.swiglu_expert(inp["x"], inp["W_gu"][0], inp["W_down"][0])
+    assert harness.max_rel_err(_np(out), dense) <= 1e-4
+
+
+def test_layer_deterministic(moe):
+    cfg, inp, C, w, x, r = _setup(moe, "qwen3_30b_a3b", T=2048)
+    lay = moe.Layer(C, w)
+    a = lay(x, r).clone()
+    b = lay(x, r)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------------ condensation
+@pytest.mark.parametrize("tau_index", [0, 1])
+def test_condense_full_size(moe, tau_index):
+    cfg, inp, C, w, x, r = _setup(moe, "luffy_condense")
+    tau = cfg.taus[tau_index]
+    _, idx, _ = moe.route(C, x, w.W_r, w.router_bias)
+    d = moe.dispatch(C, x, idx)
+    rep_of, n_rep, ncond = moe.condense(C, d["x_perm"], d["offsets"], tau)
+    torch.cuda.synchronize()
+    counts, offsets, perm, slot_of = orc.dispatch(_np(idx), cfg.E)
+    ref = orc.condense(inp["x"][perm], offsets, tau)
+    np.testing.assert_array_equal(_np(rep_of)[: cfg.P], ref)
+    assert int(ncond.item()) == int((ref != np.arange(cfg.P)).sum()) > 0
+    reps_per_bucket = [int((ref[offsets[e]:offsets[e + 1]] == np.arange(offsets[e], offsets[e + 1])).sum())
+                       for e in range(cfg.E)]
+    np.testing.assert_array_equal(_np(n_rep), reps_per_bucket)
+    _status_ok(moe)
+
+
+def test_condense_exact_duplicates_tau_one(moe):
+    cfg, inp, C, w, x, r = _setup(moe, "luffy_condense", T=2048, x_kind="duplicates")
+    _, idx, _ = moe.route(C, x, w.W_r, w.router_bias)
+    d = moe.dispatch(C, x, idx)
+    rep_of, _, ncond = moe.condense(C, d["x_perm"], d["offsets"], 1.0)
+    torch.cuda.synchronize()
+    _, offsets, perm, _ = orc.dispatch(_np(idx), cfg.E)
+    ref = orc.condense(inp["x"][perm], offsets, 1.0)
+    np.testing.assert_array_equal(_np(rep_of)[: cfg.P], ref)
+    assert int(ncond.item()) > 0
+
+
+def test_condense_tau_above_one_is_identity(moe):
+    cfg, inp, C, w, x, r = _setup(moe, "luffy_condense", T=2048)
+    _, idx, _ = moe.route(C, x, w.W_r, w.router_bias)
+    d = moe.dispatch(C, x, idx)
+    for tau in (1.5, math.nan):
+        rep_of, n_rep, ncond = moe.condense(C, d["x_perm"], d["offsets"], tau)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(_np(rep_of)[: cfg.P], np.arange(cfg.P))
+        assert int(ncond.item()) == 0
+    base = moe.Layer(C, w)(x, r)
+    same = moe.Layer(C, w, condense=True)(x, r, 1.5)
+    torch.cuda.synchronize()
+    assert torch.equal(base, same)
+
+
+def test_condensed_layer_small(moe):
+    cfg = gen.CONFIGS["luffy_condense"]
+    for tau in cfg.taus:
+        _layer_check(moe, "luffy_condense", T=SMALL_T["luffy_condense"], tau=tau)
