@@ -152,6 +152,27 @@ moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* top
                         int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* slot_of,
                         void* x_perm, void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* Same as moe_dispatch, with the same outputs, but without a workspace: it
+ * allocates nothing.  The paper has no counterpart; this exists for callers
+ * that cannot allocate device memory -- for example a host whose device memory
+ * is entirely pre-reserved by its own allocator (a cudaMalloc would fail or
+ * fragment it), or a serving loop that must not call cudaMalloc because it
+ * synchronises the device and stalls its other streams.
+ *   - Scratch is a file-scope device array of 1 MiB inside libmoe.so, held by
+ *     every GPU that loads the library until the process exits.  The scratch
+ *     needed is 8 * E * ceil(T / 128) bytes; larger shapes return
+ *     MOE_ERR_WORKSPACE before anything is launched.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call shares the array and it keeps the last call's contents
+ *     (nothing in it has to start at zero: each call writes every entry it
+ *     reads).  Calls whose kernels overlap on the GPU -- on two streams, or
+ *     from two threads -- race on the array; serialise them.              */
+moe_status moe_dispatch_static_scratch(const moe_config* cfg, const void* x,
+                                       const int32_t* topk_idx, int32_t* counts, int32_t* offsets,
+                                       int32_t* perm, int32_t* slot_of, void* x_perm,
+                                       moe_stream_t stream);
+
 /* ---------------------------------------------------------------- condensation
  * Luffy token condensation inside each expert bucket (bf16 layers).  Walking a
  * bucket in slot order with the set R of representatives, slot j is condensed

@@ -511,3 +511,50 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ dispatch without a workspace
+// For callers that cannot allocate device memory: the dispatch scratch lives
+// in this file-scope device array instead of a caller workspace.  Every GPU
+// that loads the library holds these bytes until the process exits.
+namespace moe {
+namespace {
+constexpr size_t kStaticDispatchScratchBytes = size_t(1) << 20;  // 1 MiB
+static __device__ __align__(256) unsigned char g_dispatch_scratch[kStaticDispatchScratchBytes];
+// Device address of g_dispatch_scratch, looked up once per device.  In host
+// code the array's name is only a host-side stand-in, never a device address.
+void* g_dispatch_scratch_addr[kMaxDevices] = {};
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_dispatch_static_scratch(const moe_config* cfg, const void* x,
+                                                  const int32_t* topk_idx, int32_t* counts,
+                                                  int32_t* offsets, int32_t* perm,
+                                                  int32_t* slot_of, void* x_perm,
+                                                  moe_stream_t stream) {
+  moe_status s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  MOE_PTR(counts);
+  MOE_PTR(offsets);
+  if (cfg->T > 0) {
+    MOE_PTR(x);
+    MOE_PTR(topk_idx);
+    MOE_PTR(perm);
+    MOE_PTR(slot_of);
+    MOE_PTR(x_perm);
+  }
+  if (dispatch_scratch_bytes(cfg->T, cfg->E) > kStaticDispatchScratchBytes)
+    return MOE_ERR_WORKSPACE;
+  DeviceInfo* di = device_info();
+  if (!di) return MOE_ERR_CUDA;
+  int dev = 0;
+  MOE_CUDA(cudaGetDevice(&dev));
+  if (!g_dispatch_scratch_addr[dev]) {
+    void* p = nullptr;
+    MOE_CUDA(cudaGetSymbolAddress(&p, g_dispatch_scratch));
+    g_dispatch_scratch_addr[dev] = p;
+  }
+  MOE_CUDA(launch_dispatch(cfg->act_dtype, x, topk_idx, cfg->T, cfg->d, cfg->E, cfg->k, counts,
+                           offsets, perm, slot_of, x_perm, g_dispatch_scratch_addr[dev],
+                           di->status, reinterpret_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}

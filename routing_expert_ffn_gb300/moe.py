@@ -30,7 +30,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 EXPORTED = ("moe_status_string", "moe_adaptive_tau", "moe_get_device_status", "moe_route",
             "moe_dispatch_workspace_size", "moe_dispatch", "moe_condense_workspace_size",
             "moe_condense", "moe_expert_ffn_workspace_size", "moe_expert_ffn", "moe_combine",
-            "moe_workspace_size", "moe_layer_forward")
+            "moe_workspace_size", "moe_layer_forward", "moe_dispatch_static_scratch")
 
 
 class MoEError(RuntimeError):
@@ -80,6 +80,7 @@ def lib() -> ctypes.CDLL:
         "moe_combine": (I, [CFG, P, P, P, P, P, P, P, P, P]),
         "moe_workspace_size": (S, [CFG, I]),
         "moe_layer_forward": (I, [CFG, W, P, P, F, P, P, P, P, S, P]),
+        "moe_dispatch_static_scratch": (I, [CFG, P, P, P, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -197,6 +198,22 @@ def dispatch(cfg: Config, x, topk_idx, stream=None) -> dict:
     _check(lib().moe_dispatch(ctypes.byref(c), _ptr(x), _ptr(topk_idx), _ptr(out["counts"]),
                               _ptr(out["offsets"]), _ptr(out["perm"]), _ptr(out["slot_of"]),
                               _ptr(out["x_perm"]), _ptr(ws), n, _stream(stream)), "moe_dispatch")
+    return out
+
+
+def dispatch_static_scratch(cfg: Config, x, topk_idx, stream=None) -> dict:
+    """moe_dispatch without a workspace (scratch is a fixed array inside the library)."""
+    dev = x.device
+    P = cfg.T * cfg.k
+    out = dict(counts=_empty((cfg.E,), torch.int32, dev),
+               offsets=_empty((cfg.E + 1,), torch.int32, dev),
+               perm=_empty((max(P, 1),), torch.int32, dev),
+               slot_of=_empty((cfg.T, cfg.k), torch.int32, dev),
+               x_perm=_empty((max(P, 1), cfg.d), cfg.torch_dtype, dev))
+    _check(lib().moe_dispatch_static_scratch(
+        ctypes.byref(cfg.c()), _ptr(x), _ptr(topk_idx), _ptr(out["counts"]), _ptr(out["offsets"]),
+        _ptr(out["perm"]), _ptr(out["slot_of"]), _ptr(out["x_perm"]), _stream(stream)),
+        "moe_dispatch_static_scratch")
     return out
 
 
