@@ -130,7 +130,7 @@ def work(cfg, n_condensed: int = 0) -> dict:
 
 
 def launches_per_step(cfg, condense: bool) -> int:
-    n = 2 + 4  # router (logits, top-k) + dispatch (hist, scan, scatter, gather)
+    n = (3 if cfg.dtype == "bf16" else 2) + 4  # router (split, logits, top-k) + dispatch (4)
     if condense:
         n += 6  # row stats, m-tiles, tile list, similarity GEMM, greedy scan, count
         n += 3  # compact reps, m-tiles over representatives, gather representative rows
@@ -276,6 +276,8 @@ def phase_breakdown(args, moe, C, w, x, r, tau, flush, stream, torch) -> dict:
     ncond = torch.empty((1,), dtype=i32, device=dev)
     out = torch.empty((C.T, C.d), dtype=C.torch_dtype, device=dev)
     condense = tau <= 1.0
+    nr = L.moe_route_workspace_size(ctypes.byref(c))
+    ws_r = torch.empty(max(nr, 1), dtype=torch.uint8, device=dev)
     nd = L.moe_dispatch_workspace_size(ctypes.byref(c))
     nc = L.moe_condense_workspace_size(ctypes.byref(c)) if condense else 0
     nf = L.moe_expert_ffn_workspace_size(ctypes.byref(c), int(condense))
@@ -289,7 +291,7 @@ def phase_breakdown(args, moe, C, w, x, r, tau, flush, stream, torch) -> dict:
     def step(evs):
         evs[0].record(stream)
         moe._check(L.moe_route(ctypes.byref(c), p(x), p(w.W_r), p(w.router_bias), p(logits), p(idx),
-                               p(gate), s), "route")
+                               p(gate), p(ws_r), nr, s), "route")
         evs[1].record(stream)
         moe._check(L.moe_dispatch(ctypes.byref(c), p(x), p(idx), p(counts), p(offsets), p(perm),
                                   p(slot_of), p(x_perm), p(ws_d), nd, s), "dispatch")

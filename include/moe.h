@@ -124,17 +124,23 @@ float moe_adaptive_tau(float l_norm);
 moe_status moe_get_device_status(moe_stream_t stream);
 
 /* ---------------------------------------------------------------- router
- * T_gate of FarSkip Eq. 9.  logits[t,e] = sum_i x[t,i] W_r[i,e] (+ bias[e]) in
- * fp32 FMA (no TF32); the k experts with the largest logits, largest first,
- * a tie going to the lower index; gates per cfg->gating from the fp32 logits.
+ * T_gate of FarSkip Eq. 9.  logits[t,e] = sum_i x[t,i] W_r[i,e] (+ bias[e]) to
+ * fp32 accuracy (no TF32): fp32 layers on the FMA pipe; bf16 layers on tcgen05
+ * tensor cores with W_r split exactly into three bf16 terms (x is exactly
+ * bf16, so every product is exact and the sums are fp32).  Then the k experts
+ * with the largest logits, largest first, a tie going to the lower index;
+ * gates per cfg->gating from the fp32 logits.
  *   x        [T, d] act           (in)
  *   W_r      [d, E] fp32          (in)
  *   bias     [E] fp32 or NULL     (in)
- *   logits   [T, E] fp32          (out, scratch the caller may read)
+ *   logits   [T, E] fp32          (out, the caller may read it)
  *   topk_idx [T, k] int32         (out)
- *   topk_gate[T, k] fp32          (out)                                     */
+ *   topk_gate[T, k] fp32          (out)
+ *   ws       moe_route_workspace_size(cfg) bytes (0 for fp32 layers; NULL allowed then) */
+size_t moe_route_workspace_size(const moe_config* cfg);
 moe_status moe_route(const moe_config* cfg, const void* x, const float* W_r, const float* bias,
-                     float* logits, int32_t* topk_idx, float* topk_gate, moe_stream_t stream);
+                     float* logits, int32_t* topk_idx, float* topk_gate, void* ws,
+                     size_t ws_bytes, moe_stream_t stream);
 
 /* ---------------------------------------------------------------- dispatch
  * T_Dispatch of FarSkip Eq. 9, on one GPU: the permutation that the

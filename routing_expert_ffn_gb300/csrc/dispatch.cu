@@ -81,25 +81,33 @@ __global__ void __launch_bounds__(256)
   if (threadIdx.x == 0) offsets[E] = s_off[E];
 }
 
-// One warp per chunk: walks the chunk's pairs in (token, j) order, 32 at a
-// time; lanes holding the same expert get consecutive slots in lane order.
-__global__ void __launch_bounds__(32)
+// One CTA per chunk: all threads stage the chunk's expert ids in shared
+// memory, then warp 0 walks the pairs in (token, j) order, 32 at a time; lanes
+// holding the same expert get consecutive slots in lane order.
+constexpr int kScatterThreads = 128;
+__global__ void __launch_bounds__(kScatterThreads)
     dispatch_scatter_kernel(const int32_t* __restrict__ idx, int T, int E, int k, int n_chunks,
                             const int32_t* __restrict__ chunk_base, int32_t* __restrict__ perm,
                             int32_t* __restrict__ slot_of) {
   __shared__ int base[256];
+  __shared__ int s_idx[kDispatchChunk * 32];  // k <= 32
   const int c = blockIdx.x;
-  const int lane = threadIdx.x;
-  for (int e = lane; e < E; e += 32) base[e] = chunk_base[static_cast<long long>(e) * n_chunks + c];
-  __syncwarp();
   const long long p0 = static_cast<long long>(c) * kDispatchChunk * k;
   const long long p1 = static_cast<long long>(min(T, (c + 1) * kDispatchChunk)) * k;
+  const int n = static_cast<int>(p1 - p0);
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    base[e] = chunk_base[static_cast<long long>(e) * n_chunks + c];
+  for (int i = threadIdx.x; i < n; i += blockDim.x) s_idx[i] = idx[p0 + i];
+  __syncthreads();
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
   const unsigned lt = lanemask_lt();
-  for (long long pb = p0; pb < p1; pb += 32) {
-    const long long p = pb + lane;
+  for (int ib = 0; ib < n; ib += 32) {
+    const int i = ib + lane;
+    const long long p = p0 + i;
     int e = -1;
-    if (p < p1) {
-      e = idx[p];
+    if (i < n) {
+      e = s_idx[i];
       if (e < 0 || e >= E) e = -1;
     }
     const unsigned peers = __match_any_sync(0xffffffffu, e);
@@ -248,7 +256,7 @@ cudaError_t launch_dispatch(int act_dtype, const void* x, const int32_t* topk_id
   dispatch_scan_kernel<<<1, 256, 0, stream>>>(chunk_counts, E, n_chunks, counts, offsets,
                                               chunk_base);
   if (T == 0) return cudaGetLastError();
-  dispatch_scatter_kernel<<<n_chunks, 32, 0, stream>>>(topk_idx, T, E, k, n_chunks, chunk_base,
+  dispatch_scatter_kernel<<<n_chunks, kScatterThreads, 0, stream>>>(topk_idx, T, E, k, n_chunks, chunk_base,
                                                        perm, slot_of);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

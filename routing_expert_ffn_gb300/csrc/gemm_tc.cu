@@ -17,6 +17,10 @@
 //   kStore   writes D (bf16), optionally to a remapped output row.
 //   kSimBits condensation: D is a tile of the bucket's Gram matrix; the
 //            epilogue turns cos(x_i, x_j) >= tau, j < i, into bits.
+//   kRouter  router logits: B is the fp32 router weight split exactly into
+//            three bf16 terms; the K loop runs over the three terms, split
+//            across CTAs, and the epilogue writes fp32 partial sums (N = E
+//            rounded up to 32).
 //
 // Tiles.  Rows are grouped (one group per expert / bucket); a group's rows are
 // cut into 128-row m-tiles (the last one ragged; rows past the group are
@@ -49,7 +53,7 @@ constexpr int TMEM_COLS = 512;
 constexpr int M_GROUP = 16;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align slack*/ + 256 /*barriers*/;
 
-enum Mode { kSwiGLU = 0, kStore = 1, kSimBits = 2 };
+enum Mode { kSwiGLU = 0, kStore = 1, kSimBits = 2, kRouter = 3 };
 
 struct Shared {
   uint64_t full[STAGES];
@@ -90,6 +94,17 @@ struct TileInfo {
 template <int MODE>
 __device__ __forceinline__ TileInfo tile_info(const TcGemmArgs& a, int tile) {
   int mt, nt;
+  if (MODE == kRouter) {
+    // one group of T rows; tile = (m-tile, K split), K splits fastest
+    TileInfo t;
+    const int m = tile / a.n_ntiles;
+    t.nt = tile - m * a.n_ntiles;
+    t.slice = 0;
+    t.row0 = m * BM;
+    t.nrows = min(BM, a.n_rows - t.row0);
+    t.gbase = 0;
+    return t;
+  }
   if (MODE == kSimBits) {
     int2 e = a.tile_list[tile];
     mt = e.x;
@@ -123,6 +138,7 @@ __device__ __forceinline__ TileInfo tile_info(const TcGemmArgs& a, int tile) {
 template <int MODE>
 __device__ __forceinline__ int total_tiles(const TcGemmArgs& a) {
   if (MODE == kSimBits) return *a.n_list;
+  if (MODE == kRouter) return ((a.n_rows + BM - 1) / BM) * a.n_ntiles;
   return a.group_mt_begin[a.n_groups] * a.n_ntiles;
 }
 
@@ -204,20 +220,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t sb = sa + A_BYTES;
           const int kslice = kb / args.kb_per_slice;
           const int kin = (kb - kslice * args.kb_per_slice) * BK;
-          ptx::mbar_arrive_expect_tx(full, STAGE_BYTES);
-          ptx::tma_load_2d(sa, &tmA, full, kb * BK, t.row0);
-          if (MODE == kSwiGLU) {
-            const int nslice = t.nt / args.nt_per_slice;
-            const int n0 = (t.nt - nslice * args.nt_per_slice) * (BN / 2);
-            const int z = t.slice + nslice + kslice;
-            ptx::tma_load_3d(sb, &tmB, full, kin, n0, z);
-            ptx::tma_load_3d(sb + B_BYTES / 2, &tmB, full, kin, args.b_up_offset + n0, z);
-          } else if (MODE == kStore) {
-            const int nslice = t.nt / args.nt_per_slice;
-            const int n0 = (t.nt - nslice * args.nt_per_slice) * BN;
-            ptx::tma_load_3d(sb, &tmB, full, kin, n0, t.slice + nslice + kslice);
+          if (MODE == kRouter) {
+            // K block kb of this split -> term (W1, W2 or W3) and K offset inside x
+            const int g = t.nt * args.n_kblocks + kb;
+            const int term = g / args.router_kbd;
+            const int k0 = (g - term * args.router_kbd) * BK;
+            ptx::mbar_arrive_expect_tx(full, A_BYTES + args.router_n * BK * 2);
+            ptx::tma_load_2d(sa, &tmA, full, k0, t.row0);
+            ptx::tma_load_3d(sb, &tmB, full, k0, 0, term);
           } else {
-            ptx::tma_load_3d(sb, &tmB, full, kb * BK, t.gbase + t.nt * BN, 0);
+            ptx::mbar_arrive_expect_tx(full, STAGE_BYTES);
+            ptx::tma_load_2d(sa, &tmA, full, kb * BK, t.row0);
+            if (MODE == kSwiGLU) {
+              const int nslice = t.nt / args.nt_per_slice;
+              const int n0 = (t.nt - nslice * args.nt_per_slice) * (BN / 2);
+              const int z = t.slice + nslice + kslice;
+              ptx::tma_load_3d(sb, &tmB, full, kin, n0, z);
+              ptx::tma_load_3d(sb + B_BYTES / 2, &tmB, full, kin, args.b_up_offset + n0, z);
+            } else if (MODE == kStore) {
+              const int nslice = t.nt / args.nt_per_slice;
+              const int n0 = (t.nt - nslice * args.nt_per_slice) * BN;
+              ptx::tma_load_3d(sb, &tmB, full, kin, n0, t.slice + nslice + kslice);
+            } else {
+              ptx::tma_load_3d(sb, &tmB, full, kb * BK, t.gbase + t.nt * BN, 0);
+            }
           }
         }
         __syncwarp();
@@ -238,7 +264,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN);
+    const uint32_t idesc = ptx::idesc_bf16_f32(BM, MODE == kRouter ? args.router_n : BN);
     int stage = 0;
     uint32_t phase = 0;
     int local = 0;
@@ -301,7 +327,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const TileInfo t = tile_info<MODE>(args, tile);
       const uint32_t col0 = lane_addr + acc * BN;
       const bool valid = r < t.nrows;
-      if (MODE == kSwiGLU) {
+      if (MODE == kRouter) {
+        float* prow = args.part + (static_cast<long long>(t.nt) * args.n_rows + t.row0 + r) *
+                                      args.router_n;
+#pragma unroll 1
+        for (int c = 0; c < args.router_n / 32; ++c) {
+          uint32_t v[32];
+          ptx::tmem_ld_32x32b_x32(col0 + c * 32, v);
+          ptx::tmem_ld_wait();
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(prow + c * 32);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                   __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+          }
+        }
+      } else if (MODE == kSwiGLU) {
         __nv_bfloat16* orow = args.out + (static_cast<long long>(t.row0) + r) * args.ld_out +
                               static_cast<long long>(t.nt) * (BN / 2);
 #pragma unroll 1
@@ -454,12 +496,15 @@ cudaError_t tc_gemm(int mode, const void* A, long long a_rows, int K, const void
                     cudaStream_t stream) {
   CUtensorMap ma, mb;
   if (!tc::make_map(&ma, 2, A, K, a_rows, 1, tc::BM)) return cudaErrorInvalidValue;
-  const uint32_t box_rows = mode == tc::kSwiGLU ? tc::BN / 2 : tc::BN;
+  const uint32_t box_rows = mode == tc::kSwiGLU  ? tc::BN / 2
+                            : mode == tc::kRouter ? static_cast<uint32_t>(args.router_n)
+                                                  : tc::BN;
   if (!tc::make_map(&mb, 3, B, b_cols, b_rows, b_slices, box_rows)) return cudaErrorInvalidValue;
   switch (mode) {
     case tc::kSwiGLU: return tc::launch<tc::kSwiGLU>(ma, mb, args, grid, stream);
     case tc::kStore: return tc::launch<tc::kStore>(ma, mb, args, grid, stream);
     case tc::kSimBits: return tc::launch<tc::kSimBits>(ma, mb, args, grid, stream);
+    case tc::kRouter: return tc::launch<tc::kRouter>(ma, mb, args, grid, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -9,10 +9,21 @@
 namespace moe {
 
 // ------------------------------------------------------------------ router
-// logits = x W_r (+bias), fp32 FMA; then per-token top-k and gates.
+// fp32 layers: logits = x W_r (+bias) in fp32 FMA.
 cudaError_t launch_router_logits(int act_dtype, const void* x, const float* W_r, const float* bias,
                                  float* logits, int T, int d, int E, cudaStream_t stream);
-cudaError_t launch_router_topk(const float* logits, int32_t* topk_idx, float* topk_gate, int T,
+// bf16 layers: W_r [d,E] fp32 -> W3 [3][E_pad][d] bf16 with W_r = W1 + W2 + W3 exactly,
+// then the tcgen05 GEMM writes split-K partial logits.
+int router_n_pad(int E);
+int router_splits(int T, int d, int num_sms);
+size_t router_scratch_bytes(int T, int d, int E, int num_sms);
+cudaError_t launch_router_tc(const void* x, const float* W_r, int T, int d, int E, int num_sms,
+                             void* scratch, const float** part, int* n_split, int* ld,
+                             unsigned* status, cudaStream_t stream);
+// logits[t,e] = sum_s part[s][t][e] (s in order) + bias[e]; then top-k and gates.
+// logits_out may be NULL (or equal to part when n_split == 1 and bias == NULL).
+cudaError_t launch_router_topk(const float* part, int n_split, int ld, const float* bias,
+                               float* logits_out, int32_t* topk_idx, float* topk_gate, int T,
                                int E, int k, int gating, cudaStream_t stream);
 
 // ------------------------------------------------------------------ dispatch / combine
@@ -72,8 +83,13 @@ struct TcGemmArgs {
   unsigned* bits;
   float tau;
   unsigned* status;
+  // kRouter: D = x . [W1|W2|W3] over a K range of 3*d (the three bf16 terms of W_r)
+  int router_n;        // N of the MMA = E rounded up to 32
+  int router_kbd;      // K blocks per term (d / 64)
+  int n_rows;          // T
+  float* part;         // [n_ntiles (K splits)][T][router_n] fp32 partial logits
 };
-enum TcMode { kTcSwiGLU = 0, kTcStore = 1, kTcSimBits = 2 };
+enum TcMode { kTcSwiGLU = 0, kTcStore = 1, kTcSimBits = 2, kTcRouter = 3 };
 // A: [a_rows, K] bf16 row-major.  B: [b_slices, b_rows, b_cols] bf16 (b_cols = K per slice).
 cudaError_t tc_gemm(int mode, const void* A, long long a_rows, int K, const void* B, int b_slices,
                     int b_rows, int b_cols, const TcGemmArgs& args, int grid, cudaStream_t stream);

@@ -232,9 +232,38 @@ moe_status check_weights(const moe_config* c, const moe_weights* w) {
   return MOE_OK;
 }
 
+// ------------------------------------------------------------------ router
+// Workspace sizes must be computable without a device, so they assume the
+// largest SM count the split-K choice can see; launches clamp to it as well.
+constexpr int kMaxSmsForSizing = 256;
+
+size_t route_ws_bytes(const moe_config* c) {
+  if (c->act_dtype != MOE_BF16 || c->T == 0) return 0;
+  return router_scratch_bytes(c->T, c->d, c->E, kMaxSmsForSizing);
+}
+
+moe_status run_router(const moe_config* c, const void* x, const float* W_r, const float* bias,
+                      float* logits, int32_t* idx, float* gate, void* ws, DeviceInfo* di,
+                      cudaStream_t st) {
+  if (c->act_dtype == MOE_BF16) {
+    const float* part = nullptr;
+    int n_split = 0, ld = 0;
+    MOE_CUDA(launch_router_tc(x, W_r, c->T, c->d, c->E, di->num_sms < kMaxSmsForSizing ? di->num_sms : kMaxSmsForSizing,
+                              ws, &part, &n_split, &ld, di->status, st));
+    MOE_CUDA(launch_router_topk(part, n_split, ld, bias, logits, idx, gate, c->T, c->E, c->k,
+                                c->gating, st));
+  } else {
+    MOE_CUDA(launch_router_logits(c->act_dtype, x, W_r, bias, logits, c->T, c->d, c->E, st));
+    MOE_CUDA(launch_router_topk(logits, 1, c->E, nullptr, nullptr, idx, gate, c->T, c->E, c->k,
+                                c->gating, st));
+  }
+  return MOE_OK;
+}
+
 // ------------------------------------------------------------------ layer workspace
 struct LayerScratch {
   float* logits;
+  void* route_ws;
   int32_t* topk_idx;
   float* gate;
   int32_t* counts;
@@ -258,6 +287,7 @@ size_t carve_layer(const moe_config* c, bool condense, void* ws, LayerScratch* s
   Carver cv(ws);
   LayerScratch t;
   t.logits = cv.take<float>(static_cast<size_t>(c->T) * c->E);
+  t.route_ws = cv.take<char>(route_ws_bytes(c));
   t.topk_idx = cv.take<int32_t>(P);
   t.gate = cv.take<float>(P);
   t.counts = cv.take<int32_t>(c->E);
@@ -313,8 +343,14 @@ moe_status moe_get_device_status(moe_stream_t stream) {
   return static_cast<moe_status>(v);
 }
 
+size_t moe_route_workspace_size(const moe_config* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return 0;
+  return route_ws_bytes(cfg);
+}
+
 moe_status moe_route(const moe_config* cfg, const void* x, const float* W_r, const float* bias,
-                     float* logits, int32_t* topk_idx, float* topk_gate, moe_stream_t stream) {
+                     float* logits, int32_t* topk_idx, float* topk_gate, void* ws, size_t ws_bytes,
+                     moe_stream_t stream) {
   moe_status s = check_cfg(cfg);
   if (s != MOE_OK) return s;
   if (cfg->T == 0) return MOE_OK;
@@ -324,11 +360,13 @@ moe_status moe_route(const moe_config* cfg, const void* x, const float* W_r, con
   MOE_PTR(logits);
   MOE_PTR(topk_idx);
   MOE_PTR(topk_gate);
-  if (!device_info()) return MOE_ERR_CUDA;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  MOE_CUDA(launch_router_logits(cfg->act_dtype, x, W_r, bias, logits, cfg->T, cfg->d, cfg->E, st));
-  MOE_CUDA(launch_router_topk(logits, topk_idx, topk_gate, cfg->T, cfg->E, cfg->k, cfg->gating, st));
-  return MOE_OK;
+  const size_t need = route_ws_bytes(cfg);
+  if (need > 0) MOE_PTR(ws);
+  MOE_REQUIRE(ws_bytes >= need, MOE_ERR_WORKSPACE);
+  DeviceInfo* di = device_info();
+  if (!di) return MOE_ERR_CUDA;
+  return run_router(cfg, x, W_r, bias, logits, topk_idx, topk_gate, ws, di,
+                    reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t moe_dispatch_workspace_size(const moe_config* cfg) {
@@ -485,9 +523,8 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
   LayerScratch L;
   carve_layer(cfg, condense, ws, &L);
   int32_t* idx = topk_idx_out ? topk_idx_out : L.topk_idx;
-  MOE_CUDA(launch_router_logits(cfg->act_dtype, x, w->W_r, w->router_bias, L.logits, cfg->T,
-                                cfg->d, cfg->E, st));
-  MOE_CUDA(launch_router_topk(L.logits, idx, L.gate, cfg->T, cfg->E, cfg->k, cfg->gating, st));
+  s = run_router(cfg, x, w->W_r, w->router_bias, L.logits, idx, L.gate, L.route_ws, di, st);
+  if (s != MOE_OK) return s;
   MOE_CUDA(launch_dispatch(cfg->act_dtype, x, idx, cfg->T, cfg->d, cfg->E, cfg->k, L.counts,
                            L.offsets, L.perm, L.slot_of, L.x_perm, L.dispatch_ws, di->status, st));
   const int32_t* rep_of = nullptr;

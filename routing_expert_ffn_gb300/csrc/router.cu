@@ -2,10 +2,17 @@
 //
 // The pages print no router; they cite the sparsely-gated MoE layer and Switch
 // Transformers (FarSkip-Collective review, reference list) and name its cost
-// T_gate in the overlap condition (ledger, Eq. 9).  The logits are an fp32
-// contraction with E <= 256 columns: too narrow and too precision-sensitive for
-// the bf16 tensor path (routing must agree bit for bit with an fp64 reference
-// on inputs with relative logit gaps of 1e-4), so it runs on the fp32 pipe.
+// T_gate in the overlap condition (ledger, Eq. 9).
+//
+// The logits must be fp32-accurate: routing is compared exactly with an fp64
+// reference on inputs whose logit gaps are only 1e-4 of the logit scale.
+//   bf16 layers: x is exactly bf16, and the fp32 router weight splits exactly
+//     into three bf16 terms, W_r = W1 + W2 + W3 (8 + 8 + 8 significand bits; each
+//     residual is exactly representable).  x . W_r = x.W1 + x.W2 + x.W3 with
+//     every product exact and fp32 accumulation, i.e. fp32-accurate logits on the
+//     tcgen05 tensor cores.  The three terms form one K range of 3d that is split
+//     across CTAs; the top-k kernel adds the split partials in a fixed order.
+//   fp32 layers: x is not bf16, so the logits run on the fp32 FMA pipe.
 #include <float.h>
 
 #include "common.cuh"
@@ -97,19 +104,48 @@ __global__ void __launch_bounds__(kRThreads)
   }
 }
 
-// One warp per token: k rounds of warp argmax (ties -> lower expert), then gates.
+// W3[term][e][i] for term 0..2: W_r[i][e] = W3[0] + W3[1] + W3[2] exactly; rows e >= E are zero.
 __global__ void __launch_bounds__(256)
-    router_topk_kernel(const float* __restrict__ logits, int32_t* __restrict__ topk_idx,
-                       float* __restrict__ topk_gate, int T, int E, int k, int gating) {
+    router_split_kernel(const float* __restrict__ W_r, int d, int E, int n_pad,
+                        __nv_bfloat16* __restrict__ W3) {
+  const long long n = static_cast<long long>(n_pad) * d;
+  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < n;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int e = static_cast<int>(idx / d), i = static_cast<int>(idx - static_cast<long long>(e) * d);
+    const float w = e < E ? W_r[static_cast<long long>(i) * E + e] : 0.f;
+    const __nv_bfloat16 w1 = __float2bfloat16_rn(w);
+    const float r1 = w - __bfloat162float(w1);
+    const __nv_bfloat16 w2 = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(w2);
+    W3[idx] = w1;
+    W3[n + idx] = w2;
+    W3[2 * n + idx] = __float2bfloat16_rn(r2);
+  }
+}
+
+// One warp per token: logits = ordered sum of the split partials (+ bias), then
+// k rounds of warp argmax (ties -> lower expert), then gates.
+__global__ void __launch_bounds__(256)
+    router_topk_kernel(const float* __restrict__ part, int n_split, int ld,
+                       const float* __restrict__ bias, float* __restrict__ logits_out,
+                       int32_t* __restrict__ topk_idx, float* __restrict__ topk_gate, int T, int E,
+                       int k, int gating) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= T) return;
-  const float* row = logits + static_cast<long long>(warp) * E;
   float v[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int e = lane + 32 * i;
-    v[i] = e < E ? row[e] : -INFINITY;
+    float l = -INFINITY;
+    if (e < E) {
+      l = part[static_cast<long long>(warp) * ld + e];
+      for (int s = 1; s < n_split; ++s)
+        l += part[(static_cast<long long>(s) * T + warp) * ld + e];
+      if (bias) l += bias[e];
+      if (logits_out) logits_out[static_cast<long long>(warp) * E + e] = l;
+    }
+    v[i] = l;
   }
   unsigned taken = 0;
   float sel_v[32];
@@ -188,13 +224,66 @@ cudaError_t launch_router_logits(int act_dtype, const void* x, const float* W_r,
                          stream);
 }
 
-cudaError_t launch_router_topk(const float* logits, int32_t* topk_idx, float* topk_gate, int T,
+cudaError_t launch_router_topk(const float* part, int n_split, int ld, const float* bias,
+                               float* logits_out, int32_t* topk_idx, float* topk_gate, int T,
                                int E, int k, int gating, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   const int warps_per_block = 8;
   router_topk_kernel<<<ceil_div(T, warps_per_block), 32 * warps_per_block, 0, stream>>>(
-      logits, topk_idx, topk_gate, T, E, k, gating);
+      part, n_split, ld, bias, logits_out, topk_idx, topk_gate, T, E, k, gating);
   return cudaGetLastError();
+}
+
+int router_n_pad(int E) { return ceil_div(E, 32) * 32; }
+
+// K splits: the largest divisor of the 3d/64 K blocks that keeps the tile count
+// (m-tiles x splits) within one wave of CTAs.
+int router_splits(int T, int d, int num_sms) {
+  const int kb = 3 * (d / kTcTileK);
+  const int mtiles = ceil_div(T, kMTile);
+  const int target = max(1, num_sms / max(1, mtiles));
+  int best = 1;
+  for (int s = 1; s <= min(kb, target); ++s)
+    if (kb % s == 0) best = s;
+  return best;
+}
+
+size_t router_scratch_bytes(int T, int d, int E, int num_sms) {
+  const size_t n_pad = router_n_pad(E);
+  const size_t w3 = (3 * n_pad * d * sizeof(__nv_bfloat16) + 255) & ~size_t(255);
+  const size_t part = static_cast<size_t>(router_splits(T, d, num_sms)) * T * n_pad * sizeof(float);
+  return w3 + part;
+}
+
+cudaError_t launch_router_tc(const void* x, const float* W_r, int T, int d, int E, int num_sms,
+                             void* scratch, const float** part_out, int* n_split, int* ld,
+                             unsigned* status, cudaStream_t stream) {
+  const int n_pad = router_n_pad(E);
+  const int splits = router_splits(T, d, num_sms);
+  __nv_bfloat16* W3 = static_cast<__nv_bfloat16*>(scratch);
+  float* part = reinterpret_cast<float*>(static_cast<char*>(scratch) +
+                                         ((3 * static_cast<size_t>(n_pad) * d * 2 + 255) & ~size_t(255)));
+  const long long n = static_cast<long long>(n_pad) * d;
+  const int split_blocks = static_cast<int>(n / 256 + 1 < 2048 ? n / 256 + 1 : 2048);
+  router_split_kernel<<<split_blocks, 256, 0, stream>>>(W_r, d, E, n_pad, W3);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  TcGemmArgs a = {};
+  a.n_ntiles = splits;
+  a.n_kblocks = 3 * (d / kTcTileK) / splits;
+  a.kb_per_slice = a.n_kblocks;
+  a.nt_per_slice = splits;
+  a.router_n = n_pad;
+  a.router_kbd = d / kTcTileK;
+  a.n_rows = T;
+  a.part = part;
+  a.status = status;
+  const int tiles = ceil_div(T, kMTile) * splits;
+  err = tc_gemm(kTcRouter, x, T, d, W3, 3, n_pad, d, a, min(num_sms, tiles), stream);
+  *part_out = part;
+  *n_split = splits;
+  *ld = n_pad;
+  return err;
 }
 
 }  // namespace moe

@@ -27,7 +27,8 @@ RESIDUAL = {"none": 0, "input": 1, "external": 2, "input_plus_external": 3}
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
           4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_DEVICE_INDEX"}
 
-EXPORTED = ("moe_status_string", "moe_adaptive_tau", "moe_get_device_status", "moe_route",
+EXPORTED = ("moe_status_string", "moe_adaptive_tau", "moe_get_device_status",
+            "moe_route_workspace_size", "moe_route",
             "moe_dispatch_workspace_size", "moe_dispatch", "moe_condense_workspace_size",
             "moe_condense", "moe_expert_ffn_workspace_size", "moe_expert_ffn", "moe_combine",
             "moe_workspace_size", "moe_layer_forward", "moe_dispatch_static_scratch")
@@ -70,7 +71,8 @@ def lib() -> ctypes.CDLL:
         "moe_status_string": (ctypes.c_char_p, [I]),
         "moe_adaptive_tau": (F, [F]),
         "moe_get_device_status": (I, [P]),
-        "moe_route": (I, [CFG, P, P, P, P, P, P, P]),
+        "moe_route_workspace_size": (S, [CFG]),
+        "moe_route": (I, [CFG, P, P, P, P, P, P, P, S, P]),
         "moe_dispatch_workspace_size": (S, [CFG]),
         "moe_dispatch": (I, [CFG, P, P, P, P, P, P, P, P, S, P]),
         "moe_condense_workspace_size": (S, [CFG]),
@@ -179,8 +181,11 @@ def route(cfg: Config, x, W_r, bias=None, stream=None):
     logits = _empty((cfg.T, cfg.E), torch.float32, dev)
     idx = _empty((cfg.T, cfg.k), torch.int32, dev)
     gate = _empty((cfg.T, cfg.k), torch.float32, dev)
-    _check(lib().moe_route(ctypes.byref(cfg.c()), _ptr(x), _ptr(W_r), _ptr(bias), _ptr(logits),
-                           _ptr(idx), _ptr(gate), _stream(stream)), "moe_route")
+    c = cfg.c()
+    n = lib().moe_route_workspace_size(ctypes.byref(c))
+    ws = _workspace(n, dev)
+    _check(lib().moe_route(ctypes.byref(c), _ptr(x), _ptr(W_r), _ptr(bias), _ptr(logits),
+                           _ptr(idx), _ptr(gate), _ptr(ws), n, _stream(stream)), "moe_route")
     return logits, idx, gate
 
 

@@ -61,17 +61,22 @@ def _cfg(L, **kw):
 ])
 def test_route_rejects_bad_configs(L, kw, code):
     c = _cfg(L, **kw)
-    r = L.lib().moe_route(ctypes.byref(c), FAKE, FAKE, None, FAKE, FAKE, FAKE, None)
+    r = L.lib().moe_route(ctypes.byref(c), FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, 1 << 40, None)
     assert r == code
 
 
 def test_route_rejects_null_and_misaligned(L):
     c = _cfg(L)
     lib = L.lib()
-    assert lib.moe_route(ctypes.byref(c), None, FAKE, None, FAKE, FAKE, FAKE, None) == 1
-    assert lib.moe_route(ctypes.byref(c), FAKE + 4, FAKE, None, FAKE, FAKE, FAKE, None) == 1
-    assert lib.moe_route(ctypes.byref(c), FAKE, FAKE, FAKE + 8, FAKE, FAKE, FAKE, None) == 1
-    assert lib.moe_route(None, FAKE, FAKE, None, FAKE, FAKE, FAKE, None) == 1
+    big = 1 << 40
+    assert lib.moe_route(ctypes.byref(c), None, FAKE, None, FAKE, FAKE, FAKE, FAKE, big, None) == 1
+    assert lib.moe_route(ctypes.byref(c), FAKE + 4, FAKE, None, FAKE, FAKE, FAKE, FAKE, big, None) == 1
+    assert lib.moe_route(ctypes.byref(c), FAKE, FAKE, FAKE + 8, FAKE, FAKE, FAKE, FAKE, big, None) == 1
+    assert lib.moe_route(None, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, big, None) == 1
+    need = lib.moe_route_workspace_size(ctypes.byref(c))
+    assert need > 0  # bf16 layers route on the tensor cores and need scratch
+    assert lib.moe_route(ctypes.byref(c), FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, need - 1, None) == 3
+    assert lib.moe_route_workspace_size(ctypes.byref(_cfg(L, dtype="f32"))) == 0
 
 
 def test_workspace_checks(L):
@@ -108,7 +113,7 @@ def test_workspace_checks(L):
 def test_zero_tokens_is_a_no_op(L):
     c = _cfg(L, T=0)
     lib = L.lib()
-    assert lib.moe_route(ctypes.byref(c), None, None, None, None, None, None, None) == 0
+    assert lib.moe_route(ctypes.byref(c), None, None, None, None, None, None, None, 0, None) == 0
     w = L.moe_weights(FAKE, None, FAKE, FAKE, None, None)
     assert lib.moe_layer_forward(ctypes.byref(c), ctypes.byref(w), None, None, float("nan"), None,
                                  None, None, None, 0, None) == 0
