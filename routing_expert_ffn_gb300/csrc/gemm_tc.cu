@@ -51,7 +51,7 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 512;
 constexpr int M_GROUP = 16;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align slack*/ + 256 /*barriers*/;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align slack*/ + 2048 /*barriers, tables*/;
 
 enum Mode { kSwiGLU = 0, kStore = 1, kSimBits = 2, kRouter = 3 };
 
@@ -63,6 +63,7 @@ struct Shared {
   uint64_t drain;
   uint32_t tmem_base;
   volatile int abort_flag;
+  int gmb[257];  // group_mt_begin, staged once per CTA (tile lookups stay in shared memory)
 };
 
 // Bounded mbarrier wait.  Returns false if the CTA is aborting or the limit passed.
@@ -92,7 +93,7 @@ struct TileInfo {
 };
 
 template <int MODE>
-__device__ __forceinline__ TileInfo tile_info(const TcGemmArgs& a, int tile) {
+__device__ __forceinline__ TileInfo tile_info(const TcGemmArgs& a, const int* gmb, int tile) {
   int mt, nt;
   if (MODE == kRouter) {
     // one group of T rows; tile = (m-tile, K split), K splits fastest
@@ -114,10 +115,10 @@ __device__ __forceinline__ TileInfo tile_info(const TcGemmArgs& a, int tile) {
     int lo = 0, hi = a.n_groups;  // largest g with begin[g] * NT <= tile
     while (hi - lo > 1) {
       int mid = (lo + hi) >> 1;
-      if (a.group_mt_begin[mid] * NT <= tile) lo = mid; else hi = mid;
+      if (gmb[mid] * NT <= tile) lo = mid; else hi = mid;
     }
-    const int beg = a.group_mt_begin[lo];
-    const int cnt = a.group_mt_begin[lo + 1] - beg;
+    const int beg = gmb[lo];
+    const int cnt = gmb[lo + 1] - beg;
     const int local = tile - beg * NT;
     const int blk = local / (M_GROUP * NT);
     const int within = local - blk * M_GROUP * NT;
@@ -189,6 +190,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::prefetch_tmap(&tmA);
     ptx::prefetch_tmap(&tmB);
   }
+  if (MODE == kSwiGLU || MODE == kStore) {
+    for (int g = threadIdx.x; g <= args.n_groups; g += blockDim.x)
+      sh->gmb[g] = args.group_mt_begin[g];
+  }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(&sh->tmem_base), TMEM_COLS);
     ptx::tmem_relinquish();
@@ -208,7 +213,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int s = 0; s < STAGES; ++s) issued[s] = 0, issued_phase[s] = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-      const TileInfo t = tile_info<MODE>(args, tile);
+      const TileInfo t = tile_info<MODE>(args, sh->gmb, tile);
       for (int kb = 0; kb < args.n_kblocks; ++kb) {
         if (!wait_bar(ptx::smem_u32(&sh->empty[stage]), phase ^ 1u, sh, args.status)) {
           ok = false;
@@ -324,7 +329,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t acc_phase = (local >> 1) & 1;
       if (!wait_bar(ptx::smem_u32(&sh->tmem_full[acc]), acc_phase, sh, args.status)) break;
       ptx::tc_fence_after();
-      const TileInfo t = tile_info<MODE>(args, tile);
+      const TileInfo t = tile_info<MODE>(args, sh->gmb, tile);
       const uint32_t col0 = lane_addr + acc * BN;
       const bool valid = r < t.nrows;
       if (MODE == kRouter) {
@@ -492,9 +497,10 @@ static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const TcGe
 }  // namespace tc
 
 cudaError_t tc_gemm(int mode, const void* A, long long a_rows, int K, const void* B,
-                    int b_slices, int b_rows, int b_cols, const TcGemmArgs& args, int grid,
+                    int b_slices, int b_rows, int b_cols, const TcGemmArgs& args_in, int grid,
                     cudaStream_t stream) {
   CUtensorMap ma, mb;
+  const TcGemmArgs& args = args_in;
   if (!tc::make_map(&ma, 2, A, K, a_rows, 1, tc::BM)) return cudaErrorInvalidValue;
   const uint32_t box_rows = mode == tc::kSwiGLU  ? tc::BN / 2
                             : mode == tc::kRouter ? static_cast<uint32_t>(args.router_n)
