@@ -73,4 +73,32 @@ __device__ __forceinline__ void store_vec_f32<__nv_bfloat16>(__nv_bfloat16* p, c
 
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Programmatic dependent launch.  Kernels of the layer are launched with
+// programmatic stream serialization: a kernel may be scheduled while the one
+// before it on the stream is finishing.  Each such kernel calls pdl_trigger()
+// early (its own dependent may then be scheduled once all of its blocks have
+// started) and pdl_wait() before its first global-memory access; pdl_wait
+// returns once the preceding grid has completed and its writes are visible.
+// Both are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 }  // namespace moe

@@ -8,9 +8,13 @@
 // single-GPU form of the Combine all-to-all plus the gated sum, the shared
 // expert and the residual base (Eq. 6 with its o_0 term, referee minor 1).
 //
-// Determinism: slot ranks come from per-chunk counts, an exclusive scan over
-// (expert, chunk), and an in-chunk ordered rank (warp match + popc), so the
-// permutation is the same on every run; the combine sums in a fixed order.
+// Two index paths give the same slots.  The one the ABI calls ranks pairs in
+// parallel blocks of 256 (warp match + popc, block prefix), scans the
+// (expert, block) counts in one CTA, and scatters rows pair by pair.  The
+// chunked path (per-chunk counts, scan over (expert, chunk), in-chunk ranks by
+// one warp, slot-driven row gather) serves the no-workspace entry point.  Ranks come from a
+// warp match + popc in pair order, so the permutation is the same on every
+// run; the combine sums in a fixed order.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -123,6 +127,214 @@ __global__ void __launch_bounds__(kScatterThreads)
   }
 }
 
+// Parallel stable ranks, three kernels:
+//   dispatch_local_kernel: block b takes pairs [1024 b, 1024 b + 1024); each
+//     pair's rank among the block's earlier pairs with the same expert (warp
+//     match + popc, then a prefix over the block's 32 warps), and the block's
+//     per-expert counts, stored expert-major in blk[e][b].
+//   dispatch_block_scan_kernel: exclusive prefix of blk in expert-major order
+//     (so expert e's slots start at offsets[e] and, inside e, block b's pairs
+//     follow blocks < b), plus counts and offsets.
+//   scatter_rows_kernel: slot = blk[e][b] + local rank; writes slot_of, perm and
+//     the row x_perm[slot] = x[token].
+constexpr int kLocalPairs = 1024;
+__global__ void __launch_bounds__(kLocalPairs)
+    dispatch_local_kernel(const int32_t* __restrict__ idx, int P, int E, int n_blk,
+                          int32_t* __restrict__ local_rank, int32_t* __restrict__ blk,
+                          unsigned* status) {
+  extern __shared__ int wh_flat[];  // [kLocalPairs / 32][E]
+  auto wh = [&](int w, int x) -> int& { return wh_flat[w * E + x]; };
+  pdl_trigger();
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < (kLocalPairs / 32) * E; i += blockDim.x) wh_flat[i] = 0;
+  __syncthreads();
+  const int p = blockIdx.x * kLocalPairs + threadIdx.x;
+  int e = -1;
+  if (p < P) {
+    e = idx[p];
+    if (e < 0 || e >= E) {
+      record_status(status, MOE_ERR_DEVICE_INDEX);
+      e = -1;
+    }
+  }
+  const unsigned peers = __match_any_sync(0xffffffffu, e);
+  const int r = __popc(peers & lanemask_lt());
+  if (e >= 0 && lane == __ffs(peers) - 1) wh(warp, e) = __popc(peers);
+  __syncthreads();
+  for (int x = threadIdx.x; x < E; x += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < kLocalPairs / 32; ++w) {
+      const int c = wh(w, x);
+      wh(w, x) = run;
+      run += c;
+    }
+    blk[static_cast<long long>(x) * n_blk + blockIdx.x] = run;
+  }
+  __syncthreads();
+  if (p < P) local_rank[p] = e >= 0 ? wh(warp, e) + r : -1;
+}
+
+// One CTA: blk <- exclusive prefix of blk (expert-major), counts, offsets.
+// The table goes through shared memory in coalesced pieces of kScanPiece
+// entries; each thread scans 8 consecutive entries of a piece.
+constexpr int kScanPiece = 8192;
+__global__ void __launch_bounds__(1024)
+    dispatch_block_scan_kernel(int32_t* __restrict__ blk, int E, int n_blk,
+                               int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
+  __shared__ int piece[kScanPiece];
+  __shared__ int warp_sum[32];
+  __shared__ int carry;
+  const long long N = static_cast<long long>(E) * n_blk;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  pdl_trigger();
+  pdl_wait();
+  if (threadIdx.x == 0) carry = 0;
+  for (long long base = 0; base < N; base += kScanPiece) {
+    const int n = static_cast<int>(min(static_cast<long long>(kScanPiece), N - base));
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) piece[i] = blk[base + i];
+    __syncthreads();
+    const int a = threadIdx.x * 8;
+    int v[8], mine = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      v[u] = a + u < n ? piece[a + u] : 0;
+      mine += v[u];
+    }
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const int w = warp_sum[lane];
+      int wi = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += y;
+      }
+      warp_sum[lane] = wi - w;
+    }
+    __syncthreads();
+    int run = carry + warp_sum[warp] + incl - mine;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (a + u < n) piece[a + u] = run;
+      run += v[u];
+    }
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) carry = run;  // the last thread's run is the total so far
+    for (int i = threadIdx.x; i < n; i += blockDim.x) blk[base + i] = piece[i];
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) offsets[e] = blk[static_cast<long long>(e) * n_blk];
+  if (threadIdx.x == 0) offsets[E] = carry;
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) counts[e] = offsets[e + 1] - offsets[e];
+}
+
+// Exclusive prefix of a[0..n) in shared memory by the whole CTA; returns the total.
+__device__ int block_scan_smem(int* a, int n, int* wsum /* 33 ints */) {
+  const int nt = blockDim.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int seg = (n + nt - 1) / nt;
+  const int lo = min(n, t * seg), hi = min(n, lo + seg);
+  int mine = 0;
+  for (int i = lo; i < hi; ++i) mine += a[i];
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int v = lane < (nt >> 5) ? wsum[lane] : 0;
+    int wi = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    wsum[lane] = wi - v;
+    if (lane == 31) wsum[32] = wi;
+  }
+  __syncthreads();
+  int run = wsum[warp] + incl - mine;
+  for (int i = lo; i < hi; ++i) {
+    const int c = a[i];
+    a[i] = run;
+    run += c;
+  }
+  __syncthreads();
+  return wsum[32];
+}
+
+// For every pair p: slot = base[e][p / kLocalPairs] + local_rank[p]; slot_of[p] = slot,
+// perm[slot] = p / k, x_perm[slot] = x[p / k].  One warp per pair, 16-byte
+// vectors.  A pair with an out-of-range expert gets slot_of -1 and no row.
+// SCAN: blk holds the raw (expert, block) counts; every CTA scans the table in
+// shared memory (it is small: E x ceil(P / 1024) entries) and CTA 0 writes
+// counts and offsets -- this replaces a separate scan launch.  Otherwise blk
+// is already the exclusive prefix.
+template <typename T, bool SCAN>
+__global__ void __launch_bounds__(256)
+    scatter_rows_kernel(const T* __restrict__ x, const int32_t* __restrict__ idx,
+                        const int32_t* __restrict__ local_rank, const int32_t* __restrict__ blk,
+                        int n_blk, int E, int P, int k, int d, T* __restrict__ x_perm,
+                        int32_t* __restrict__ perm, int32_t* __restrict__ slot_of,
+                        int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                        unsigned* status) {
+  constexpr int V = Act<T>::kVec;
+  const int nv = d / V;
+  extern __shared__ int tab[];
+  __shared__ int wsum[33];
+  pdl_trigger();
+  pdl_wait();
+  const int32_t* base_tab = blk;
+  if (SCAN) {
+    const int N = E * n_blk;
+    for (int i = threadIdx.x; i < N; i += blockDim.x) tab[i] = blk[i];
+    __syncthreads();
+    const int total = block_scan_smem(tab, N, wsum);
+    if (blockIdx.x == 0) {
+      for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int o = tab[e * n_blk];
+        offsets[e] = o;
+        counts[e] = (e + 1 < E ? tab[(e + 1) * n_blk] : total) - o;
+      }
+      if (threadIdx.x == 0) offsets[E] = total;
+    }
+    base_tab = tab;
+  }
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  for (int p = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; p < P; p += warps) {
+    const int e = idx[p];
+    const int lr = local_rank[p];
+    if (e < 0 || e >= E || lr < 0) {
+      if (lane == 0) slot_of[p] = -1;
+      continue;
+    }
+    const int s = base_tab[static_cast<long long>(e) * n_blk + p / kLocalPairs] + lr;
+    if (s >= P) {
+      if (lane == 0) record_status(status, MOE_ERR_DEVICE_INDEX);
+      continue;
+    }
+    if (lane == 0) slot_of[p] = s;
+    const int t = p / k;
+    if (lane == 0) perm[s] = t;
+    const uint4* a = reinterpret_cast<const uint4*>(x + static_cast<long long>(t) * d);
+    uint4* b = reinterpret_cast<uint4*>(x_perm + static_cast<long long>(s) * d);
+    for (int v = lane; v < nv; v += 32) b[v] = a[v];
+  }
+}
+
 // dst[r] = src[rows[r]] for r < *n_rows_dev; one warp per row, 16-byte vectors.
 template <typename T>
 __global__ void __launch_bounds__(256)
@@ -147,8 +359,10 @@ __global__ void __launch_bounds__(256)
 }
 
 // out[t] = r[t] + shared[t] + sum_j g[t,j] * y[rep(slot_of[t,j])], fp32 accumulate.
+// One CTA per token, one 16-byte vector per thread (blockDim = d / V), so every
+// load of a thread is issued before its single store.
 template <typename T>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(1024)
     combine_kernel(const T* __restrict__ y, const T* __restrict__ shared_out,
                    const int32_t* __restrict__ slot_of, const int32_t* __restrict__ rep_of,
                    const float* __restrict__ gate, const T* __restrict__ x,
@@ -158,6 +372,8 @@ __global__ void __launch_bounds__(128)
   __shared__ long long s_row[32];
   __shared__ float s_g[32];
   const int t = blockIdx.x;
+  pdl_trigger();
+  pdl_wait();
   if (threadIdx.x < k) {
     int s = slot_of[static_cast<long long>(t) * k + threadIdx.x];
     if (s >= 0 && s < P && rep_of) s = rep_of[s];
@@ -209,6 +425,8 @@ __global__ void __launch_bounds__(256)
   __shared__ int s_rows[256];
   __shared__ int s_off[257];
   __shared__ int s_mt[257];
+  pdl_trigger();
+  pdl_wait();
   for (int g = threadIdx.x; g < n_groups; g += blockDim.x)
     s_rows[g] = counts ? counts[g] : offsets_in ? offsets_in[g + 1] - offsets_in[g] : fixed_rows;
   __syncthreads();
@@ -263,6 +481,63 @@ cudaError_t launch_dispatch(int act_dtype, const void* x, const int32_t* topk_id
   return launch_gather_rows(act_dtype, x, T, perm, offsets + E, T * k, d, x_perm, status, stream);
 }
 
+size_t dispatch_auto_scratch_bytes(int T, int k, int E) {
+  const size_t P = static_cast<size_t>(T) * k;
+  const size_t n_blk = (P + kLocalPairs - 1) / kLocalPairs;
+  return ((P * sizeof(int32_t) + 255) & ~size_t(255)) + n_blk * E * sizeof(int32_t);
+}
+
+cudaError_t launch_dispatch_auto(int act_dtype, const void* x, const int32_t* topk_idx, int T,
+                                 int d, int E, int k, int32_t* counts, int32_t* offsets,
+                                 int32_t* perm, int32_t* slot_of, void* x_perm, void* scratch,
+                                 int num_sms, unsigned* status, cudaStream_t stream) {
+  const long long P = static_cast<long long>(T) * k;
+  if (P == 0)
+    return launch_dispatch(act_dtype, x, topk_idx, T, d, E, k, counts, offsets, perm, slot_of,
+                           x_perm, scratch, status, stream);
+  const int n_blk = static_cast<int>((P + kLocalPairs - 1) / kLocalPairs);
+  int32_t* local_rank = static_cast<int32_t*>(scratch);
+  int32_t* blk = reinterpret_cast<int32_t*>(static_cast<char*>(scratch) +
+                                            ((P * sizeof(int32_t) + 255) & ~size_t(255)));
+  cudaError_t err = launch_pdl(dispatch_local_kernel, dim3(n_blk), dim3(kLocalPairs),
+                               sizeof(int) * (kLocalPairs / 32) * E, stream, topk_idx,
+                               static_cast<int>(P), E, n_blk, local_rank, blk, status);
+  if (err != cudaSuccess) return err;
+  const long long table = static_cast<long long>(E) * n_blk;
+  const bool scan_in_smem = table <= 12288;  // 48 KB of shared memory per CTA
+  if (!scan_in_smem) {
+    err = launch_pdl(dispatch_block_scan_kernel, dim3(1), dim3(1024), 0, stream, blk, E, n_blk,
+                     counts, offsets);
+    if (err != cudaSuccess) return err;
+  }
+  const long long want = (P + 7) / 8;
+  const int blocks = static_cast<int>(want < 8ll * num_sms ? want : 8ll * num_sms);
+  const size_t smem = scan_in_smem ? sizeof(int) * table : 0;
+  const int Pi = static_cast<int>(P);
+  if (act_dtype == MOE_F32) {
+    const float* xf = static_cast<const float*>(x);
+    float* xp = static_cast<float*>(x_perm);
+    err = scan_in_smem ? launch_pdl(scatter_rows_kernel<float, true>, dim3(blocks), dim3(256), smem,
+                                    stream, xf, topk_idx, local_rank, blk, n_blk, E, Pi, k, d, xp,
+                                    perm, slot_of, counts, offsets, status)
+                       : launch_pdl(scatter_rows_kernel<float, false>, dim3(blocks), dim3(256), 0,
+                                    stream, xf, topk_idx, local_rank, blk, n_blk, E, Pi, k, d, xp,
+                                    perm, slot_of, counts, offsets, status);
+  } else {
+    const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+    __nv_bfloat16* xp = static_cast<__nv_bfloat16*>(x_perm);
+    err = scan_in_smem
+              ? launch_pdl(scatter_rows_kernel<__nv_bfloat16, true>, dim3(blocks), dim3(256), smem,
+                           stream, xb, topk_idx, local_rank, blk, n_blk, E, Pi, k, d, xp, perm,
+                           slot_of, counts, offsets, status)
+              : launch_pdl(scatter_rows_kernel<__nv_bfloat16, false>, dim3(blocks), dim3(256), 0,
+                           stream, xb, topk_idx, local_rank, blk, n_blk, E, Pi, k, d, xp, perm,
+                           slot_of, counts, offsets, status);
+  }
+  if (err != cudaSuccess) return err;
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gather_rows(int act_dtype, const void* src, int src_rows, const int32_t* rows,
                                const int* n_rows_dev, int max_rows, int d, void* dst,
                                unsigned* status, cudaStream_t stream) {
@@ -284,26 +559,27 @@ cudaError_t launch_combine(int act_dtype, const void* y_perm, const void* shared
                            const void* x, const void* residual, int residual_mode, void* out, int T,
                            int d, int k, int P, unsigned* status, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
+  const int vec = act_dtype == MOE_F32 ? 4 : 8;
+  const int threads = min(1024, max(32, ceil_div(d / vec, 32) * 32));
   if (act_dtype == MOE_F32)
-    combine_kernel<float><<<T, 128, 0, stream>>>(
-        static_cast<const float*>(y_perm), static_cast<const float*>(shared_out), slot_of, rep_of,
-        topk_gate, static_cast<const float*>(x), static_cast<const float*>(residual),
-        residual_mode, static_cast<float*>(out), d, k, P, status);
-  else
-    combine_kernel<__nv_bfloat16><<<T, 128, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(y_perm), static_cast<const __nv_bfloat16*>(shared_out),
-        slot_of, rep_of, topk_gate, static_cast<const __nv_bfloat16*>(x),
-        static_cast<const __nv_bfloat16*>(residual), residual_mode,
-        static_cast<__nv_bfloat16*>(out), d, k, P, status);
-  return cudaGetLastError();
+    return launch_pdl(combine_kernel<float>, dim3(T), dim3(threads), 0, stream,
+                      static_cast<const float*>(y_perm), static_cast<const float*>(shared_out),
+                      slot_of, rep_of, topk_gate, static_cast<const float*>(x),
+                      static_cast<const float*>(residual), residual_mode,
+                      static_cast<float*>(out), d, k, P, status);
+  return launch_pdl(combine_kernel<__nv_bfloat16>, dim3(T), dim3(threads), 0, stream,
+                    static_cast<const __nv_bfloat16*>(y_perm),
+                    static_cast<const __nv_bfloat16*>(shared_out), slot_of, rep_of, topk_gate,
+                    static_cast<const __nv_bfloat16*>(x),
+                    static_cast<const __nv_bfloat16*>(residual), residual_mode,
+                    static_cast<__nv_bfloat16*>(out), d, k, P, status);
 }
 
 cudaError_t launch_build_mtiles(const int32_t* counts, const int32_t* offsets_in, int fixed_rows,
                                 int n_groups, int32_t* offsets_out, int4* mt_info,
                                 int32_t* group_mt_begin, cudaStream_t stream) {
-  build_mtiles_kernel<<<1, 256, 0, stream>>>(counts, offsets_in, fixed_rows, n_groups, offsets_out,
-                                             mt_info, group_mt_begin);
-  return cudaGetLastError();
+  return launch_pdl(build_mtiles_kernel, dim3(1), dim3(256), 0, stream, counts, offsets_in,
+                    fixed_rows, n_groups, offsets_out, mt_info, group_mt_begin);
 }
 
 }  // namespace moe

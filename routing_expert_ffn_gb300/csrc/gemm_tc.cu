@@ -190,6 +190,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::prefetch_tmap(&tmA);
     ptx::prefetch_tmap(&tmB);
   }
+  // Barrier set-up above and TMEM allocation below touch no global memory, so
+  // they overlap the previous kernel's tail; everything after waits for it.
+  pdl_wait();
   if (MODE == kSwiGLU || MODE == kStore) {
     for (int g = threadIdx.x; g <= args.n_groups; g += blockDim.x)
       sh->gmb[g] = args.group_mt_begin[g];
@@ -442,6 +445,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   }
 
+  // This CTA's work is done: the next kernel on the stream may be scheduled.
+  pdl_trigger();
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -490,8 +495,8 @@ static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const TcGe
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  grouped_gemm_kernel<MODE><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(a, b, args);
-  return cudaGetLastError();
+  return launch_pdl(grouped_gemm_kernel<MODE>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, stream, a,
+                    b, args);
 }
 
 }  // namespace tc

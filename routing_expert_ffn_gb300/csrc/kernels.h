@@ -33,6 +33,13 @@ cudaError_t launch_dispatch(int act_dtype, const void* x, const int32_t* topk_id
                             int E, int k, int32_t* counts, int32_t* offsets, int32_t* perm,
                             int32_t* slot_of, void* x_perm, void* scratch, unsigned* status,
                             cudaStream_t stream);
+// Same outputs as launch_dispatch, with ranks computed in parallel blocks of
+// 256 pairs; scratch: dispatch_auto_scratch_bytes.
+size_t dispatch_auto_scratch_bytes(int T, int k, int E);
+cudaError_t launch_dispatch_auto(int act_dtype, const void* x, const int32_t* topk_idx, int T,
+                                 int d, int E, int k, int32_t* counts, int32_t* offsets,
+                                 int32_t* perm, int32_t* slot_of, void* x_perm, void* scratch,
+                                 int num_sms, unsigned* status, cudaStream_t stream);
 // dst[r] = src[rows[r]] for r < *n_rows_dev (<= max_rows); rows outside [0, src_rows) are flagged.
 cudaError_t launch_gather_rows(int act_dtype, const void* src, int src_rows, const int32_t* rows,
                                const int* n_rows_dev, int max_rows, int d, void* dst,

@@ -295,7 +295,8 @@ size_t carve_layer(const moe_config* c, bool condense, void* ws, LayerScratch* s
   t.perm = cv.take<int32_t>(P);
   t.slot_of = cv.take<int32_t>(P);
   t.x_perm = cv.take<char>(static_cast<size_t>(P) * c->d * ab);
-  t.dispatch_ws = cv.take<char>(dispatch_scratch_bytes(c->T, c->E));
+  t.dispatch_ws = cv.take<char>(dispatch_auto_scratch_bytes(c->T, c->k, c->E) +
+                                dispatch_scratch_bytes(c->T, c->E));
   t.rep_of = cv.take<int32_t>(P);
   t.n_rep = cv.take<int32_t>(c->E);
   t.n_condensed = cv.take<int32_t>(1);
@@ -371,7 +372,9 @@ moe_status moe_route(const moe_config* cfg, const void* x, const float* W_r, con
 
 size_t moe_dispatch_workspace_size(const moe_config* cfg) {
   if (check_cfg(cfg) != MOE_OK) return 0;
-  return align256(dispatch_scratch_bytes(cfg->T, cfg->E));
+  const size_t a = dispatch_scratch_bytes(cfg->T, cfg->E);
+  const size_t b = dispatch_auto_scratch_bytes(cfg->T, cfg->k, cfg->E);
+  return align256(a > b ? a : b);
 }
 
 moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx,
@@ -394,8 +397,9 @@ moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* top
   DeviceInfo* di = device_info();
   if (!di) return MOE_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  MOE_CUDA(launch_dispatch(cfg->act_dtype, x, topk_idx, cfg->T, cfg->d, cfg->E, cfg->k, counts,
-                           offsets, perm, slot_of, x_perm, ws, di->status, st));
+  MOE_CUDA(launch_dispatch_auto(cfg->act_dtype, x, topk_idx, cfg->T, cfg->d, cfg->E, cfg->k,
+                                counts, offsets, perm, slot_of, x_perm, ws, di->num_sms,
+                                di->status, st));
   return MOE_OK;
 }
 
@@ -525,8 +529,9 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
   int32_t* idx = topk_idx_out ? topk_idx_out : L.topk_idx;
   s = run_router(cfg, x, w->W_r, w->router_bias, L.logits, idx, L.gate, L.route_ws, di, st);
   if (s != MOE_OK) return s;
-  MOE_CUDA(launch_dispatch(cfg->act_dtype, x, idx, cfg->T, cfg->d, cfg->E, cfg->k, L.counts,
-                           L.offsets, L.perm, L.slot_of, L.x_perm, L.dispatch_ws, di->status, st));
+  MOE_CUDA(launch_dispatch_auto(cfg->act_dtype, x, idx, cfg->T, cfg->d, cfg->E, cfg->k,
+                                L.counts, L.offsets, L.perm, L.slot_of, L.x_perm, L.dispatch_ws,
+                                di->num_sms, di->status, st));
   const int32_t* rep_of = nullptr;
   if (condense) {
     MOE_CUDA(launch_condense(static_cast<const __nv_bfloat16*>(L.x_perm), L.offsets,

@@ -108,6 +108,8 @@ __global__ void __launch_bounds__(kRThreads)
 __global__ void __launch_bounds__(256)
     router_split_kernel(const float* __restrict__ W_r, int d, int E, int n_pad,
                         __nv_bfloat16* __restrict__ W3) {
+  pdl_trigger();
+  pdl_wait();
   const long long n = static_cast<long long>(n_pad) * d;
   for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < n;
        idx += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -132,6 +134,8 @@ __global__ void __launch_bounds__(256)
                        int k, int gating) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
+  pdl_trigger();
+  pdl_wait();
   if (warp >= T) return;
   float v[8];
 #pragma unroll
@@ -229,9 +233,9 @@ cudaError_t launch_router_topk(const float* part, int n_split, int ld, const flo
                                int E, int k, int gating, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   const int warps_per_block = 8;
-  router_topk_kernel<<<ceil_div(T, warps_per_block), 32 * warps_per_block, 0, stream>>>(
-      part, n_split, ld, bias, logits_out, topk_idx, topk_gate, T, E, k, gating);
-  return cudaGetLastError();
+  return launch_pdl(router_topk_kernel, dim3(ceil_div(T, warps_per_block)),
+                    dim3(32 * warps_per_block), 0, stream, part, n_split, ld, bias, logits_out,
+                    topk_idx, topk_gate, T, E, k, gating);
 }
 
 int router_n_pad(int E) { return ceil_div(E, 32) * 32; }
@@ -265,8 +269,8 @@ cudaError_t launch_router_tc(const void* x, const float* W_r, int T, int d, int 
                                          ((3 * static_cast<size_t>(n_pad) * d * 2 + 255) & ~size_t(255)));
   const long long n = static_cast<long long>(n_pad) * d;
   const int split_blocks = static_cast<int>(n / 256 + 1 < 2048 ? n / 256 + 1 : 2048);
-  router_split_kernel<<<split_blocks, 256, 0, stream>>>(W_r, d, E, n_pad, W3);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_pdl(router_split_kernel, dim3(split_blocks), dim3(256), 0, stream, W_r,
+                               d, E, n_pad, W3);
   if (err != cudaSuccess) return err;
   TcGemmArgs a = {};
   a.n_ntiles = splits;
