@@ -160,6 +160,62 @@ __device__ bool rows_identical(const __nv_bfloat16* rows, int d, int i, int j) {
   return true;
 }
 
+// Epilogue of one FFN tile for one TMEM lane (output row r of the tile): the
+// SwiGLU tile writes h = SiLU(gate) * up, the store tile writes D, both bf16.
+template <int MODE>
+__device__ __forceinline__ void ffn_epilogue(const TcGemmArgs& args, const TileInfo& t,
+                                             uint32_t col0, int r, bool valid) {
+  if (MODE == kSwiGLU) {
+    __nv_bfloat16* orow = args.out + (static_cast<long long>(t.row0) + r) * args.ld_out +
+                          static_cast<long long>(t.nt) * (BN / 2);
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t g[32], u[32];
+      ptx::tmem_ld_32x32b_x32(col0 + c * 32, g);
+      ptx::tmem_ld_32x32b_x32(col0 + BN / 2 + c * 32, u);
+      ptx::tmem_ld_wait();
+      if (valid) {
+        uint32_t p[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float h0 = silu_f(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
+          const float h1 =
+              silu_f(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
+          p[i] = pack_bf16x2(h0, h1);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          dst[v] = make_uint4(p[4 * v], p[4 * v + 1], p[4 * v + 2], p[4 * v + 3]);
+      }
+    }
+  } else {
+    long long orow_idx = static_cast<long long>(t.row0) + r;
+    if (valid && args.out_rowmap) orow_idx = args.out_rowmap[orow_idx];
+    __nv_bfloat16* orow =
+        args.out + orow_idx * args.ld_out + static_cast<long long>(t.nt) * BN;
+#pragma unroll 1
+    for (int c = 0; c < 8; c += 2) {
+      uint32_t v0[32], v1[32];
+      ptx::tmem_ld_32x32b_x32(col0 + c * 32, v0);
+      ptx::tmem_ld_32x32b_x32(col0 + (c + 1) * 32, v1);
+      ptx::tmem_ld_wait();
+      if (valid) {
+        uint32_t p[32];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          p[i] = pack_bf16x2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
+          p[16 + i] = pack_bf16x2(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1]));
+        }
+        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+          dst[v] = make_uint4(p[4 * v], p[4 * v + 1], p[4 * v + 2], p[4 * v + 3]);
+      }
+    }
+  }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -351,54 +407,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                    __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
           }
         }
-      } else if (MODE == kSwiGLU) {
-        __nv_bfloat16* orow = args.out + (static_cast<long long>(t.row0) + r) * args.ld_out +
-                              static_cast<long long>(t.nt) * (BN / 2);
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t g[32], u[32];
-          ptx::tmem_ld_32x32b_x32(col0 + c * 32, g);
-          ptx::tmem_ld_32x32b_x32(col0 + BN / 2 + c * 32, u);
-          ptx::tmem_ld_wait();
-          if (valid) {
-            uint32_t p[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float h0 = silu_f(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
-              const float h1 =
-                  silu_f(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
-              p[i] = pack_bf16x2(h0, h1);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(p[4 * v], p[4 * v + 1], p[4 * v + 2], p[4 * v + 3]);
-          }
-        }
-      } else if (MODE == kStore) {
-        long long orow_idx = static_cast<long long>(t.row0) + r;
-        if (valid && args.out_rowmap) orow_idx = args.out_rowmap[orow_idx];
-        __nv_bfloat16* orow =
-            args.out + orow_idx * args.ld_out + static_cast<long long>(t.nt) * BN;
-#pragma unroll 1
-        for (int c = 0; c < 8; c += 2) {
-          uint32_t v0[32], v1[32];
-          ptx::tmem_ld_32x32b_x32(col0 + c * 32, v0);
-          ptx::tmem_ld_32x32b_x32(col0 + (c + 1) * 32, v1);
-          ptx::tmem_ld_wait();
-          if (valid) {
-            uint32_t p[32];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              p[i] = pack_bf16x2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
-              p[16 + i] = pack_bf16x2(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1]));
-            }
-            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-              dst[v] = make_uint4(p[4 * v], p[4 * v + 1], p[4 * v + 2], p[4 * v + 3]);
-          }
-        }
+      } else if (MODE == kSwiGLU || MODE == kStore) {
+        ffn_epilogue<MODE>(args, t, col0, r, valid);
       } else {
         // Gram tile of bucket `slice`: row slot i = row0 + r, column slot j = gbase + nt*256 + c.
         const int e = t.slice;
@@ -453,6 +463,278 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 1) ptx::tmem_dealloc(tmem_base, TMEM_COLS);
 }
 
+// ---------------------------------------------------------------- CTA-pair kernel
+// The FFN GEMMs on pairs of SMs (clusters of two CTAs, tcgen05 cta_group::2).
+// A pair tile is 256 rows x 256 columns: CTA r of the pair holds rows
+// [128 r, 128 r + 128) of A and the r-th 128-row half of the B tile (gate rows
+// then up rows for the SwiGLU tile), so a stage is 32 KB per SM instead of
+// 48 KB and six stages fit.  The even (leader) CTA issues M=256 x N=256 MMAs
+// that read both CTAs' shared memory and write each CTA's own TMEM rows; each
+// CTA runs its own epilogue exactly as the single-CTA kernel does.
+//   full[s]       leader only; both CTAs' TMA loads complete on it (64 KB)
+//   empty[s]      both CTAs; the leader's MMA commit arrives on both
+//   tmem_full[a]  both CTAs; the leader's commit arrives on both
+//   tmem_empty[a] leader only; 4 epilogue warps of each CTA arrive (8)
+// A pair tile is two consecutive m-tiles of one group; when the group has an
+// odd number of m-tiles, the peer's half of its last pair tile has no rows
+// (it still loads its B half, computes, and stores nothing).
+namespace pr {
+constexpr int STAGES = 6;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = (BN / 2) * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 3072;
+constexpr int PAIR_GROUP = M_GROUP / 2;
+
+struct Shared {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  volatile int abort_flag;
+  int gmb[257];  // first m-tile of each group
+  int gpb[257];  // first pair of each group
+};
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Shared* sh,
+                                         unsigned* status) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (sh->abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        sh->abort_flag = 1;
+        record_status(status, MOE_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// Pair tile -> this CTA's m-tile.  Groups are walked in order; inside a group,
+// blocks of PAIR_GROUP pairs, N tiles with the pairs fastest.
+__device__ __forceinline__ TileInfo tile_info(const TcGemmArgs& a, const Shared* sh, int tile,
+                                              uint32_t rank) {
+  const int NT = a.n_ntiles;
+  int lo = 0, hi = a.n_groups;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (sh->gpb[mid] * NT <= tile) lo = mid; else hi = mid;
+  }
+  const int beg = sh->gpb[lo], cnt = sh->gpb[lo + 1] - beg;
+  const int local = tile - beg * NT;
+  const int blk = local / (PAIR_GROUP * NT);
+  const int within = local - blk * PAIR_GROUP * NT;
+  const int bs = min(PAIR_GROUP, cnt - blk * PAIR_GROUP);
+  const int nt = within / bs;
+  const int pi = blk * PAIR_GROUP + (within - nt * bs);
+  const int m_in_group = 2 * pi + static_cast<int>(rank);
+  TileInfo t;
+  t.nt = nt;
+  if (m_in_group < sh->gmb[lo + 1] - sh->gmb[lo]) {
+    const int4 m = a.mt_info[sh->gmb[lo] + m_in_group];
+    t.slice = m.x;
+    t.row0 = m.y;
+    t.nrows = m.z;
+    t.gbase = m.w;
+  } else {
+    const int4 m = a.mt_info[sh->gmb[lo] + 2 * pi];  // the leader's m-tile
+    t.slice = m.x;
+    t.row0 = m.y + BM;
+    t.nrows = 0;
+    t.gbase = m.w;
+  }
+  return t;
+}
+
+// This CTA's loads of K block kb: its A rows and its half of B, completing on
+// the leader's barrier `full`.
+template <int MODE>
+__device__ __forceinline__ void issue_kblock(const TcGemmArgs& args, const CUtensorMap* tmA,
+                                             const CUtensorMap* tmB, const TileInfo& t, int kb,
+                                             uint32_t rank, uint32_t full, uint32_t sa,
+                                             uint32_t sb) {
+  const int kslice = kb / args.kb_per_slice;
+  const int kin = (kb - kslice * args.kb_per_slice) * BK;
+  const int nslice = t.nt / args.nt_per_slice;
+  const int z = t.slice + nslice + kslice;
+  ptx::tma_load_2d_pair(sa, tmA, full, kb * BK, t.row0);
+  if (MODE == kSwiGLU) {
+    const int n0 = (t.nt - nslice * args.nt_per_slice) * (BN / 2);
+    ptx::tma_load_3d_pair(sb, tmB, full, kin, (rank ? args.b_up_offset : 0) + n0, z);
+  } else {
+    const int n0 = (t.nt - nslice * args.nt_per_slice) * BN + static_cast<int>(rank) * (BN / 2);
+    ptx::tma_load_3d_pair(sb, tmB, full, kin, n0, z);
+  }
+}
+}  // namespace pr
+
+template <int MODE>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                             const __grid_constant__ CUtensorMap tmB, const TcGemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  pr::Shared* sh = reinterpret_cast<pr::Shared*>(smem + pr::STAGES * pr::STAGE_BYTES);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const uint32_t smem0 = ptx::smem_u32(smem);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < pr::STAGES; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&sh->full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&sh->empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(ptx::smem_u32(&sh->tmem_full[a]), 1);
+      ptx::mbar_init(ptx::smem_u32(&sh->tmem_empty[a]), 8);
+    }
+    ptx::mbar_init(ptx::smem_u32(&sh->drain), 1);
+    sh->abort_flag = 0;
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(ptx::smem_u32(&sh->tmem_base), TMEM_COLS);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  ptx::cluster_sync();  // both CTAs' barriers and the pair's TMEM exist from here on
+  ptx::tc_fence_after();
+  pdl_wait();
+  for (int g = threadIdx.x; g <= args.n_groups; g += blockDim.x) sh->gmb[g] = args.group_mt_begin[g];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int g = 0; g < args.n_groups; ++g) {
+      sh->gpb[g] = run;
+      run += (sh->gmb[g + 1] - sh->gmb[g] + 1) >> 1;
+    }
+    sh->gpb[args.n_groups] = run;
+  }
+  __syncthreads();
+  const uint32_t tmem_base = sh->tmem_base;
+  const int n_tiles = sh->gpb[args.n_groups] * args.n_ntiles;
+  const int cluster = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int tile = cluster; tile < n_tiles && ok; tile += n_clusters) {
+      const TileInfo t = pr::tile_info(args, sh, tile, rank);
+      for (int kb = 0; kb < args.n_kblocks; ++kb) {
+        if (!pr::wait_bar(ptx::smem_u32(&sh->empty[stage]), phase ^ 1u, sh, args.status)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t full = ptx::smem_u32(&sh->full[stage]) & ptx::kLeaderMask;
+          const uint32_t sa = smem0 + stage * pr::STAGE_BYTES;
+          if (rank == 0) ptx::mbar_arrive_expect_tx(full, 2 * pr::STAGE_BYTES);
+          pr::issue_kblock<MODE>(args, &tmA, &tmB, t, kb, rank, full, sa, sa + pr::A_BYTES);
+        }
+        __syncwarp();
+        if (++stage == pr::STAGES) stage = 0, phase ^= 1u;
+      }
+    }
+    if (!ok) {
+      // give loads already issued time to land (microseconds) before the pair exits
+      const uint64_t t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 200000ull) {
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (leader only)
+    if (rank == 0) {
+      const uint32_t idesc = ptx::idesc_bf16_f32(2 * BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true;
+      for (int tile = cluster; tile < n_tiles && ok; tile += n_clusters, ++local) {
+        const int acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        if (!pr::wait_bar(ptx::smem_u32(&sh->tmem_empty[acc]), acc_phase ^ 1u, sh, args.status)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < args.n_kblocks; ++kb) {
+          if (!pr::wait_bar(ptx::smem_u32(&sh->full[stage]), phase, sh, args.status)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          if (lane == 0) {
+            const uint32_t sa = smem0 + stage * pr::STAGE_BYTES;
+            const uint64_t adesc = ptx::sw128_kmajor_desc(sa);
+            const uint64_t bdesc = ptx::sw128_kmajor_desc(sa + pr::A_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              ptx::umma_bf16_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc,
+                                  (kb > 0 || kk > 0) ? 1u : 0u);
+            ptx::umma_commit_pair(ptx::smem_u32(&sh->empty[stage]), 0x3);
+          }
+          __syncwarp();
+          if (++stage == pr::STAGES) stage = 0, phase ^= 1u;
+        }
+        if (!ok) break;
+        if (lane == 0) ptx::umma_commit_pair(ptx::smem_u32(&sh->tmem_full[acc]), 0x3);
+        __syncwarp();
+      }
+      if (!ok) {
+        if (lane == 0) ptx::umma_commit_pair_local(ptx::smem_u32(&sh->drain));
+        __syncwarp();
+        const uint64_t t0 = globaltimer_ns();
+        while (!ptx::mbar_try_wait(ptx::smem_u32(&sh->drain), 0) &&
+               globaltimer_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5, both CTAs)
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    int local = 0;
+    for (int tile = cluster; tile < n_tiles; tile += n_clusters, ++local) {
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      if (!pr::wait_bar(ptx::smem_u32(&sh->tmem_full[acc]), acc_phase, sh, args.status)) break;
+      ptx::tc_fence_after();
+      const TileInfo t = pr::tile_info(args, sh, tile, rank);
+      ffn_epilogue<MODE>(args, t, lane_addr + acc * BN, r, r < t.nrows);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        const uint32_t e = ptx::smem_u32(&sh->tmem_empty[acc]);
+        if (rank == 0) ptx::mbar_arrive(e);
+        else ptx::mbar_arrive_cluster(ptx::mapa(e, 0));
+      }
+    }
+  }
+
+  pdl_trigger();
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();  // the leader's MMAs into this CTA's TMEM and all remote arrivals are done
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
+}
+
 // ---------------------------------------------------------------- host side
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -484,6 +766,56 @@ static bool make_map(CUtensorMap* m, int rank, const void* base, uint64_t inner,
 }
 
 template <int MODE>
+static cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const TcGemmArgs& args,
+                               int num_sms, cudaStream_t stream) {
+  static bool attr_set[64] = {};
+  static int max_clusters[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaLaunchConfig_t cfg = {};
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         pr::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    // Pairs of SMs that can hold a cluster at once: the persistent grid uses no more.
+    cudaLaunchAttribute ca;
+    ca.id = cudaLaunchAttributeClusterDimension;
+    ca.val.clusterDim.x = 2;
+    ca.val.clusterDim.y = 1;
+    ca.val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * (num_sms / 2));
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = pr::SMEM_BYTES;
+    cfg.attrs = &ca;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<MODE>, &cfg) != cudaSuccess ||
+        n <= 0)
+      n = num_sms / 2;
+    max_clusters[dev] = n;
+    attr_set[dev] = true;
+  }
+  const int clusters = dev < 64 ? (max_clusters[dev] < num_sms / 2 ? max_clusters[dev] : num_sms / 2)
+                                : num_sms / 2;
+  cfg = cudaLaunchConfig_t{};
+  cfg.gridDim = dim3(2 * clusters);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = pr::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = 2;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<MODE>, a, b, args);
+}
+
+template <int MODE>
 static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const TcGemmArgs& args,
                           int grid, cudaStream_t stream) {
   static bool attr_set[64] = {};
@@ -507,13 +839,15 @@ cudaError_t tc_gemm(int mode, const void* A, long long a_rows, int K, const void
   CUtensorMap ma, mb;
   const TcGemmArgs& args = args_in;
   if (!tc::make_map(&ma, 2, A, K, a_rows, 1, tc::BM)) return cudaErrorInvalidValue;
-  const uint32_t box_rows = mode == tc::kSwiGLU  ? tc::BN / 2
+  // The FFN modes run on CTA pairs, each CTA loading half of the 256-row B tile.
+  const bool pair = mode == tc::kSwiGLU || mode == tc::kStore;
+  const uint32_t box_rows = pair                  ? tc::BN / 2
                             : mode == tc::kRouter ? static_cast<uint32_t>(args.router_n)
                                                   : tc::BN;
   if (!tc::make_map(&mb, 3, B, b_cols, b_rows, b_slices, box_rows)) return cudaErrorInvalidValue;
   switch (mode) {
-    case tc::kSwiGLU: return tc::launch<tc::kSwiGLU>(ma, mb, args, grid, stream);
-    case tc::kStore: return tc::launch<tc::kStore>(ma, mb, args, grid, stream);
+    case tc::kSwiGLU: return tc::launch_pair<tc::kSwiGLU>(ma, mb, args, grid, stream);
+    case tc::kStore: return tc::launch_pair<tc::kStore>(ma, mb, args, grid, stream);
     case tc::kSimBits: return tc::launch<tc::kSimBits>(ma, mb, args, grid, stream);
     case tc::kRouter: return tc::launch<tc::kRouter>(ma, mb, args, grid, stream);
   }
