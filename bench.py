@@ -34,6 +34,10 @@ if ROOT not in sys.path:
 
 METRIC = "MoE-layer tokens/s on 1 GB300; expert-GEMM % of BF16 peak; dispatch GB/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# DRAM bytes (read + write) of the four grouped-GEMM launches of one moe_expert_ffn call,
+# from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the current kernel
+# on that workload; workloads without a capture report null.
+GEMM_DRAM_BYTES = {"dsv2_lite": 1496.4e6}
 
 
 def load_peaks() -> tuple[dict, str]:
@@ -261,7 +265,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         "roofline": {"bound": "tensor", "kernel": "grouped expert GEMM (moe_expert_ffn)",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_source": f"{peak_src} bf16 burst",
-                     "traffic": None},
+                     "traffic": GEMM_DRAM_BYTES.get(cfg.name)},
         "dispatch": {"GB/s": disp_gbs, "frac_of_hbm": disp_gbs / hbm,
                      "bytes": wk["dispatch_bytes"]},
         "combine": {"GB/s": comb_gbs, "frac_of_hbm": comb_gbs / hbm, "bytes": wk["combine_bytes"]},
