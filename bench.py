@@ -37,7 +37,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of the four grouped-GEMM launches of one moe_expert_ffn call,
 # from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the current kernel
 # on that workload; workloads without a capture report null.
-GEMM_DRAM_BYTES = {"dsv2_lite": 1496.4e6}
+GEMM_DRAM_BYTES = {"dsv2_lite": 1496.8e6}
 
 
 def load_peaks() -> tuple[dict, str]:
@@ -422,7 +422,12 @@ def _as_f64(inp):
 
 
 def cpu_baseline(cfg, inp, target_s: float = 12.0) -> dict:
-    """The oracle as it stands on this host's cores, on a prefix of the workload's tokens."""
+    """The oracle as it stands on this host's cores, on the workload's tokens.
+
+    A 128-token prefix first; if that is quick, a longer prefix (up to the whole
+    batch) and, if the whole batch is still quick, repeated whole-batch calls,
+    until about target_s seconds of host work have been timed.
+    """
     from oracle import moe_oracle as orc
     inp64 = _as_f64(inp)
     T_s = min(cfg.T, 128)
@@ -431,12 +436,17 @@ def cpu_baseline(cfg, inp, target_s: float = 12.0) -> dict:
     dt = time.perf_counter() - t0
     if dt < target_s / 3 and T_s < cfg.T:
         T_s = min(cfg.T, max(T_s, int(T_s * target_s / max(dt, 1e-3))))
-        t0 = time.perf_counter()
+    reps, tokens, t0 = 0, 0, time.perf_counter()
+    while True:
         _oracle_call(orc, cfg, inp64, T_s)
+        reps += 1
+        tokens += T_s
         dt = time.perf_counter() - t0
-    return {"value": T_s / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"first {T_s} of {cfg.T} tokens as one fp64 layer call ({dt:.1f} s); "
-                      "weights pre-cast to float64"}
+        if dt >= target_s or reps >= 50:
+            break
+    return {"value": tokens / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{reps} fp64 layer call(s) on the first {T_s} of {cfg.T} tokens "
+                      f"({dt:.1f} s); weights pre-cast to float64"}
 
 
 def run_reference(args, rank: int) -> None:
