@@ -148,6 +148,21 @@ def launches_per_step(cfg, condense: bool) -> int:
     return n
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest value over all ranks (the slowest replica's step time)."""
+    if world <= 1:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput: every replica's tokens over the slowest replica's time."""
+    return world * tokens_per_rank / (max_ms / 1e3)
+
+
 def capture(torch, fn):
     """CUDA graph of fn() (fn launches on torch's current stream); fn runs once first."""
     side = torch.cuda.Stream()
@@ -216,11 +231,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     clocks = sampler.stop()
     barrier()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    ms = sum(step_ms) / len(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(sum(step_ms) / len(step_ms), world, dev)
 
     # per-phase breakdown (FarSkip Eq. 9 terms): the same step as separate ABI calls
     phases = phase_breakdown(args, moe, C, w, x, r, tau, flush, stream, torch)
@@ -244,7 +255,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     comb_gbs = wk["combine_bytes"] / (phases["T_combine_ms"] / 1e3) / 1e9
     line = {
         "metric": METRIC,
-        "value": world * C.T / (ms / 1e3),
+        "value": job_tokens_per_s(C.T, world, ms),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -486,7 +497,7 @@ def main() -> None:
     ap.add_argument("--workload", default="dsv2_lite")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--reference-tokens", type=int, default=96)
+    ap.add_argument("--reference-tokens", type=int, default=1024)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
