@@ -34,7 +34,7 @@ cudaError_t launch_dispatch(int act_dtype, const void* x, const int32_t* topk_id
                             int32_t* slot_of, void* x_perm, void* scratch, unsigned* status,
                             cudaStream_t stream);
 // Same outputs as launch_dispatch, with ranks computed in parallel blocks of
-// 256 pairs; scratch: dispatch_auto_scratch_bytes.
+// 1024 pairs; scratch: dispatch_auto_scratch_bytes.
 size_t dispatch_auto_scratch_bytes(int T, int k, int E);
 cudaError_t launch_dispatch_auto(int act_dtype, const void* x, const int32_t* topk_idx, int T,
                                  int d, int E, int k, int32_t* counts, int32_t* offsets,
