@@ -3,9 +3,10 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
-A step is one moe_layer_forward call (router -> dispatch -> [condensation] ->
-expert FFN -> combine) over one batch of T synthetic tokens already resident
-in HBM.  Default workload: the DeepSeek-V2-Lite-shaped bf16 layer (T=4096,
+A step is one moe_layer_forward_ex call (router -> dispatch -> [condensation] ->
+routed experts -> combine, with the shared experts on a second stream beside
+dispatch and the routed experts) over one batch of T synthetic tokens already
+resident in HBM; the single-stream moe_layer_forward is timed beside it.  Default workload: the DeepSeek-V2-Lite-shaped bf16 layer (T=4096,
 d=2048, 64 experts top-6, hidden 1408, 2 shared experts).  Inputs and weights
 are seeded synthetic draws (routing_expert_ffn_gb300.inputs); the weights
 (1.1 GB) exceed L2 and L2 is additionally flushed (a 256 MB write) between
@@ -207,7 +208,30 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
 
     # One layer call is captured once as a CUDA graph and replayed every step, so
     # the timed region holds device work only (no per-kernel host launch cost).
-    graph = capture(torch, lambda: layer(x, r, tau, out=out, n_condensed_out=ncond))
+    # The step is moe_layer_forward_ex: with shared experts they run on a second
+    # stream after the router, beside dispatch and the routed experts (FarSkip's
+    # overlap of the routing-independent work); under FarSkip wiring (an external
+    # residual stream) the partial activation r + shared is written as well.
+    # (a higher-priority second stream measured best: its GEMM tiles get SMs first
+    # as the dispatch kernels retire)
+    aux = torch.cuda.Stream(priority=-1) if C.n_shared > 0 else None
+    part = torch.empty_like(out) if C.residual in ("external", "input_plus_external") else None
+
+    def layer_step():
+        layer(x, r, tau, out=out, n_condensed_out=ncond, partial_out=part, aux_stream=aux)
+
+    def timed(g) -> float:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            evs[i][0].record(stream)
+            g.replay()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in evs) / args.steps
+
+    graph = capture(torch, layer_step)
     for _ in range(args.warmup):
         graph.replay()
     torch.cuda.synchronize()
@@ -217,21 +241,22 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     n_condensed = int(ncond.item())
 
     sampler = ClockSampler(local_rank)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
     sampler.start()
-    for i in range(args.steps):
-        flush.zero_()
-        ev[i][0].record(stream)
-        graph.replay()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
+    ms = timed(graph)
     clocks = sampler.stop()
     barrier()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    ms = max_over_ranks(sum(step_ms) / len(step_ms), world, dev)
+    ms = max_over_ranks(ms, world, dev)
+
+    # For comparison: the same layer as one moe_layer_forward call on a single stream.
+    g_serial = capture(torch, lambda: layer(x, r, tau, out=out, n_condensed_out=ncond))
+    for _ in range(args.warmup):
+        g_serial.replay()
+    torch.cuda.synchronize()
+    ms_serial = max_over_ranks(timed(g_serial), world, dev)
+    serial = {"ms_per_step": ms_serial, "tokens_per_s": job_tokens_per_s(C.T, world, ms_serial),
+              "path": "moe_layer_forward, every kernel on one stream"}
 
     # per-phase breakdown (FarSkip Eq. 9 terms): the same step as separate ABI calls
     phases = phase_breakdown(args, moe, C, w, x, r, tau, flush, stream, torch)
@@ -247,7 +272,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         return
     peaks, peak_src = load_peaks()
     wk = work(C, n_condensed)
-    ffn_s = phases["T_routed_ms"] / 1e3
+    ffn_s = phases["T_experts_ms"] / 1e3
     achieved = wk["ffn_flops"] / ffn_s / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
@@ -270,7 +295,9 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
                                f"H={C.H} shared={C.n_shared}x{C.H_shared} residual={C.residual}"
                                + (f" tau={tau:.6f}" if condense else ""),
                    "tokens_per_gpu": C.T, "parallelism": f"replicas x{world}",
-                   "launch": "each step replays one CUDA graph of moe_layer_forward",
+                   "launch": "each step replays one CUDA graph of moe_layer_forward_ex"
+                  + (" (shared experts on a second stream)" if aux is not None else "")
+                  + (", partial activation written" if part is not None else ""),
                    "l2": "256 MB write between timed steps (outside the timed events); weights "
                          f"{(C.E * 3 * C.H + C.n_shared * 3 * C.H_shared) * C.d * 2 / 1e9:.2f} GB > L2"},
         "roofline": {"bound": "tensor", "kernel": "grouped expert GEMM (moe_expert_ffn)",
@@ -281,6 +308,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
                      "bytes": wk["dispatch_bytes"]},
         "combine": {"GB/s": comb_gbs, "frac_of_hbm": comb_gbs / hbm, "bytes": wk["combine_bytes"]},
         "phases_ms": phases,
+        "eq9": eq9_report(ms, phases),
+        "serial": serial,
         "condensed": n_condensed,
         "gpu_launches": launches_per_step(C, condense) * args.steps,
         "clocks": clocks,
@@ -355,35 +384,65 @@ def phase_breakdown(args, moe, C, w, x, r, tau, flush, stream, torch) -> dict:
                                  p(rep_of) if condense else None, p(gate), p(x), p(r), p(out), s),
                    "combine")
 
-    fns = [ph_route, ph_dispatch, ph_condense, ph_ffn, ph_combine]
+    # the routed experts alone (the same call with the shared experts switched off)
+    c_routed = C.c()
+    c_routed.n_shared = 0
+    nf_r = L.moe_expert_ffn_workspace_size(ctypes.byref(c_routed), int(condense))
+
+    def ph_routed_only():
+        s = cur()
+        moe._check(L.moe_expert_ffn(ctypes.byref(c_routed), ctypes.byref(wc), p(x_perm), p(offsets),
+                                    p(rep_of) if condense else None, p(x), p(y_perm), None,
+                                    p(ws_f), nf_r, s), "expert_ffn (routed only)")
+
+    fns = [ph_route, ph_dispatch, ph_condense, ph_ffn, ph_combine, ph_routed_only]
     graphs = [capture(torch, f) if (f is not ph_condense or condense) else None for f in fns]
 
     def step(evs):
         for i, g in enumerate(graphs):
-            evs[i].record(stream)
+            if i == len(graphs) - 1:
+                flush.zero_()  # the routed-only pass starts from a cold L2 as well
+            evs[2 * i].record(stream)
             if g is not None:
                 g.replay()
-        evs[5].record(stream)
+            evs[2 * i + 1].record(stream)
 
+    n_ev = 2 * len(graphs)
     for _ in range(max(1, args.warmup)):
-        step([torch.cuda.Event(enable_timing=True) for _ in range(6)])
+        step([torch.cuda.Event(enable_timing=True) for _ in range(n_ev)])
     torch.cuda.synchronize()
     all_evs = []
     for _ in range(args.steps):
         flush.zero_()
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
         step(evs)
         all_evs.append(evs)
     torch.cuda.synchronize()
-    names = ["T_gate_ms", "T_dispatch_ms", "T_condense_ms", "T_routed_ms", "T_combine_ms"]
+    names = ["T_gate_ms", "T_dispatch_ms", "T_condense_ms", "T_experts_ms", "T_combine_ms",
+             "T_routed_ms"]
     res = {n: 0.0 for n in names}
     for evs in all_evs:
         for i, n in enumerate(names):
-            res[n] += evs[i].elapsed_time(evs[i + 1]) / len(all_evs)
+            res[n] += evs[2 * i].elapsed_time(evs[2 * i + 1]) / len(all_evs)
+    res["T_shared_ms"] = max(0.0, res["T_experts_ms"] - res["T_routed_ms"])
     res["note"] = ("each phase is one ABI call captured as a CUDA graph and replayed in layer order; "
-                   "T_routed = moe_expert_ffn: routed + shared grouped GEMMs (tcgen05) and their "
-                   "m-tile table kernels")
+                   "T_experts = moe_expert_ffn (routed + shared grouped GEMMs on tcgen05 and their "
+                   "m-tile tables); T_routed = the same call without the shared experts; "
+                   "T_shared = their difference")
     return res
+
+
+def eq9_report(ms_layer: float, phases: dict) -> dict:
+    """FarSkip-Collective's overlap condition (review ledger, Section 4.1, Eq. 9): the
+    exchange steps fit in the window the layer leaves beside the routed experts and the
+    gate, T_Dispatch + T_Combine <= T_layer - T_routed - T_gate.  On one GPU the
+    exchange steps are the local dispatch permutation and the combine."""
+    window = ms_layer - phases["T_routed_ms"] - phases["T_gate_ms"]
+    comm = phases["T_dispatch_ms"] + phases["T_combine_ms"]
+    return {"T_layer_ms": ms_layer, "T_gate_ms": phases["T_gate_ms"],
+            "T_routed_ms": phases["T_routed_ms"], "T_dispatch_ms": phases["T_dispatch_ms"],
+            "T_combine_ms": phases["T_combine_ms"], "window_ms": window, "dispatch_plus_combine_ms": comm,
+            "holds": comm <= window}
 
 
 def end_to_end(args, C, graph, x, r, out, stream, torch) -> dict:

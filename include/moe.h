@@ -237,6 +237,30 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
                              int32_t* n_condensed_out, void* ws, size_t ws_bytes,
                              moe_stream_t stream);
 
+/* ---------------------------------------------------------------- whole layer, FarSkip overlap
+ * moe_layer_forward with the two pieces of FarSkip-Collective's single-device
+ * execution.  "Core claim": under FarSkip wiring the next attention sub-block
+ * reads a partial activation that holds the shared-expert output but not the
+ * routed experts.  Section 4 and Eq. 9: the work that does not depend on the
+ * routing runs on a second hardware queue beside the dispatch/routed/combine
+ * chain.
+ *   partial_out [T, d] act or NULL (out): p[t] = r[t] + sum_s shared_s(x)[t], the
+ *     combine's fp32 sum before the routed terms, rounded once (r per cfg->residual).
+ *     It must not alias an input or out.
+ *   aux_stream (may be NULL or equal to `stream`, then everything runs on
+ *     `stream`): with n_shared > 0 the shared experts run on aux_stream, after
+ *     the router and beside dispatch, condensation and the routed experts; the
+ *     combine on `stream` waits for them.  On return, all work of the call is
+ *     ordered before later work on `stream` (aux_stream holds none of it
+ *     afterwards).  Capturable in a CUDA graph that begins on `stream`.  The
+ *     fork/join events are created once per host thread and device.  Measured
+ *     on a GB300, an aux_stream of higher priority than `stream` overlaps best.
+ * Other arguments, workspace and errors: as moe_layer_forward.                  */
+moe_status moe_layer_forward_ex(const moe_config* cfg, const moe_weights* w, const void* x,
+                                const void* residual, float tau, void* out, void* partial_out,
+                                int32_t* topk_idx_out, int32_t* n_condensed_out, void* ws,
+                                size_t ws_bytes, moe_stream_t stream, moe_stream_t aux_stream);
+
 #ifdef __cplusplus
 } /* extern "C" */
 #endif

@@ -297,7 +297,12 @@ def layer_forward(x, W_r, bias, W_gu, W_down, Ws_gu, Ws_down, k, gating,
     ``tokens`` restricts the expert and combine work to a subset of tokens
     (routing, dispatch and condensation always run over all T tokens, since
     slots and representatives depend on every token).  Returns a dict with
-    logits, idx, gates, counts, offsets, perm, slot_of, rep_of, tokens, out.
+    logits, idx, gates, counts, offsets, perm, slot_of, rep_of, tokens, out,
+    partial.
+
+    ``partial`` = base + shared: FarSkip-Collective review, "Core claim" -- the
+    attention sub-block under FarSkip wiring reads a partial activation that
+    already holds the shared-expert output but none of the routed experts.
     """
     x = np.asarray(x)
     T = x.shape[0]
@@ -323,5 +328,6 @@ def layer_forward(x, W_r, bias, W_gu, W_down, Ws_gu, Ws_down, k, gating,
     shared = shared_experts(x[tok], Ws_gu, Ws_down) if len(Ws_gu) else None
     base = residual_base(x[tok], None if residual is None else residual[tok], residual_mode)
     out = combine(y_pairs, g[tok], base, shared)
+    partial = base + shared if shared is not None else base
     return dict(logits=logits, idx=idx, gates=g, counts=counts, offsets=offsets, perm=perm,
-                slot_of=slot_of, rep_of=rep_of, tokens=tok, out=out)
+                slot_of=slot_of, rep_of=rep_of, tokens=tok, out=out, partial=partial)

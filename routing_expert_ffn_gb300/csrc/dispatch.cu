@@ -359,6 +359,8 @@ __global__ void __launch_bounds__(256)
 }
 
 // out[t] = r[t] + shared[t] + sum_j g[t,j] * y[rep(slot_of[t,j])], fp32 accumulate.
+// partial (nullable): p[t] = r[t] + shared[t], the same fp32 sum before the
+// routed terms, rounded once.
 // One CTA per token, one 16-byte vector per thread (blockDim = d / V), so every
 // load of a thread is issued before its single store.
 template <typename T>
@@ -366,8 +368,8 @@ __global__ void __launch_bounds__(1024)
     combine_kernel(const T* __restrict__ y, const T* __restrict__ shared_out,
                    const int32_t* __restrict__ slot_of, const int32_t* __restrict__ rep_of,
                    const float* __restrict__ gate, const T* __restrict__ x,
-                   const T* residual, int residual_mode, T* out, int d, int k, int P,
-                   unsigned* status) {
+                   const T* residual, int residual_mode, T* out, T* __restrict__ partial, int d,
+                   int k, int P, unsigned* status) {
   constexpr int V = Act<T>::kVec;
   __shared__ long long s_row[32];
   __shared__ float s_g[32];
@@ -405,6 +407,7 @@ __global__ void __launch_bounds__(1024)
 #pragma unroll
       for (int i = 0; i < V; ++i) acc[i] += tmp[i];
     }
+    if (partial) store_vec_f32<T>(partial + rowoff + v * V, acc);
     for (int j = 0; j < k; ++j) {
       const long long s = s_row[j];
       if (s < 0) continue;
@@ -557,7 +560,8 @@ cudaError_t launch_gather_rows(int act_dtype, const void* src, int src_rows, con
 cudaError_t launch_combine(int act_dtype, const void* y_perm, const void* shared_out,
                            const int32_t* slot_of, const int32_t* rep_of, const float* topk_gate,
                            const void* x, const void* residual, int residual_mode, void* out, int T,
-                           int d, int k, int P, unsigned* status, cudaStream_t stream) {
+                           int d, int k, int P, unsigned* status, cudaStream_t stream,
+                           void* partial) {
   if (T == 0) return cudaSuccess;
   const int vec = act_dtype == MOE_F32 ? 4 : 8;
   const int threads = min(1024, max(32, ceil_div(d / vec, 32) * 32));
@@ -566,13 +570,14 @@ cudaError_t launch_combine(int act_dtype, const void* y_perm, const void* shared
                       static_cast<const float*>(y_perm), static_cast<const float*>(shared_out),
                       slot_of, rep_of, topk_gate, static_cast<const float*>(x),
                       static_cast<const float*>(residual), residual_mode,
-                      static_cast<float*>(out), d, k, P, status);
+                      static_cast<float*>(out), static_cast<float*>(partial), d, k, P, status);
   return launch_pdl(combine_kernel<__nv_bfloat16>, dim3(T), dim3(threads), 0, stream,
                     static_cast<const __nv_bfloat16*>(y_perm),
                     static_cast<const __nv_bfloat16*>(shared_out), slot_of, rep_of, topk_gate,
                     static_cast<const __nv_bfloat16*>(x),
                     static_cast<const __nv_bfloat16*>(residual), residual_mode,
-                    static_cast<__nv_bfloat16*>(out), d, k, P, status);
+                    static_cast<__nv_bfloat16*>(out), static_cast<__nv_bfloat16*>(partial), d, k,
+                    P, status);
 }
 
 cudaError_t launch_build_mtiles(const int32_t* counts, const int32_t* offsets_in, int fixed_rows,

@@ -44,10 +44,12 @@ cudaError_t launch_dispatch_auto(int act_dtype, const void* x, const int32_t* to
 cudaError_t launch_gather_rows(int act_dtype, const void* src, int src_rows, const int32_t* rows,
                                const int* n_rows_dev, int max_rows, int d, void* dst,
                                unsigned* status, cudaStream_t stream);
+// partial (nullable): also writes p = r + shared_out, the sum before the routed terms.
 cudaError_t launch_combine(int act_dtype, const void* y_perm, const void* shared_out,
                            const int32_t* slot_of, const int32_t* rep_of, const float* topk_gate,
                            const void* x, const void* residual, int residual_mode, void* out, int T,
-                           int d, int k, int P, unsigned* status, cudaStream_t stream);
+                           int d, int k, int P, unsigned* status, cudaStream_t stream,
+                           void* partial = nullptr);
 
 // ------------------------------------------------------------------ m-tile tables
 // Groups of rows (experts, buckets, or one group of fixed_rows rows when counts

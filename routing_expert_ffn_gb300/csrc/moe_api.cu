@@ -123,14 +123,12 @@ size_t carve_ffn(const moe_config* c, bool condense, void* ws, FfnScratch* s) {
   return cv.off;
 }
 
-moe_status run_expert_ffn(const moe_config* c, const moe_weights* w, const void* x_perm,
-                          const int32_t* offsets, const int32_t* rep_of, const void* x,
-                          void* y_perm, void* shared_out, const FfnScratch& s, DeviceInfo* di,
-                          cudaStream_t st) {
-  const int T = c->T, d = c->d, E = c->E, H = c->H, S = c->n_shared, Hs = c->H_shared;
+// Routed experts: m-tile tables, gate/up + SwiGLU, down projection.
+moe_status run_routed_ffn(const moe_config* c, const moe_weights* w, const void* x_perm,
+                          const int32_t* offsets, const int32_t* rep_of, void* y_perm,
+                          const FfnScratch& s, DeviceInfo* di, cudaStream_t st) {
+  const int T = c->T, d = c->d, E = c->E, H = c->H;
   const long long P = static_cast<long long>(T) * c->k;
-  if (T == 0) return MOE_OK;
-  const bool bf16 = c->act_dtype == MOE_BF16;
   // Rows the routed experts run on: every slot, or the representatives only.
   const void* A1 = x_perm;
   const int32_t* rowmap = nullptr;
@@ -146,14 +144,10 @@ moe_status run_expert_ffn(const moe_config* c, const moe_weights* w, const void*
   } else {
     MOE_CUDA(launch_build_mtiles(nullptr, offsets, 0, E, nullptr, s.mt_routed, s.gmb_routed, st));
   }
-  if (S > 0) MOE_CUDA(launch_build_mtiles(nullptr, nullptr, T, 1, nullptr, s.mt_shared, s.gmb_shared, st));
-  const int mt_routed_max = max_mtiles(P, E);
-  const int mt_shared_max = max_mtiles(T, 1);
-
-  if (bf16) {
+  if (c->act_dtype == MOE_BF16) {
     TcGemmArgs a = {};
     a.status = di->status;
-    // routed gate/up + SwiGLU
+    // gate/up + SwiGLU
     a.mt_info = s.mt_routed;
     a.group_mt_begin = s.gmb_routed;
     a.n_groups = E;
@@ -165,7 +159,7 @@ moe_status run_expert_ffn(const moe_config* c, const moe_weights* w, const void*
     a.out = static_cast<__nv_bfloat16*>(s.h);
     a.ld_out = H;
     MOE_CUDA(tc_gemm(kTcSwiGLU, A1, P, d, w->W_gu, E, 2 * H, d, a, di->num_sms, st));
-    // routed down projection
+    // down projection
     a.n_ntiles = d / kTcTileN;
     a.nt_per_slice = a.n_ntiles;
     a.n_kblocks = H / kTcTileK;
@@ -175,50 +169,69 @@ moe_status run_expert_ffn(const moe_config* c, const moe_weights* w, const void*
     a.ld_out = d;
     a.out_rowmap = rowmap;
     MOE_CUDA(tc_gemm(kTcStore, s.h, P, H, w->W_down, E, d, H, a, di->num_sms, st));
-    if (S > 0) {
-      TcGemmArgs b = {};
-      b.status = di->status;
-      b.mt_info = s.mt_shared;
-      b.group_mt_begin = s.gmb_shared;
-      b.n_groups = 1;
-      b.n_ntiles = S * Hs / 128;
-      b.nt_per_slice = Hs / 128;
-      b.n_kblocks = d / kTcTileK;
-      b.kb_per_slice = b.n_kblocks;
-      b.b_up_offset = Hs;
-      b.out = static_cast<__nv_bfloat16*>(s.h_shared);
-      b.ld_out = static_cast<long long>(S) * Hs;
-      MOE_CUDA(tc_gemm(kTcSwiGLU, x, T, d, w->Ws_gu, S, 2 * Hs, d, b, di->num_sms, st));
-      b.n_ntiles = d / kTcTileN;
-      b.nt_per_slice = b.n_ntiles;
-      b.n_kblocks = S * Hs / kTcTileK;
-      b.kb_per_slice = Hs / kTcTileK;
-      b.b_up_offset = 0;
-      b.out = static_cast<__nv_bfloat16*>(shared_out);
-      b.ld_out = d;
-      MOE_CUDA(tc_gemm(kTcStore, s.h_shared, T, S * Hs, w->Ws_down, S, d, Hs, b, di->num_sms,
-                       st));
-    }
   } else {
-    const float* Wgu = static_cast<const float*>(w->W_gu);
-    const float* Wdn = static_cast<const float*>(w->W_down);
-    MOE_CUDA(simt_gemm_swiglu(static_cast<const float*>(A1), Wgu, E, 2 * H, d, 0, H / 64, H, H,
-                              s.mt_routed, s.gmb_routed, E, mt_routed_max,
+    const int mt_max = max_mtiles(P, E);
+    MOE_CUDA(simt_gemm_swiglu(static_cast<const float*>(A1), static_cast<const float*>(w->W_gu), E,
+                              2 * H, d, 0, H / 64, H, H, s.mt_routed, s.gmb_routed, E, mt_max,
                               static_cast<float*>(s.h), st));
-    MOE_CUDA(simt_gemm_store(static_cast<const float*>(s.h), Wdn, E, d, H, H, d, s.mt_routed,
-                             s.gmb_routed, E, mt_routed_max, rowmap, static_cast<float*>(y_perm),
-                             st));
-    if (S > 0) {
-      MOE_CUDA(simt_gemm_swiglu(static_cast<const float*>(x), static_cast<const float*>(w->Ws_gu),
-                                S, 2 * Hs, d, 0, Hs / 64, S * Hs, Hs, s.mt_shared, s.gmb_shared, 1,
-                                mt_shared_max, static_cast<float*>(s.h_shared), st));
-      MOE_CUDA(simt_gemm_store(static_cast<const float*>(s.h_shared),
-                               static_cast<const float*>(w->Ws_down), S, d, S * Hs, Hs, d,
-                               s.mt_shared, s.gmb_shared, 1, mt_shared_max, nullptr,
-                               static_cast<float*>(shared_out), st));
-    }
+    MOE_CUDA(simt_gemm_store(static_cast<const float*>(s.h), static_cast<const float*>(w->W_down),
+                             E, d, H, H, d, s.mt_routed, s.gmb_routed, E, mt_max, rowmap,
+                             static_cast<float*>(y_perm), st));
   }
   return MOE_OK;
+}
+
+// Shared experts on all T rows of x: shared_out[t] = sum over shared experts.
+// Uses only its own scratch (mt_shared, gmb_shared, h_shared), so it may run
+// on another stream concurrently with run_routed_ffn.
+moe_status run_shared_ffn(const moe_config* c, const moe_weights* w, const void* x,
+                          void* shared_out, const FfnScratch& s, DeviceInfo* di, cudaStream_t st) {
+  const int T = c->T, d = c->d, S = c->n_shared, Hs = c->H_shared;
+  if (S == 0) return MOE_OK;
+  MOE_CUDA(launch_build_mtiles(nullptr, nullptr, T, 1, nullptr, s.mt_shared, s.gmb_shared, st));
+  if (c->act_dtype == MOE_BF16) {
+    TcGemmArgs b = {};
+    b.status = di->status;
+    b.mt_info = s.mt_shared;
+    b.group_mt_begin = s.gmb_shared;
+    b.n_groups = 1;
+    b.n_ntiles = S * Hs / 128;
+    b.nt_per_slice = Hs / 128;
+    b.n_kblocks = d / kTcTileK;
+    b.kb_per_slice = b.n_kblocks;
+    b.b_up_offset = Hs;
+    b.out = static_cast<__nv_bfloat16*>(s.h_shared);
+    b.ld_out = static_cast<long long>(S) * Hs;
+    MOE_CUDA(tc_gemm(kTcSwiGLU, x, T, d, w->Ws_gu, S, 2 * Hs, d, b, di->num_sms, st));
+    b.n_ntiles = d / kTcTileN;
+    b.nt_per_slice = b.n_ntiles;
+    b.n_kblocks = S * Hs / kTcTileK;
+    b.kb_per_slice = Hs / kTcTileK;
+    b.b_up_offset = 0;
+    b.out = static_cast<__nv_bfloat16*>(shared_out);
+    b.ld_out = d;
+    MOE_CUDA(tc_gemm(kTcStore, s.h_shared, T, S * Hs, w->Ws_down, S, d, Hs, b, di->num_sms, st));
+  } else {
+    const int mt_max = max_mtiles(T, 1);
+    MOE_CUDA(simt_gemm_swiglu(static_cast<const float*>(x), static_cast<const float*>(w->Ws_gu), S,
+                              2 * Hs, d, 0, Hs / 64, S * Hs, Hs, s.mt_shared, s.gmb_shared, 1,
+                              mt_max, static_cast<float*>(s.h_shared), st));
+    MOE_CUDA(simt_gemm_store(static_cast<const float*>(s.h_shared),
+                             static_cast<const float*>(w->Ws_down), S, d, S * Hs, Hs, d,
+                             s.mt_shared, s.gmb_shared, 1, mt_max, nullptr,
+                             static_cast<float*>(shared_out), st));
+  }
+  return MOE_OK;
+}
+
+moe_status run_expert_ffn(const moe_config* c, const moe_weights* w, const void* x_perm,
+                          const int32_t* offsets, const int32_t* rep_of, const void* x,
+                          void* y_perm, void* shared_out, const FfnScratch& s, DeviceInfo* di,
+                          cudaStream_t st) {
+  if (c->T == 0) return MOE_OK;
+  moe_status r = run_routed_ffn(c, w, x_perm, offsets, rep_of, y_perm, s, di, st);
+  if (r != MOE_OK) return r;
+  return run_shared_ffn(c, w, x, shared_out, s, di, st);
 }
 
 moe_status check_weights(const moe_config* c, const moe_weights* w) {
@@ -499,10 +512,31 @@ size_t moe_workspace_size(const moe_config* cfg, int with_condensation) {
   return carve_layer(cfg, with_condensation != 0, nullptr, nullptr);
 }
 
-moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const void* x,
-                             const void* residual, float tau, void* out, int32_t* topk_idx_out,
-                             int32_t* n_condensed_out, void* ws, size_t ws_bytes,
-                             moe_stream_t stream) {
+}  // extern "C"
+
+namespace moe {
+namespace {
+
+// Fork/join events of moe_layer_forward_ex, one pair per host thread and device
+// (created on first use, kept for the life of the process), so concurrent
+// callers on different threads never share one.
+thread_local cudaEvent_t t_events[kMaxDevices][2] = {};
+
+bool overlap_events(cudaEvent_t** ev) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  for (int i = 0; i < 2; ++i)
+    if (!t_events[dev][i] &&
+        cudaEventCreateWithFlags(&t_events[dev][i], cudaEventDisableTiming) != cudaSuccess)
+      return false;
+  *ev = t_events[dev];
+  return true;
+}
+
+moe_status layer_forward_impl(const moe_config* cfg, const moe_weights* w, const void* x,
+                              const void* residual, float tau, void* out, void* partial_out,
+                              int32_t* topk_idx_out, int32_t* n_condensed_out, void* ws,
+                              size_t ws_bytes, cudaStream_t st, cudaStream_t aux) {
   moe_status s = check_cfg(cfg);
   if (s != MOE_OK) return s;
   if (cfg->T == 0) return MOE_OK;
@@ -512,6 +546,7 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
   MOE_OPT_PTR(w->router_bias);
   MOE_PTR(x);
   MOE_PTR(out);
+  MOE_OPT_PTR(partial_out);
   MOE_OPT_PTR(topk_idx_out);
   MOE_OPT_PTR(n_condensed_out);
   if (cfg->residual == MOE_RES_EXTERNAL || cfg->residual == MOE_RES_INPUT_PLUS_EXTERNAL)
@@ -523,12 +558,27 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
   MOE_REQUIRE(ws_bytes >= moe_workspace_size(cfg, condense), MOE_ERR_WORKSPACE);
   DeviceInfo* di = device_info();
   if (!di) return MOE_ERR_CUDA;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   LayerScratch L;
   carve_layer(cfg, condense, ws, &L);
+  FfnScratch fs;
+  carve_ffn(cfg, condense, L.ffn_ws, &fs);
+  const bool overlap = aux != nullptr && aux != st && cfg->n_shared > 0;
+  cudaEvent_t* ev = nullptr;
+  if (overlap && !overlap_events(&ev)) return MOE_ERR_CUDA;
+
   int32_t* idx = topk_idx_out ? topk_idx_out : L.topk_idx;
   s = run_router(cfg, x, w->W_r, w->router_bias, L.logits, idx, L.gate, L.route_ws, di, st);
   if (s != MOE_OK) return s;
+  if (overlap) {
+    // The shared experts need only x: they start on the second stream once the
+    // router is done (the router's tensor-core GEMM would not fit beside them
+    // on an SM) and run beside dispatch and the routed experts.
+    MOE_CUDA(cudaEventRecord(ev[0], st));
+    MOE_CUDA(cudaStreamWaitEvent(aux, ev[0], 0));
+    s = run_shared_ffn(cfg, w, x, L.shared_out, fs, di, aux);
+    if (s != MOE_OK) return s;
+    MOE_CUDA(cudaEventRecord(ev[1], aux));
+  }
   MOE_CUDA(launch_dispatch_auto(cfg->act_dtype, x, idx, cfg->T, cfg->d, cfg->E, cfg->k,
                                 L.counts, L.offsets, L.perm, L.slot_of, L.x_perm, L.dispatch_ws,
                                 di->num_sms, di->status, st));
@@ -542,14 +592,42 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
   } else if (n_condensed_out) {
     MOE_CUDA(cudaMemsetAsync(n_condensed_out, 0, sizeof(int32_t), st));
   }
-  FfnScratch fs;
-  carve_ffn(cfg, condense, L.ffn_ws, &fs);
-  s = run_expert_ffn(cfg, w, L.x_perm, L.offsets, rep_of, x, L.y_perm, L.shared_out, fs, di, st);
+  s = run_routed_ffn(cfg, w, L.x_perm, L.offsets, rep_of, L.y_perm, fs, di, st);
   if (s != MOE_OK) return s;
+  if (overlap) {
+    MOE_CUDA(cudaStreamWaitEvent(st, ev[1], 0));
+  } else {
+    s = run_shared_ffn(cfg, w, x, L.shared_out, fs, di, st);
+    if (s != MOE_OK) return s;
+  }
   MOE_CUDA(launch_combine(cfg->act_dtype, L.y_perm, cfg->n_shared > 0 ? L.shared_out : nullptr,
                           L.slot_of, rep_of, L.gate, x, residual, cfg->residual, out, cfg->T,
-                          cfg->d, cfg->k, static_cast<int>(P), di->status, st));
+                          cfg->d, cfg->k, static_cast<int>(P), di->status, st, partial_out));
   return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" {
+
+moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const void* x,
+                             const void* residual, float tau, void* out, int32_t* topk_idx_out,
+                             int32_t* n_condensed_out, void* ws, size_t ws_bytes,
+                             moe_stream_t stream) {
+  return moe::layer_forward_impl(cfg, w, x, residual, tau, out, nullptr, topk_idx_out,
+                                 n_condensed_out, ws, ws_bytes,
+                                 reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+moe_status moe_layer_forward_ex(const moe_config* cfg, const moe_weights* w, const void* x,
+                                const void* residual, float tau, void* out, void* partial_out,
+                                int32_t* topk_idx_out, int32_t* n_condensed_out, void* ws,
+                                size_t ws_bytes, moe_stream_t stream, moe_stream_t aux_stream) {
+  return moe::layer_forward_impl(cfg, w, x, residual, tau, out, partial_out, topk_idx_out,
+                                 n_condensed_out, ws, ws_bytes,
+                                 reinterpret_cast<cudaStream_t>(stream),
+                                 reinterpret_cast<cudaStream_t>(aux_stream));
 }
 
 }  // extern "C"

@@ -31,7 +31,8 @@ EXPORTED = ("moe_status_string", "moe_adaptive_tau", "moe_get_device_status",
             "moe_route_workspace_size", "moe_route",
             "moe_dispatch_workspace_size", "moe_dispatch", "moe_condense_workspace_size",
             "moe_condense", "moe_expert_ffn_workspace_size", "moe_expert_ffn", "moe_combine",
-            "moe_workspace_size", "moe_layer_forward", "moe_dispatch_static_scratch")
+            "moe_workspace_size", "moe_layer_forward", "moe_layer_forward_ex",
+            "moe_dispatch_static_scratch")
 
 
 class MoEError(RuntimeError):
@@ -82,6 +83,7 @@ def lib() -> ctypes.CDLL:
         "moe_combine": (I, [CFG, P, P, P, P, P, P, P, P, P]),
         "moe_workspace_size": (S, [CFG, I]),
         "moe_layer_forward": (I, [CFG, W, P, P, F, P, P, P, P, S, P]),
+        "moe_layer_forward_ex": (I, [CFG, W, P, P, F, P, P, P, P, P, S, P, P]),
         "moe_dispatch_static_scratch": (I, [CFG, P, P, P, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
@@ -274,6 +276,9 @@ class Layer:
 
     ``layer(x, residual, tau)`` is one ``moe_layer_forward`` call on the
     current stream.  tau <= 1 enables condensation; tau = nan disables it.
+    With ``partial_out`` (FarSkip's partial activation r + shared) or
+    ``aux_stream`` (shared experts on a second stream) it is one
+    ``moe_layer_forward_ex`` call.
     """
 
     def __init__(self, cfg: Config, w: Weights, condense: bool = False, device=None):
@@ -287,15 +292,23 @@ class Layer:
         self.ws = _workspace(self.ws_bytes, self.device)
 
     def __call__(self, x, residual=None, tau: float = math.nan, out=None, topk_idx_out=None,
-                 n_condensed_out=None, stream=None):
+                 n_condensed_out=None, stream=None, partial_out=None, aux_stream=None):
         if out is None:
             out = _empty((self.cfg.T, self.cfg.d), self.cfg.torch_dtype, self.device)
         if tau <= 1.0 and not self.condense:
             raise ValueError("layer was built without condensation workspace")
-        _check(lib().moe_layer_forward(ctypes.byref(self._c), ctypes.byref(self._wc), _ptr(x),
-                                       _ptr(residual), tau, _ptr(out), _ptr(topk_idx_out),
-                                       _ptr(n_condensed_out), _ptr(self.ws), self.ws_bytes,
-                                       _stream(stream)), "moe_layer_forward")
+        if partial_out is None and aux_stream is None:
+            _check(lib().moe_layer_forward(ctypes.byref(self._c), ctypes.byref(self._wc), _ptr(x),
+                                           _ptr(residual), tau, _ptr(out), _ptr(topk_idx_out),
+                                           _ptr(n_condensed_out), _ptr(self.ws), self.ws_bytes,
+                                           _stream(stream)), "moe_layer_forward")
+        else:
+            aux = aux_stream.cuda_stream if aux_stream is not None else None
+            _check(lib().moe_layer_forward_ex(ctypes.byref(self._c), ctypes.byref(self._wc),
+                                              _ptr(x), _ptr(residual), tau, _ptr(out),
+                                              _ptr(partial_out), _ptr(topk_idx_out),
+                                              _ptr(n_condensed_out), _ptr(self.ws), self.ws_bytes,
+                                              _stream(stream), aux), "moe_layer_forward_ex")
         return out
 
 

@@ -110,6 +110,24 @@ def test_workspace_checks(L):
     assert r == 1
 
 
+def test_layer_forward_ex_argument_checks(L):
+    lib = L.lib()
+    c = _cfg(L)
+    w = L.moe_weights(FAKE, None, FAKE, FAKE, None, None)
+    full = lib.moe_workspace_size(ctypes.byref(c), 0)
+    # workspace too small, misaligned partial output, missing output
+    assert lib.moe_layer_forward_ex(ctypes.byref(c), ctypes.byref(w), FAKE, None, float("nan"),
+                                    FAKE, FAKE, None, None, FAKE, full - 1, None, None) == 3
+    assert lib.moe_layer_forward_ex(ctypes.byref(c), ctypes.byref(w), FAKE, None, float("nan"),
+                                    FAKE, FAKE + 2, None, None, FAKE, full, None, None) == 1
+    assert lib.moe_layer_forward_ex(ctypes.byref(c), ctypes.byref(w), FAKE, None, float("nan"),
+                                    None, FAKE, None, None, FAKE, full, None, None) == 1
+    # zero tokens: nothing to do, with or without a second stream
+    c0 = _cfg(L, T=0)
+    assert lib.moe_layer_forward_ex(ctypes.byref(c0), ctypes.byref(w), None, None, float("nan"),
+                                    None, None, None, None, None, 0, None, FAKE) == 0
+
+
 def test_zero_tokens_is_a_no_op(L):
     c = _cfg(L, T=0)
     lib = L.lib()

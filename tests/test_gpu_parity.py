@@ -226,6 +226,63 @@ def test_layer_deterministic(moe):
     assert torch.equal(a, b)
 
 
+# ------------------------------------------------------------------ FarSkip partial output + overlap
+@pytest.mark.parametrize("name", ["dsv2_lite", "llama4_scout_farskip", "tiny_fp32"])
+def test_layer_ex_partial_and_shared_on_second_stream(moe, name):
+    """moe_layer_forward_ex: out is bit-identical to moe_layer_forward (same kernels, the
+    shared experts merely run on a second stream), and the partial activation r + shared
+    matches the oracle."""
+    cfg, inp, C, w, x, r = _setup(moe, name, T=SMALL_T[name])
+    lay = moe.Layer(C, w)
+    ref_out = lay(x, r).clone()
+    aux = torch.cuda.Stream()
+    part = torch.empty_like(ref_out)
+    out = lay(x, r, partial_out=part, aux_stream=aux)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_out)
+    ref = orc.layer_forward(inp["x"], inp["W_r"], inp["bias"], inp["W_gu"], inp["W_down"],
+                            inp["Ws_gu"], inp["Ws_down"], cfg.k, cfg.gating,
+                            residual_mode=C.residual, residual=inp["residual"])
+    assert harness.max_rel_err(_np(part), ref["partial"]) <= harness.tolerance(cfg)
+    assert harness.max_rel_err(_np(out), ref["out"]) <= harness.tolerance(cfg)
+    # partial output without a second stream: the same values
+    part2 = torch.empty_like(part)
+    lay(x, r, partial_out=part2)
+    torch.cuda.synchronize()
+    assert torch.equal(part, part2)
+    _status_ok(moe)
+
+
+def test_layer_ex_second_stream_in_cuda_graph(moe):
+    """The fork/join of the shared experts is captured into one graph that begins on the
+    calling stream; replays reproduce the eager result bit for bit."""
+    cfg, inp, C, w, x, r = _setup(moe, "dsv2_lite", T=SMALL_T["dsv2_lite"])
+    lay = moe.Layer(C, w)
+    eager = lay(x, r).clone()
+    aux = torch.cuda.Stream()
+    out = torch.empty_like(eager)
+    part = torch.empty_like(eager)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        lay(x, r, out=out, partial_out=part, aux_stream=aux)  # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        lay(x, r, out=out, partial_out=part, aux_stream=aux)
+    out.zero_()
+    part.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
+    ref = orc.layer_forward(inp["x"], inp["W_r"], inp["bias"], inp["W_gu"], inp["W_down"],
+                            inp["Ws_gu"], inp["Ws_down"], cfg.k, cfg.gating,
+                            residual_mode=C.residual, residual=inp["residual"])
+    assert harness.max_rel_err(_np(part), ref["partial"]) <= harness.tolerance(cfg)
+    _status_ok(moe)
+
+
 # ------------------------------------------------------------------ condensation
 @pytest.mark.parametrize("tau_index", [0, 1])
 def test_condense_full_size(moe, tau_index):

@@ -242,6 +242,26 @@ def test_residual_modes_and_zero_experts():
     np.testing.assert_array_equal(z, inp["residual"].astype(np.float64) + shared)
 
 
+def test_partial_activation_is_the_output_without_routed_experts():
+    """FarSkip's partial activation: what the layer outputs when the routed experts
+    contribute nothing, and independent of the routed experts' weights."""
+    cfg, inp = harness.workload("tiny_fp32")
+    common = dict(residual_mode="external", residual=inp["residual"])
+    zero = orc.layer_forward(inp["x"], inp["W_r"], None, np.zeros_like(inp["W_gu"]),
+                             np.zeros_like(inp["W_down"]), inp["Ws_gu"], inp["Ws_down"], cfg.k,
+                             cfg.gating, **common)
+    np.testing.assert_array_equal(zero["partial"], zero["out"])
+    full = orc.layer_forward(inp["x"], inp["W_r"], inp["bias"], inp["W_gu"], inp["W_down"],
+                             inp["Ws_gu"], inp["Ws_down"], cfg.k, cfg.gating, **common)
+    np.testing.assert_array_equal(full["partial"], zero["partial"])
+    assert np.max(np.abs(full["out"] - full["partial"])) > 1e-3
+    # no shared experts and no residual: nothing is left
+    none = orc.layer_forward(inp["x"], inp["W_r"], None, inp["W_gu"], inp["W_down"],
+                             inp["Ws_gu"][:0], inp["Ws_down"][:0], cfg.k, cfg.gating,
+                             residual_mode="none")
+    assert not np.any(none["partial"])
+
+
 def test_layer_subset_equals_full():
     cfg, inp = harness.workload("tiny_fp32")
     args = (inp["x"], inp["W_r"], inp["bias"], inp["W_gu"], inp["W_down"], inp["Ws_gu"],
