@@ -473,7 +473,7 @@ def end_to_end(args, C, graph, x, r, out, stream, torch) -> dict:
     d2h = outh.numel() * outh.element_size()
     return {"value": C.T / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "path": "pinned host -> device copy, moe_layer_forward (CUDA graph), device -> pinned host"}
+            "path": "pinned host -> device copy, the timed layer step (CUDA graph), device -> pinned host"}
 
 
 # ------------------------------------------------------------------ oracle (CPU) timing
