@@ -276,22 +276,27 @@ __device__ int block_scan_smem(int* a, int n, int* wsum /* 33 ints */) {
 }
 
 // For every pair p: slot = base[e][p / kLocalPairs] + local_rank[p]; slot_of[p] = slot,
-// perm[slot] = p / k, x_perm[slot] = x[p / k].  One warp per pair, 16-byte
-// vectors.  A pair with an out-of-range expert gets slot_of -1 and no row.
+// perm[slot] = p / k, x_perm[slot] = x[p / k].  One warp per token: lane j < k
+// resolves pair (t, j), the warp reads the token's row once (in chunks of
+// kRowChunk 16-byte vectors per lane, held in registers) and writes it to each
+// of the token's k slots.  A pair with an out-of-range expert gets slot_of -1
+// and no row.
 // SCAN: blk holds the raw (expert, block) counts; every CTA scans the table in
 // shared memory (it is small: E x ceil(P / 1024) entries) and CTA 0 writes
 // counts and offsets -- this replaces a separate scan launch.  Otherwise blk
 // is already the exclusive prefix.
+constexpr int kRowChunk = 8;
 template <typename T, bool SCAN>
 __global__ void __launch_bounds__(256)
     scatter_rows_kernel(const T* __restrict__ x, const int32_t* __restrict__ idx,
                         const int32_t* __restrict__ local_rank, const int32_t* __restrict__ blk,
-                        int n_blk, int E, int P, int k, int d, T* __restrict__ x_perm,
+                        int n_blk, int E, int T_tok, int k, int d, T* __restrict__ x_perm,
                         int32_t* __restrict__ perm, int32_t* __restrict__ slot_of,
                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                         unsigned* status) {
   constexpr int V = Act<T>::kVec;
   const int nv = d / V;
+  const int P = T_tok * k;
   extern __shared__ int tab[];
   __shared__ int wsum[33];
   pdl_trigger();
@@ -314,24 +319,41 @@ __global__ void __launch_bounds__(256)
   }
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int lane = threadIdx.x & 31;
-  for (int p = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; p < P; p += warps) {
-    const int e = idx[p];
-    const int lr = local_rank[p];
-    if (e < 0 || e >= E || lr < 0) {
-      if (lane == 0) slot_of[p] = -1;
-      continue;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T_tok; t += warps) {
+    int slot = -1;
+    if (lane < k) {
+      const int p = t * k + lane;
+      const int e = idx[p];
+      const int lr = local_rank[p];
+      if (e >= 0 && e < E && lr >= 0) {
+        slot = base_tab[static_cast<long long>(e) * n_blk + p / kLocalPairs] + lr;
+        if (slot >= P) {
+          record_status(status, MOE_ERR_DEVICE_INDEX);
+          slot = -1;
+        }
+      }
+      slot_of[p] = slot;
+      if (slot >= 0) perm[slot] = t;
     }
-    const int s = base_tab[static_cast<long long>(e) * n_blk + p / kLocalPairs] + lr;
-    if (s >= P) {
-      if (lane == 0) record_status(status, MOE_ERR_DEVICE_INDEX);
-      continue;
+    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<long long>(t) * d);
+    for (int v0 = 0; v0 < nv; v0 += 32 * kRowChunk) {
+      uint4 r[kRowChunk];
+#pragma unroll
+      for (int u = 0; u < kRowChunk; ++u) {
+        const int v = v0 + u * 32 + lane;
+        if (v < nv) r[u] = src[v];
+      }
+      for (int j = 0; j < k; ++j) {
+        const int s = __shfl_sync(0xffffffffu, slot, j);
+        if (s < 0) continue;
+        uint4* dst = reinterpret_cast<uint4*>(x_perm + static_cast<long long>(s) * d);
+#pragma unroll
+        for (int u = 0; u < kRowChunk; ++u) {
+          const int v = v0 + u * 32 + lane;
+          if (v < nv) dst[v] = r[u];
+        }
+      }
     }
-    if (lane == 0) slot_of[p] = s;
-    const int t = p / k;
-    if (lane == 0) perm[s] = t;
-    const uint4* a = reinterpret_cast<const uint4*>(x + static_cast<long long>(t) * d);
-    uint4* b = reinterpret_cast<uint4*>(x_perm + static_cast<long long>(s) * d);
-    for (int v = lane; v < nv; v += 32) b[v] = a[v];
   }
 }
 
@@ -513,28 +535,27 @@ cudaError_t launch_dispatch_auto(int act_dtype, const void* x, const int32_t* to
                      counts, offsets);
     if (err != cudaSuccess) return err;
   }
-  const long long want = (P + 7) / 8;
+  const long long want = (static_cast<long long>(T) + 7) / 8;  // one warp per token
   const int blocks = static_cast<int>(want < 8ll * num_sms ? want : 8ll * num_sms);
   const size_t smem = scan_in_smem ? sizeof(int) * table : 0;
-  const int Pi = static_cast<int>(P);
   if (act_dtype == MOE_F32) {
     const float* xf = static_cast<const float*>(x);
     float* xp = static_cast<float*>(x_perm);
     err = scan_in_smem ? launch_pdl(scatter_rows_kernel<float, true>, dim3(blocks), dim3(256), smem,
-                                    stream, xf, topk_idx, local_rank, blk, n_blk, E, Pi, k, d, xp,
+                                    stream, xf, topk_idx, local_rank, blk, n_blk, E, T, k, d, xp,
                                     perm, slot_of, counts, offsets, status)
                        : launch_pdl(scatter_rows_kernel<float, false>, dim3(blocks), dim3(256), 0,
-                                    stream, xf, topk_idx, local_rank, blk, n_blk, E, Pi, k, d, xp,
+                                    stream, xf, topk_idx, local_rank, blk, n_blk, E, T, k, d, xp,
                                     perm, slot_of, counts, offsets, status);
   } else {
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
     __nv_bfloat16* xp = static_cast<__nv_bfloat16*>(x_perm);
     err = scan_in_smem
               ? launch_pdl(scatter_rows_kernel<__nv_bfloat16, true>, dim3(blocks), dim3(256), smem,
-                           stream, xb, topk_idx, local_rank, blk, n_blk, E, Pi, k, d, xp, perm,
+                           stream, xb, topk_idx, local_rank, blk, n_blk, E, T, k, d, xp, perm,
                            slot_of, counts, offsets, status)
               : launch_pdl(scatter_rows_kernel<__nv_bfloat16, false>, dim3(blocks), dim3(256), 0,
-                           stream, xb, topk_idx, local_rank, blk, n_blk, E, Pi, k, d, xp, perm,
+                           stream, xb, topk_idx, local_rank, blk, n_blk, E, T, k, d, xp, perm,
                            slot_of, counts, offsets, status);
   }
   if (err != cudaSuccess) return err;
