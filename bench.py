@@ -118,10 +118,19 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ work accounting
-def work(cfg, n_condensed: int = 0) -> dict:
-    """Algorithmic FLOPs and bytes of one layer call (no padding rows, no re-reads)."""
+def work(cfg, n_condensed: int = 0, active_experts: int | None = None) -> dict:
+    """Algorithmic FLOPs and bytes of one layer call (no padding rows, no re-reads).
+
+    ffn_bytes: what the expert GEMMs must move at least -- the weights of every expert
+    that received a token (active_experts, all E when not given) and of the shared
+    experts, once, plus x_perm / x read, h written and read back, y / shared written.
+    """
     b = 2 if cfg.dtype == "bf16" else 4
     P = cfg.T * cfg.k
+    n_act = cfg.E if active_experts is None else active_experts
+    ffn_bytes = ((n_act * 3 * cfg.H + cfg.n_shared * 3 * cfg.H_shared) * cfg.d * b
+                 + (P - n_condensed) * (2 * cfg.d + 2 * cfg.H) * b
+                 + cfg.T * cfg.n_shared * (2 * cfg.d + 2 * cfg.H_shared) * b)
     routed_flops = 6.0 * cfg.d * cfg.H * (P - n_condensed)
     shared_flops = 6.0 * cfg.d * cfg.H_shared * cfg.T * cfg.n_shared
     idx_bytes = P * 4
@@ -130,7 +139,8 @@ def work(cfg, n_condensed: int = 0) -> dict:
     combine_bytes = (P * cfg.d * b + cfg.T * cfg.d * b * (1 + res_reads + (1 if cfg.n_shared else 0))
                      + idx_bytes * 2)
     return dict(routed_flops=routed_flops, shared_flops=shared_flops,
-                ffn_flops=routed_flops + shared_flops, dispatch_bytes=dispatch_bytes,
+                ffn_flops=routed_flops + shared_flops, ffn_bytes=ffn_bytes,
+                dispatch_bytes=dispatch_bytes,
                 combine_bytes=combine_bytes, router_flops=2.0 * cfg.T * cfg.d * cfg.E)
 
 
@@ -258,6 +268,10 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     serial = {"ms_per_step": ms_serial, "tokens_per_s": job_tokens_per_s(C.T, world, ms_serial),
               "path": "moe_layer_forward, every kernel on one stream"}
 
+    # experts that received at least one token (the weights a step has to stream)
+    _, idx_chk, _ = moe.route(C, x, w.W_r, w.router_bias)
+    active = int((torch.bincount(idx_chk.flatten().long(), minlength=C.E) > 0).sum().item())
+
     # per-phase breakdown (FarSkip Eq. 9 terms): the same step as separate ABI calls
     phases = phase_breakdown(args, moe, C, w, x, r, tau, flush, stream, torch)
     # the layer's outputs after all timing passes still come from the same graph
@@ -271,11 +285,24 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     if rank != 0:
         return
     peaks, peak_src = load_peaks()
-    wk = work(C, n_condensed)
+    wk = work(C, n_condensed, active_experts=active)
     ffn_s = phases["T_experts_ms"] / 1e3
-    achieved = wk["ffn_flops"] / ffn_s / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    # The expert GEMMs are bound by the tensor pipes when their arithmetic intensity is
+    # above the machine's ridge (peak FLOP/s over HBM bytes/s), else by streaming the
+    # weights from HBM (decode-shaped steps).
+    if wk["ffn_flops"] / wk["ffn_bytes"] >= peak * 1e12 / (hbm * 1e9):
+        roofline = {"bound": "tensor", "kernel": "grouped expert GEMM (moe_expert_ffn)",
+                    "achieved": wk["ffn_flops"] / ffn_s / 1e12, "peak": peak, "unit": "TFLOP/s",
+                    "peak_source": f"{peak_src} bf16 burst"}
+    else:
+        roofline = {"bound": "hbm", "kernel": "grouped expert GEMM (moe_expert_ffn), weight stream",
+                    "achieved": wk["ffn_bytes"] / ffn_s / 1e9, "peak": hbm, "unit": "GB/s",
+                    "peak_source": f"{peak_src} HBM copy", "bytes": wk["ffn_bytes"],
+                    "active_experts": active}
+    roofline["frac"] = roofline["achieved"] / roofline["peak"]
+    roofline["traffic"] = GEMM_DRAM_BYTES.get(cfg.name)
     disp_gbs = wk["dispatch_bytes"] / (phases["T_dispatch_ms"] / 1e3) / 1e9
     comb_gbs = wk["combine_bytes"] / (phases["T_combine_ms"] / 1e3) / 1e9
     line = {
@@ -300,10 +327,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
                   + (", partial activation written" if part is not None else ""),
                    "l2": "256 MB write between timed steps (outside the timed events); weights "
                          f"{(C.E * 3 * C.H + C.n_shared * 3 * C.H_shared) * C.d * 2 / 1e9:.2f} GB > L2"},
-        "roofline": {"bound": "tensor", "kernel": "grouped expert GEMM (moe_expert_ffn)",
-                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "peak_source": f"{peak_src} bf16 burst",
-                     "traffic": GEMM_DRAM_BYTES.get(cfg.name)},
+        "roofline": roofline,
         "dispatch": {"GB/s": disp_gbs, "frac_of_hbm": disp_gbs / hbm,
                      "bytes": wk["dispatch_bytes"]},
         "combine": {"GB/s": comb_gbs, "frac_of_hbm": comb_gbs / hbm, "bytes": wk["combine_bytes"]},

@@ -41,11 +41,13 @@ __device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16* p, flo
 }
 
 // CTA tile: 64 tokens x BN experts; thread tile TM tokens x 4 experts, TM = BN / 16.
+// Split K: CTA z of gridDim.z sums K range [z k_len, (z+1) k_len) and writes its
+// partial logits at logits + z * T * E (k_len = d, one split, writes the logits).
 template <typename TX, int BN>
 __global__ void __launch_bounds__(kRThreads)
     router_logits_kernel(const TX* __restrict__ x, const float* __restrict__ W_r,
                          const float* __restrict__ bias, float* __restrict__ logits, int T, int d,
-                         int E) {
+                         int E, int k_len) {
   constexpr int TM = BN / 16;
   constexpr int NX = BN / 4;  // threads along experts
   __shared__ __align__(16) float xs[kRBK][kRBM + 4];
@@ -62,18 +64,23 @@ __global__ void __launch_bounds__(kRThreads)
 
   // x tile loader: 64 rows x 16 k = 256 threads x 4 consecutive k
   const int lm = tid >> 2, lk = (tid & 3) * 4;
-  for (int k0 = 0; k0 < d; k0 += kRBK) {
+  const int k_begin = blockIdx.z * k_len;
+  const int k_end = min(d, k_begin + k_len);
+  logits += static_cast<long long>(blockIdx.z) * T * E;
+  pdl_trigger();
+  pdl_wait();
+  for (int k0 = k_begin; k0 < k_end; k0 += kRBK) {
     {
       float v[4] = {0.f, 0.f, 0.f, 0.f};
       const int t = t0 + lm, kk = k0 + lk;
-      if (t < T && kk < d) load4<TX>(x + static_cast<long long>(t) * d + kk, v);
+      if (t < T && kk < k_end) load4<TX>(x + static_cast<long long>(t) * d + kk, v);
 #pragma unroll
       for (int i = 0; i < 4; ++i) xs[lk + i][lm] = v[i];
     }
     for (int i = tid; i < kRBK * BN; i += kRThreads) {
       const int kk = i / BN, n = i % BN;
       const int gk = k0 + kk, ge = e0 + n;
-      ws[kk][n] = (gk < d && ge < E) ? W_r[static_cast<long long>(gk) * E + ge] : 0.f;
+      ws[kk][n] = (gk < k_end && ge < E) ? W_r[static_cast<long long>(gk) * E + ge] : 0.f;
     }
     __syncthreads();
 #pragma unroll
@@ -137,19 +144,41 @@ __global__ void __launch_bounds__(256)
   pdl_trigger();
   pdl_wait();
   if (warp >= T) return;
+  // logits: the split partials added in split order.  Loads are issued kChunk
+  // splits x 8 expert slots at a time, so their latencies overlap.
+  constexpr int kChunk = 4;
   float v[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int e = lane + 32 * i;
-    float l = -INFINITY;
+    v[i] = e < E ? part[static_cast<long long>(warp) * ld + e] : 0.f;
+  }
+  for (int s0 = 1; s0 < n_split; s0 += kChunk) {
+    float q[kChunk][8];
+#pragma unroll
+    for (int u = 0; u < kChunk; ++u)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = lane + 32 * i;
+        q[u][i] = (e < E && s0 + u < n_split)
+                      ? part[(static_cast<long long>(s0 + u) * T + warp) * ld + e]
+                      : 0.f;
+      }
+#pragma unroll
+    for (int u = 0; u < kChunk; ++u)
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (s0 + u < n_split) v[i] += q[u][i];
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
     if (e < E) {
-      l = part[static_cast<long long>(warp) * ld + e];
-      for (int s = 1; s < n_split; ++s)
-        l += part[(static_cast<long long>(s) * T + warp) * ld + e];
-      if (bias) l += bias[e];
-      if (logits_out) logits_out[static_cast<long long>(warp) * E + e] = l;
+      if (bias) v[i] += bias[e];
+      if (logits_out) logits_out[static_cast<long long>(warp) * E + e] = v[i];
+    } else {
+      v[i] = -INFINITY;
     }
-    v[i] = l;
   }
   unsigned taken = 0;
   float sel_v[32];
@@ -204,17 +233,17 @@ __global__ void __launch_bounds__(256)
 
 template <typename TX>
 cudaError_t logits_dispatch(const TX* x, const float* W_r, const float* bias, float* logits, int T,
-                            int d, int E, cudaStream_t s) {
+                            int d, int E, int n_split, cudaStream_t s) {
   const int gx = ceil_div(T, kRBM);
-  if (E <= 16) {
-    router_logits_kernel<TX, 16><<<dim3(gx, 1), kRThreads, 0, s>>>(x, W_r, bias, logits, T, d, E);
-  } else if (E <= 32) {
-    router_logits_kernel<TX, 32><<<dim3(gx, 1), kRThreads, 0, s>>>(x, W_r, bias, logits, T, d, E);
-  } else {
-    router_logits_kernel<TX, 64>
-        <<<dim3(gx, ceil_div(E, 64)), kRThreads, 0, s>>>(x, W_r, bias, logits, T, d, E);
-  }
-  return cudaGetLastError();
+  const int k_len = d / n_split;
+  if (E <= 16)
+    return launch_pdl(router_logits_kernel<TX, 16>, dim3(gx, 1, n_split), dim3(kRThreads), 0, s,
+                      x, W_r, bias, logits, T, d, E, k_len);
+  if (E <= 32)
+    return launch_pdl(router_logits_kernel<TX, 32>, dim3(gx, 1, n_split), dim3(kRThreads), 0, s,
+                      x, W_r, bias, logits, T, d, E, k_len);
+  return launch_pdl(router_logits_kernel<TX, 64>, dim3(gx, ceil_div(E, 64), n_split),
+                    dim3(kRThreads), 0, s, x, W_r, bias, logits, T, d, E, k_len);
 }
 
 }  // namespace
@@ -223,9 +252,25 @@ cudaError_t launch_router_logits(int act_dtype, const void* x, const float* W_r,
                                  float* logits, int T, int d, int E, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   if (act_dtype == MOE_F32)
-    return logits_dispatch(static_cast<const float*>(x), W_r, bias, logits, T, d, E, stream);
-  return logits_dispatch(static_cast<const __nv_bfloat16*>(x), W_r, bias, logits, T, d, E,
+    return logits_dispatch(static_cast<const float*>(x), W_r, bias, logits, T, d, E, 1, stream);
+  return logits_dispatch(static_cast<const __nv_bfloat16*>(x), W_r, bias, logits, T, d, E, 1,
                          stream);
+}
+
+bool router_small_t(int T) { return T <= kRouterSmallT; }
+
+int router_simt_splits(int d) { return d % 64 == 0 ? d / 64 : 1; }
+
+cudaError_t launch_router_simt_split(const void* x, const float* W_r, int T, int d, int E,
+                                     void* scratch, const float** part_out, int* n_split,
+                                     int* ld, cudaStream_t stream) {
+  const int splits = router_simt_splits(d);
+  float* part = static_cast<float*>(scratch);
+  *part_out = part;
+  *n_split = splits;
+  *ld = E;
+  return logits_dispatch(static_cast<const __nv_bfloat16*>(x), W_r, nullptr, part, T, d, E,
+                         splits, stream);
 }
 
 cudaError_t launch_router_topk(const float* part, int n_split, int ld, const float* bias,
@@ -253,6 +298,8 @@ int router_splits(int T, int d, int num_sms) {
 }
 
 size_t router_scratch_bytes(int T, int d, int E, int num_sms) {
+  if (router_small_t(T))
+    return static_cast<size_t>(router_simt_splits(d)) * T * E * sizeof(float);
   const size_t n_pad = router_n_pad(E);
   const size_t w3 = (3 * n_pad * d * sizeof(__nv_bfloat16) + 255) & ~size_t(255);
   const size_t part = static_cast<size_t>(router_splits(T, d, num_sms)) * T * n_pad * sizeof(float);

@@ -102,8 +102,14 @@ CONFIGS: dict[str, MoEConfig] = {
         taus=(0.95, adaptive_tau_l_norm_minus_3()), seed=1005),
 }
 
+# Decode-shaped layer: the DeepSeek-V2-Lite shapes and weights with one decode step of 64
+# tokens, where the expert GEMMs are bound by streaming the weights from HBM
+# (FarSkip-Collective review, Figure 7: decoding is memory-bandwidth bound).
+CONFIGS["dsv2_lite_decode"] = replace(CONFIGS["dsv2_lite"], name="dsv2_lite_decode", T=64)
+
 # Order used by tests and the bench: the small fp32 case first, then the bf16 shapes.
 CONFIG_ORDER = ["tiny_fp32", "dsv2_lite", "qwen3_30b_a3b", "llama4_scout_farskip", "luffy_condense"]
+DECODE_CONFIGS = ["dsv2_lite_decode"]
 
 
 def _rng(seed: int, *key: int) -> np.random.Generator:

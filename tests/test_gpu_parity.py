@@ -226,6 +226,17 @@ def test_layer_deterministic(moe):
     assert torch.equal(a, b)
 
 
+# ------------------------------------------------------------------ decode-shaped layer
+def test_decode_layer_every_token(moe):
+    """One decode step (64 tokens) through the full DeepSeek-V2-Lite weights: routing bit for
+    bit and every output row against the oracle, through both layer entry points."""
+    out, _ = _layer_check(moe, "dsv2_lite_decode")
+    cfg, inp, C, w, x, r = _setup(moe, "dsv2_lite_decode")
+    out_ex = moe.Layer(C, w)(x, r, aux_stream=torch.cuda.Stream())
+    torch.cuda.synchronize()
+    assert torch.equal(out_ex, out)
+
+
 # ------------------------------------------------------------------ FarSkip partial output + overlap
 @pytest.mark.parametrize("name", ["dsv2_lite", "llama4_scout_farskip", "tiny_fp32"])
 def test_layer_ex_partial_and_shared_on_second_stream(moe, name):
