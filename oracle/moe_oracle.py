@@ -331,3 +331,122 @@ def layer_forward(x, W_r, bias, W_gu, W_down, Ws_gu, Ws_down, k, gating,
     partial = base + shared if shared is not None else base
     return dict(logits=logits, idx=idx, gates=g, counts=counts, offsets=offsets, perm=perm,
                 slot_of=slot_of, rep_of=rep_of, tokens=tok, out=out, partial=partial)
+
+
+# --------------------------------------------------------------------------- backward
+def sigmoid(z):
+    z = np.asarray(z, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return 1.0 / (1.0 + np.exp(-z))
+
+
+def swiglu_expert_backward(xrows, W_gu, W_down, dy):
+    """Gradients of one SwiGLU expert y = W_down (SiLU(a) * u), a = W_gate x, u = W_up x.
+
+    Given dL/dy for every row: returns (dL/dx [n, d], dL/dW_gu [2H, d], dL/dW_down [d, H]),
+    by the chain rule with SiLU'(a) = s(a) (1 + a (1 - s(a))), s the logistic function.
+    """
+    X = np.asarray(xrows, dtype=np.float64)
+    W = np.asarray(W_gu, dtype=np.float64)
+    Wd = np.asarray(W_down, dtype=np.float64)
+    DY = np.asarray(dy, dtype=np.float64)
+    H = W.shape[0] // 2
+    a = X @ W[:H].T
+    u = X @ W[H:].T
+    s = sigmoid(a)
+    h = a * s * u
+    dh = DY @ Wd
+    da = dh * u * (s * (1.0 + a * (1.0 - s)))
+    du = dh * a * s
+    dx = da @ W[:H] + du @ W[H:]
+    dW_gu = np.concatenate([da.T @ X, du.T @ X], axis=0)
+    dW_down = DY.T @ h
+    return dx, dW_gu, dW_down
+
+
+def gate_backward(logits, idx, gating, dg):
+    """dL/dlogits [T, E] from dL/dgates [T, k] (the top-k selection itself is piecewise
+    constant and passes no gradient).
+
+    * softmax_topk:        g_j = p[e_j], p = softmax(l): dl = p * (dp - <dp, p>), dp[e_j] = dg_j.
+    * softmax_topk_renorm: g = softmax(l[sel]): dl[e_j] = g_j (dg_j - sum_i dg_i g_i).
+    * sigmoid_topk:        g_j = s(l[e_j]): dl[e_j] = dg_j s (1 - s).
+    """
+    l = np.asarray(logits, dtype=np.float64)
+    ix = idx.astype(np.int64)
+    dg = np.asarray(dg, dtype=np.float64)
+    T, E = l.shape
+    dl = np.zeros((T, E))
+    if gating == "softmax_topk":
+        p = np.exp(l - l.max(axis=1, keepdims=True))
+        p /= p.sum(axis=1, keepdims=True)
+        dp = np.zeros((T, E))
+        np.put_along_axis(dp, ix, dg, axis=1)
+        return p * (dp - np.sum(dp * p, axis=1, keepdims=True))
+    g = gate_values(l, idx, gating)
+    if gating == "softmax_topk_renorm":
+        sel = g * (dg - np.sum(dg * g, axis=1, keepdims=True))
+    elif gating == "sigmoid_topk":
+        sel = dg * g * (1.0 - g)
+    else:
+        raise ValueError(f"unknown gating {gating!r}")
+    np.put_along_axis(dl, ix, sel, axis=1)
+    return dl
+
+
+def layer_backward(x, W_r, bias, W_gu, W_down, Ws_gu, Ws_down, k, gating, d_out,
+                   residual_mode="input", residual=None, tau=None):
+    """Gradients of layer_forward's output for an output gradient d_out [T, d].
+
+    Plain chain rule through the forward's own definition: the residual base, the shared
+    experts on every token, and for every routed pair (t, j) the term g[t, j] * E_e(x[src])
+    where src is the token of the pair's representative slot.  A condensed pair therefore
+    sends its expert gradient to its representative's input, never to its own token: Luffy
+    review, referee major comment 1 -- for a condensed token the gradient in that path is
+    zero.  Its gate still receives dg = <d_out[t], E_e(x[src])>.
+
+    Returns dx, d_residual (None unless the mode reads r), dW_r, d_bias (None without a
+    bias), dW_gu, dW_down, dWs_gu, dWs_down, all float64.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    dO = np.asarray(d_out, dtype=np.float64)
+    T, d = x.shape
+    E = W_gu.shape[0]
+    logits, idx, g = route(x, W_r, bias, k, gating)
+    counts, offsets, perm, slot_of = dispatch(idx, E)
+    use_tau = tau is not None and tau <= 1.0
+    rep_of = condense(x[perm], offsets, tau) if use_tau else np.arange(len(perm))
+    src = perm[rep_of[slot_of]]                               # [T, k] input token of each pair
+    dx = np.zeros((T, d))
+    if residual_mode in ("input", "input_plus_external"):
+        dx += dO
+    d_residual = dO.copy() if residual_mode in ("external", "input_plus_external") else None
+    dWs_gu = np.zeros(np.shape(Ws_gu))
+    dWs_down = np.zeros(np.shape(Ws_down))
+    for s in range(len(Ws_gu)):
+        gx, gW, gD = swiglu_expert_backward(x, Ws_gu[s], Ws_down[s], dO)
+        dx += gx
+        dWs_gu[s] = gW
+        dWs_down[s] = gD
+    dW_gu = np.zeros(np.shape(W_gu))
+    dW_down = np.zeros(np.shape(W_down))
+    dg = np.zeros((T, k))
+    for e in range(E):
+        t_sel, j_sel = np.nonzero(idx == e)
+        if len(t_sel) == 0:
+            continue
+        rows = src[t_sel, j_sel]
+        y = swiglu_expert(x[rows], W_gu[e], W_down[e])
+        dg[t_sel, j_sel] = np.sum(dO[t_sel] * y, axis=1)
+        dy = g[t_sel, j_sel][:, None] * dO[t_sel]
+        gx, gW, gD = swiglu_expert_backward(x[rows], W_gu[e], W_down[e], dy)
+        np.add.at(dx, rows, gx)
+        dW_gu[e] = gW
+        dW_down[e] = gD
+    dl = gate_backward(logits, idx, gating, dg)
+    Wr = np.asarray(W_r, dtype=np.float64)
+    dx += dl @ Wr.T
+    dW_r = x.T @ dl
+    d_bias = dl.sum(axis=0) if bias is not None else None
+    return dict(dx=dx, d_residual=d_residual, dW_r=dW_r, d_bias=d_bias, dW_gu=dW_gu,
+                dW_down=dW_down, dWs_gu=dWs_gu, dWs_down=dWs_down, idx=idx, rep_of=rep_of)

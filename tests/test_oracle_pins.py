@@ -397,3 +397,130 @@ def test_conditioned_workloads_have_routing_margins():
     for name in ("tiny_fp32", "luffy_condense"):
         cfg, inp = harness.workload(name, T=2048 if name == "luffy_condense" else None)
         assert len(harness.near_tie_tokens(inp, cfg.k)) == 0
+
+
+# ------------------------------------------------------------------ backward
+def _fd_case(gating, residual_mode, tau=None, x_kind=None, T=32):
+    if x_kind is None:
+        cfg, inp = harness.workload("tiny_fp32", T)
+    else:
+        # near-duplicate tokens: half the tokens are copies of 4 centroids plus 2 % noise
+        from dataclasses import replace
+        cfg = replace(gen.CONFIGS["tiny_fp32"], name="tiny_fp32_near_dup", T=T, x_kind=x_kind,
+                      copy_fraction=0.5, n_centroids=4, noise_rel=0.02)
+        inp = harness.condition(cfg, gen.make_inputs(cfg))
+    rng = np.random.default_rng(7)
+    E = cfg.E
+    bias = rng.standard_normal(E) * 0.3 if gating != "sigmoid_topk" else rng.standard_normal(E) * 0.1
+    params = dict(x=inp["x"].astype(np.float64), W_r=inp["W_r"].astype(np.float64), bias=bias,
+                  W_gu=inp["W_gu"].astype(np.float64), W_down=inp["W_down"].astype(np.float64),
+                  Ws_gu=inp["Ws_gu"].astype(np.float64), Ws_down=inp["Ws_down"].astype(np.float64),
+                  residual=inp["residual"].astype(np.float64))
+    d_out = rng.standard_normal((T, cfg.d))
+    return cfg, params, d_out
+
+
+def _loss(cfg, p, d_out, gating, residual_mode, tau):
+    f = orc.layer_forward(p["x"], p["W_r"], p["bias"], p["W_gu"], p["W_down"], p["Ws_gu"],
+                          p["Ws_down"], cfg.k, gating, residual_mode=residual_mode,
+                          residual=p["residual"], tau=tau)
+    return float(np.sum(d_out * f["out"])), f
+
+
+@pytest.mark.parametrize("gating,residual_mode", [("softmax_topk", "input"),
+                                                  ("softmax_topk_renorm", "external"),
+                                                  ("sigmoid_topk", "input_plus_external")])
+def test_backward_matches_finite_differences(gating, residual_mode):
+    """Every gradient against the central difference of the forward's loss <d_out, out> along
+    a random direction (h = 1e-6 moves no routing decision on the margin-conditioned inputs)."""
+    cfg, p, d_out = _fd_case(gating, residual_mode)
+    g = orc.layer_backward(p["x"], p["W_r"], p["bias"], p["W_gu"], p["W_down"], p["Ws_gu"],
+                           p["Ws_down"], cfg.k, gating, d_out, residual_mode=residual_mode,
+                           residual=p["residual"])
+    grads = dict(x=g["dx"], W_r=g["dW_r"], bias=g["d_bias"], W_gu=g["dW_gu"], W_down=g["dW_down"],
+                 Ws_gu=g["dWs_gu"], Ws_down=g["dWs_down"], residual=g["d_residual"])
+    rng = np.random.default_rng(11)
+    h = 1e-6
+    _, f0 = _loss(cfg, p, d_out, gating, residual_mode, None)
+    for name, grad in grads.items():
+        v = rng.standard_normal(p[name].shape)
+        plus = dict(p); plus[name] = p[name] + h * v
+        minus = dict(p); minus[name] = p[name] - h * v
+        lp, fp = _loss(cfg, plus, d_out, gating, residual_mode, None)
+        lm, fm = _loss(cfg, minus, d_out, gating, residual_mode, None)
+        assert np.array_equal(fp["idx"], f0["idx"]) and np.array_equal(fm["idx"], f0["idx"])
+        fd = (lp - lm) / (2 * h)
+        an = 0.0 if grad is None else float(np.sum(grad * v))
+        assert abs(fd - an) <= 1e-6 * max(1.0, abs(fd)), (gating, name, fd, an)
+
+
+def test_backward_with_condensation_matches_finite_differences():
+    """Near-duplicate tokens condensed at tau = 0.95: the finite difference of the forward
+    (which feeds a condensed pair its representative's input) agrees with the gradient,
+    including for the condensed tokens' own inputs."""
+    cfg, p, d_out = _fd_case("softmax_topk", "input", x_kind="centroids", T=48)
+    tau = 0.95
+    g = orc.layer_backward(p["x"], p["W_r"], p["bias"], p["W_gu"], p["W_down"], p["Ws_gu"],
+                           p["Ws_down"], cfg.k, "softmax_topk", d_out, residual_mode="input",
+                           tau=tau)
+    assert np.any(g["rep_of"] != np.arange(len(g["rep_of"])))  # something is condensed
+    rng = np.random.default_rng(3)
+    h = 1e-7
+    _, f0 = _loss(cfg, p, d_out, "softmax_topk", "input", tau)
+    for name, grad in dict(x=g["dx"], W_gu=g["dW_gu"], W_down=g["dW_down"], W_r=g["dW_r"]).items():
+        v = rng.standard_normal(p[name].shape)
+        plus = dict(p); plus[name] = p[name] + h * v
+        minus = dict(p); minus[name] = p[name] - h * v
+        lp, fp = _loss(cfg, plus, d_out, "softmax_topk", "input", tau)
+        lm, fm = _loss(cfg, minus, d_out, "softmax_topk", "input", tau)
+        assert np.array_equal(fp["rep_of"], f0["rep_of"]) and np.array_equal(fm["rep_of"], f0["rep_of"])
+        fd = (lp - lm) / (2 * h)
+        assert abs(fd - float(np.sum(grad * v))) <= 1e-5 * max(1.0, abs(fd)), name
+
+
+def test_backward_condensed_token_gets_no_expert_gradient():
+    """With W_r = 0 (no router gradient reaches x) and no shared experts, a token whose every
+    pair is condensed onto another token's slot receives only the residual's gradient."""
+    cfg, p, d_out = _fd_case("softmax_topk", "input", x_kind="centroids", T=48)
+    W_r = np.zeros_like(p["W_r"])
+    g = orc.layer_backward(p["x"], W_r, None, p["W_gu"], p["W_down"], p["Ws_gu"][:0],
+                           p["Ws_down"][:0], cfg.k, "softmax_topk", d_out, residual_mode="input",
+                           tau=0.95)
+    counts, offsets, perm, slot_of = orc.dispatch(g["idx"], cfg.E)
+    condensed_all = [t for t in range(d_out.shape[0])
+                     if all(g["rep_of"][slot_of[t, j]] != slot_of[t, j] for j in range(cfg.k))]
+    assert condensed_all, "the near-duplicate workload condenses some token in every bucket it visits"
+    checked = 0
+    for t in condensed_all:
+        own = [perm[g["rep_of"][s]] for s in range(len(perm)) if perm[g["rep_of"][s]] == t]
+        if not own:  # t is nobody's representative
+            np.testing.assert_array_equal(g["dx"][t], d_out[t])
+            checked += 1
+    assert checked > 0
+
+
+def test_backward_dense_case_matches_autograd():
+    """k = E identical experts with renormalised gates is one dense SwiGLU FFN: its input
+    gradient and the summed expert weight gradients equal torch autograd's (float64)."""
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    cfg, inp = harness.workload("tiny_fp32", 40)
+    E = 4
+    x = inp["x"].astype(np.float64)
+    W_gu = np.repeat(inp["W_gu"][:1], E, axis=0).astype(np.float64)
+    W_down = np.repeat(inp["W_down"][:1], E, axis=0).astype(np.float64)
+    W_r = inp["W_r"][:, :E].astype(np.float64)
+    d_out = np.random.default_rng(5).standard_normal(x.shape)
+    g = orc.layer_backward(x, W_r, None, W_gu, W_down, np.zeros((0, 2, cfg.d)),
+                           np.zeros((0, cfg.d, 1)), E, "softmax_topk_renorm", d_out,
+                           residual_mode="none")
+    H = cfg.H
+    xt = torch.tensor(x, requires_grad=True)
+    wg = torch.tensor(W_gu[0], requires_grad=True)
+    wd = torch.tensor(W_down[0], requires_grad=True)
+    y = F.linear(F.silu(F.linear(xt, wg[:H])) * F.linear(xt, wg[H:]), wd)
+    (y * torch.tensor(d_out)).sum().backward()
+    np.testing.assert_allclose(g["dx"], xt.grad.numpy(), rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(g["dW_gu"].sum(axis=0), wg.grad.numpy(), rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(g["dW_down"].sum(axis=0), wd.grad.numpy(), rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(g["dW_r"], 0.0, atol=1e-9)
