@@ -261,6 +261,33 @@ moe_status moe_layer_forward_ex(const moe_config* cfg, const moe_weights* w, con
                                 int32_t* topk_idx_out, int32_t* n_condensed_out, void* ws,
                                 size_t ws_bytes, moe_stream_t stream, moe_stream_t aux_stream);
 
+/* ---------------------------------------------------------------- layer backward
+ * Gradients of moe_layer_forward's output (tau > 1: no condensation) for an output
+ * gradient d_out, by the chain rule through the residual base, the shared experts,
+ * the routed experts' gated SwiGLU and the router's gates (the top-k selection passes
+ * no gradient).  The forward pass is recomputed from x (routing, dispatch, the
+ * experts' pre-activations), then the expert gradients run on tcgen05 tensor cores
+ * (bf16 operands, fp32 accumulation).  Each routing group is padded to a multiple of
+ * 64 rows so the weight gradients contract over whole 64-row blocks.  The steps of the
+ * path follow FarSkip-Collective's pre-training execution (review page, Figures 11-12):
+ * router, Dispatch, routed and shared experts, Combine.
+ * bf16 layers only (fp32 layers: MOE_ERR_UNSUPPORTED).
+ *   x [T, d] bf16 (in)   d_out [T, d] bf16 (in)
+ *   d_x [T, d] bf16 (out): gradient w.r.t. x (x also feeds the residual base in the
+ *       input modes), summed in fp32, rounded once
+ *   d_residual [T, d] bf16 or NULL (out): gradient w.r.t. the external residual
+ *       (= d_out; zeros when the mode reads none)
+ *   dW_r [d, E] fp32 (out)   d_bias [E] fp32 or NULL (out; zeros without a router bias)
+ *   dW_gu [E, 2H, d] fp32, dW_down [E, d, H] fp32 (out)
+ *   dWs_gu [S, 2Hs, d], dWs_down [S, d, Hs] fp32 (out; NULL when n_shared == 0)
+ *   ws: moe_layer_backward_workspace_size(cfg) bytes
+ * Deterministic: no atomics; every sum in a fixed order.                       */
+size_t moe_layer_backward_workspace_size(const moe_config* cfg);
+moe_status moe_layer_backward(const moe_config* cfg, const moe_weights* w, const void* x,
+                              const void* d_out, void* d_x, void* d_residual, float* dW_r,
+                              float* d_bias, float* dW_gu, float* dW_down, float* dWs_gu,
+                              float* dWs_down, void* ws, size_t ws_bytes, moe_stream_t stream);
+
 #ifdef __cplusplus
 } /* extern "C" */
 #endif

@@ -395,7 +395,7 @@ def gate_backward(logits, idx, gating, dg):
 
 
 def layer_backward(x, W_r, bias, W_gu, W_down, Ws_gu, Ws_down, k, gating, d_out,
-                   residual_mode="input", residual=None, tau=None):
+                   residual_mode="input", residual=None, tau=None, grad_experts=None):
     """Gradients of layer_forward's output for an output gradient d_out [T, d].
 
     Plain chain rule through the forward's own definition: the residual base, the shared
@@ -406,7 +406,9 @@ def layer_backward(x, W_r, bias, W_gu, W_down, Ws_gu, Ws_down, k, gating, d_out,
     zero.  Its gate still receives dg = <d_out[t], E_e(x[src])>.
 
     Returns dx, d_residual (None unless the mode reads r), dW_r, d_bias (None without a
-    bias), dW_gu, dW_down, dWs_gu, dWs_down, all float64.
+    bias), dW_gu, dW_down, dWs_gu, dWs_down, all float64.  ``grad_experts`` (a list of
+    expert ids) limits dW_gu / dW_down to those experts, returned as dicts keyed by
+    expert (every other output is complete); None returns full arrays.
     """
     x = np.asarray(x, dtype=np.float64)
     dO = np.asarray(d_out, dtype=np.float64)
@@ -428,8 +430,12 @@ def layer_backward(x, W_r, bias, W_gu, W_down, Ws_gu, Ws_down, k, gating, d_out,
         dx += gx
         dWs_gu[s] = gW
         dWs_down[s] = gD
-    dW_gu = np.zeros(np.shape(W_gu))
-    dW_down = np.zeros(np.shape(W_down))
+    if grad_experts is None:
+        dW_gu = np.zeros(np.shape(W_gu))
+        dW_down = np.zeros(np.shape(W_down))
+    else:
+        dW_gu = {e: np.zeros(np.shape(W_gu)[1:]) for e in grad_experts}
+        dW_down = {e: np.zeros(np.shape(W_down)[1:]) for e in grad_experts}
     dg = np.zeros((T, k))
     for e in range(E):
         t_sel, j_sel = np.nonzero(idx == e)
@@ -441,8 +447,9 @@ def layer_backward(x, W_r, bias, W_gu, W_down, Ws_gu, Ws_down, k, gating, d_out,
         dy = g[t_sel, j_sel][:, None] * dO[t_sel]
         gx, gW, gD = swiglu_expert_backward(x[rows], W_gu[e], W_down[e], dy)
         np.add.at(dx, rows, gx)
-        dW_gu[e] = gW
-        dW_down[e] = gD
+        if grad_experts is None or e in dW_gu:
+            dW_gu[e] = gW
+            dW_down[e] = gD
     dl = gate_backward(logits, idx, gating, dg)
     Wr = np.asarray(W_r, dtype=np.float64)
     dx += dl @ Wr.T

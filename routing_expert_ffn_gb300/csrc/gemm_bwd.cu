@@ -1,0 +1,578 @@
+// Backward GEMMs of the routed/shared SwiGLU experts on CTA pairs (tcgen05
+// cta_group::2, sm_103a), with MN-major shared-memory operands where the
+// contraction runs along a tensor's rows.
+//
+// Rows live in the padded slot space: every group (expert) starts at a
+// multiple of 64 rows and its pad rows hold zeros in x_pad and dy_pad, so a
+// K loop over a group's rows needs no masking (zero rows add nothing).
+//
+//   kBwdDH    dh = dy . W_down[e]            token rows x H   (K = d)
+//             A = dy_pad (K-major), B = W_down [E][d][H] read MN-major;
+//             epilogue: dA = [dh * u * SiLU'(a) | dh * SiLU(a)] from the
+//             recomputed pre-activations AU = [a | u] (bf16).
+//   kBwdDX    dz = dA . W_gu[e]              token rows x d   (K = 2H)
+//             A = dA_pad (K-major), B = W_gu [E][2H][d] read MN-major; fp32 out.
+//   kBwdDWD   dW_down[e] = dy^T . h          d x H            (K = rows of e)
+//             A = dy_pad read MN-major, B = h_pad read MN-major; fp32 out.
+//   kBwdDWGU  dW_gu[e] = dA^T . x            2H x d           (K = rows of e)
+//             A = dA_pad read MN-major, B = x_pad read MN-major; fp32 out.
+//
+// An MN-major tile is staged as 64-wide boxes of 64 K rows (128-byte
+// swizzle): the MMA descriptor's leading-byte offset is the stride between
+// 64-wide boxes (8 KB), the stride-byte offset the stride between 8-row K
+// groups (1 KB), and a K step of 16 advances the start by 2 KB.
+//
+// Pair tile: M = 256 (128 rows per CTA), N = 256 or 128 (N/2 rows of B per
+// CTA).  Warp roles, the barrier protocol, bounded waits and the abort path
+// follow the forward pair kernel (gemm_tc.cu).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace bw {
+
+constexpr int BK = 64;
+constexpr int STAGES = 6;
+constexpr int A_BYTES = 128 * BK * 2;  // 16 KB
+constexpr int B_BYTES = 128 * BK * 2;  // 16 KB (N = 256); N = 128 uses half
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_THREADS = 192;
+constexpr int TMEM_COLS = 512;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 3072;
+constexpr int PAIR_GROUP = 8;
+
+struct Shared {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  volatile int abort_flag;
+  int gmb[257];  // token-row modes: first m-tile of each group; weight modes: unused
+  int gpb[257];  // token-row modes: first pair of each group
+};
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Shared* sh,
+                                         unsigned* status) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (sh->abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        sh->abort_flag = 1;
+        record_status(status, MOE_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle; K-major (lbo unused, 16) or
+// MN-major (lbo = stride between 64-wide boxes).
+__device__ __forceinline__ uint64_t desc(uint32_t addr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+
+constexpr bool a_mn(int mode) { return mode == kBwdDWD || mode == kBwdDWGU; }
+constexpr int tile_n(int mode) { return (mode == kBwdDH || mode == kBwdDWD) ? 128 : 256; }
+
+struct Tile {
+  int group;   // expert / shared slice
+  int m0;      // token modes: first token row of this CTA's m-tile; weight modes: first output row of this CTA
+  int nrows;   // token modes: valid rows of this CTA's m-tile (0 for an empty peer half)
+  int n0;      // first output column of the pair tile
+  int k_rows;  // weight modes: first token row of the group (K origin)
+  int n_kb;    // K blocks
+};
+
+// Pair tile -> this CTA's work.  Token modes walk (group, blocks of PAIR_GROUP
+// pairs of m-tiles, N tiles with the pairs fastest) like the forward kernel;
+// weight modes walk (group, output-row tile, output-column tile).
+template <int MODE>
+__device__ __forceinline__ Tile tile_info(const BwdArgs& a, const Shared* sh, int tile,
+                                          uint32_t rank) {
+  Tile t;
+  if (!a_mn(MODE)) {
+    const int NT = a.n_ntiles;
+    int lo = 0, hi = a.n_groups;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (sh->gpb[mid] * NT <= tile) lo = mid; else hi = mid;
+    }
+    const int beg = sh->gpb[lo], cnt = sh->gpb[lo + 1] - beg;
+    const int local = tile - beg * NT;
+    const int blk = local / (PAIR_GROUP * NT);
+    const int within = local - blk * PAIR_GROUP * NT;
+    const int bs = min(PAIR_GROUP, cnt - blk * PAIR_GROUP);
+    const int nt = within / bs;
+    const int pi = blk * PAIR_GROUP + (within - nt * bs);
+    const int m_in_group = 2 * pi + static_cast<int>(rank);
+    const int4 lead = a.mt_info[sh->gmb[lo] + 2 * pi];
+    t.group = lead.x;
+    if (m_in_group < sh->gmb[lo + 1] - sh->gmb[lo]) {
+      const int4 m = a.mt_info[sh->gmb[lo] + m_in_group];
+      t.m0 = m.y;
+      t.nrows = m.z;
+    } else {
+      t.m0 = lead.y + lead.z;
+      t.nrows = 0;
+    }
+    t.n0 = nt * tile_n(MODE);
+    t.k_rows = 0;
+    t.n_kb = a.n_kblocks;
+  } else {
+    const int per_group = a.n_mtiles * a.n_ntiles;
+    t.group = tile / per_group;
+    const int local = tile - t.group * per_group;
+    const int mt = local / a.n_ntiles;
+    const int nt = local - mt * a.n_ntiles;
+    t.m0 = mt * 256 + static_cast<int>(rank) * 128;
+    t.nrows = 128;
+    t.n0 = nt * tile_n(MODE);
+    if (a.group_rows) {
+      t.k_rows = a.group_rows[t.group];
+      t.n_kb = (a.group_rows[t.group + 1] - t.k_rows) / BK;
+    } else {
+      t.k_rows = 0;
+      t.n_kb = a.rows_shared / BK;
+    }
+  }
+  return t;
+}
+
+template <int MODE>
+__device__ __forceinline__ int total_tiles(const BwdArgs& a, const Shared* sh) {
+  if (!a_mn(MODE)) return sh->gpb[a.n_groups] * a.n_ntiles;
+  return a.n_groups * a.n_mtiles * a.n_ntiles;
+}
+
+// This CTA's loads of K block kb (both CTAs complete on the leader's `full`).
+template <int MODE>
+__device__ __forceinline__ void issue_kblock(const BwdArgs& a, const CUtensorMap* tmA,
+                                             const CUtensorMap* tmB, const Tile& t, int kb,
+                                             uint32_t rank, uint32_t full, uint32_t sa,
+                                             uint32_t sb) {
+  const int r = static_cast<int>(rank);
+  if (MODE == kBwdDH) {
+    // A: dy rows, K = d.  B: W_down[slice] rows f (K) x columns h (N), 64 h per CTA.
+    const int slice = t.group + t.n0 / a.n_per_slice;
+    const int h0 = t.n0 - (t.n0 / a.n_per_slice) * a.n_per_slice + r * 64;
+    ptx::tma_load_2d_pair(sa, tmA, full, kb * BK, t.m0);
+    ptx::tma_load_3d_pair(sb, tmB, full, h0, kb * BK, slice);
+  } else if (MODE == kBwdDX) {
+    // A: dA rows, K = 2H (spanning slices for the shared experts).  B: W_gu[slice]
+    // rows j (K) x columns c (N), 128 c per CTA as two 64-wide boxes.
+    const int kslice = kb / a.kb_per_slice;
+    const int kin = (kb - kslice * a.kb_per_slice) * BK;
+    const int c0 = t.n0 + r * 128;
+    ptx::tma_load_2d_pair(sa, tmA, full, kb * BK, t.m0);
+    ptx::tma_load_3d_pair(sb, tmB, full, c0, kin, t.group + kslice);
+    ptx::tma_load_3d_pair(sb + 8192, tmB, full, c0 + 64, kin, t.group + kslice);
+  } else if (MODE == kBwdDWD) {
+    // A: dy^T: rows f of this CTA (two 64-wide boxes), K = the group's token rows.
+    // B: h^T: 64 columns h per CTA.
+    const int krow = t.k_rows + kb * BK;
+    const int hcol = a.b_col0 + t.group * a.b_col_stride + t.n0 + r * 64;
+    ptx::tma_load_2d_pair(sa, tmA, full, t.m0, krow);
+    ptx::tma_load_2d_pair(sa + 8192, tmA, full, t.m0 + 64, krow);
+    ptx::tma_load_2d_pair(sb, tmB, full, hcol, krow);
+  } else {  // kBwdDWGU
+    const int krow = t.k_rows + kb * BK;
+    const int jcol = t.group * a.a_col_stride + t.m0;
+    const int c0 = t.n0 + r * 128;
+    ptx::tma_load_2d_pair(sa, tmA, full, jcol, krow);
+    ptx::tma_load_2d_pair(sa + 8192, tmA, full, jcol + 64, krow);
+    ptx::tma_load_2d_pair(sb, tmB, full, c0, krow);
+    ptx::tma_load_2d_pair(sb + 8192, tmB, full, c0 + 64, krow);
+  }
+}
+
+__device__ __forceinline__ float sigm(float z) { return 1.0f / (1.0f + __expf(-z)); }
+
+__device__ __forceinline__ void unpack8(const uint4& v, float* f) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 p = __bfloat1622float2(h[i]);
+    f[2 * i] = p.x;
+    f[2 * i + 1] = p.y;
+  }
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Epilogue for output row `r` (TMEM lane) of this CTA, columns col0.. of the accumulator.
+template <int MODE>
+__device__ __forceinline__ void epilogue(const BwdArgs& a, const Tile& t, uint32_t col0, int r) {
+  constexpr int NCOL = (MODE == kBwdDH || MODE == kBwdDWD) ? 128 : 256;
+  const bool valid = r < t.nrows;
+  if (MODE == kBwdDH) {
+    // dh for hidden units [n0, n0 + 128) of row m0 + r; AU = [a | u] per slice.
+    const long long row = static_cast<long long>(t.m0) + r;
+    const int slice_local = t.n0 / a.n_per_slice;
+    const int h_in = t.n0 - slice_local * a.n_per_slice;
+    const long long au_base = row * a.ld_au + static_cast<long long>(slice_local) * 2 * a.n_per_slice;
+#pragma unroll 1
+    for (int c = 0; c < NCOL / 32; ++c) {
+      uint32_t v[32];
+      ptx::tmem_ld_32x32b_x32(col0 + c * 32, v);
+      ptx::tmem_ld_wait();
+      if (!valid) continue;
+      const __nv_bfloat16* ap = a.au + au_base + h_in + c * 32;
+      const __nv_bfloat16* up = ap + a.n_per_slice;
+      __nv_bfloat16* dap = a.out_bf16 + row * a.ld_out + (au_base - row * a.ld_au) + h_in + c * 32;
+      __nv_bfloat16* dup = dap + a.n_per_slice;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float av[8], uv[8];
+        unpack8(reinterpret_cast<const uint4*>(ap)[q], av);
+        unpack8(reinterpret_cast<const uint4*>(up)[q], uv);
+        uint32_t pa[4], pu[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float da2[2], du2[2];
+#pragma unroll
+          for (int z = 0; z < 2; ++z) {
+            const int e = 2 * i + z;
+            const float dh = __uint_as_float(v[q * 8 + e]);
+            const float s = sigm(av[e]);
+            da2[z] = dh * uv[e] * (s * (1.0f + av[e] * (1.0f - s)));
+            du2[z] = dh * av[e] * s;
+          }
+          pa[i] = pack2(da2[0], da2[1]);
+          pu[i] = pack2(du2[0], du2[1]);
+        }
+        reinterpret_cast<uint4*>(dap)[q] = make_uint4(pa[0], pa[1], pa[2], pa[3]);
+        reinterpret_cast<uint4*>(dup)[q] = make_uint4(pu[0], pu[1], pu[2], pu[3]);
+      }
+    }
+  } else {
+    float* orow;
+    if (MODE == kBwdDX)
+      orow = a.out_f32 + (static_cast<long long>(t.m0) + r) * a.ld_out + t.n0;
+    else
+      orow = a.out_f32 + static_cast<long long>(t.group) * a.out_group_stride +
+             (static_cast<long long>(t.m0) + r) * a.ld_out + t.n0;
+    // a group without rows (no K blocks) has a zero gradient, not the stale accumulator
+    const bool zero = t.n_kb == 0;
+#pragma unroll 1
+    for (int c = 0; c < NCOL / 32; ++c) {
+      uint32_t v[32];
+      ptx::tmem_ld_32x32b_x32(col0 + c * 32, v);
+      ptx::tmem_ld_wait();
+      if (!valid) continue;
+      if (zero) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0u;
+      }
+      float4* dst = reinterpret_cast<float4*>(orow + c * 32);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                             __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+    }
+  }
+}
+
+}  // namespace bw
+
+template <int MODE>
+__global__ void __launch_bounds__(bw::NUM_THREADS, 1)
+    bwd_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                         const __grid_constant__ CUtensorMap tmB, const BwdArgs args) {
+  using namespace bw;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  Shared* sh = reinterpret_cast<Shared*>(smem + STAGES * STAGE_BYTES);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const uint32_t smem0 = ptx::smem_u32(smem);
+  constexpr int NB = tile_n(MODE);
+  // bytes both CTAs load per stage: A 16 KB each, B N/2 rows each
+  constexpr uint32_t TX = 2u * (A_BYTES + (NB / 2) * BK * 2);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&sh->full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&sh->empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(ptx::smem_u32(&sh->tmem_full[a]), 1);
+      ptx::mbar_init(ptx::smem_u32(&sh->tmem_empty[a]), 8);
+    }
+    ptx::mbar_init(ptx::smem_u32(&sh->drain), 1);
+    sh->abort_flag = 0;
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(ptx::smem_u32(&sh->tmem_base), TMEM_COLS);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  ptx::cluster_sync();
+  ptx::tc_fence_after();
+  pdl_wait();
+  if (!a_mn(MODE)) {
+    for (int g = threadIdx.x; g <= args.n_groups; g += blockDim.x)
+      sh->gmb[g] = args.group_mt_begin[g];
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int run = 0;
+      for (int g = 0; g < args.n_groups; ++g) {
+        sh->gpb[g] = run;
+        run += (sh->gmb[g + 1] - sh->gmb[g] + 1) >> 1;
+      }
+      sh->gpb[args.n_groups] = run;
+    }
+  }
+  __syncthreads();
+  const uint32_t tmem_base = sh->tmem_base;
+  const int n_tiles = total_tiles<MODE>(args, sh);
+  const int cluster = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int tile = cluster; tile < n_tiles && ok; tile += n_clusters) {
+      const Tile t = tile_info<MODE>(args, sh, tile, rank);
+      for (int kb = 0; kb < t.n_kb; ++kb) {
+        if (!wait_bar(ptx::smem_u32(&sh->empty[stage]), phase ^ 1u, sh, args.status)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t full = ptx::smem_u32(&sh->full[stage]) & ptx::kLeaderMask;
+          const uint32_t sa = smem0 + stage * STAGE_BYTES;
+          if (rank == 0) ptx::mbar_arrive_expect_tx(full, TX);
+          bw::issue_kblock<MODE>(args, &tmA, &tmB, t, kb, rank, full, sa, sa + A_BYTES);
+        }
+        __syncwarp();
+        if (++stage == STAGES) stage = 0, phase ^= 1u;
+      }
+    }
+    if (!ok) {
+      const uint64_t t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 200000ull) {
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (leader only)
+    if (rank == 0) {
+      const uint32_t idesc = ptx::idesc_bf16_f32(256, NB) |
+                             (static_cast<uint32_t>(a_mn(MODE)) << 15) | (1u << 16);
+      const uint32_t a_lbo = a_mn(MODE) ? 8192u : 16u;
+      const uint32_t a_step = a_mn(MODE) ? (2048u >> 4) : (32u >> 4);
+      const uint32_t b_step = 2048u >> 4;
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true;
+      for (int tile = cluster; tile < n_tiles && ok; tile += n_clusters, ++local) {
+        const Tile t = tile_info<MODE>(args, sh, tile, rank);
+        const int acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        if (!wait_bar(ptx::smem_u32(&sh->tmem_empty[acc]), acc_phase ^ 1u, sh, args.status)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * 256;
+        for (int kb = 0; kb < t.n_kb; ++kb) {
+          if (!wait_bar(ptx::smem_u32(&sh->full[stage]), phase, sh, args.status)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          if (lane == 0) {
+            const uint32_t sa = smem0 + stage * STAGE_BYTES;
+            const uint64_t adesc = bw::desc(sa, a_lbo);
+            const uint64_t bdesc = bw::desc(sa + A_BYTES, 8192u);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              ptx::umma_bf16_pair(d_tmem, adesc + a_step * kk, bdesc + b_step * kk, idesc,
+                                  (kb > 0 || kk > 0) ? 1u : 0u);
+            ptx::umma_commit_pair(ptx::smem_u32(&sh->empty[stage]), 0x3);
+          }
+          __syncwarp();
+          if (++stage == STAGES) stage = 0, phase ^= 1u;
+        }
+        if (!ok) break;
+        if (lane == 0) ptx::umma_commit_pair(ptx::smem_u32(&sh->tmem_full[acc]), 0x3);
+        __syncwarp();
+      }
+      if (!ok) {
+        if (lane == 0) ptx::umma_commit_pair_local(ptx::smem_u32(&sh->drain));
+        __syncwarp();
+        const uint64_t t0 = globaltimer_ns();
+        while (!ptx::mbar_try_wait(ptx::smem_u32(&sh->drain), 0) &&
+               globaltimer_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5, both CTAs)
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    int local = 0;
+    for (int tile = cluster; tile < n_tiles; tile += n_clusters, ++local) {
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      if (!wait_bar(ptx::smem_u32(&sh->tmem_full[acc]), acc_phase, sh, args.status)) break;
+      ptx::tc_fence_after();
+      const Tile t = tile_info<MODE>(args, sh, tile, rank);
+      bw::epilogue<MODE>(args, t, lane_addr + acc * 256, r);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        const uint32_t e = ptx::smem_u32(&sh->tmem_empty[acc]);
+        if (rank == 0) ptx::mbar_arrive(e);
+        else ptx::mbar_arrive_cluster(ptx::mapa(e, 0));
+      }
+    }
+  }
+
+  pdl_trigger();
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
+}
+
+// ---------------------------------------------------------------- host side
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// bf16 tensor map, 128-byte swizzle, box {64, box_rows[, 1]} over [outer][rows][inner].
+bool make_map(CUtensorMap* m, int rank, const void* base, uint64_t inner, uint64_t rows,
+              uint64_t outer, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {inner, rows, outer};
+  cuuint64_t strides[2] = {inner * 2, inner * rows * 2};
+  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MODE>
+cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const BwdArgs& args, int num_sms,
+                   cudaStream_t stream) {
+  static bool attr_set[64] = {};
+  static int max_clusters[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(bwd_gemm_pair_kernel<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         bw::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t q = {};
+    cudaLaunchAttribute ca;
+    ca.id = cudaLaunchAttributeClusterDimension;
+    ca.val.clusterDim.x = 2;
+    ca.val.clusterDim.y = 1;
+    ca.val.clusterDim.z = 1;
+    q.gridDim = dim3(2 * (num_sms / 2));
+    q.blockDim = dim3(bw::NUM_THREADS);
+    q.dynamicSmemBytes = bw::SMEM_BYTES;
+    q.attrs = &ca;
+    q.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, bwd_gemm_pair_kernel<MODE>, &q) != cudaSuccess || n <= 0)
+      n = num_sms / 2;
+    max_clusters[dev] = n;
+    attr_set[dev] = true;
+  }
+  int clusters = num_sms / 2;
+  if (dev < 64 && max_clusters[dev] < clusters) clusters = max_clusters[dev];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * clusters);
+  cfg.blockDim = dim3(bw::NUM_THREADS);
+  cfg.dynamicSmemBytes = bw::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = 2;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, bwd_gemm_pair_kernel<MODE>, ma, mb, args);
+}
+
+}  // namespace
+
+cudaError_t bwd_gemm(int mode, const BwdGemmOperands& op, const BwdArgs& args, int num_sms,
+                     cudaStream_t stream) {
+  CUtensorMap ma, mb;
+  switch (mode) {
+    case kBwdDH:
+      // A: dy_pad [rows][K]; B: W_down [slices][K = d][N = H] read MN-major (box 64 x 64)
+      if (!make_map(&ma, 2, op.A, op.a_inner, op.a_rows, 1, 128) ||
+          !make_map(&mb, 3, op.B, op.b_inner, op.b_rows, op.b_slices, 64))
+        return cudaErrorInvalidValue;
+      return launch<kBwdDH>(ma, mb, args, num_sms, stream);
+    case kBwdDX:
+      if (!make_map(&ma, 2, op.A, op.a_inner, op.a_rows, 1, 128) ||
+          !make_map(&mb, 3, op.B, op.b_inner, op.b_rows, op.b_slices, 64))
+        return cudaErrorInvalidValue;
+      return launch<kBwdDX>(ma, mb, args, num_sms, stream);
+    case kBwdDWD:
+      if (!make_map(&ma, 2, op.A, op.a_inner, op.a_rows, 1, 64) ||
+          !make_map(&mb, 2, op.B, op.b_inner, op.b_rows, 1, 64))
+        return cudaErrorInvalidValue;
+      return launch<kBwdDWD>(ma, mb, args, num_sms, stream);
+    case kBwdDWGU:
+      if (!make_map(&ma, 2, op.A, op.a_inner, op.a_rows, 1, 64) ||
+          !make_map(&mb, 2, op.B, op.b_inner, op.b_rows, 1, 64))
+        return cudaErrorInvalidValue;
+      return launch<kBwdDWGU>(ma, mb, args, num_sms, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

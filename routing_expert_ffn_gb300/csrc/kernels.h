@@ -113,6 +113,68 @@ cudaError_t tc_gemm(int mode, const void* A, long long a_rows, int K, const void
 constexpr int kTcTileN = 256;
 constexpr int kTcTileK = 64;
 
+// ------------------------------------------------------------------ backward GEMMs (gemm_bwd.cu)
+// Rows in the padded slot space (each group's rows start at a multiple of 64,
+// pad rows zero).  See gemm_bwd.cu for the four products.
+enum BwdMode { kBwdDH = 0, kBwdDX = 1, kBwdDWD = 2, kBwdDWGU = 3 };
+struct BwdArgs {
+  // token-row modes (kBwdDH, kBwdDX): m-tiles over the padded groups
+  const int4* mt_info;
+  const int32_t* group_mt_begin;
+  int n_groups;        // groups (experts, or shared slices for the weight modes)
+  int n_ntiles;        // N tiles (128 columns for kBwdDH/kBwdDWD, 256 otherwise)
+  int n_kblocks;       // token modes: K blocks
+  int n_per_slice;     // kBwdDH: hidden units per weight slice (H or H_shared)
+  int kb_per_slice;    // kBwdDX: K blocks per W_gu slice (2H / 64)
+  // weight modes (kBwdDWD, kBwdDWGU)
+  int n_mtiles;        // output-row tiles of 256 per group
+  const int32_t* group_rows;  // [n_groups + 1] padded row offsets, or NULL: every group spans rows_shared rows from row 0
+  int rows_shared;
+  int a_col_stride;    // kBwdDWGU: A column offset per group (2H_shared for shared slices, 0 routed)
+  int b_col0, b_col_stride;  // kBwdDWD: B column offset = b_col0 + group * b_col_stride
+  // epilogue
+  const __nv_bfloat16* au;  // kBwdDH: recomputed [a | u] per slice, row stride ld_au
+  long long ld_au;
+  __nv_bfloat16* out_bf16;  // kBwdDH: dA, row stride ld_out (= ld_au)
+  float* out_f32;           // other modes
+  long long ld_out;
+  long long out_group_stride;  // weight modes: elements between groups' gradients
+  unsigned* status;
+};
+struct BwdGemmOperands {
+  const void* A;
+  long long a_inner, a_rows;  // A as [a_rows][a_inner] bf16
+  const void* B;
+  long long b_inner, b_rows, b_slices;  // B as [b_slices][b_rows][b_inner] bf16
+};
+cudaError_t bwd_gemm(int mode, const BwdGemmOperands& op, const BwdArgs& args, int num_sms,
+                     cudaStream_t stream);
+
+// ------------------------------------------------------------------ backward support (backward.cu)
+constexpr int kBwdPad = 64;  // group rows start at multiples of this in the padded slot space
+cudaError_t launch_pad_counts(const int32_t* counts, int E, int32_t* pcounts, cudaStream_t st);
+cudaError_t launch_pad_rows(const void* x_perm, const int32_t* offsets, const int32_t* poffsets,
+                            int E, int max_rows, int d, void* x_pad, void* dy_pad, cudaStream_t st);
+cudaError_t launch_pad_tokens(const void* src, int T, int T_pad, int d, void* dst, cudaStream_t st);
+cudaError_t launch_swiglu_from_au(const void* au, const int* n_rows_dev, int rows_max, int S,
+                                  int Hs, void* h, cudaStream_t st);
+cudaError_t launch_combine_bwd(const void* d_out, const void* y_pad, const int32_t* topk_idx,
+                               const int32_t* slot_of, const int32_t* offsets,
+                               const int32_t* poffsets, const float* gate, int T, int d, int k,
+                               void* dy_pad, float* dg, cudaStream_t st);
+cudaError_t launch_router_bwd(const float* logits, const int32_t* topk_idx, const float* gate,
+                              const float* dg, int T, int E, int k, int gating, float* dl,
+                              cudaStream_t st);
+size_t router_bwd_scratch_bytes(int T, int d, int E);
+cudaError_t launch_router_param_grads(const void* x, const float* dl, const float* W_r, int T,
+                                      int d, int E, float* dW_r, float* d_bias, float* dx_router,
+                                      void* scratch, cudaStream_t st);
+cudaError_t launch_dx_assemble(const void* d_out, int add_dout, const float* dx_router,
+                               const float* dz_shared, const float* dz, const int32_t* topk_idx,
+                               const int32_t* slot_of, const int32_t* offsets,
+                               const int32_t* poffsets, int T, int d, int k, void* dx,
+                               cudaStream_t st);
+
 // ------------------------------------------------------------------ fp32 SIMT grouped GEMM
 // Same tables and tile semantics as the tensor-core path, fp32 FMA throughout.
 cudaError_t simt_gemm_swiglu(const float* A, const float* B, int b_slices, int b_rows, int K,

@@ -636,6 +636,324 @@ moe_status moe_layer_forward_ex(const moe_config* cfg, const moe_weights* w, con
 
 }  // extern "C"
 
+// ------------------------------------------------------------------ layer backward
+namespace moe {
+namespace {
+
+struct BwdScratch {
+  float* logits;
+  void* route_ws;
+  int32_t* idx;
+  float* gate;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* perm;
+  int32_t* slot_of;
+  void* x_perm;
+  void* dispatch_ws;
+  int32_t* pcounts;
+  int32_t* poffsets;
+  int4* mt;
+  int32_t* gmb;
+  void* x_pad;
+  void* au;
+  void* h;
+  void* y;
+  void* dy;
+  void* dA;
+  float* dz;
+  float* dg;
+  float* dl;
+  float* dx_router;
+  void* router_ws;
+  // shared experts
+  void* x_s;
+  void* dout_s;
+  void* au_s;
+  void* h_s;
+  void* dA_s;
+  float* dz_s;
+  int4* mt_s;
+  int32_t* gmb_s;
+};
+
+// rows of the padded slot space: every group rounded up to kBwdPad rows
+long long bwd_rows_max(const moe_config* c) {
+  return static_cast<long long>(c->T) * c->k + static_cast<long long>(kBwdPad) * c->E;
+}
+int bwd_tokens_padded(const moe_config* c) { return (c->T + kBwdPad - 1) / kBwdPad * kBwdPad; }
+
+size_t carve_bwd(const moe_config* c, void* ws, BwdScratch* s) {
+  const long long P = static_cast<long long>(c->T) * c->k;
+  const long long R = bwd_rows_max(c);
+  const int Tp = bwd_tokens_padded(c);
+  const size_t d = c->d, H = c->H, S = c->n_shared, Hs = c->H_shared;
+  Carver cv(ws);
+  BwdScratch t;
+  t.logits = cv.take<float>(static_cast<size_t>(c->T) * c->E);
+  t.route_ws = cv.take<char>(route_ws_bytes(c));
+  t.idx = cv.take<int32_t>(P);
+  t.gate = cv.take<float>(P);
+  t.counts = cv.take<int32_t>(c->E);
+  t.offsets = cv.take<int32_t>(c->E + 1);
+  t.perm = cv.take<int32_t>(P);
+  t.slot_of = cv.take<int32_t>(P);
+  t.x_perm = cv.take<__nv_bfloat16>(P * d);
+  t.dispatch_ws = cv.take<char>(dispatch_auto_scratch_bytes(c->T, c->k, c->E));
+  t.pcounts = cv.take<int32_t>(c->E);
+  t.poffsets = cv.take<int32_t>(c->E + 1);
+  t.mt = cv.take<int4>(max_mtiles(R, c->E));
+  t.gmb = cv.take<int32_t>(c->E + 1);
+  t.x_pad = cv.take<__nv_bfloat16>(R * d);
+  t.au = cv.take<__nv_bfloat16>(R * 2 * H);
+  t.h = cv.take<__nv_bfloat16>(R * H);
+  t.y = cv.take<__nv_bfloat16>(R * d);
+  t.dy = cv.take<__nv_bfloat16>(R * d);
+  t.dA = cv.take<__nv_bfloat16>(R * 2 * H);
+  t.dz = cv.take<float>(R * d);
+  t.dg = cv.take<float>(P);
+  t.dl = cv.take<float>(static_cast<size_t>(c->T) * c->E);
+  t.dx_router = cv.take<float>(static_cast<size_t>(c->T) * d);
+  t.router_ws = cv.take<char>(router_bwd_scratch_bytes(c->T, c->d, c->E));
+  t.x_s = t.dout_s = t.au_s = t.h_s = t.dA_s = nullptr;
+  t.dz_s = nullptr;
+  t.mt_s = nullptr;
+  t.gmb_s = nullptr;
+  if (S > 0) {
+    t.x_s = cv.take<__nv_bfloat16>(Tp * d);
+    t.dout_s = cv.take<__nv_bfloat16>(Tp * d);
+    t.au_s = cv.take<__nv_bfloat16>(Tp * S * 2 * Hs);
+    t.h_s = cv.take<__nv_bfloat16>(Tp * S * Hs);
+    t.dA_s = cv.take<__nv_bfloat16>(Tp * S * 2 * Hs);
+    t.dz_s = cv.take<float>(Tp * d);
+    t.mt_s = cv.take<int4>(max_mtiles(Tp, 1));
+    t.gmb_s = cv.take<int32_t>(2);
+  }
+  if (s) *s = t;
+  return cv.off;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" size_t moe_layer_backward_workspace_size(const moe_config* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return 0;
+  return carve_bwd(cfg, nullptr, nullptr);
+}
+
+extern "C" moe_status moe_layer_backward(const moe_config* cfg, const moe_weights* w,
+                                         const void* x, const void* d_out, void* d_x,
+                                         void* d_residual, float* dW_r, float* d_bias,
+                                         float* dW_gu, float* dW_down, float* dWs_gu,
+                                         float* dWs_down, void* ws, size_t ws_bytes,
+                                         moe_stream_t stream) {
+  moe_status s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (cfg->T == 0) return MOE_OK;
+  if (cfg->act_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  s = check_weights(cfg, w);
+  if (s != MOE_OK) return s;
+  MOE_PTR(w->W_r);
+  MOE_OPT_PTR(w->router_bias);
+  MOE_PTR(x);
+  MOE_PTR(d_out);
+  MOE_PTR(d_x);
+  MOE_OPT_PTR(d_residual);
+  MOE_PTR(dW_r);
+  MOE_OPT_PTR(d_bias);
+  MOE_PTR(dW_gu);
+  MOE_PTR(dW_down);
+  if (cfg->n_shared > 0) {
+    MOE_PTR(dWs_gu);
+    MOE_PTR(dWs_down);
+  }
+  MOE_PTR(ws);
+  MOE_REQUIRE(ws_bytes >= moe_layer_backward_workspace_size(cfg), MOE_ERR_WORKSPACE);
+  DeviceInfo* di = device_info();
+  if (!di) return MOE_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int T = cfg->T, d = cfg->d, E = cfg->E, k = cfg->k, H = cfg->H, S = cfg->n_shared,
+            Hs = cfg->H_shared;
+  const long long R = bwd_rows_max(cfg);
+  const int Tp = bwd_tokens_padded(cfg);
+  BwdScratch b;
+  carve_bwd(cfg, ws, &b);
+  const int sms = di->num_sms;
+
+  // forward recompute: routing, dispatch, padded slot space, [a | u], h, y
+  s = run_router(cfg, x, w->W_r, w->router_bias, b.logits, b.idx, b.gate, b.route_ws, di, st);
+  if (s != MOE_OK) return s;
+  MOE_CUDA(launch_dispatch_auto(cfg->act_dtype, x, b.idx, T, d, E, k, b.counts, b.offsets, b.perm,
+                                b.slot_of, b.x_perm, b.dispatch_ws, sms, di->status, st));
+  MOE_CUDA(launch_pad_counts(b.counts, E, b.pcounts, st));
+  MOE_CUDA(launch_build_mtiles(b.pcounts, nullptr, 0, E, b.poffsets, b.mt, b.gmb, st));
+  MOE_CUDA(launch_pad_rows(b.x_perm, b.offsets, b.poffsets, E, static_cast<int>(R), d, b.x_pad,
+                           b.dy, st));
+  {
+    TcGemmArgs a = {};
+    a.status = di->status;
+    a.mt_info = b.mt;
+    a.group_mt_begin = b.gmb;
+    a.n_groups = E;
+    a.n_ntiles = 2 * H / kTcTileN;
+    a.nt_per_slice = a.n_ntiles;
+    a.n_kblocks = d / kTcTileK;
+    a.kb_per_slice = a.n_kblocks;
+    a.out = static_cast<__nv_bfloat16*>(b.au);
+    a.ld_out = 2 * H;
+    MOE_CUDA(tc_gemm(kTcStore, b.x_pad, R, d, w->W_gu, E, 2 * H, d, a, sms, st));
+  }
+  MOE_CUDA(launch_swiglu_from_au(b.au, b.poffsets + E, static_cast<int>(R), 1, H, b.h, st));
+  {
+    TcGemmArgs a = {};
+    a.status = di->status;
+    a.mt_info = b.mt;
+    a.group_mt_begin = b.gmb;
+    a.n_groups = E;
+    a.n_ntiles = d / kTcTileN;
+    a.nt_per_slice = a.n_ntiles;
+    a.n_kblocks = H / kTcTileK;
+    a.kb_per_slice = a.n_kblocks;
+    a.out = static_cast<__nv_bfloat16*>(b.y);
+    a.ld_out = d;
+    MOE_CUDA(tc_gemm(kTcStore, b.h, R, H, w->W_down, E, d, H, a, sms, st));
+  }
+
+  // combine and router backward
+  MOE_CUDA(launch_combine_bwd(d_out, b.y, b.idx, b.slot_of, b.offsets, b.poffsets, b.gate, T, d,
+                              k, b.dy, b.dg, st));
+  MOE_CUDA(launch_router_bwd(b.logits, b.idx, b.gate, b.dg, T, E, k, cfg->gating, b.dl, st));
+  MOE_CUDA(launch_router_param_grads(x, b.dl, w->W_r, T, d, E, dW_r,
+                                     w->router_bias ? d_bias : nullptr, b.dx_router, b.router_ws,
+                                     st));
+  if (d_bias && !w->router_bias) MOE_CUDA(cudaMemsetAsync(d_bias, 0, sizeof(float) * E, st));
+
+  // routed experts
+  {
+    BwdArgs a = {};
+    a.status = di->status;
+    a.mt_info = b.mt;
+    a.group_mt_begin = b.gmb;
+    a.n_groups = E;
+    BwdGemmOperands op = {};
+    // dA = SwiGLU'(dy . W_down)
+    a.n_ntiles = H / 128;
+    a.n_kblocks = d / 64;
+    a.n_per_slice = H;
+    a.au = static_cast<const __nv_bfloat16*>(b.au);
+    a.ld_au = 2 * H;
+    a.out_bf16 = static_cast<__nv_bfloat16*>(b.dA);
+    a.ld_out = 2 * H;
+    op = {b.dy, d, R, w->W_down, H, d, E};
+    MOE_CUDA(bwd_gemm(kBwdDH, op, a, sms, st));
+    // dz = dA . W_gu
+    a.n_ntiles = d / 256;
+    a.n_kblocks = 2 * H / 64;
+    a.kb_per_slice = a.n_kblocks;
+    a.out_f32 = b.dz;
+    a.ld_out = d;
+    op = {b.dA, 2 * H, R, w->W_gu, d, 2 * H, E};
+    MOE_CUDA(bwd_gemm(kBwdDX, op, a, sms, st));
+    // dW_down[e] = dy^T . h
+    a.n_mtiles = d / 256;
+    a.n_ntiles = H / 128;
+    a.group_rows = b.poffsets;
+    a.out_f32 = dW_down;
+    a.ld_out = H;
+    a.out_group_stride = static_cast<long long>(d) * H;
+    op = {b.dy, d, R, b.h, H, R, 1};
+    MOE_CUDA(bwd_gemm(kBwdDWD, op, a, sms, st));
+    // dW_gu[e] = dA^T . x
+    a.n_mtiles = 2 * H / 256;
+    a.n_ntiles = d / 256;
+    a.out_f32 = dW_gu;
+    a.ld_out = d;
+    a.out_group_stride = 2ll * H * d;
+    op = {b.dA, 2 * H, R, b.x_pad, d, R, 1};
+    MOE_CUDA(bwd_gemm(kBwdDWGU, op, a, sms, st));
+  }
+
+  // shared experts: every token, gate 1, so their output gradient is d_out itself
+  if (S > 0) {
+    MOE_CUDA(launch_pad_tokens(x, T, Tp, d, b.x_s, st));
+    MOE_CUDA(launch_pad_tokens(d_out, T, Tp, d, b.dout_s, st));
+    MOE_CUDA(launch_build_mtiles(nullptr, nullptr, Tp, 1, nullptr, b.mt_s, b.gmb_s, st));
+    {
+      TcGemmArgs a = {};
+      a.status = di->status;
+      a.mt_info = b.mt_s;
+      a.group_mt_begin = b.gmb_s;
+      a.n_groups = 1;
+      a.n_ntiles = S * 2 * Hs / kTcTileN;
+      a.nt_per_slice = 2 * Hs / kTcTileN;
+      a.n_kblocks = d / kTcTileK;
+      a.kb_per_slice = a.n_kblocks;
+      a.out = static_cast<__nv_bfloat16*>(b.au_s);
+      a.ld_out = static_cast<long long>(S) * 2 * Hs;
+      MOE_CUDA(tc_gemm(kTcStore, b.x_s, Tp, d, w->Ws_gu, S, 2 * Hs, d, a, sms, st));
+    }
+    MOE_CUDA(launch_swiglu_from_au(b.au_s, nullptr, Tp, S, Hs, b.h_s, st));
+    BwdArgs a = {};
+    a.status = di->status;
+    a.mt_info = b.mt_s;
+    a.group_mt_begin = b.gmb_s;
+    a.n_groups = 1;
+    BwdGemmOperands op = {};
+    a.n_ntiles = S * Hs / 128;
+    a.n_kblocks = d / 64;
+    a.n_per_slice = Hs;
+    a.au = static_cast<const __nv_bfloat16*>(b.au_s);
+    a.ld_au = static_cast<long long>(S) * 2 * Hs;
+    a.out_bf16 = static_cast<__nv_bfloat16*>(b.dA_s);
+    a.ld_out = a.ld_au;
+    op = {b.dout_s, d, Tp, w->Ws_down, Hs, d, S};
+    MOE_CUDA(bwd_gemm(kBwdDH, op, a, sms, st));
+    a.n_ntiles = d / 256;
+    a.n_kblocks = S * 2 * Hs / 64;
+    a.kb_per_slice = 2 * Hs / 64;
+    a.out_f32 = b.dz_s;
+    a.ld_out = d;
+    op = {b.dA_s, static_cast<long long>(S) * 2 * Hs, Tp, w->Ws_gu, d, 2 * Hs, S};
+    MOE_CUDA(bwd_gemm(kBwdDX, op, a, sms, st));
+    BwdArgs g = {};
+    g.status = di->status;
+    g.n_groups = S;
+    g.group_rows = nullptr;
+    g.rows_shared = Tp;
+    g.n_mtiles = d / 256;
+    g.n_ntiles = Hs / 128;
+    g.b_col0 = 0;
+    g.b_col_stride = Hs;
+    g.out_f32 = dWs_down;
+    g.ld_out = Hs;
+    g.out_group_stride = static_cast<long long>(d) * Hs;
+    op = {b.dout_s, d, Tp, b.h_s, static_cast<long long>(S) * Hs, Tp, 1};
+    MOE_CUDA(bwd_gemm(kBwdDWD, op, g, sms, st));
+    g.n_mtiles = 2 * Hs / 256;
+    g.n_ntiles = d / 256;
+    g.a_col_stride = 2 * Hs;
+    g.out_f32 = dWs_gu;
+    g.ld_out = d;
+    g.out_group_stride = 2ll * Hs * d;
+    op = {b.dA_s, static_cast<long long>(S) * 2 * Hs, Tp, b.x_s, d, Tp, 1};
+    MOE_CUDA(bwd_gemm(kBwdDWGU, op, g, sms, st));
+  }
+
+  // input gradient and the residual stream's gradient
+  const bool dout_to_x =
+      cfg->residual == MOE_RES_INPUT || cfg->residual == MOE_RES_INPUT_PLUS_EXTERNAL;
+  MOE_CUDA(launch_dx_assemble(d_out, dout_to_x ? 1 : 0, b.dx_router, S > 0 ? b.dz_s : nullptr,
+                              b.dz, b.idx, b.slot_of, b.offsets, b.poffsets, T, d, k, d_x, st));
+  if (d_residual) {
+    if (cfg->residual == MOE_RES_EXTERNAL || cfg->residual == MOE_RES_INPUT_PLUS_EXTERNAL)
+      MOE_CUDA(cudaMemcpyAsync(d_residual, d_out, static_cast<size_t>(T) * d * 2,
+                               cudaMemcpyDeviceToDevice, st));
+    else
+      MOE_CUDA(cudaMemsetAsync(d_residual, 0, static_cast<size_t>(T) * d * 2, st));
+  }
+  return MOE_OK;
+}
+
 // ------------------------------------------------------------------ dispatch without a workspace
 // For callers that cannot allocate device memory: the dispatch scratch lives
 // in this file-scope device array instead of a caller workspace.  Every GPU

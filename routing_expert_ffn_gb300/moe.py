@@ -32,7 +32,8 @@ EXPORTED = ("moe_status_string", "moe_adaptive_tau", "moe_get_device_status",
             "moe_dispatch_workspace_size", "moe_dispatch", "moe_condense_workspace_size",
             "moe_condense", "moe_expert_ffn_workspace_size", "moe_expert_ffn", "moe_combine",
             "moe_workspace_size", "moe_layer_forward", "moe_layer_forward_ex",
-            "moe_dispatch_static_scratch")
+            "moe_dispatch_static_scratch", "moe_layer_backward_workspace_size",
+            "moe_layer_backward")
 
 
 class MoEError(RuntimeError):
@@ -85,6 +86,8 @@ def lib() -> ctypes.CDLL:
         "moe_layer_forward": (I, [CFG, W, P, P, F, P, P, P, P, S, P]),
         "moe_layer_forward_ex": (I, [CFG, W, P, P, F, P, P, P, P, P, S, P, P]),
         "moe_dispatch_static_scratch": (I, [CFG, P, P, P, P, P, P, P, P]),
+        "moe_layer_backward_workspace_size": (S, [CFG]),
+        "moe_layer_backward": (I, [CFG, W, P, P, P, P, P, P, P, P, P, P, P, S, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -314,6 +317,31 @@ class Layer:
 
 def layer_forward(cfg: Config, w: Weights, x, residual=None, tau: float = math.nan, stream=None):
     return Layer(cfg, w, condense=tau <= 1.0, device=x.device)(x, residual, tau, stream=stream)
+
+
+def layer_backward(cfg: Config, w: Weights, x, d_out, d_residual: bool = False, stream=None) -> dict:
+    """Gradients of the layer output (no condensation) for d_out: dict with d_x,
+    d_residual (or None), dW_r, d_bias (or None), dW_gu, dW_down, dWs_gu, dWs_down (or None)."""
+    dev = x.device
+    f32 = torch.float32
+    c = cfg.c()
+    out = dict(d_x=_empty((cfg.T, cfg.d), cfg.torch_dtype, dev),
+               d_residual=_empty((cfg.T, cfg.d), cfg.torch_dtype, dev) if d_residual else None,
+               dW_r=_empty((cfg.d, cfg.E), f32, dev),
+               d_bias=_empty((cfg.E,), f32, dev) if w.router_bias is not None else None,
+               dW_gu=_empty((cfg.E, 2 * cfg.H, cfg.d), f32, dev),
+               dW_down=_empty((cfg.E, cfg.d, cfg.H), f32, dev),
+               dWs_gu=_empty((cfg.n_shared, 2 * cfg.H_shared, cfg.d), f32, dev) if cfg.n_shared else None,
+               dWs_down=_empty((cfg.n_shared, cfg.d, cfg.H_shared), f32, dev) if cfg.n_shared else None)
+    n = lib().moe_layer_backward_workspace_size(ctypes.byref(c))
+    ws = _workspace(n, dev)
+    wc = w.c()
+    _check(lib().moe_layer_backward(ctypes.byref(c), ctypes.byref(wc), _ptr(x), _ptr(d_out),
+                                    _ptr(out["d_x"]), _ptr(out["d_residual"]), _ptr(out["dW_r"]),
+                                    _ptr(out["d_bias"]), _ptr(out["dW_gu"]), _ptr(out["dW_down"]),
+                                    _ptr(out["dWs_gu"]), _ptr(out["dWs_down"]), _ptr(ws), n,
+                                    _stream(stream)), "moe_layer_backward")
+    return out
 
 
 # ------------------------------------------------------------------ input upload
