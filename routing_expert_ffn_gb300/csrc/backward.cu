@@ -73,26 +73,34 @@ __global__ void __launch_bounds__(256)
 }
 
 // h[row][s][i] = SiLU(a) * u with [a | u] = au[row][s][0..2Hs) (bf16 in, bf16 out).
+// Rows on blockIdx.y (grid-strided), 8 hidden units (16 bytes) per thread.
 __global__ void __launch_bounds__(256)
     swiglu_from_au_kernel(const __nv_bfloat16* __restrict__ au, const int* __restrict__ n_rows_dev,
                           int rows_max, int S, int Hs, __nv_bfloat16* __restrict__ h) {
   pdl_trigger();
   pdl_wait();
   const int rows = n_rows_dev ? min(*n_rows_dev, rows_max) : rows_max;
-  const long long per_row = static_cast<long long>(S) * Hs / 2;  // bf16 pairs per row of h
-  const long long total = static_cast<long long>(rows) * per_row;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long row = i / per_row;
-    const long long w = i - row * per_row;  // pair index inside the row of h
-    const long long s = (2 * w) / Hs;
-    const long long col = 2 * w - s * Hs;
-    const __nv_bfloat16* base = au + row * 2 * S * Hs + s * 2 * Hs + col;
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(base));
-    const float2 u = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(base + Hs));
-    const float h0 = a.x / (1.0f + __expf(-a.x)) * u.x;
-    const float h1 = a.y / (1.0f + __expf(-a.y)) * u.y;
-    *reinterpret_cast<__nv_bfloat162*>(h + row * S * Hs + 2 * w) = __floats2bfloat162_rn(h0, h1);
+  const int vec_per_row = S * Hs / 8;
+  for (int row = blockIdx.y; row < rows; row += gridDim.y) {
+    for (int v = blockIdx.x * blockDim.x + threadIdx.x; v < vec_per_row; v += gridDim.x * blockDim.x) {
+      const int s = (v * 8) / Hs;
+      const int col = v * 8 - s * Hs;
+      const __nv_bfloat16* base = au + static_cast<long long>(row) * 2 * S * Hs + s * 2 * Hs + col;
+      const uint4 av = *reinterpret_cast<const uint4*>(base);
+      const uint4 uv = *reinterpret_cast<const uint4*>(base + Hs);
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&av);
+      const __nv_bfloat162* u2 = reinterpret_cast<const __nv_bfloat162*>(&uv);
+      uint4 out;
+      __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&out);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 a = __bfloat1622float2(a2[i]);
+        const float2 u = __bfloat1622float2(u2[i]);
+        o2[i] = __floats2bfloat162_rn(a.x / (1.0f + __expf(-a.x)) * u.x,
+                                      a.y / (1.0f + __expf(-a.y)) * u.y);
+      }
+      *reinterpret_cast<uint4*>(h + static_cast<long long>(row) * S * Hs + v * 8) = out;
+    }
   }
 }
 
@@ -212,7 +220,8 @@ __global__ void __launch_bounds__(256)
 
 // C[z][m][n] = sum_{k in split z} A(m, k) B(k, n), fp32 FMA; 64 x 64 tiles, 16-deep
 // K steps.  A(m, k) = A[m * sam + k * sak]; B(k, n) = B[k * sbk + n * sbn].
-template <typename TA>
+// KFAST: the staging loads walk K fastest (operands contiguous along K), else M/N fastest.
+template <typename TA, bool KFAST>
 __global__ void __launch_bounds__(256)
     small_gemm_kernel(const TA* __restrict__ A, long long sam, long long sak,
                       const float* __restrict__ B, long long sbk, long long sbn, int M, int N,
@@ -227,7 +236,7 @@ __global__ void __launch_bounds__(256)
   float acc[4][4] = {};
   for (int k0 = k_begin; k0 < k_end; k0 += 16) {
     for (int i = threadIdx.x; i < 16 * 64; i += 256) {
-      const int kk = i >> 6, mm = i & 63;
+      const int kk = KFAST ? (i & 15) : (i >> 6), mm = KFAST ? (i >> 4) : (i & 63);
       const int gk = k0 + kk;
       As[kk][mm] = (gk < k_end && m0 + mm < M)
                        ? Act<TA>::to_f(A[(m0 + mm) * sam + static_cast<long long>(gk) * sak])
@@ -353,9 +362,10 @@ cudaError_t launch_pad_tokens(const void* src, int T, int T_pad, int d, void* ds
 
 cudaError_t launch_swiglu_from_au(const void* au, const int* n_rows_dev, int rows_max, int S,
                                   int Hs, void* h, cudaStream_t st) {
-  const long long total = static_cast<long long>(rows_max) * S * Hs / 2;
-  const int blocks = static_cast<int>(min(static_cast<long long>(16384), (total + 255) / 256));
-  return launch_pdl(swiglu_from_au_kernel, dim3(blocks > 0 ? blocks : 1), dim3(256), 0, st,
+  const int vec_per_row = S * Hs / 8;
+  const int gx = ceil_div(vec_per_row, 256);
+  const int gy = max(1, min(rows_max, 65535));
+  return launch_pdl(swiglu_from_au_kernel, dim3(gx, gy), dim3(256), 0, st,
                     static_cast<const __nv_bfloat16*>(au), n_rows_dev, rows_max, S, Hs,
                     static_cast<__nv_bfloat16*>(h));
 }
@@ -389,7 +399,7 @@ cudaError_t launch_router_param_grads(const void* x, const float* dl, const floa
                                       int d, int E, float* dW_r, float* d_bias, float* dx_router,
                                       void* scratch, cudaStream_t st) {
   // dx_router[T][d] = dl[T][E] . W_r^T   (W_r is [d][E])
-  cudaError_t err = launch_pdl(small_gemm_kernel<float>, dim3(ceil_div(T, 64), ceil_div(d, 64), 1),
+  cudaError_t err = launch_pdl(small_gemm_kernel<float, true>, dim3(ceil_div(T, 64), ceil_div(d, 64), 1),
                                dim3(256), 0, st, dl, static_cast<long long>(E), 1ll, W_r, 1ll,
                                static_cast<long long>(E), T, d, E, E, dx_router);
   if (err != cudaSuccess) return err;
@@ -398,7 +408,7 @@ cudaError_t launch_router_param_grads(const void* x, const float* dl, const floa
   const int k_len = ceil_div(ceil_div(T, splits), 16) * 16;
   const int n_split = ceil_div(T, k_len);
   float* part = static_cast<float*>(scratch);
-  err = launch_pdl(small_gemm_kernel<__nv_bfloat16>, dim3(ceil_div(d, 64), ceil_div(E, 64), n_split),
+  err = launch_pdl(small_gemm_kernel<__nv_bfloat16, false>, dim3(ceil_div(d, 64), ceil_div(E, 64), n_split),
                    dim3(256), 0, st, static_cast<const __nv_bfloat16*>(x), 1ll,
                    static_cast<long long>(d), dl, static_cast<long long>(E), 1ll, d, E, T, k_len,
                    part);

@@ -43,10 +43,11 @@ constexpr int B_BYTES = 128 * BK * 2;  // 16 KB (N = 256); N = 128 uses half
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 512;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 3072;
+constexpr int EPI_STAGE_FLOATS = 32 * 33;  // per epilogue warp
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 3072 + 4 * EPI_STAGE_FLOATS * 4;
 constexpr int PAIR_GROUP = 8;
 
-struct Shared {
+struct Shared {  // must stay below 3072 bytes: the epilogue staging tiles follow it
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
   uint64_t tmem_full[2];
@@ -57,6 +58,8 @@ struct Shared {
   int gmb[257];  // token-row modes: first m-tile of each group; weight modes: unused
   int gpb[257];  // token-row modes: first pair of each group
 };
+
+static_assert(sizeof(Shared) <= 3072, "control block overlaps the epilogue staging tiles");
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Shared* sh,
                                          unsigned* status) {
@@ -219,8 +222,10 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 }
 
 // Epilogue for output row `r` (TMEM lane) of this CTA, columns col0.. of the accumulator.
+// `stage`: this warp's 32 x 33 fp32 staging tile in shared memory.
 template <int MODE>
-__device__ __forceinline__ void epilogue(const BwdArgs& a, const Tile& t, uint32_t col0, int r) {
+__device__ __forceinline__ void epilogue(const BwdArgs& a, const Tile& t, uint32_t col0, int r,
+                                         float* stage) {
   constexpr int NCOL = (MODE == kBwdDH || MODE == kBwdDWD) ? 128 : 256;
   const bool valid = r < t.nrows;
   if (MODE == kBwdDH) {
@@ -264,12 +269,17 @@ __device__ __forceinline__ void epilogue(const BwdArgs& a, const Tile& t, uint32
       }
     }
   } else {
-    float* orow;
+    // fp32 output: each 32-row x 32-column chunk of this warp goes through a padded
+    // shared-memory tile, so every store instruction writes one row's 128 contiguous bytes
+    const int lane = r & 31;
+    const int row_w = r - lane;  // first row of this warp's quarter
+    float* obase;
     if (MODE == kBwdDX)
-      orow = a.out_f32 + (static_cast<long long>(t.m0) + r) * a.ld_out + t.n0;
+      obase = a.out_f32 + (static_cast<long long>(t.m0) + row_w) * a.ld_out + t.n0;
     else
-      orow = a.out_f32 + static_cast<long long>(t.group) * a.out_group_stride +
-             (static_cast<long long>(t.m0) + r) * a.ld_out + t.n0;
+      obase = a.out_f32 + static_cast<long long>(t.group) * a.out_group_stride +
+              (static_cast<long long>(t.m0) + row_w) * a.ld_out + t.n0;
+    const int rows_here = min(32, t.nrows - row_w);  // valid rows of this warp's quarter
     // a group without rows (no K blocks) has a zero gradient, not the stale accumulator
     const bool zero = t.n_kb == 0;
 #pragma unroll 1
@@ -277,16 +287,12 @@ __device__ __forceinline__ void epilogue(const BwdArgs& a, const Tile& t, uint32
       uint32_t v[32];
       ptx::tmem_ld_32x32b_x32(col0 + c * 32, v);
       ptx::tmem_ld_wait();
-      if (!valid) continue;
-      if (zero) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = 0u;
-      }
-      float4* dst = reinterpret_cast<float4*>(orow + c * 32);
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                             __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+      for (int i = 0; i < 32; ++i) stage[lane * 33 + i] = zero ? 0.f : __uint_as_float(v[i]);
+      __syncwarp();
+      for (int i = 0; i < rows_here; ++i)
+        obase[static_cast<long long>(i) * a.ld_out + c * 32 + lane] = stage[i * 33 + lane];
+      __syncwarp();
     }
   }
 }
@@ -440,6 +446,9 @@ __global__ void __launch_bounds__(bw::NUM_THREADS, 1)
     const int q = warp & 3;
     const int r = q * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    // after the control block (Shared, < 3 KB): 4 x 32 x 33 floats, inside SMEM_BYTES
+    float* epi_stage = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + 3072) +
+                       (warp - 2) * EPI_STAGE_FLOATS;
     int local = 0;
     for (int tile = cluster; tile < n_tiles; tile += n_clusters, ++local) {
       const int acc = local & 1;
@@ -447,7 +456,7 @@ __global__ void __launch_bounds__(bw::NUM_THREADS, 1)
       if (!wait_bar(ptx::smem_u32(&sh->tmem_full[acc]), acc_phase, sh, args.status)) break;
       ptx::tc_fence_after();
       const Tile t = tile_info<MODE>(args, sh, tile, rank);
-      bw::epilogue<MODE>(args, t, lane_addr + acc * 256, r);
+      bw::epilogue<MODE>(args, t, lane_addr + acc * 256, r, epi_stage);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) {
