@@ -268,6 +268,31 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     serial = {"ms_per_step": ms_serial, "tokens_per_s": job_tokens_per_s(C.T, world, ms_serial),
               "path": "moe_layer_forward, every kernel on one stream"}
 
+    # The layer's backward (moe_layer_backward) on the same tokens: a seeded output
+    # gradient, one CUDA graph per step, L2 flushed between steps like the forward.
+    backward = None
+    if C.dtype == "bf16" and not condense and not args.no_backward:
+        bwd = moe.Backward(C, w, device=dev)
+        g_out = torch.randn((C.T, C.d), generator=torch.Generator(device=dev).manual_seed(7),
+                            device=dev).to(C.torch_dtype)
+        g_bwd = capture(torch, lambda: bwd(x, g_out))
+        for _ in range(args.warmup):
+            g_bwd.replay()
+        torch.cuda.synchronize()
+        ms_b = max_over_ranks(timed(g_bwd), world, dev)
+        wkb = work(C)
+        b_flops = 2.0 * wkb["ffn_flops"]  # input and weight gradients: 12 d H per pair (+ shared)
+        backward = {"ms_per_step": ms_b, "tokens_per_s": job_tokens_per_s(C.T, world, ms_b),
+                    "algorithmic_TFLOP_s": b_flops / (ms_b / 1e3) / 1e12,
+                    "frac_of_bf16_peak": b_flops / (ms_b / 1e3) / 1e12 /
+                    float(load_peaks()[0].get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])),
+                    "path": "moe_layer_backward (forward recomputed inside), CUDA graph",
+                    "flops_note": "12 d H per routed pair + 12 d H_shared per token and shared "
+                                  "expert; the recompute of the forward (6 d H per pair) is not counted"}
+        st = moe.get_device_status()
+        if st != 0:
+            raise RuntimeError(f"device status after the backward: {moe.status_string(st)}")
+
     # experts that received at least one token (the weights a step has to stream)
     _, idx_chk, _ = moe.route(C, x, w.W_r, w.router_bias)
     active = int((torch.bincount(idx_chk.flatten().long(), minlength=C.E) > 0).sum().item())
@@ -334,6 +359,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         "phases_ms": phases,
         "eq9": eq9_report(ms, phases),
         "serial": serial,
+        "backward": backward,
         "condensed": n_condensed,
         "gpu_launches": launches_per_step(C, condense) * args.steps,
         "clocks": clocks,
@@ -578,6 +604,7 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="dsv2_lite")
+    ap.add_argument("--no-backward", action="store_true", help="skip timing the layer backward")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--reference-tokens", type=int, default=1024)

@@ -319,29 +319,46 @@ def layer_forward(cfg: Config, w: Weights, x, residual=None, tau: float = math.n
     return Layer(cfg, w, condense=tau <= 1.0, device=x.device)(x, residual, tau, stream=stream)
 
 
+class Backward:
+    """The layer's backward with a preallocated workspace and gradient buffers.
+
+    ``bwd(x, d_out)`` is one ``moe_layer_backward`` call on the current stream and
+    returns the gradient dict (the same tensors every call): d_x, d_residual (or None),
+    dW_r, d_bias (or None), dW_gu, dW_down, dWs_gu, dWs_down (or None).
+    """
+
+    def __init__(self, cfg: Config, w: Weights, d_residual: bool = False, device=None):
+        self.cfg, self.w = cfg, w
+        dev = device or w.W_gu.device
+        f32 = torch.float32
+        self._c = cfg.c()
+        self._wc = w.c()
+        self.grads = dict(
+            d_x=_empty((cfg.T, cfg.d), cfg.torch_dtype, dev),
+            d_residual=_empty((cfg.T, cfg.d), cfg.torch_dtype, dev) if d_residual else None,
+            dW_r=_empty((cfg.d, cfg.E), f32, dev),
+            d_bias=_empty((cfg.E,), f32, dev) if w.router_bias is not None else None,
+            dW_gu=_empty((cfg.E, 2 * cfg.H, cfg.d), f32, dev),
+            dW_down=_empty((cfg.E, cfg.d, cfg.H), f32, dev),
+            dWs_gu=_empty((cfg.n_shared, 2 * cfg.H_shared, cfg.d), f32, dev) if cfg.n_shared else None,
+            dWs_down=_empty((cfg.n_shared, cfg.d, cfg.H_shared), f32, dev) if cfg.n_shared else None)
+        self.ws_bytes = int(lib().moe_layer_backward_workspace_size(ctypes.byref(self._c)))
+        self.ws = _workspace(self.ws_bytes, dev)
+
+    def __call__(self, x, d_out, stream=None) -> dict:
+        g = self.grads
+        _check(lib().moe_layer_backward(ctypes.byref(self._c), ctypes.byref(self._wc), _ptr(x),
+                                        _ptr(d_out), _ptr(g["d_x"]), _ptr(g["d_residual"]),
+                                        _ptr(g["dW_r"]), _ptr(g["d_bias"]), _ptr(g["dW_gu"]),
+                                        _ptr(g["dW_down"]), _ptr(g["dWs_gu"]), _ptr(g["dWs_down"]),
+                                        _ptr(self.ws), self.ws_bytes, _stream(stream)),
+               "moe_layer_backward")
+        return g
+
+
 def layer_backward(cfg: Config, w: Weights, x, d_out, d_residual: bool = False, stream=None) -> dict:
-    """Gradients of the layer output (no condensation) for d_out: dict with d_x,
-    d_residual (or None), dW_r, d_bias (or None), dW_gu, dW_down, dWs_gu, dWs_down (or None)."""
-    dev = x.device
-    f32 = torch.float32
-    c = cfg.c()
-    out = dict(d_x=_empty((cfg.T, cfg.d), cfg.torch_dtype, dev),
-               d_residual=_empty((cfg.T, cfg.d), cfg.torch_dtype, dev) if d_residual else None,
-               dW_r=_empty((cfg.d, cfg.E), f32, dev),
-               d_bias=_empty((cfg.E,), f32, dev) if w.router_bias is not None else None,
-               dW_gu=_empty((cfg.E, 2 * cfg.H, cfg.d), f32, dev),
-               dW_down=_empty((cfg.E, cfg.d, cfg.H), f32, dev),
-               dWs_gu=_empty((cfg.n_shared, 2 * cfg.H_shared, cfg.d), f32, dev) if cfg.n_shared else None,
-               dWs_down=_empty((cfg.n_shared, cfg.d, cfg.H_shared), f32, dev) if cfg.n_shared else None)
-    n = lib().moe_layer_backward_workspace_size(ctypes.byref(c))
-    ws = _workspace(n, dev)
-    wc = w.c()
-    _check(lib().moe_layer_backward(ctypes.byref(c), ctypes.byref(wc), _ptr(x), _ptr(d_out),
-                                    _ptr(out["d_x"]), _ptr(out["d_residual"]), _ptr(out["dW_r"]),
-                                    _ptr(out["d_bias"]), _ptr(out["dW_gu"]), _ptr(out["dW_down"]),
-                                    _ptr(out["dWs_gu"]), _ptr(out["dWs_down"]), _ptr(ws), n,
-                                    _stream(stream)), "moe_layer_backward")
-    return out
+    """Gradients of the layer output (no condensation) for d_out (fresh buffers): see Backward."""
+    return Backward(cfg, w, d_residual, x.device)(x, d_out, stream)
 
 
 # ------------------------------------------------------------------ input upload
