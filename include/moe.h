@@ -262,17 +262,20 @@ moe_status moe_layer_forward_ex(const moe_config* cfg, const moe_weights* w, con
                                 size_t ws_bytes, moe_stream_t stream, moe_stream_t aux_stream);
 
 /* ---------------------------------------------------------------- layer backward
- * Gradients of moe_layer_forward's output (tau > 1: no condensation) for an output
- * gradient d_out, by the chain rule through the residual base, the shared experts,
- * the routed experts' gated SwiGLU and the router's gates (the top-k selection passes
- * no gradient).  The forward pass is recomputed from x (routing, dispatch, the
+ * Gradients of moe_layer_forward's output (with the same tau) for an output gradient
+ * d_out, by the chain rule through the residual base, the shared experts, the routed
+ * experts' gated SwiGLU and the router's gates (the top-k selection passes no gradient).
+ * With condensation (tau <= 1) a condensed pair's expert ran on its representative's
+ * input, so that pair's expert gradient reaches the representative's token and none
+ * reaches its own (Luffy review, referee major comment 1); its gate still gets
+ * <d_out, y_rep>.  The forward pass is recomputed from x (routing, dispatch, the
  * experts' pre-activations), then the expert gradients run on tcgen05 tensor cores
  * (bf16 operands, fp32 accumulation).  Each routing group is padded to a multiple of
  * 64 rows so the weight gradients contract over whole 64-row blocks.  The steps of the
  * path follow FarSkip-Collective's pre-training execution (review page, Figures 11-12):
  * router, Dispatch, routed and shared experts, Combine.
- * bf16 layers only (fp32 layers: MOE_ERR_UNSUPPORTED).
- *   x [T, d] bf16 (in)   d_out [T, d] bf16 (in)
+ * bf16 layers only (fp32 layers: MOE_ERR_UNSUPPORTED); condensation needs T*k <= 65536.
+ *   x [T, d] bf16 (in)   d_out [T, d] bf16 (in)   tau: as moe_layer_forward
  *   d_x [T, d] bf16 (out): gradient w.r.t. x (x also feeds the residual base in the
  *       input modes), summed in fp32, rounded once
  *   d_residual [T, d] bf16 or NULL (out): gradient w.r.t. the external residual
@@ -280,11 +283,11 @@ moe_status moe_layer_forward_ex(const moe_config* cfg, const moe_weights* w, con
  *   dW_r [d, E] fp32 (out)   d_bias [E] fp32 or NULL (out; zeros without a router bias)
  *   dW_gu [E, 2H, d] fp32, dW_down [E, d, H] fp32 (out)
  *   dWs_gu [S, 2Hs, d], dWs_down [S, d, Hs] fp32 (out; NULL when n_shared == 0)
- *   ws: moe_layer_backward_workspace_size(cfg) bytes
+ *   ws: moe_layer_backward_workspace_size(cfg, tau <= 1) bytes
  * Deterministic: no atomics; every sum in a fixed order.                       */
-size_t moe_layer_backward_workspace_size(const moe_config* cfg);
+size_t moe_layer_backward_workspace_size(const moe_config* cfg, int with_condensation);
 moe_status moe_layer_backward(const moe_config* cfg, const moe_weights* w, const void* x,
-                              const void* d_out, void* d_x, void* d_residual, float* dW_r,
+                              const void* d_out, float tau, void* d_x, void* d_residual, float* dW_r,
                               float* d_bias, float* dW_gu, float* dW_down, float* dWs_gu,
                               float* dWs_down, void* ws, size_t ws_bytes, moe_stream_t stream);
 

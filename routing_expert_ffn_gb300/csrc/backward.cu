@@ -20,13 +20,15 @@ __global__ void pad_counts_kernel(const int32_t* __restrict__ counts, int E,
   for (int e = threadIdx.x; e < E; e += blockDim.x) pcounts[e] = (counts[e] + kPad - 1) & ~(kPad - 1);
 }
 
-// One warp per padded row q < poffsets[E]: x_pad[q] = x_perm[offsets[e] + q - poffsets[e]] for a
-// real row of group e, zeros for a pad row (whose dy_pad row is zeroed as well).
+// One warp per padded row q < poffsets[E]: x_pad[q] = x_perm[src] for a real row of group e,
+// src = offsets[e] + q - poffsets[e] (or its representative rep_of[src] when condensing: a
+// condensed slot's expert input is its representative's row), zeros for a pad row (whose
+// dy_pad row is zeroed as well).
 template <typename T>
 __global__ void __launch_bounds__(256)
     pad_rows_kernel(const T* __restrict__ x_perm, const int32_t* __restrict__ offsets,
-                    const int32_t* __restrict__ poffsets, int E, int max_rows, int d,
-                    T* __restrict__ x_pad, T* __restrict__ dy_pad) {
+                    const int32_t* __restrict__ poffsets, const int32_t* __restrict__ rep_of,
+                    int E, int max_rows, int d, T* __restrict__ x_pad, T* __restrict__ dy_pad) {
   pdl_trigger();
   pdl_wait();
   const int total = poffsets[E];
@@ -42,8 +44,9 @@ __global__ void __launch_bounds__(256)
     const int i = q - poffsets[lo];
     uint4* dst = reinterpret_cast<uint4*>(x_pad + static_cast<long long>(q) * d);
     if (i < offsets[lo + 1] - offsets[lo]) {
-      const uint4* src =
-          reinterpret_cast<const uint4*>(x_perm + static_cast<long long>(offsets[lo] + i) * d);
+      int slot = offsets[lo] + i;
+      if (rep_of) slot = rep_of[slot];
+      const uint4* src = reinterpret_cast<const uint4*>(x_perm + static_cast<long long>(slot) * d);
       for (int v = lane; v < nv; v += 32) dst[v] = src[v];
     } else {
       uint4* dz = reinterpret_cast<uint4*>(dy_pad + static_cast<long long>(q) * d);
@@ -293,16 +296,50 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Members of every representative slot (the slots condensed onto it), in ascending slot
+// order: mem_list[mem_off[r] .. mem_off[r] + mem_cnt[r]).  One CTA per bucket; thread 0
+// counts and fills sequentially; bucket e's lists lie inside [offsets[e], offsets[e+1])
+// (a bucket has fewer members than slots), so buckets never share an entry.
+__global__ void __launch_bounds__(32)
+    members_kernel(const int32_t* __restrict__ rep_of, const int32_t* __restrict__ offsets,
+                   int32_t* __restrict__ mem_off, int32_t* __restrict__ mem_cnt,
+                   int32_t* __restrict__ mem_list) {
+  pdl_trigger();
+  pdl_wait();
+  if (threadIdx.x != 0) return;
+  const int a = offsets[blockIdx.x], b = offsets[blockIdx.x + 1];
+  for (int s = a; s < b; ++s) mem_cnt[s] = 0;
+  for (int s = a; s < b; ++s)
+    if (rep_of[s] != s) ++mem_cnt[rep_of[s]];
+  int run = a;
+  for (int s = a; s < b; ++s) {
+    mem_off[s] = run;
+    run += mem_cnt[s];
+  }
+  for (int s = a; s < b; ++s) {
+    const int r = rep_of[s];
+    if (r != s) mem_list[mem_off[r]++] = s;  // mem_off[r] runs as the fill cursor ...
+  }
+  for (int s = a; s < b; ++s) mem_off[s] -= mem_cnt[s];  // ... and is moved back to the start
+}
+
 // dx[t] = [d_out[t] if the residual is x] + dx_router[t] + dz_shared[t] + sum_j dz[slot(t, j)],
-// fp32 in that order, rounded once.  One CTA per token, 4 fp32 per thread.
+// fp32 in that order, rounded once.  With condensation the expert-input gradient of a slot
+// belongs to the token whose row the slot read: a representative slot of t adds its own dz
+// and then its members' dz (ascending slot), a condensed slot of t adds nothing.
+// One CTA per token, 4 fp32 per thread.
 template <typename T>
 __global__ void __launch_bounds__(256)
     dx_assemble_kernel(const T* __restrict__ d_out, int add_dout, const float* __restrict__ dx_router,
                        const float* __restrict__ dz_shared, const float* __restrict__ dz,
                        const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ slot_of,
                        const int32_t* __restrict__ offsets, const int32_t* __restrict__ poffsets,
+                       const int32_t* __restrict__ rep_of, const int32_t* __restrict__ mem_off,
+                       const int32_t* __restrict__ mem_cnt, const int32_t* __restrict__ mem_list,
                        int d, int k, T* __restrict__ dx) {
   __shared__ long long s_row[32];
+  __shared__ int s_mem[32][2];  // member range of each pair's slot (representatives only)
+  __shared__ int s_shift[32];   // padded-row shift of the pair's bucket
   const int t = blockIdx.x;
   pdl_trigger();
   pdl_wait();
@@ -310,7 +347,18 @@ __global__ void __launch_bounds__(256)
     const long long p = static_cast<long long>(t) * k + threadIdx.x;
     const int s = slot_of[p];
     const int e = topk_idx[p];
-    s_row[threadIdx.x] = s >= 0 ? static_cast<long long>(s - offsets[e] + poffsets[e]) : -1;
+    const int shift = s >= 0 ? poffsets[e] - offsets[e] : 0;
+    s_shift[threadIdx.x] = shift;
+    s_mem[threadIdx.x][0] = s_mem[threadIdx.x][1] = 0;
+    if (s >= 0 && rep_of && rep_of[s] != s) {
+      s_row[threadIdx.x] = -1;  // condensed: its gradient went to the representative's token
+    } else {
+      s_row[threadIdx.x] = s >= 0 ? static_cast<long long>(s + shift) : -1;
+      if (s >= 0 && rep_of) {
+        s_mem[threadIdx.x][0] = mem_off[s];
+        s_mem[threadIdx.x][1] = mem_off[s] + mem_cnt[s];
+      }
+    }
   }
   __syncthreads();
   const long long rowoff = static_cast<long long>(t) * d;
@@ -331,6 +379,11 @@ __global__ void __launch_bounds__(256)
       if (s < 0) continue;
       const float4 z = *reinterpret_cast<const float4*>(dz + s * d + c);
       acc[0] += z.x; acc[1] += z.y; acc[2] += z.z; acc[3] += z.w;
+      for (int m = s_mem[j][0]; m < s_mem[j][1]; ++m) {
+        const long long ms = static_cast<long long>(mem_list[m]) + s_shift[j];
+        const float4 w = *reinterpret_cast<const float4*>(dz + ms * d + c);
+        acc[0] += w.x; acc[1] += w.y; acc[2] += w.z; acc[3] += w.w;
+      }
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) dx[rowoff + c + i] = Act<T>::from_f(acc[i]);
@@ -344,12 +397,13 @@ cudaError_t launch_pad_counts(const int32_t* counts, int E, int32_t* pcounts, cu
 }
 
 cudaError_t launch_pad_rows(const void* x_perm, const int32_t* offsets, const int32_t* poffsets,
-                            int E, int max_rows, int d, void* x_pad, void* dy_pad,
-                            cudaStream_t st) {
+                            const int32_t* rep_of, int E, int max_rows, int d, void* x_pad,
+                            void* dy_pad, cudaStream_t st) {
   const int blocks = min(ceil_div(max_rows, 8), 8192);
   return launch_pdl(pad_rows_kernel<__nv_bfloat16>, dim3(blocks), dim3(256), 0, st,
-                    static_cast<const __nv_bfloat16*>(x_perm), offsets, poffsets, E, max_rows, d,
-                    static_cast<__nv_bfloat16*>(x_pad), static_cast<__nv_bfloat16*>(dy_pad));
+                    static_cast<const __nv_bfloat16*>(x_perm), offsets, poffsets, rep_of, E,
+                    max_rows, d, static_cast<__nv_bfloat16*>(x_pad),
+                    static_cast<__nv_bfloat16*>(dy_pad));
 }
 
 cudaError_t launch_pad_tokens(const void* src, int T, int T_pad, int d, void* dst,
@@ -429,15 +483,24 @@ cudaError_t launch_router_param_grads(const void* x, const float* dl, const floa
   return err;
 }
 
+cudaError_t launch_members(const int32_t* rep_of, const int32_t* offsets, int E, int32_t* mem_off,
+                           int32_t* mem_cnt, int32_t* mem_list, cudaStream_t st) {
+  return launch_pdl(members_kernel, dim3(E), dim3(32), 0, st, rep_of, offsets, mem_off, mem_cnt,
+                    mem_list);
+}
+
 cudaError_t launch_dx_assemble(const void* d_out, int add_dout, const float* dx_router,
                                const float* dz_shared, const float* dz, const int32_t* topk_idx,
                                const int32_t* slot_of, const int32_t* offsets,
-                               const int32_t* poffsets, int T, int d, int k, void* dx,
+                               const int32_t* poffsets, const int32_t* rep_of,
+                               const int32_t* mem_off, const int32_t* mem_cnt,
+                               const int32_t* mem_list, int T, int d, int k, void* dx,
                                cudaStream_t st) {
   const int threads = min(256, max(32, ceil_div(d / 4, 32) * 32));
   return launch_pdl(dx_assemble_kernel<__nv_bfloat16>, dim3(T), dim3(threads), 0, st,
                     static_cast<const __nv_bfloat16*>(d_out), add_dout, dx_router, dz_shared, dz,
-                    topk_idx, slot_of, offsets, poffsets, d, k, static_cast<__nv_bfloat16*>(dx));
+                    topk_idx, slot_of, offsets, poffsets, rep_of, mem_off, mem_cnt, mem_list, d,
+                    k, static_cast<__nv_bfloat16*>(dx));
 }
 
 }  // namespace moe

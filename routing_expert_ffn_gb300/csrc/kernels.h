@@ -154,7 +154,12 @@ cudaError_t bwd_gemm(int mode, const BwdGemmOperands& op, const BwdArgs& args, i
 constexpr int kBwdPad = 64;  // group rows start at multiples of this in the padded slot space
 cudaError_t launch_pad_counts(const int32_t* counts, int E, int32_t* pcounts, cudaStream_t st);
 cudaError_t launch_pad_rows(const void* x_perm, const int32_t* offsets, const int32_t* poffsets,
-                            int E, int max_rows, int d, void* x_pad, void* dy_pad, cudaStream_t st);
+                            const int32_t* rep_of, int E, int max_rows, int d, void* x_pad,
+                            void* dy_pad, cudaStream_t st);
+// mem_off [P], mem_cnt [P], mem_list [P]: the slots condensed onto each representative
+// slot r are mem_list[mem_off[r] .. mem_off[r] + mem_cnt[r]), ascending.
+cudaError_t launch_members(const int32_t* rep_of, const int32_t* offsets, int E, int32_t* mem_off,
+                           int32_t* mem_cnt, int32_t* mem_list, cudaStream_t st);
 cudaError_t launch_pad_tokens(const void* src, int T, int T_pad, int d, void* dst, cudaStream_t st);
 cudaError_t launch_swiglu_from_au(const void* au, const int* n_rows_dev, int rows_max, int S,
                                   int Hs, void* h, cudaStream_t st);
@@ -172,7 +177,9 @@ cudaError_t launch_router_param_grads(const void* x, const float* dl, const floa
 cudaError_t launch_dx_assemble(const void* d_out, int add_dout, const float* dx_router,
                                const float* dz_shared, const float* dz, const int32_t* topk_idx,
                                const int32_t* slot_of, const int32_t* offsets,
-                               const int32_t* poffsets, int T, int d, int k, void* dx,
+                               const int32_t* poffsets, const int32_t* rep_of,
+                               const int32_t* mem_off, const int32_t* mem_cnt,
+                               const int32_t* mem_list, int T, int d, int k, void* dx,
                                cudaStream_t st);
 
 // ------------------------------------------------------------------ fp32 SIMT grouped GEMM

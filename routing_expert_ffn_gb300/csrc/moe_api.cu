@@ -675,6 +675,14 @@ struct BwdScratch {
   float* dz_s;
   int4* mt_s;
   int32_t* gmb_s;
+  // condensation
+  void* condense_ws;
+  int32_t* rep_of;
+  int32_t* n_rep;
+  int32_t* n_condensed;
+  int32_t* mem_off;
+  int32_t* mem_cnt;
+  int32_t* mem_list;
 };
 
 // rows of the padded slot space: every group rounded up to kBwdPad rows
@@ -683,7 +691,7 @@ long long bwd_rows_max(const moe_config* c) {
 }
 int bwd_tokens_padded(const moe_config* c) { return (c->T + kBwdPad - 1) / kBwdPad * kBwdPad; }
 
-size_t carve_bwd(const moe_config* c, void* ws, BwdScratch* s) {
+size_t carve_bwd(const moe_config* c, bool condense, void* ws, BwdScratch* s) {
   const long long P = static_cast<long long>(c->T) * c->k;
   const long long R = bwd_rows_max(c);
   const int Tp = bwd_tokens_padded(c);
@@ -729,6 +737,17 @@ size_t carve_bwd(const moe_config* c, void* ws, BwdScratch* s) {
     t.mt_s = cv.take<int4>(max_mtiles(Tp, 1));
     t.gmb_s = cv.take<int32_t>(2);
   }
+  t.condense_ws = nullptr;
+  t.rep_of = t.n_rep = t.n_condensed = t.mem_off = t.mem_cnt = t.mem_list = nullptr;
+  if (condense) {
+    t.condense_ws = cv.take<char>(condense_scratch_bytes(c->T, c->k, c->E));
+    t.rep_of = cv.take<int32_t>(P);
+    t.n_rep = cv.take<int32_t>(c->E);
+    t.n_condensed = cv.take<int32_t>(1);
+    t.mem_off = cv.take<int32_t>(P);
+    t.mem_cnt = cv.take<int32_t>(P);
+    t.mem_list = cv.take<int32_t>(P);
+  }
   if (s) *s = t;
   return cv.off;
 }
@@ -736,13 +755,13 @@ size_t carve_bwd(const moe_config* c, void* ws, BwdScratch* s) {
 }  // namespace
 }  // namespace moe
 
-extern "C" size_t moe_layer_backward_workspace_size(const moe_config* cfg) {
+extern "C" size_t moe_layer_backward_workspace_size(const moe_config* cfg, int with_condensation) {
   if (check_cfg(cfg) != MOE_OK) return 0;
-  return carve_bwd(cfg, nullptr, nullptr);
+  return carve_bwd(cfg, with_condensation != 0, nullptr, nullptr);
 }
 
 extern "C" moe_status moe_layer_backward(const moe_config* cfg, const moe_weights* w,
-                                         const void* x, const void* d_out, void* d_x,
+                                         const void* x, const void* d_out, float tau, void* d_x,
                                          void* d_residual, float* dW_r, float* d_bias,
                                          float* dW_gu, float* dW_down, float* dWs_gu,
                                          float* dWs_down, void* ws, size_t ws_bytes,
@@ -751,6 +770,8 @@ extern "C" moe_status moe_layer_backward(const moe_config* cfg, const moe_weight
   if (s != MOE_OK) return s;
   if (cfg->T == 0) return MOE_OK;
   if (cfg->act_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  const bool condense = tau <= 1.0f;
+  if (condense && static_cast<long long>(cfg->T) * cfg->k > 65536) return MOE_ERR_UNSUPPORTED;
   s = check_weights(cfg, w);
   if (s != MOE_OK) return s;
   MOE_PTR(w->W_r);
@@ -768,7 +789,7 @@ extern "C" moe_status moe_layer_backward(const moe_config* cfg, const moe_weight
     MOE_PTR(dWs_down);
   }
   MOE_PTR(ws);
-  MOE_REQUIRE(ws_bytes >= moe_layer_backward_workspace_size(cfg), MOE_ERR_WORKSPACE);
+  MOE_REQUIRE(ws_bytes >= moe_layer_backward_workspace_size(cfg, condense), MOE_ERR_WORKSPACE);
   DeviceInfo* di = device_info();
   if (!di) return MOE_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -777,7 +798,7 @@ extern "C" moe_status moe_layer_backward(const moe_config* cfg, const moe_weight
   const long long R = bwd_rows_max(cfg);
   const int Tp = bwd_tokens_padded(cfg);
   BwdScratch b;
-  carve_bwd(cfg, ws, &b);
+  carve_bwd(cfg, condense, ws, &b);
   const int sms = di->num_sms;
 
   // forward recompute: routing, dispatch, padded slot space, [a | u], h, y
@@ -785,10 +806,17 @@ extern "C" moe_status moe_layer_backward(const moe_config* cfg, const moe_weight
   if (s != MOE_OK) return s;
   MOE_CUDA(launch_dispatch_auto(cfg->act_dtype, x, b.idx, T, d, E, k, b.counts, b.offsets, b.perm,
                                 b.slot_of, b.x_perm, b.dispatch_ws, sms, di->status, st));
+  if (condense) {
+    // Luffy condensation: a condensed slot's expert input is its representative's row
+    MOE_CUDA(launch_condense(static_cast<const __nv_bfloat16*>(b.x_perm), b.offsets,
+                             static_cast<int>(static_cast<long long>(T) * k), d, E, tau, sms,
+                             b.rep_of, b.n_rep, b.n_condensed, b.condense_ws, di->status, st));
+    MOE_CUDA(launch_members(b.rep_of, b.offsets, E, b.mem_off, b.mem_cnt, b.mem_list, st));
+  }
   MOE_CUDA(launch_pad_counts(b.counts, E, b.pcounts, st));
   MOE_CUDA(launch_build_mtiles(b.pcounts, nullptr, 0, E, b.poffsets, b.mt, b.gmb, st));
-  MOE_CUDA(launch_pad_rows(b.x_perm, b.offsets, b.poffsets, E, static_cast<int>(R), d, b.x_pad,
-                           b.dy, st));
+  MOE_CUDA(launch_pad_rows(b.x_perm, b.offsets, b.poffsets, b.rep_of, E, static_cast<int>(R), d,
+                           b.x_pad, b.dy, st));
   {
     TcGemmArgs a = {};
     a.status = di->status;
@@ -943,7 +971,8 @@ extern "C" moe_status moe_layer_backward(const moe_config* cfg, const moe_weight
   const bool dout_to_x =
       cfg->residual == MOE_RES_INPUT || cfg->residual == MOE_RES_INPUT_PLUS_EXTERNAL;
   MOE_CUDA(launch_dx_assemble(d_out, dout_to_x ? 1 : 0, b.dx_router, S > 0 ? b.dz_s : nullptr,
-                              b.dz, b.idx, b.slot_of, b.offsets, b.poffsets, T, d, k, d_x, st));
+                              b.dz, b.idx, b.slot_of, b.offsets, b.poffsets, b.rep_of, b.mem_off,
+                              b.mem_cnt, b.mem_list, T, d, k, d_x, st));
   if (d_residual) {
     if (cfg->residual == MOE_RES_EXTERNAL || cfg->residual == MOE_RES_INPUT_PLUS_EXTERNAL)
       MOE_CUDA(cudaMemcpyAsync(d_residual, d_out, static_cast<size_t>(T) * d * 2,

@@ -86,8 +86,8 @@ def lib() -> ctypes.CDLL:
         "moe_layer_forward": (I, [CFG, W, P, P, F, P, P, P, P, S, P]),
         "moe_layer_forward_ex": (I, [CFG, W, P, P, F, P, P, P, P, P, S, P, P]),
         "moe_dispatch_static_scratch": (I, [CFG, P, P, P, P, P, P, P, P]),
-        "moe_layer_backward_workspace_size": (S, [CFG]),
-        "moe_layer_backward": (I, [CFG, W, P, P, P, P, P, P, P, P, P, P, P, S, P]),
+        "moe_layer_backward_workspace_size": (S, [CFG, I]),
+        "moe_layer_backward": (I, [CFG, W, P, P, F, P, P, P, P, P, P, P, P, P, S, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -327,8 +327,10 @@ class Backward:
     dW_r, d_bias (or None), dW_gu, dW_down, dWs_gu, dWs_down (or None).
     """
 
-    def __init__(self, cfg: Config, w: Weights, d_residual: bool = False, device=None):
+    def __init__(self, cfg: Config, w: Weights, d_residual: bool = False, device=None,
+                 condense: bool = False):
         self.cfg, self.w = cfg, w
+        self.condense = condense
         dev = device or w.W_gu.device
         f32 = torch.float32
         self._c = cfg.c()
@@ -342,13 +344,16 @@ class Backward:
             dW_down=_empty((cfg.E, cfg.d, cfg.H), f32, dev),
             dWs_gu=_empty((cfg.n_shared, 2 * cfg.H_shared, cfg.d), f32, dev) if cfg.n_shared else None,
             dWs_down=_empty((cfg.n_shared, cfg.d, cfg.H_shared), f32, dev) if cfg.n_shared else None)
-        self.ws_bytes = int(lib().moe_layer_backward_workspace_size(ctypes.byref(self._c)))
+        self.ws_bytes = int(lib().moe_layer_backward_workspace_size(ctypes.byref(self._c),
+                                                                    int(condense)))
         self.ws = _workspace(self.ws_bytes, dev)
 
-    def __call__(self, x, d_out, stream=None) -> dict:
+    def __call__(self, x, d_out, tau: float = math.nan, stream=None) -> dict:
+        if tau <= 1.0 and not self.condense:
+            raise ValueError("backward was built without condensation workspace")
         g = self.grads
         _check(lib().moe_layer_backward(ctypes.byref(self._c), ctypes.byref(self._wc), _ptr(x),
-                                        _ptr(d_out), _ptr(g["d_x"]), _ptr(g["d_residual"]),
+                                        _ptr(d_out), tau, _ptr(g["d_x"]), _ptr(g["d_residual"]),
                                         _ptr(g["dW_r"]), _ptr(g["d_bias"]), _ptr(g["dW_gu"]),
                                         _ptr(g["dW_down"]), _ptr(g["dWs_gu"]), _ptr(g["dWs_down"]),
                                         _ptr(self.ws), self.ws_bytes, _stream(stream)),
@@ -356,9 +361,10 @@ class Backward:
         return g
 
 
-def layer_backward(cfg: Config, w: Weights, x, d_out, d_residual: bool = False, stream=None) -> dict:
-    """Gradients of the layer output (no condensation) for d_out (fresh buffers): see Backward."""
-    return Backward(cfg, w, d_residual, x.device)(x, d_out, stream)
+def layer_backward(cfg: Config, w: Weights, x, d_out, d_residual: bool = False,
+                   tau: float = math.nan, stream=None) -> dict:
+    """Gradients of the layer output for d_out (fresh buffers; tau <= 1 condenses): see Backward."""
+    return Backward(cfg, w, d_residual, x.device, condense=tau <= 1.0)(x, d_out, tau, stream)
 
 
 # ------------------------------------------------------------------ input upload

@@ -128,6 +128,27 @@ def test_layer_forward_ex_argument_checks(L):
                                     None, None, None, None, None, 0, None, FAKE) == 0
 
 
+def test_layer_backward_argument_checks(L):
+    lib = L.lib()
+    w = L.moe_weights(FAKE, None, FAKE, FAKE, None, None)
+    c = _cfg(L)
+    need = lib.moe_layer_backward_workspace_size(ctypes.byref(c), 0)
+    assert lib.moe_layer_backward_workspace_size(ctypes.byref(c), 1) > need > 0
+    nan = float("nan")
+    args = lambda cfg, d_out, tau, ws_bytes: (ctypes.byref(cfg), ctypes.byref(w), FAKE, d_out, tau,
+                                              FAKE, None, FAKE, None, FAKE, FAKE, None, None, FAKE,
+                                              ws_bytes, None)
+    assert lib.moe_layer_backward(*args(c, FAKE, nan, need - 1)) == 3      # workspace too small
+    assert lib.moe_layer_backward(*args(c, None, nan, need)) == 1          # no output gradient
+    c32 = _cfg(L, dtype="f32")
+    assert lib.moe_layer_backward(*args(c32, FAKE, nan, 1 << 40)) == 2     # fp32 layers
+    cbig = _cfg(L, T=70000)
+    assert lib.moe_layer_backward(*args(cbig, FAKE, 0.9, 1 << 40)) == 2    # condensing T*k > 65536
+    c0 = _cfg(L, T=0)
+    assert lib.moe_layer_backward(ctypes.byref(c0), ctypes.byref(w), None, None, nan, None, None,
+                                  None, None, None, None, None, None, None, 0, None) == 0
+
+
 def test_zero_tokens_is_a_no_op(L):
     c = _cfg(L, T=0)
     lib = L.lib()
