@@ -401,12 +401,14 @@ __global__ void __launch_bounds__(1024)
   if (threadIdx.x < k) {
     int s = slot_of[static_cast<long long>(t) * k + threadIdx.x];
     if (s >= 0 && s < P && rep_of) s = rep_of[s];
+    float g = gate[static_cast<long long>(t) * k + threadIdx.x];
     if (s < 0 || s >= P) {
       record_status(status, MOE_ERR_DEVICE_INDEX);
-      s = -1;
+      s = 0;  // read a valid row with weight 0: the loop below needs no branch
+      g = 0.f;
     }
     s_row[threadIdx.x] = s;
-    s_g[threadIdx.x] = gate[static_cast<long long>(t) * k + threadIdx.x];
+    s_g[threadIdx.x] = g;
   }
   __syncthreads();
   const long long rowoff = static_cast<long long>(t) * d;
@@ -430,11 +432,11 @@ __global__ void __launch_bounds__(1024)
       for (int i = 0; i < V; ++i) acc[i] += tmp[i];
     }
     if (partial) store_vec_f32<T>(partial + rowoff + v * V, acc);
+    // branch-free over the k routed rows (unrolled, so several row loads are in flight)
+#pragma unroll 4
     for (int j = 0; j < k; ++j) {
-      const long long s = s_row[j];
-      if (s < 0) continue;
       const float g = s_g[j];
-      load_vec_f32<T>(y + s * d + v * V, tmp);
+      load_vec_f32<T>(y + s_row[j] * d + v * V, tmp);
 #pragma unroll
       for (int i = 0; i < V; ++i) acc[i] = fmaf(g, tmp[i], acc[i]);
     }

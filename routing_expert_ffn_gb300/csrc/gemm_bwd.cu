@@ -43,7 +43,8 @@ constexpr int B_BYTES = 128 * BK * 2;  // 16 KB (N = 256); N = 128 uses half
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 512;
-constexpr int EPI_STAGE_FLOATS = 32 * 33;  // per epilogue warp
+// per epilogue warp: 32 x 33 fp32 (gradient chunks) or two 32 x 40 bf16 tiles (kBwdDH)
+constexpr int EPI_STAGE_FLOATS = 32 * 40;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 3072 + 4 * EPI_STAGE_FLOATS * 4;
 constexpr int PAIR_GROUP = 8;
 
@@ -60,6 +61,9 @@ struct Shared {  // must stay below 3072 bytes: the epilogue staging tiles follo
 };
 
 static_assert(sizeof(Shared) <= 3072, "control block overlaps the epilogue staging tiles");
+static_assert(2 * 32 * 40 * 2 <= EPI_STAGE_FLOATS * 4 && 32 * 33 <= EPI_STAGE_FLOATS,
+              "epilogue staging tiles exceed a warp's area");
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory above the per-CTA limit");
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Shared* sh,
                                          unsigned* status) {
@@ -91,13 +95,18 @@ __device__ __forceinline__ uint64_t desc(uint32_t addr, uint32_t lbo) {
 }
 
 constexpr bool a_mn(int mode) { return mode == kBwdDWD || mode == kBwdDWGU; }
-constexpr int tile_n(int mode) { return (mode == kBwdDH || mode == kBwdDWD) ? 128 : 256; }
+// kBwdDH and kBwdDWD tile the hidden units (H per weight slice, a multiple of 128): N = 256,
+// and 128 for the last tile of a slice when H is an odd multiple of 128.
+constexpr bool n_tiles_hidden(int mode) { return mode == kBwdDH || mode == kBwdDWD; }
 
 struct Tile {
   int group;   // expert / shared slice
   int m0;      // token modes: first token row of this CTA's m-tile; weight modes: first output row of this CTA
   int nrows;   // token modes: valid rows of this CTA's m-tile (0 for an empty peer half)
   int n0;      // first output column of the pair tile
+  int ncols;   // output columns of the pair tile (MMA N): 256, or 128 at the end of a slice
+  int sl;      // kBwdDH: weight slice of the tile (shared experts), 0 routed
+  int h_in;    // kBwdDH: first hidden unit of the tile inside its slice
   int k_rows;  // weight modes: first token row of the group (K origin)
   int n_kb;    // K blocks
 };
@@ -134,7 +143,17 @@ __device__ __forceinline__ Tile tile_info(const BwdArgs& a, const Shared* sh, in
       t.m0 = lead.y + lead.z;
       t.nrows = 0;
     }
-    t.n0 = nt * tile_n(MODE);
+    if (MODE == kBwdDH) {
+      t.sl = nt / a.nt_per_slice;
+      t.h_in = (nt - t.sl * a.nt_per_slice) * 256;
+      t.ncols = min(256, a.n_per_slice - t.h_in);
+      t.n0 = t.sl * a.n_per_slice + t.h_in;
+    } else {
+      t.sl = 0;
+      t.h_in = 0;
+      t.ncols = 256;
+      t.n0 = nt * 256;
+    }
     t.k_rows = 0;
     t.n_kb = a.n_kblocks;
   } else {
@@ -145,7 +164,10 @@ __device__ __forceinline__ Tile tile_info(const BwdArgs& a, const Shared* sh, in
     const int nt = local - mt * a.n_ntiles;
     t.m0 = mt * 256 + static_cast<int>(rank) * 128;
     t.nrows = 128;
-    t.n0 = nt * tile_n(MODE);
+    t.n0 = nt * 256;
+    t.ncols = n_tiles_hidden(MODE) ? min(256, a.n_cols - t.n0) : 256;
+    t.sl = 0;
+    t.h_in = 0;
     if (a.group_rows) {
       t.k_rows = a.group_rows[t.group];
       t.n_kb = (a.group_rows[t.group + 1] - t.k_rows) / BK;
@@ -171,11 +193,12 @@ __device__ __forceinline__ void issue_kblock(const BwdArgs& a, const CUtensorMap
                                              uint32_t sb) {
   const int r = static_cast<int>(rank);
   if (MODE == kBwdDH) {
-    // A: dy rows, K = d.  B: W_down[slice] rows f (K) x columns h (N), 64 h per CTA.
-    const int slice = t.group + t.n0 / a.n_per_slice;
-    const int h0 = t.n0 - (t.n0 / a.n_per_slice) * a.n_per_slice + r * 64;
+    // A: dy rows, K = d.  B: W_down[slice] rows f (K) x columns h (N): ncols/2 h per CTA
+    // as 64-wide boxes.
+    const int h0 = t.h_in + r * (t.ncols / 2);
     ptx::tma_load_2d_pair(sa, tmA, full, kb * BK, t.m0);
-    ptx::tma_load_3d_pair(sb, tmB, full, h0, kb * BK, slice);
+    for (int b = 0; b < t.ncols / 128; ++b)
+      ptx::tma_load_3d_pair(sb + b * 8192, tmB, full, h0 + 64 * b, kb * BK, t.group + t.sl);
   } else if (MODE == kBwdDX) {
     // A: dA rows, K = 2H (spanning slices for the shared experts).  B: W_gu[slice]
     // rows j (K) x columns c (N), 128 c per CTA as two 64-wide boxes.
@@ -189,10 +212,11 @@ __device__ __forceinline__ void issue_kblock(const BwdArgs& a, const CUtensorMap
     // A: dy^T: rows f of this CTA (two 64-wide boxes), K = the group's token rows.
     // B: h^T: 64 columns h per CTA.
     const int krow = t.k_rows + kb * BK;
-    const int hcol = a.b_col0 + t.group * a.b_col_stride + t.n0 + r * 64;
+    const int hcol = a.b_col0 + t.group * a.b_col_stride + t.n0 + r * (t.ncols / 2);
     ptx::tma_load_2d_pair(sa, tmA, full, t.m0, krow);
     ptx::tma_load_2d_pair(sa + 8192, tmA, full, t.m0 + 64, krow);
-    ptx::tma_load_2d_pair(sb, tmB, full, hcol, krow);
+    for (int b = 0; b < t.ncols / 128; ++b)
+      ptx::tma_load_2d_pair(sb + b * 8192, tmB, full, hcol + 64 * b, krow);
   } else {  // kBwdDWGU
     const int krow = t.k_rows + kb * BK;
     const int jcol = t.group * a.a_col_stride + t.m0;
@@ -222,33 +246,63 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 }
 
 // Epilogue for output row `r` (TMEM lane) of this CTA, columns col0.. of the accumulator.
-// `stage`: this warp's 32 x 33 fp32 staging tile in shared memory.
+// `stage`: this warp's EPI_STAGE_FLOATS-float staging area in shared memory.
 template <int MODE>
 __device__ __forceinline__ void epilogue(const BwdArgs& a, const Tile& t, uint32_t col0, int r,
                                          float* stage) {
-  constexpr int NCOL = (MODE == kBwdDH || MODE == kBwdDWD) ? 128 : 256;
+  const int NCOL = t.ncols;
   const bool valid = r < t.nrows;
   if (MODE == kBwdDH) {
-    // dh for hidden units [n0, n0 + 128) of row m0 + r; AU = [a | u] per slice.
-    const long long row = static_cast<long long>(t.m0) + r;
-    const int slice_local = t.n0 / a.n_per_slice;
-    const int h_in = t.n0 - slice_local * a.n_per_slice;
-    const long long au_base = row * a.ld_au + static_cast<long long>(slice_local) * 2 * a.n_per_slice;
+    // dh for hidden units [n0, n0 + 128) of this warp's 32 rows; AU = [a | u] per slice.
+    // Per 32-column chunk the warp brings a and u of its 32 rows into shared memory with
+    // 4 lanes per row (64 contiguous bytes each), every thread turns its row into
+    // [da | du] in place, and the warp writes them back the same way.
+    const int lane = r & 31;
+    const int row_w = r - lane;
+    const int rows_here = min(32, t.nrows - row_w);
+    const long long col_a = static_cast<long long>(t.sl) * 2 * a.n_per_slice + t.h_in;
+    const long long row0 = static_cast<long long>(t.m0) + row_w;
+    // two 32 x 32 bf16 tiles (a, u) with rows padded to 40 elements (80 bytes: 16-byte
+    // aligned rows; the 4-lane row accesses of a quarter-warp hit distinct banks)
+    __nv_bfloat16* ta = reinterpret_cast<__nv_bfloat16*>(stage);
+    __nv_bfloat16* tu = ta + 32 * 40;
+    const int lr = lane >> 2, lseg = lane & 3;  // cooperative access: row lr + 8 i, 16-byte segment lseg
+    // [a, u] of the next chunk are loaded into registers while the current one is
+    // computed, so a chunk's global loads overlap the previous chunk's work.
+    uint4 na[4], nu[4];
+    auto load_au = [&](int c) {
+      const long long col = col_a + c * 32;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int rr = lr + 8 * i;
+        na[i] = nu[i] = make_uint4(0, 0, 0, 0);
+        if (rr < rows_here) {
+          const __nv_bfloat16* src = a.au + (row0 + rr) * a.ld_au + col + lseg * 8;
+          na[i] = *reinterpret_cast<const uint4*>(src);
+          nu[i] = *reinterpret_cast<const uint4*>(src + a.n_per_slice);
+        }
+      }
+    };
+    load_au(0);
 #pragma unroll 1
     for (int c = 0; c < NCOL / 32; ++c) {
       uint32_t v[32];
       ptx::tmem_ld_32x32b_x32(col0 + c * 32, v);
       ptx::tmem_ld_wait();
-      if (!valid) continue;
-      const __nv_bfloat16* ap = a.au + au_base + h_in + c * 32;
-      const __nv_bfloat16* up = ap + a.n_per_slice;
-      __nv_bfloat16* dap = a.out_bf16 + row * a.ld_out + (au_base - row * a.ld_au) + h_in + c * 32;
-      __nv_bfloat16* dup = dap + a.n_per_slice;
+      const long long col = col_a + c * 32;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int rr = lr + 8 * i;
+        *reinterpret_cast<uint4*>(ta + rr * 40 + lseg * 8) = na[i];
+        *reinterpret_cast<uint4*>(tu + rr * 40 + lseg * 8) = nu[i];
+      }
+      if (c + 1 < NCOL / 32) load_au(c + 1);
+      __syncwarp();
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         float av[8], uv[8];
-        unpack8(reinterpret_cast<const uint4*>(ap)[q], av);
-        unpack8(reinterpret_cast<const uint4*>(up)[q], uv);
+        unpack8(*reinterpret_cast<const uint4*>(ta + lane * 40 + q * 8), av);
+        unpack8(*reinterpret_cast<const uint4*>(tu + lane * 40 + q * 8), uv);
         uint32_t pa[4], pu[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -257,16 +311,28 @@ __device__ __forceinline__ void epilogue(const BwdArgs& a, const Tile& t, uint32
           for (int z = 0; z < 2; ++z) {
             const int e = 2 * i + z;
             const float dh = __uint_as_float(v[q * 8 + e]);
-            const float s = sigm(av[e]);
-            da2[z] = dh * uv[e] * (s * (1.0f + av[e] * (1.0f - s)));
-            du2[z] = dh * av[e] * s;
+            const float sg = sigm(av[e]);
+            da2[z] = dh * uv[e] * (sg * (1.0f + av[e] * (1.0f - sg)));
+            du2[z] = dh * av[e] * sg;
           }
           pa[i] = pack2(da2[0], da2[1]);
           pu[i] = pack2(du2[0], du2[1]);
         }
-        reinterpret_cast<uint4*>(dap)[q] = make_uint4(pa[0], pa[1], pa[2], pa[3]);
-        reinterpret_cast<uint4*>(dup)[q] = make_uint4(pu[0], pu[1], pu[2], pu[3]);
+        *reinterpret_cast<uint4*>(ta + lane * 40 + q * 8) = make_uint4(pa[0], pa[1], pa[2], pa[3]);
+        *reinterpret_cast<uint4*>(tu + lane * 40 + q * 8) = make_uint4(pu[0], pu[1], pu[2], pu[3]);
       }
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int rr = lr + 8 * i;
+        if (rr < rows_here) {
+          __nv_bfloat16* dst = a.out_bf16 + (row0 + rr) * a.ld_out + col + lseg * 8;
+          *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(ta + rr * 40 + lseg * 8);
+          *reinterpret_cast<uint4*>(dst + a.n_per_slice) =
+              *reinterpret_cast<const uint4*>(tu + rr * 40 + lseg * 8);
+        }
+      }
+      __syncwarp();
     }
   } else {
     // fp32 output: each 32-row x 32-column chunk of this warp goes through a padded
@@ -312,9 +378,7 @@ __global__ void __launch_bounds__(bw::NUM_THREADS, 1)
   const int lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();
   const uint32_t smem0 = ptx::smem_u32(smem);
-  constexpr int NB = tile_n(MODE);
-  // bytes both CTAs load per stage: A 16 KB each, B N/2 rows each
-  constexpr uint32_t TX = 2u * (A_BYTES + (NB / 2) * BK * 2);
+  // bytes both CTAs load per stage: A 16 KB each, B ncols/2 rows each
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -367,6 +431,7 @@ __global__ void __launch_bounds__(bw::NUM_THREADS, 1)
     bool ok = true;
     for (int tile = cluster; tile < n_tiles && ok; tile += n_clusters) {
       const Tile t = tile_info<MODE>(args, sh, tile, rank);
+      const uint32_t TX = 2u * static_cast<uint32_t>(A_BYTES + (t.ncols / 2) * BK * 2);
       for (int kb = 0; kb < t.n_kb; ++kb) {
         if (!wait_bar(ptx::smem_u32(&sh->empty[stage]), phase ^ 1u, sh, args.status)) {
           ok = false;
@@ -390,8 +455,7 @@ __global__ void __launch_bounds__(bw::NUM_THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader only)
     if (rank == 0) {
-      const uint32_t idesc = ptx::idesc_bf16_f32(256, NB) |
-                             (static_cast<uint32_t>(a_mn(MODE)) << 15) | (1u << 16);
+      const uint32_t idesc_flags = (static_cast<uint32_t>(a_mn(MODE)) << 15) | (1u << 16);
       const uint32_t a_lbo = a_mn(MODE) ? 8192u : 16u;
       const uint32_t a_step = a_mn(MODE) ? (2048u >> 4) : (32u >> 4);
       const uint32_t b_step = 2048u >> 4;
@@ -401,6 +465,7 @@ __global__ void __launch_bounds__(bw::NUM_THREADS, 1)
       bool ok = true;
       for (int tile = cluster; tile < n_tiles && ok; tile += n_clusters, ++local) {
         const Tile t = tile_info<MODE>(args, sh, tile, rank);
+        const uint32_t idesc = ptx::idesc_bf16_f32(256, t.ncols) | idesc_flags;
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
         if (!wait_bar(ptx::smem_u32(&sh->tmem_empty[acc]), acc_phase ^ 1u, sh, args.status)) {
@@ -446,7 +511,7 @@ __global__ void __launch_bounds__(bw::NUM_THREADS, 1)
     const int q = warp & 3;
     const int r = q * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    // after the control block (Shared, < 3 KB): 4 x 32 x 33 floats, inside SMEM_BYTES
+    // after the control block (Shared, < 3 KB): 4 x EPI_STAGE_FLOATS floats, inside SMEM_BYTES
     float* epi_stage = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + 3072) +
                        (warp - 2) * EPI_STAGE_FLOATS;
     int local = 0;

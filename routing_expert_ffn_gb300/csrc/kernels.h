@@ -122,9 +122,11 @@ struct BwdArgs {
   const int4* mt_info;
   const int32_t* group_mt_begin;
   int n_groups;        // groups (experts, or shared slices for the weight modes)
-  int n_ntiles;        // N tiles (128 columns for kBwdDH/kBwdDWD, 256 otherwise)
+  int n_ntiles;        // N tiles of 256 columns (kBwdDH/kBwdDWD: per slice, the last may be 128)
   int n_kblocks;       // token modes: K blocks
   int n_per_slice;     // kBwdDH: hidden units per weight slice (H or H_shared)
+  int nt_per_slice;    // kBwdDH: N tiles per slice, ceil(n_per_slice / 256)
+  int n_cols;          // kBwdDWD: output columns per group (H or H_shared)
   int kb_per_slice;    // kBwdDX: K blocks per W_gu slice (2H / 64)
   // weight modes (kBwdDWD, kBwdDWGU)
   int n_mtiles;        // output-row tiles of 256 per group

@@ -865,7 +865,8 @@ extern "C" moe_status moe_layer_backward(const moe_config* cfg, const moe_weight
     a.n_groups = E;
     BwdGemmOperands op = {};
     // dA = SwiGLU'(dy . W_down)
-    a.n_ntiles = H / 128;
+    a.nt_per_slice = (H + 255) / 256;
+    a.n_ntiles = a.nt_per_slice;
     a.n_kblocks = d / 64;
     a.n_per_slice = H;
     a.au = static_cast<const __nv_bfloat16*>(b.au);
@@ -884,7 +885,8 @@ extern "C" moe_status moe_layer_backward(const moe_config* cfg, const moe_weight
     MOE_CUDA(bwd_gemm(kBwdDX, op, a, sms, st));
     // dW_down[e] = dy^T . h
     a.n_mtiles = d / 256;
-    a.n_ntiles = H / 128;
+    a.n_ntiles = (H + 255) / 256;
+    a.n_cols = H;
     a.group_rows = b.poffsets;
     a.out_f32 = dW_down;
     a.ld_out = H;
@@ -927,7 +929,8 @@ extern "C" moe_status moe_layer_backward(const moe_config* cfg, const moe_weight
     a.group_mt_begin = b.gmb_s;
     a.n_groups = 1;
     BwdGemmOperands op = {};
-    a.n_ntiles = S * Hs / 128;
+    a.nt_per_slice = (Hs + 255) / 256;
+    a.n_ntiles = S * a.nt_per_slice;
     a.n_kblocks = d / 64;
     a.n_per_slice = Hs;
     a.au = static_cast<const __nv_bfloat16*>(b.au_s);
@@ -949,7 +952,8 @@ extern "C" moe_status moe_layer_backward(const moe_config* cfg, const moe_weight
     g.group_rows = nullptr;
     g.rows_shared = Tp;
     g.n_mtiles = d / 256;
-    g.n_ntiles = Hs / 128;
+    g.n_ntiles = (Hs + 255) / 256;
+    g.n_cols = Hs;
     g.b_col0 = 0;
     g.b_col_stride = Hs;
     g.out_f32 = dWs_down;
