@@ -320,6 +320,14 @@ __global__ void __launch_bounds__(256)
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int lane = threadIdx.x & 31;
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T_tok; t += warps) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<long long>(t) * d);
+    // the row's first chunk does not depend on the routing: start reading it now
+    uint4 r[kRowChunk];
+#pragma unroll
+    for (int u = 0; u < kRowChunk; ++u) {
+      const int v = u * 32 + lane;
+      if (v < nv) r[u] = src[v];
+    }
     int slot = -1;
     if (lane < k) {
       const int p = t * k + lane;
@@ -335,13 +343,13 @@ __global__ void __launch_bounds__(256)
       slot_of[p] = slot;
       if (slot >= 0) perm[slot] = t;
     }
-    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<long long>(t) * d);
     for (int v0 = 0; v0 < nv; v0 += 32 * kRowChunk) {
-      uint4 r[kRowChunk];
+      if (v0 > 0) {
 #pragma unroll
-      for (int u = 0; u < kRowChunk; ++u) {
-        const int v = v0 + u * 32 + lane;
-        if (v < nv) r[u] = src[v];
+        for (int u = 0; u < kRowChunk; ++u) {
+          const int v = v0 + u * 32 + lane;
+          if (v < nv) r[u] = src[v];
+        }
       }
       for (int j = 0; j < k; ++j) {
         const int s = __shfl_sync(0xffffffffu, slot, j);
