@@ -90,6 +90,7 @@ struct TileInfo {
   int nrows;  // valid rows (<= 128)
   int gbase;  // first row of the group (bucket offset)
   int nt;     // N tile (or column tile for kSimBits)
+  int tail = 0;  // CTA-pair kernel: 1 for a tail tile (weights as M, the m-tile's rows as N)
 };
 
 template <int MODE>
@@ -211,6 +212,61 @@ __device__ __forceinline__ void ffn_epilogue(const TcGemmArgs& args, const TileI
 #pragma unroll
         for (int v = 0; v < 8; ++v)
           dst[v] = make_uint4(p[4 * v], p[4 * v + 1], p[4 * v + 2], p[4 * v + 3]);
+      }
+    }
+  }
+}
+
+// Tail tile of the CTA-pair kernel: the accumulator is transposed, TMEM lane =
+// weight row of this CTA's 128-row half of the N tile, column = token of the
+// tail (t.nrows <= 128 of them).  Warp quarter q holds lanes [32q, 32q + 32).
+//   kSwiGLU  lanes 32q + j (j < 16) are gate rows and lanes 32q + 16 + j the up
+//            rows of hidden unit 64 rank + 16 q + j of the tile, so a lane and
+//            its partner 16 apart swap half of each 32-token chunk: the low lane
+//            ends with (gate, up) of tokens 0..15 of the chunk, the high lane
+//            with those of tokens 16..31.
+//   kStore   lane 32q + j is output column 128 rank + 32 q + j of the N tile.
+template <int MODE>
+__device__ __forceinline__ void tail_epilogue(const TcGemmArgs& args, const TileInfo& t,
+                                              uint32_t col0, int q, int lane, uint32_t rank) {
+  const int n = t.nrows;
+  if (MODE == kSwiGLU) {
+    const bool hi = lane >= 16;
+    const long long col = static_cast<long long>(t.nt) * (BN / 2) + 64 * static_cast<int>(rank) +
+                          16 * q + (lane & 15);
+    __nv_bfloat16* out = args.out + col;
+#pragma unroll 1
+    for (int c0 = 0; c0 < n; c0 += 32) {
+      uint32_t v[32];
+      ptx::tmem_ld_32x32b_x32(col0 + c0, v);
+      ptx::tmem_ld_wait();
+      const int cb = c0 + (hi ? 16 : 0);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t other = __shfl_xor_sync(0xffffffffu, hi ? v[i] : v[16 + i], 16);
+        const float g = __uint_as_float(hi ? other : v[i]);
+        const float u = __uint_as_float(hi ? v[16 + i] : other);
+        if (cb + i < n)
+          out[(static_cast<long long>(t.row0) + cb + i) * args.ld_out] =
+              __float2bfloat16_rn(silu_f(g) * u);
+      }
+    }
+  } else {
+    const long long col = static_cast<long long>(t.nt) * BN + 128 * static_cast<int>(rank) +
+                          32 * q + lane;
+    __nv_bfloat16* out = args.out + col;
+#pragma unroll 1
+    for (int c0 = 0; c0 < n; c0 += 32) {
+      uint32_t v[32];
+      ptx::tmem_ld_32x32b_x32(col0 + c0, v);
+      ptx::tmem_ld_wait();
+      // lane i looks up the output row of token c0 + i
+      long long my_row = static_cast<long long>(t.row0) + c0 + lane;
+      if (args.out_rowmap && c0 + lane < n) my_row = args.out_rowmap[my_row];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const long long orow = __shfl_sync(0xffffffffu, my_row, i);
+        if (c0 + i < n) out[orow * args.ld_out] = __float2bfloat16_rn(__uint_as_float(v[i]));
       }
     }
   }
@@ -475,16 +531,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 //   empty[s]      both CTAs; the leader's MMA commit arrives on both
 //   tmem_full[a]  both CTAs; the leader's commit arrives on both
 //   tmem_empty[a] leader only; 4 epilogue warps of each CTA arrive (8)
-// A pair tile is two consecutive m-tiles of one group; when the group has an
-// odd number of m-tiles, the peer's half of its last pair tile has no rows
-// (it still loads its B half, computes, and stores nothing).
+// A pair tile is two consecutive m-tiles of one group.  When a group ends in a
+// single m-tile (1 to 128 rows left after its pairs), that m-tile runs as a
+// tail tile with the roles of the operands swapped: A is the 256 weight rows
+// of the N tile (128 per CTA), B is the left-over rows (N = their count
+// rounded up to 16, half in each CTA), so D is transposed in TMEM.  An MMA
+// issue costs about the same for any N, so the tail saves no tensor time; it
+// saves the load of the pair's second 128 token rows (its tokens come in one
+// 64-row box per CTA), which in a pair would be rows past the group's end.
+//   kSwiGLU tail A rows, per CTA: for q = 0..3, 16 gate rows then 16 up rows
+//           of hidden units 64 rank + 16 q + [0, 16) of the tile (tail_epilogue),
+//           one TMA box of a 5-D view of the gate/up weights.
+//   kStore  tail A rows: the same 128 weight rows the CTA loads as B in a pair tile.
 namespace pr {
 constexpr int STAGES = 6;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = (BN / 2) * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 3072;
+constexpr int SHARED_BYTES = 4096;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + SHARED_BYTES;
 constexpr int PAIR_GROUP = M_GROUP / 2;
+constexpr int TAIL_ROWS = BM / 2;  // token rows a CTA loads for a tail tile (box height)
+constexpr int TAIL_W_ROWS = 16;    // hidden units per gate (or up) run of a kSwiGLU tail
+constexpr int TAIL_TX = 2 * (A_BYTES + TAIL_ROWS * BK * 2);  // both CTAs, one K block
+static_assert(TAIL_ROWS * BK * 2 <= B_BYTES, "tail tokens fit the B region");
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 
 struct Shared {
   uint64_t full[STAGES];
@@ -494,9 +565,11 @@ struct Shared {
   uint64_t drain;
   uint32_t tmem_base;
   volatile int abort_flag;
-  int gmb[257];  // first m-tile of each group
-  int gpb[257];  // first pair of each group
+  int gmb[257];    // first m-tile of each group
+  int gub[257];    // first unit (pair or tail) of each group
+  int gpt[256];    // pairs of each group | rows of its tail (0..128) << 16
 };
+static_assert(sizeof(Shared) <= SHARED_BYTES, "pair kernel barriers and tables");
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Shared* sh,
                                          unsigned* status) {
@@ -515,60 +588,70 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Shared* 
   }
 }
 
-// Pair tile -> this CTA's m-tile.  Groups are walked in order; inside a group,
-// blocks of PAIR_GROUP pairs, N tiles with the pairs fastest.
+// Tile -> this CTA's part.  Groups are walked in order; inside a group, blocks
+// of PAIR_GROUP units (pairs first, then tails), N tiles with the units
+// fastest, so a group's tails run beside its pairs and share their weights in L2.
 __device__ __forceinline__ TileInfo tile_info(const TcGemmArgs& a, const Shared* sh, int tile,
                                               uint32_t rank) {
   const int NT = a.n_ntiles;
   int lo = 0, hi = a.n_groups;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (sh->gpb[mid] * NT <= tile) lo = mid; else hi = mid;
+    if (sh->gub[mid] * NT <= tile) lo = mid; else hi = mid;
   }
-  const int beg = sh->gpb[lo], cnt = sh->gpb[lo + 1] - beg;
+  const int beg = sh->gub[lo], cnt = sh->gub[lo + 1] - beg;
   const int local = tile - beg * NT;
   const int blk = local / (PAIR_GROUP * NT);
   const int within = local - blk * PAIR_GROUP * NT;
   const int bs = min(PAIR_GROUP, cnt - blk * PAIR_GROUP);
   const int nt = within / bs;
-  const int pi = blk * PAIR_GROUP + (within - nt * bs);
-  const int m_in_group = 2 * pi + static_cast<int>(rank);
+  const int u = blk * PAIR_GROUP + (within - nt * bs);
+  const int np = sh->gpt[lo] & 0xffff;
+  const bool tail = u >= np;
+  const int4 m = a.mt_info[sh->gmb[lo] + (tail ? 2 * np : 2 * u + static_cast<int>(rank))];
   TileInfo t;
   t.nt = nt;
-  if (m_in_group < sh->gmb[lo + 1] - sh->gmb[lo]) {
-    const int4 m = a.mt_info[sh->gmb[lo] + m_in_group];
-    t.slice = m.x;
-    t.row0 = m.y;
-    t.nrows = m.z;
-    t.gbase = m.w;
-  } else {
-    const int4 m = a.mt_info[sh->gmb[lo] + 2 * pi];  // the leader's m-tile
-    t.slice = m.x;
-    t.row0 = m.y + BM;
-    t.nrows = 0;
-    t.gbase = m.w;
-  }
+  t.slice = m.x;
+  t.row0 = m.y;
+  t.nrows = tail ? sh->gpt[lo] >> 16 : m.z;
+  t.gbase = m.w;
+  t.tail = tail ? 1 : 0;
   return t;
 }
 
-// This CTA's loads of K block kb: its A rows and its half of B, completing on
-// the leader's barrier `full`.
+// This CTA's loads of K block kb, completing on the leader's barrier `full`:
+// for a pair tile its A rows and its half of the B tile; for a tail tile its
+// 128 weight rows (into the A region) and its half of the tail's token rows
+// (into the B region).
 template <int MODE>
 __device__ __forceinline__ void issue_kblock(const TcGemmArgs& args, const CUtensorMap* tmA,
-                                             const CUtensorMap* tmB, const TileInfo& t, int kb,
+                                             const CUtensorMap* tmB, const CUtensorMap* tmA64,
+                                             const CUtensorMap* tmW5, const TileInfo& t, int kb,
                                              uint32_t rank, uint32_t full, uint32_t sa,
                                              uint32_t sb) {
   const int kslice = kb / args.kb_per_slice;
   const int kin = (kb - kslice * args.kb_per_slice) * BK;
   const int nslice = t.nt / args.nt_per_slice;
   const int z = t.slice + nslice + kslice;
-  ptx::tma_load_2d_pair(sa, tmA, full, kb * BK, t.row0);
+  if (t.tail) {
+    const int half = ((t.nrows + 15) & ~15) >> 1;
+    ptx::tma_load_2d_pair(sb, tmA64, full, kb * BK, t.row0 + static_cast<int>(rank) * half);
+  } else {
+    ptx::tma_load_2d_pair(sa, tmA, full, kb * BK, t.row0);
+  }
+  const uint32_t dw = t.tail ? sa : sb;  // the weights' region
   if (MODE == kSwiGLU) {
-    const int n0 = (t.nt - nslice * args.nt_per_slice) * (BN / 2);
-    ptx::tma_load_3d_pair(sb, tmB, full, kin, (rank ? args.b_up_offset : 0) + n0, z);
+    const int ntl = (t.nt - nslice * args.nt_per_slice) * (BN / 2);
+    if (t.tail) {
+      // box {64 K, 16 units, gate|up, 4 runs}: smem rows [q][gate|up][16]
+      ptx::tma_load_5d_pair(dw, tmW5, full, kin, 0, 0,
+                            (ntl + 64 * static_cast<int>(rank)) / TAIL_W_ROWS, z);
+    } else {
+      ptx::tma_load_3d_pair(dw, tmB, full, kin, (rank ? args.b_up_offset : 0) + ntl, z);
+    }
   } else {
     const int n0 = (t.nt - nslice * args.nt_per_slice) * BN + static_cast<int>(rank) * (BN / 2);
-    ptx::tma_load_3d_pair(sb, tmB, full, kin, n0, z);
+    ptx::tma_load_3d_pair(dw, tmB, full, kin, n0, z);
   }
 }
 }  // namespace pr
@@ -576,7 +659,9 @@ __device__ __forceinline__ void issue_kblock(const TcGemmArgs& args, const CUten
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
-                             const __grid_constant__ CUtensorMap tmB, const TcGemmArgs args) {
+                             const __grid_constant__ CUtensorMap tmB,
+                             const __grid_constant__ CUtensorMap tmA64,
+                             const __grid_constant__ CUtensorMap tmW5, const TcGemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -603,6 +688,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&tmA);
     ptx::prefetch_tmap(&tmB);
+    ptx::prefetch_tmap(&tmA64);
+    ptx::prefetch_tmap(&tmW5);
   }
   if (warp == 1) {
     ptx::tmem_alloc_pair(ptx::smem_u32(&sh->tmem_base), TMEM_COLS);
@@ -614,17 +701,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   pdl_wait();
   for (int g = threadIdx.x; g <= args.n_groups; g += blockDim.x) sh->gmb[g] = args.group_mt_begin[g];
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int run = 0;
-    for (int g = 0; g < args.n_groups; ++g) {
-      sh->gpb[g] = run;
-      run += (sh->gmb[g + 1] - sh->gmb[g] + 1) >> 1;
+  // Units of each group: pairs of m-tiles, then a tail if a single m-tile is left.
+  for (int g = threadIdx.x; g < args.n_groups; g += blockDim.x) {
+    const int m = sh->gmb[g + 1] - sh->gmb[g];
+    int np = 0, tail_rows = 0;
+    if (m > 0) {
+      const int rows = (m - 1) * BM + args.mt_info[sh->gmb[g + 1] - 1].z;
+      np = m >> 1;
+      tail_rows = (m & 1) ? rows - np * 2 * BM : 0;
     }
-    sh->gpb[args.n_groups] = run;
+    sh->gpt[g] = np | (tail_rows << 16);
+    sh->gub[g] = np + (tail_rows > 0 ? 1 : 0);  // units, turned into offsets below
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // exclusive scan of the unit counts, lane l owning groups [8 l, 8 l + 8)
+    const int per = (args.n_groups + 31) >> 5;
+    const int g0 = lane * per;
+    int sum = 0;
+    for (int i = 0; i < per; ++i)
+      if (g0 + i < args.n_groups) sum += sh->gub[g0 + i];
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - sum;
+    __syncwarp();
+    for (int i = 0; i < per; ++i) {
+      if (g0 + i < args.n_groups) {
+        const int c = sh->gub[g0 + i];
+        sh->gub[g0 + i] = run;
+        run += c;
+      }
+    }
+    if (lane == 31) sh->gub[args.n_groups] = incl;
   }
   __syncthreads();
   const uint32_t tmem_base = sh->tmem_base;
-  const int n_tiles = sh->gpb[args.n_groups] * args.n_ntiles;
+  const int n_tiles = sh->gub[args.n_groups] * args.n_ntiles;
   const int cluster = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
 
   if (warp == 0) {
@@ -642,8 +758,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
           const uint32_t full = ptx::smem_u32(&sh->full[stage]) & ptx::kLeaderMask;
           const uint32_t sa = smem0 + stage * pr::STAGE_BYTES;
-          if (rank == 0) ptx::mbar_arrive_expect_tx(full, 2 * pr::STAGE_BYTES);
-          pr::issue_kblock<MODE>(args, &tmA, &tmB, t, kb, rank, full, sa, sa + pr::A_BYTES);
+          if (rank == 0)
+            ptx::mbar_arrive_expect_tx(full, t.tail ? pr::TAIL_TX : 2 * pr::STAGE_BYTES);
+          pr::issue_kblock<MODE>(args, &tmA, &tmB, &tmA64, &tmW5, t, kb, rank, full, sa,
+                                 sa + pr::A_BYTES);
         }
         __syncwarp();
         if (++stage == pr::STAGES) stage = 0, phase ^= 1u;
@@ -658,12 +776,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader only)
     if (rank == 0) {
-      const uint32_t idesc = ptx::idesc_bf16_f32(2 * BM, BN);
+      const uint32_t idesc_pair = ptx::idesc_bf16_f32(2 * BM, BN);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
       for (int tile = cluster; tile < n_tiles && ok; tile += n_clusters, ++local) {
+        const TileInfo t = pr::tile_info(args, sh, tile, 0);
+        const uint32_t idesc =
+            t.tail ? ptx::idesc_bf16_f32(2 * BM, (t.nrows + 15) & ~15) : idesc_pair;
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
         if (!pr::wait_bar(ptx::smem_u32(&sh->tmem_empty[acc]), acc_phase ^ 1u, sh, args.status)) {
@@ -716,7 +837,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!pr::wait_bar(ptx::smem_u32(&sh->tmem_full[acc]), acc_phase, sh, args.status)) break;
       ptx::tc_fence_after();
       const TileInfo t = pr::tile_info(args, sh, tile, rank);
-      ffn_epilogue<MODE>(args, t, lane_addr + acc * BN, r, r < t.nrows);
+      if (t.tail) tail_epilogue<MODE>(args, t, lane_addr + acc * BN, q, lane, rank);
+      else ffn_epilogue<MODE>(args, t, lane_addr + acc * BN, r, r < t.nrows);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -765,9 +887,30 @@ static bool make_map(CUtensorMap* m, int rank, const void* base, uint64_t inner,
   return r == CUDA_SUCCESS;
 }
 
+// 5-D view of gate/up weights [slices][2H][K] for the kSwiGLU tail tiles:
+// {K, unit in a run of 16, gate|up, run, slice}, box {64, 16, 2, 4, 1}, so one
+// load puts, for four runs of 16 hidden units, 16 gate rows then 16 up rows.
+static bool make_gate_up_map(CUtensorMap* m, const void* base, uint64_t K, uint64_t H,
+                             uint64_t slices) {
+  auto fn = encode_fn();
+  if (!fn || H % pr::TAIL_W_ROWS != 0) return false;
+  const uint64_t row = K * 2;
+  cuuint64_t dims[5] = {K, static_cast<cuuint64_t>(pr::TAIL_W_ROWS), 2, H / pr::TAIL_W_ROWS,
+                        slices};
+  cuuint64_t strides[4] = {row, H * row, pr::TAIL_W_ROWS * row, 2 * H * row};
+  cuuint32_t box[5] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(pr::TAIL_W_ROWS), 2,
+                       4, 1};
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <int MODE>
-static cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const TcGemmArgs& args,
-                               int num_sms, cudaStream_t stream) {
+static cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& a64,
+                               const CUtensorMap& w5, const TcGemmArgs& args, int num_sms,
+                               cudaStream_t stream) {
   static bool attr_set[64] = {};
   static int max_clusters[64] = {};
   int dev = 0;
@@ -812,7 +955,7 @@ static cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<MODE>, a, b, args);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<MODE>, a, b, a64, w5, args);
 }
 
 template <int MODE>
@@ -845,9 +988,15 @@ cudaError_t tc_gemm(int mode, const void* A, long long a_rows, int K, const void
                             : mode == tc::kRouter ? static_cast<uint32_t>(args.router_n)
                                                   : tc::BN;
   if (!tc::make_map(&mb, 3, B, b_cols, b_rows, b_slices, box_rows)) return cudaErrorInvalidValue;
+  // Tail tiles: a 64-row token box, and for kSwiGLU the interleaved gate/up view.
+  CUtensorMap ma64, mw5 = mb;
+  if (pair && !tc::make_map(&ma64, 2, A, K, a_rows, 1, tc::pr::TAIL_ROWS))
+    return cudaErrorInvalidValue;
+  if (mode == tc::kSwiGLU && !tc::make_gate_up_map(&mw5, B, b_cols, args.b_up_offset, b_slices))
+    return cudaErrorInvalidValue;
   switch (mode) {
-    case tc::kSwiGLU: return tc::launch_pair<tc::kSwiGLU>(ma, mb, args, grid, stream);
-    case tc::kStore: return tc::launch_pair<tc::kStore>(ma, mb, args, grid, stream);
+    case tc::kSwiGLU: return tc::launch_pair<tc::kSwiGLU>(ma, mb, ma64, mw5, args, grid, stream);
+    case tc::kStore: return tc::launch_pair<tc::kStore>(ma, mb, ma64, mw5, args, grid, stream);
     case tc::kSimBits: return tc::launch<tc::kSimBits>(ma, mb, args, grid, stream);
     case tc::kRouter: return tc::launch<tc::kRouter>(ma, mb, args, grid, stream);
   }

@@ -137,6 +137,37 @@ def test_expert_ffn_full_size(moe, name):
     _ffn_check(moe, name, None)
 
 
+# Group sizes around every tile boundary of the expert GEMMs: empty, one row, and one short of,
+# at and one past 16, 128, 256, 384 and 512 rows, so that every way a group splits into
+# 256-row pair tiles and tail tiles of at most 128 rows (N rounded up to 16) occurs.
+GROUP_SIZES = [0, 1, 15, 16, 17, 127, 128, 129, 255, 256, 257, 383, 384, 385, 511, 512, 513, 200]
+
+
+def test_expert_ffn_group_sizes_every_row(moe):
+    T = 700
+    cfg, inp, C, w, x, r = _setup(moe, "dsv2_lite", T=T)
+    P = cfg.P
+    sizes = GROUP_SIZES + [0] * (cfg.E - len(GROUP_SIZES))
+    sizes[-1] = P - sum(GROUP_SIZES)
+    assert sizes[-1] > 0
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    _, rows_inp = harness.workload("dsv2_lite", P)  # any bf16 rows; weights do not depend on T
+    rows = rows_inp["x"]
+    x_perm = torch.from_numpy(rows).to(device=x.device, dtype=C.torch_dtype)
+    off_d = torch.from_numpy(offsets).to(x.device)
+    y, _ = moe.expert_ffn(C, w, x_perm, off_d, None, x)
+    torch.cuda.synchronize()
+    yg = _np(y)
+    for e, n in enumerate(sizes):
+        if n == 0:
+            continue
+        sl = slice(int(offsets[e]), int(offsets[e + 1]))
+        ref = orc.swiglu_expert(rows[sl], inp["W_gu"][e], inp["W_down"][e])
+        err = harness.max_rel_err(yg[sl], ref)
+        assert err <= harness.tolerance(cfg), (e, n, err)
+    _status_ok(moe)
+
+
 # ------------------------------------------------------------------ combine / round trip
 def test_round_trip_identity_experts(moe):
     """dispatch -> identity experts (y = x_perm) -> combine with gates summing to 1 == x."""
