@@ -44,6 +44,7 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 512;
 // per epilogue warp: 32 x 33 fp32 (gradient chunks) or two 32 x 40 bf16 tiles (kBwdDH)
+// (the fp32 path's full quarters use the first 4 KB as a {32, 32} TMA store box)
 constexpr int EPI_STAGE_FLOATS = 32 * 40;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 3072 + 4 * EPI_STAGE_FLOATS * 4;
 constexpr int PAIR_GROUP = 8;
@@ -64,6 +65,9 @@ static_assert(sizeof(Shared) <= 3072, "control block overlaps the epilogue stagi
 static_assert(2 * 32 * 40 * 2 <= EPI_STAGE_FLOATS * 4 && 32 * 33 <= EPI_STAGE_FLOATS,
               "epilogue staging tiles exceed a warp's area");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory above the per-CTA limit");
+static_assert(32 * 32 * 4 <= EPI_STAGE_FLOATS * 4 && (EPI_STAGE_FLOATS * 4) % 1024 == 0 &&
+                  (STAGES * STAGE_BYTES + 3072) % 1024 == 0,
+              "each warp's staging area holds a 1024-byte-aligned {32, 32} fp32 TMA box");
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Shared* sh,
                                          unsigned* status) {
@@ -249,7 +253,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 // `stage`: this warp's EPI_STAGE_FLOATS-float staging area in shared memory.
 template <int MODE>
 __device__ __forceinline__ void epilogue(const BwdArgs& a, const Tile& t, uint32_t col0, int r,
-                                         float* stage) {
+                                         float* stage, const CUtensorMap* tmO) {
   const int NCOL = t.ncols;
   const bool valid = r < t.nrows;
   if (MODE == kBwdDH) {
@@ -335,19 +339,54 @@ __device__ __forceinline__ void epilogue(const BwdArgs& a, const Tile& t, uint32
       __syncwarp();
     }
   } else {
-    // fp32 output: each 32-row x 32-column chunk of this warp goes through a padded
-    // shared-memory tile, so every store instruction writes one row's 128 contiguous bytes
     const int lane = r & 31;
     const int row_w = r - lane;  // first row of this warp's quarter
+    const int rows_here = min(32, t.nrows - row_w);  // valid rows of this warp's quarter
+    // a group without rows (no K blocks) has a zero gradient, not the stale accumulator
+    const bool zero = t.n_kb == 0;
+    if (rows_here == 32) {
+      // fp32 output of a full quarter: each 32 x 32 chunk is written to shared memory in
+      // the 128-byte-swizzled layout of a {32, 32} TMA box (thread = row, eight 16-byte
+      // stores to distinct banks per quarter-warp) and stored by one TMA bulk store
+      const int orow = MODE == kBwdDX
+                           ? t.m0 + row_w
+                           : static_cast<int>(t.group * a.out_group_rows) + t.m0 + row_w;
+      uint8_t* my_row = reinterpret_cast<uint8_t*>(stage) + lane * 128;
+      const uint32_t src = ptx::smem_u32(stage);
+#pragma unroll 1
+      for (int c = 0; c < NCOL / 32; ++c) {
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(col0 + c * 32, v);
+        ptx::tmem_ld_wait();
+        if (c > 0) {
+          if (lane == 0) ptx::bulk_wait_read0();  // the previous chunk's store has read the box
+          __syncwarp();
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint4 q = zero ? make_uint4(0, 0, 0, 0)
+                               : make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          *reinterpret_cast<uint4*>(my_row + ((j ^ (lane & 7)) << 4)) = q;
+        }
+        ptx::fence_proxy_async_smem_cta();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tma_store_2d(tmO, src, t.n0 + c * 32, orow);
+          ptx::bulk_commit();
+        }
+      }
+      if (lane == 0) ptx::bulk_wait_read0();  // the box is free for the next tile
+      __syncwarp();
+      return;
+    }
+    // a partial quarter: each 32-row x 32-column chunk goes through a padded shared-memory
+    // tile, so every store instruction writes one row's 128 contiguous bytes
     float* obase;
     if (MODE == kBwdDX)
       obase = a.out_f32 + (static_cast<long long>(t.m0) + row_w) * a.ld_out + t.n0;
     else
       obase = a.out_f32 + static_cast<long long>(t.group) * a.out_group_stride +
               (static_cast<long long>(t.m0) + row_w) * a.ld_out + t.n0;
-    const int rows_here = min(32, t.nrows - row_w);  // valid rows of this warp's quarter
-    // a group without rows (no K blocks) has a zero gradient, not the stale accumulator
-    const bool zero = t.n_kb == 0;
 #pragma unroll 1
     for (int c = 0; c < NCOL / 32; ++c) {
       uint32_t v[32];
@@ -368,7 +407,8 @@ __device__ __forceinline__ void epilogue(const BwdArgs& a, const Tile& t, uint32
 template <int MODE>
 __global__ void __launch_bounds__(bw::NUM_THREADS, 1)
     bwd_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
-                         const __grid_constant__ CUtensorMap tmB, const BwdArgs args) {
+                         const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmO, const BwdArgs args) {
   using namespace bw;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -397,6 +437,7 @@ __global__ void __launch_bounds__(bw::NUM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&tmA);
     ptx::prefetch_tmap(&tmB);
+    if (MODE != kBwdDH) ptx::prefetch_tmap(&tmO);
   }
   if (warp == 1) {
     ptx::tmem_alloc_pair(ptx::smem_u32(&sh->tmem_base), TMEM_COLS);
@@ -521,7 +562,7 @@ __global__ void __launch_bounds__(bw::NUM_THREADS, 1)
       if (!wait_bar(ptx::smem_u32(&sh->tmem_full[acc]), acc_phase, sh, args.status)) break;
       ptx::tc_fence_after();
       const Tile t = tile_info<MODE>(args, sh, tile, rank);
-      bw::epilogue<MODE>(args, t, lane_addr + acc * 256, r, epi_stage);
+      bw::epilogue<MODE>(args, t, lane_addr + acc * 256, r, epi_stage, &tmO);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -530,6 +571,8 @@ __global__ void __launch_bounds__(bw::NUM_THREADS, 1)
         else ptx::mbar_arrive_cluster(ptx::mapa(e, 0));
       }
     }
+    if (MODE != kBwdDH && lane == 0) ptx::bulk_wait0();  // this warp's TMA stores are performed
+    __syncwarp();
   }
 
   pdl_trigger();
@@ -570,9 +613,22 @@ bool make_map(CUtensorMap* m, int rank, const void* base, uint64_t inner, uint64
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 output [rows][inner] for TMA stores of {32, 32} boxes, 128-byte swizzle
+bool make_out_map(CUtensorMap* m, float* base, uint64_t inner, uint64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int MODE>
-cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const BwdArgs& args, int num_sms,
-                   cudaStream_t stream) {
+cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
+                   const BwdArgs& args, int num_sms, cudaStream_t stream) {
   static bool attr_set[64] = {};
   static int max_clusters[64] = {};
   int dev = 0;
@@ -615,36 +671,41 @@ cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const BwdArgs& 
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, bwd_gemm_pair_kernel<MODE>, ma, mb, args);
+  return cudaLaunchKernelEx(&cfg, bwd_gemm_pair_kernel<MODE>, ma, mb, mo, args);
 }
 
 }  // namespace
 
-cudaError_t bwd_gemm(int mode, const BwdGemmOperands& op, const BwdArgs& args, int num_sms,
+cudaError_t bwd_gemm(int mode, const BwdGemmOperands& op, const BwdArgs& args_in, int num_sms,
                      cudaStream_t stream) {
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, mo;
+  BwdArgs args = args_in;
   switch (mode) {
     case kBwdDH:
       // A: dy_pad [rows][K]; B: W_down [slices][K = d][N = H] read MN-major (box 64 x 64)
       if (!make_map(&ma, 2, op.A, op.a_inner, op.a_rows, 1, 128) ||
           !make_map(&mb, 3, op.B, op.b_inner, op.b_rows, op.b_slices, 64))
         return cudaErrorInvalidValue;
-      return launch<kBwdDH>(ma, mb, args, num_sms, stream);
+      return launch<kBwdDH>(ma, mb, ma, args, num_sms, stream);
     case kBwdDX:
+      // output dz [rows of A][ld_out]
       if (!make_map(&ma, 2, op.A, op.a_inner, op.a_rows, 1, 128) ||
-          !make_map(&mb, 3, op.B, op.b_inner, op.b_rows, op.b_slices, 64))
+          !make_map(&mb, 3, op.B, op.b_inner, op.b_rows, op.b_slices, 64) ||
+          !make_out_map(&mo, args.out_f32, args.ld_out, op.a_rows))
         return cudaErrorInvalidValue;
-      return launch<kBwdDX>(ma, mb, args, num_sms, stream);
+      return launch<kBwdDX>(ma, mb, mo, args, num_sms, stream);
     case kBwdDWD:
+    case kBwdDWGU: {
+      // output: n_groups gradients of out_group_stride elements, rows of ld_out
+      if (args.ld_out <= 0 || args.out_group_stride % args.ld_out != 0) return cudaErrorInvalidValue;
+      args.out_group_rows = args.out_group_stride / args.ld_out;
       if (!make_map(&ma, 2, op.A, op.a_inner, op.a_rows, 1, 64) ||
-          !make_map(&mb, 2, op.B, op.b_inner, op.b_rows, 1, 64))
+          !make_map(&mb, 2, op.B, op.b_inner, op.b_rows, 1, 64) ||
+          !make_out_map(&mo, args.out_f32, args.ld_out, args.out_group_rows * args.n_groups))
         return cudaErrorInvalidValue;
-      return launch<kBwdDWD>(ma, mb, args, num_sms, stream);
-    case kBwdDWGU:
-      if (!make_map(&ma, 2, op.A, op.a_inner, op.a_rows, 1, 64) ||
-          !make_map(&mb, 2, op.B, op.b_inner, op.b_rows, 1, 64))
-        return cudaErrorInvalidValue;
-      return launch<kBwdDWGU>(ma, mb, args, num_sms, stream);
+      return mode == kBwdDWD ? launch<kBwdDWD>(ma, mb, mo, args, num_sms, stream)
+                             : launch<kBwdDWGU>(ma, mb, mo, args, num_sms, stream);
+    }
   }
   return cudaErrorInvalidValue;
 }

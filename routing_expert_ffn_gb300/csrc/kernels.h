@@ -141,6 +141,7 @@ struct BwdArgs {
   float* out_f32;           // other modes
   long long ld_out;
   long long out_group_stride;  // weight modes: elements between groups' gradients
+  long long out_group_rows;    // weight modes: out_group_stride / ld_out (set by bwd_gemm)
   unsigned* status;
 };
 struct BwdGemmOperands {
