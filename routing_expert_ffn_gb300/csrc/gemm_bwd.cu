@@ -232,7 +232,8 @@ __device__ __forceinline__ void issue_kblock(const BwdArgs& a, const CUtensorMap
   }
 }
 
-__device__ __forceinline__ float sigm(float z) { return 1.0f / (1.0f + __expf(-z)); }
+// logistic sigmoid with the approximate divide (its error is far below the bf16 rounding of dA)
+__device__ __forceinline__ float sigm(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
 
 __device__ __forceinline__ void unpack8(const uint4& v, float* f) {
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
