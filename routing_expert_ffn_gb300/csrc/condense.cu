@@ -17,6 +17,11 @@
 //                   cos = 1; a zero row is otherwise dissimilar).
 //   4. greedy scan: one CTA per bucket walks the rows in order with R as a bitset;
 //                   j's candidates are A[j] & R, its representative the lowest.
+//                   Rows go 32 at a time, one per lane: a row's lowest candidate
+//                   among the representatives chosen before its group is its
+//                   answer (they all precede the group's own); only rows with none
+//                   are resolved in order against the group's new representatives,
+//                   on one 32-bit word.
 // The decision cos >= tau is taken in fp32.
 #include "common.cuh"
 #include "kernels.h"
@@ -24,9 +29,22 @@
 namespace moe {
 namespace {
 
-constexpr int kScanThreads = 256;
+constexpr int kScanThreads = 128;     // warp 0 scans, warps 1-3 stage bit rows
 constexpr int kMaxBucketRows = 65536;
 constexpr int kMaxWords = kMaxBucketRows / 32;
+constexpr int kScanBufWords = 12288;  // one of two staging buffers (48 KB)
+
+// 4-byte asynchronous global -> shared copy (no register round trip: every copy
+// a thread issues is in flight at once), and the wait for all of a thread's copies.
+__device__ __forceinline__ void cp_async4(unsigned* dst, const unsigned* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
 
 __global__ void __launch_bounds__(256)
     row_stats_kernel(const __nv_bfloat16* __restrict__ rows, const int32_t* __restrict__ offsets,
@@ -116,15 +134,18 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// One CTA per bucket.  Bit rows are staged into shared memory a chunk at a
-// time by all threads; warp 0 then walks the chunk's rows in order.
+// One CTA per bucket.  Warps 1-3 stage the bit rows of the next chunk of rows
+// into one of two buffers (row pitch odd, so 32 rows at the same word offset sit
+// in distinct banks) while warp 0 scans the current chunk 32 rows at a time.
+// Buckets whose 32-row group does not fit a buffer (more than 12256 rows) take
+// the row-by-row walk over staged rows instead.
 __global__ void __launch_bounds__(kScanThreads)
     greedy_scan_kernel(const unsigned* __restrict__ bits, const long long* __restrict__ bits_base,
                        const int32_t* __restrict__ offsets, int32_t* __restrict__ rep_of,
                        int32_t* __restrict__ n_rep, unsigned* status) {
   extern __shared__ unsigned scan_smem[];
-  unsigned* R = scan_smem;                 // kMaxWords
-  unsigned* stage = scan_smem + kMaxWords;  // chunk rows x W
+  unsigned* R = scan_smem;                  // kMaxWords: representatives so far, as a bitset
+  unsigned* buf = scan_smem + kMaxWords;    // 2 x kScanBufWords
   const int e = blockIdx.x;
   const int off = offsets[e];
   const int n = offsets[e + 1] - off;
@@ -135,44 +156,112 @@ __global__ void __launch_bounds__(kScanThreads)
   }
   for (int w = threadIdx.x; w < W; w += blockDim.x) R[w] = 0u;
   const unsigned* B = bits + bits_base[e];
-  const int stage_words = 8192;  // 32 KB
-  const int rows_per_chunk = W > 0 ? max(1, stage_words / W) : 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pitch = W | 1;
   int reps = 0;
-  for (int r0 = 0; r0 < n; r0 += rows_per_chunk) {
-    const int rows = min(rows_per_chunk, n - r0);
-    __syncthreads();
-    for (int i = threadIdx.x; i < rows * W; i += blockDim.x) {
-      const int rr = i / W, w = i - rr * W;
-      // only words strictly below the row's own index are meaningful
-      stage[i] = (w * 32 < r0 + rr) ? B[static_cast<long long>(r0 + rr) * W + w] : 0u;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      for (int rr = 0; rr < rows; ++rr) {
+  if (32 * pitch <= kScanBufWords) {
+    const int rows_chunk = 32 * (kScanBufWords / (32 * pitch));
+    const int n_chunks = (n + rows_chunk - 1) / rows_chunk;
+    // rows [c * rows_chunk, ...) of chunk c: row li needs words 0 .. li / 32 only;
+    // the copies are asynchronous and waited for once, before the chunk's barrier
+    auto stage_chunk = [&](int c, unsigned* dst) {
+      const int r0 = c * rows_chunk;
+      const int rows = min(rows_chunk, n - r0);
+      for (int rr = warp - 1; rr < rows; rr += 3) {
         const int li = r0 + rr;
-        const int nw = (li + 31) >> 5;  // words holding columns < li
-        int found = -1;
-        for (int w0 = 0; w0 < nw && found < 0; w0 += 32) {
-          const int w = w0 + lane;
-          const unsigned cand = (w < nw) ? (stage[rr * W + w] & R[w]) : 0u;
-          const unsigned hit = __ballot_sync(0xffffffffu, cand != 0u);
-          if (hit) {
-            const int src = __ffs(hit) - 1;
-            const unsigned cw = __shfl_sync(0xffffffffu, cand, src);
-            found = (w0 + src) * 32 + __ffs(cw) - 1;
+        const unsigned* src = B + static_cast<long long>(li) * W;
+        unsigned* d = dst + rr * pitch;
+        for (int w = lane; w <= (li >> 5); w += 32) cp_async4(d + w, src + w);
+      }
+      cp_async_wait_all();
+    };
+    if (warp != 0) stage_chunk(0, buf);
+    __syncthreads();
+    for (int c = 0; c < n_chunks; ++c) {
+      const unsigned* cur = buf + (c & 1) * kScanBufWords;
+      if (warp != 0) {
+        if (c + 1 < n_chunks) stage_chunk(c + 1, buf + ((c + 1) & 1) * kScanBufWords);
+      } else {
+        const int r0 = c * rows_chunk;
+        const int rows = min(rows_chunk, n - r0);
+        for (int g0 = 0; g0 < rows; g0 += 32) {
+          const int i0 = r0 + g0;  // a multiple of 32: the group's columns are word i0 / 32
+          const int li = i0 + lane;
+          const bool live = g0 + lane < rows;
+          const unsigned* row = cur + (g0 + lane) * pitch;
+          const int nw_old = i0 >> 5;
+          int old_hit = -1;  // lowest representative chosen before the group with A[li][r]
+          if (live) {
+            for (int w = 0; w < nw_old; ++w) {
+              const unsigned m = row[w] & R[w];
+              if (m) {
+                old_hit = (w << 5) + __ffs(m) - 1;
+                break;
+              }
+            }
           }
-        }
-        if (lane == 0) {
-          if (found < 0) {
-            R[li >> 5] |= 1u << (li & 31);
-            rep_of[off + li] = off + li;
-          } else {
-            rep_of[off + li] = off + found;
+          // similarities to the group's earlier rows (A holds only columns below the row)
+          const unsigned inw = live ? (row[nw_old] & ((1u << lane) - 1u)) : 0u;
+          const unsigned open = __ballot_sync(0xffffffffu, live && old_hit < 0);
+          unsigned fresh = 0u;  // the group's new representatives, in order
+          for (int b = 0; b < 32; ++b) {
+            const unsigned ib = __shfl_sync(0xffffffffu, inw, b);
+            if (((open >> b) & 1u) && !(ib & fresh)) fresh |= 1u << b;
           }
+          if (live) {
+            int rp;
+            if (old_hit >= 0) rp = old_hit;
+            else if ((fresh >> lane) & 1u) rp = li;
+            else rp = i0 + __ffs(inw & fresh) - 1;
+            rep_of[off + li] = off + rp;
+          }
+          reps += __popc(fresh);
+          if (lane == 0) R[nw_old] = fresh;
+          __syncwarp();
         }
-        if (found < 0) ++reps;
-        __syncwarp();
+      }
+      __syncthreads();
+    }
+  } else {
+    // wide buckets: stage as many whole rows as fit both buffers, walk them one by one
+    unsigned* stage = buf;
+    const int stage_words = 2 * kScanBufWords;
+    const int rows_per_chunk = max(1, stage_words / W);
+    for (int r0 = 0; r0 < n; r0 += rows_per_chunk) {
+      const int rows = min(rows_per_chunk, n - r0);
+      __syncthreads();
+      for (int i = threadIdx.x; i < rows * W; i += blockDim.x) {
+        const int rr = i / W, w = i - rr * W;
+        // only words strictly below the row's own index are meaningful
+        stage[i] = (w * 32 < r0 + rr) ? B[static_cast<long long>(r0 + rr) * W + w] : 0u;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        for (int rr = 0; rr < rows; ++rr) {
+          const int li = r0 + rr;
+          const int nw = (li + 31) >> 5;  // words holding columns < li
+          int found = -1;
+          for (int w0 = 0; w0 < nw && found < 0; w0 += 32) {
+            const int w = w0 + lane;
+            const unsigned cand = (w < nw) ? (stage[rr * W + w] & R[w]) : 0u;
+            const unsigned hit = __ballot_sync(0xffffffffu, cand != 0u);
+            if (hit) {
+              const int src = __ffs(hit) - 1;
+              const unsigned cw = __shfl_sync(0xffffffffu, cand, src);
+              found = (w0 + src) * 32 + __ffs(cw) - 1;
+            }
+          }
+          if (lane == 0) {
+            if (found < 0) {
+              R[li >> 5] |= 1u << (li & 31);
+              rep_of[off + li] = off + li;
+            } else {
+              rep_of[off + li] = off + found;
+            }
+          }
+          if (found < 0) ++reps;
+          __syncwarp();
+        }
       }
     }
   }
@@ -329,7 +418,7 @@ cudaError_t launch_condense(const __nv_bfloat16* x_perm, const int32_t* offsets,
   a.status = status;
   err = tc_gemm(kTcSimBits, x_perm, P, d, x_perm, 1, P, d, a, num_sms, stream);
   if (err != cudaSuccess) return err;
-  const size_t smem = sizeof(unsigned) * (kMaxWords + 8192);
+  const size_t smem = sizeof(unsigned) * (kMaxWords + 2 * kScanBufWords);
   static bool attr = false;
   if (!attr) {
     err = cudaFuncSetAttribute(greedy_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -467,13 +467,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ffn_epilogue<MODE>(args, t, col0, r, valid);
       } else {
         // Gram tile of bucket `slice`: row slot i = row0 + r, column slot j = gbase + nt*256 + c.
+        // cos(x_i, x_j) = D[i][j] / (|x_i| |x_j|), taken as D * (1/|x_i|) * (1/|x_j|) in fp32,
+        // clamped to [-1, 1]; a zero row is dissimilar unless the rows are identical.
         const int e = t.slice;
         const int n_e = args.bucket_off[e + 1] - args.bucket_off[e];
         const int W = (n_e + 31) >> 5;
         const int i = t.row0 + r;
         const int li = i - t.gbase;
         const float ni = valid ? args.norm[i] : 0.f;
+        const float inv_ni = ni > 0.f ? 1.0f / ni : 0.f;
         const unsigned long long hi = valid ? args.row_hash[i] : 0ull;
+        const uint32_t hi_lo = static_cast<uint32_t>(hi);
         unsigned* brow = args.bits + args.bits_base[e] + static_cast<long long>(li) * W;
 #pragma unroll 1
         for (int c = 0; c < 8; ++c) {
@@ -481,28 +485,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ptx::tmem_ld_32x32b_x32(col0 + c * 32, v);
           ptx::tmem_ld_wait();
           const int lj0 = t.nt * BN + c * 32;
-          if (valid && lj0 < li) {
-            uint32_t word = 0;
-#pragma unroll 4
-            for (int b = 0; b < 32; ++b) {
-              const int lj = lj0 + b;
-              if (lj >= li) break;
-              const int j = t.gbase + lj;
-              const float nj = args.norm[j];
-              bool similar;
-              if (args.row_hash[j] == hi && rows_identical(args.rows, args.d, i, j)) {
-                similar = true;  // identical rows: similarity exactly 1
-              } else if (ni == 0.f || nj == 0.f) {
-                similar = false;
-              } else {
-                float s = __uint_as_float(v[b]) / (ni * nj);
-                s = fminf(fmaxf(s, -1.f), 1.f);
-                similar = s >= args.tau;
-              }
-              word |= static_cast<uint32_t>(similar) << b;
-            }
-            brow[lj0 >> 5] = word;
+          // a chunk that lies above every row of this warp's quarter holds no bit
+          if (!__any_sync(0xffffffffu, valid && lj0 < li)) continue;
+          // lane b fetches column lj0 + b's norm and hash once; each row takes them by shuffle
+          const bool col_in = lj0 + lane < n_e;
+          const float nj_l = col_in ? args.norm[t.gbase + lj0 + lane] : 0.f;
+          const float inv_nj_l = nj_l > 0.f ? 1.0f / nj_l : 0.f;
+          const uint32_t hj_lo_l =
+              col_in ? static_cast<uint32_t>(args.row_hash[t.gbase + lj0 + lane]) : 0u;
+          const int n_in = min(32, li - lj0);  // columns of this chunk below row li
+          uint32_t word = 0, same_hash = 0;
+#pragma unroll
+          for (int b = 0; b < 32; ++b) {
+            const float inv_nj = __shfl_sync(0xffffffffu, inv_nj_l, b);
+            const uint32_t hj_lo = __shfl_sync(0xffffffffu, hj_lo_l, b);
+            const float s =
+                fminf(fmaxf(__uint_as_float(v[b]) * inv_ni * inv_nj, -1.f), 1.f);
+            const bool in = b < n_in;
+            word |= static_cast<uint32_t>(in && inv_ni > 0.f && inv_nj > 0.f && s >= args.tau) << b;
+            same_hash |= static_cast<uint32_t>(in && hj_lo == hi_lo) << b;
           }
+          // identical rows: similarity exactly 1 (full hash, then the rows themselves)
+          while (valid && same_hash) {
+            const int b = __ffs(same_hash) - 1;
+            same_hash &= same_hash - 1;
+            const int j = t.gbase + lj0 + b;
+            if (args.row_hash[j] == hi && rows_identical(args.rows, args.d, i, j)) word |= 1u << b;
+          }
+          if (valid && lj0 < li) brow[lj0 >> 5] = word;
         }
       }
       ptx::tc_fence_before();
