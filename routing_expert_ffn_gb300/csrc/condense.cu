@@ -107,13 +107,31 @@ __global__ void __launch_bounds__(256)
       s_cnt[i] = cnt;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      int run = s_carry;
-      for (int i = 0; i < 1024; ++i) {
-        s_beg[i] = run;
-        run += s_cnt[i];
+    {
+      // exclusive scan of the 1024 counts: 4 consecutive entries per thread, then the
+      // threads' sums across each warp (shuffles) and across the warps (shared memory)
+      __shared__ int s_wsum[32];
+      const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+      const int per = 1024 / blockDim.x;  // 4 with 256 threads
+      const int i0 = threadIdx.x * per;
+      int mine = 0;
+      for (int q = 0; q < per; ++q) mine += s_cnt[i0 + q];
+      int incl = mine;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
       }
-      s_beg[1024] = run;
+      if (lane == 31) s_wsum[warp] = incl;
+      __syncthreads();
+      int before = s_carry;
+      for (int w = 0; w < warp; ++w) before += s_wsum[w];
+      int run = before + incl - mine;
+      for (int q = 0; q < per; ++q) {
+        s_beg[i0 + q] = run;
+        run += s_cnt[i0 + q];
+      }
+      if (threadIdx.x == blockDim.x - 1) s_beg[1024] = run;
     }
     __syncthreads();
     for (int i = threadIdx.x; i < 1024; i += blockDim.x) {
@@ -192,10 +210,15 @@ __global__ void __launch_bounds__(kScanThreads)
           const int nw_old = i0 >> 5;
           int old_hit = -1;  // lowest representative chosen before the group with A[li][r]
           if (live) {
-            for (int w = 0; w < nw_old; ++w) {
-              const unsigned m = row[w] & R[w];
-              if (m) {
-                old_hit = (w << 5) + __ffs(m) - 1;
+            // four words per step: the loads of a step do not wait on each other
+            for (int w = 0; w < nw_old; w += 4) {
+              unsigned m[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) m[q] = (w + q < nw_old) ? (row[w + q] & R[w + q]) : 0u;
+              if (m[0] | m[1] | m[2] | m[3]) {
+                const int q = m[0] ? 0 : m[1] ? 1 : m[2] ? 2 : 3;
+                const unsigned mq = m[0] ? m[0] : m[1] ? m[1] : m[2] ? m[2] : m[3];
+                old_hit = ((w + q) << 5) + __ffs(mq) - 1;
                 break;
               }
             }
