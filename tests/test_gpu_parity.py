@@ -356,6 +356,35 @@ def test_condense_exact_duplicates_tau_one(moe):
     assert int(ncond.item()) > 0
 
 
+@pytest.mark.parametrize("sizes", [(16400, 3000), (12300, 12200)])
+def test_condense_duplicates_wide_buckets(moe, sizes):
+    """Buckets above and below the scan's 12256-row group limit, exact duplicates at tau = 1.
+
+    Closed form (no oracle run at this size): every row's representative is the first
+    identical row of its bucket, since distinct random rows are far from cosine 1.
+    """
+    rng = np.random.default_rng(7)
+    d = 256  # bf16 layers take d in multiples of 256
+    pool = gen.round_to_bf16(rng.standard_normal((40, d)).astype(np.float32))
+    ids = [rng.integers(0, len(pool), n) for n in sizes]
+    rows = np.concatenate([pool[i] for i in ids])
+    P = len(rows)
+    C = moe.Config(T=P, d=d, E=len(sizes), k=1, H=128, n_shared=0, H_shared=0, dtype="bf16",
+                   gating="softmax_topk", residual="none")
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    x_perm = torch.from_numpy(rows).to(device="cuda", dtype=torch.bfloat16)
+    rep_of, n_rep, ncond = moe.condense(C, x_perm, torch.from_numpy(offsets).cuda(), 1.0)
+    torch.cuda.synchronize()
+    expect = np.empty(P, np.int64)
+    for e, ie in enumerate(ids):
+        first = {}
+        for s, v in enumerate(ie):
+            expect[offsets[e] + s] = offsets[e] + first.setdefault(int(v), s)
+    np.testing.assert_array_equal(_np(rep_of)[:P], expect)
+    assert int(ncond.item()) == P - sum(len(set(ie.tolist())) for ie in ids)
+    _status_ok(moe)
+
+
 def test_condense_tau_above_one_is_identity(moe):
     cfg, inp, C, w, x, r = _setup(moe, "luffy_condense", T=2048)
     _, idx, _ = moe.route(C, x, w.W_r, w.router_bias)
