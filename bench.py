@@ -306,7 +306,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     def layer_on(xb, rb, ob):
         return capture(torch, lambda: layer(xb, rb, tau, out=ob, n_condensed_out=ncond,
                                             partial_out=part, aux_stream=aux))
-    e2e = end_to_end(args, C, graph, layer_on, x, r, out, stream, torch)
+    e2e = end_to_end(args, C, graph, layer_on, x, r, out, stream, torch, world, dev)
     st = moe.get_device_status()
     if st != 0:
         raise RuntimeError(f"device status after timing: {moe.status_string(st)}")
@@ -499,7 +499,7 @@ def eq9_report(ms_layer: float, phases: dict) -> dict:
             "holds": comm <= window}
 
 
-def end_to_end(args, C, graph, layer_on, x, r, out, stream, torch) -> dict:
+def end_to_end(args, C, graph, layer_on, x, r, out, stream, torch, world=1, dev=None) -> dict:
     """Every step: its pinned host input x (and residual) -> a device input buffer, one
     layer call (a captured graph), its whole output -> a pinned host buffer.  Two device
     buffer sets alternate: step i+1's host-to-device copy and step i-1's device-to-host
@@ -550,10 +550,11 @@ def end_to_end(args, C, graph, layer_on, x, r, out, stream, torch) -> dict:
     s_out.wait_stream(stream)
     b.record(s_out)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / args.steps
+    # whole job: every rank's tokens over the slowest rank's time
+    ms = max_over_ranks(a.elapsed_time(b) / args.steps, world, dev)
     h2d = xh.numel() * xh.element_size() + (rh.numel() * rh.element_size() if rh is not None else 0)
     d2h = outh[0].numel() * outh[0].element_size()
-    return {"value": C.T / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+    return {"value": job_tokens_per_s(C.T, world, ms), "unit": "tokens/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "path": "every step: pinned host -> device copy of its input, the layer step (CUDA "
                     "graph), device -> pinned host copy of its output; two device buffer sets, "
