@@ -210,14 +210,20 @@ __global__ void __launch_bounds__(kScanThreads)
           const int nw_old = i0 >> 5;
           int old_hit = -1;  // lowest representative chosen before the group with A[li][r]
           if (live) {
-            // four words per step: the loads of a step do not wait on each other
-            for (int w = 0; w < nw_old; w += 4) {
-              unsigned m[4];
+            // eight words per step: the loads of a step do not wait on each other
+            for (int w = 0; w < nw_old; w += 8) {
+              unsigned m[8], any = 0u;
 #pragma unroll
-              for (int q = 0; q < 4; ++q) m[q] = (w + q < nw_old) ? (row[w + q] & R[w + q]) : 0u;
-              if (m[0] | m[1] | m[2] | m[3]) {
-                const int q = m[0] ? 0 : m[1] ? 1 : m[2] ? 2 : 3;
-                const unsigned mq = m[0] ? m[0] : m[1] ? m[1] : m[2] ? m[2] : m[3];
+              for (int q = 0; q < 8; ++q) {
+                m[q] = (w + q < nw_old) ? (row[w + q] & R[w + q]) : 0u;
+                any |= m[q];
+              }
+              if (any) {
+                int q = 7;
+                unsigned mq = m[7];
+#pragma unroll
+                for (int u = 6; u >= 0; --u)
+                  if (m[u]) q = u, mq = m[u];
                 old_hit = ((w + q) << 5) + __ffs(mq) - 1;
                 break;
               }
@@ -227,10 +233,12 @@ __global__ void __launch_bounds__(kScanThreads)
           const unsigned inw = live ? (row[nw_old] & ((1u << lane) - 1u)) : 0u;
           const unsigned open = __ballot_sync(0xffffffffu, live && old_hit < 0);
           unsigned fresh = 0u;  // the group's new representatives, in order
-          for (int b = 0; b < 32; ++b) {
-            const unsigned ib = __shfl_sync(0xffffffffu, inw, b);
-            if (((open >> b) & 1u) && !(ib & fresh)) fresh |= 1u << b;
-          }
+          unsigned ib[32];      // every row's in-group word, fetched before the ordered pass
+#pragma unroll
+          for (int b = 0; b < 32; ++b) ib[b] = __shfl_sync(0xffffffffu, inw, b);
+#pragma unroll
+          for (int b = 0; b < 32; ++b)
+            if (((open >> b) & 1u) && !(ib[b] & fresh)) fresh |= 1u << b;
           if (live) {
             int rp;
             if (old_hit >= 0) rp = old_hit;
