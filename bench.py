@@ -347,9 +347,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         "vs_baseline": None,
         "dtype": C.dtype,
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02^2) weights, router N(0,1/d)); no dataset",
-        "config": {"workload": f"{cfg.name}: T={C.T} d={C.d} E={C.E} top-{C.k} {C.gating} "
-                               f"H={C.H} shared={C.n_shared}x{C.H_shared} residual={C.residual}"
-                               + (f" tau={tau:.6f}" if condense else ""),
+        "config": {"workload": workload_desc(cfg),
                    "tokens_per_gpu": C.T, "parallelism": f"replicas x{world}",
                    "launch": "each step replays one CUDA graph of moe_layer_forward_ex"
                   + (" (shared experts on a second stream)" if aux is not None else "")
@@ -604,6 +602,14 @@ def cpu_baseline(cfg, inp, target_s: float = 12.0) -> dict:
                       f"({dt:.1f} s); weights pre-cast to float64"}
 
 
+def workload_desc(cfg) -> str:
+    """The workload named by its shape (the same string in both arms' config)."""
+    tau = cfg.taus[0] if cfg.taus else math.nan
+    return (f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E} top-{cfg.k} {cfg.gating} "
+            f"H={cfg.H} shared={cfg.n_shared}x{cfg.H_shared} residual={cfg.residual}"
+            + (f" tau={tau:.6f}" if tau <= 1.0 else ""))
+
+
 def run_reference(args, rank: int) -> None:
     if rank != 0:
         return
@@ -624,7 +630,7 @@ def run_reference(args, rank: int) -> None:
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": cfg.name, "tokens_per_step": T_s},
+            "data": "synthetic", "config": {"workload": workload_desc(cfg), "tokens_per_step": T_s},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
