@@ -450,12 +450,15 @@ cudaError_t launch_condense(const __nv_bfloat16* x_perm, const int32_t* offsets,
   err = tc_gemm(kTcSimBits, x_perm, P, d, x_perm, 1, P, d, a, num_sms, stream);
   if (err != cudaSuccess) return err;
   const size_t smem = sizeof(unsigned) * (kMaxWords + 2 * kScanBufWords);
-  static bool attr = false;
-  if (!attr) {
+  // the shared-memory limit is a per-device attribute of the function
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 64 || !attr_set[dev]) {
     err = cudaFuncSetAttribute(greedy_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    attr = true;
+    if (dev < 64) attr_set[dev] = true;
   }
   greedy_scan_kernel<<<E, kScanThreads, smem, stream>>>(s.bits, s.bits_base, offsets, rep_of,
                                                         n_rep, status);
