@@ -905,8 +905,15 @@ extern "C" moe_status moe_layer_backward(const moe_config* cfg, const moe_weight
 
   // shared experts: every token, gate 1, so their output gradient is d_out itself
   if (S > 0) {
-    MOE_CUDA(launch_pad_tokens(x, T, Tp, d, b.x_s, st));
-    MOE_CUDA(launch_pad_tokens(d_out, T, Tp, d, b.dout_s, st));
+    // x and d_out padded to Tp rows; when T is already a multiple of the pad they are used as is
+    const void* xs = x;
+    const void* douts = d_out;
+    if (Tp != T) {
+      MOE_CUDA(launch_pad_tokens(x, T, Tp, d, b.x_s, st));
+      MOE_CUDA(launch_pad_tokens(d_out, T, Tp, d, b.dout_s, st));
+      xs = b.x_s;
+      douts = b.dout_s;
+    }
     MOE_CUDA(launch_build_mtiles(nullptr, nullptr, Tp, 1, nullptr, b.mt_s, b.gmb_s, st));
     {
       TcGemmArgs a = {};
@@ -920,7 +927,7 @@ extern "C" moe_status moe_layer_backward(const moe_config* cfg, const moe_weight
       a.kb_per_slice = a.n_kblocks;
       a.out = static_cast<__nv_bfloat16*>(b.au_s);
       a.ld_out = static_cast<long long>(S) * 2 * Hs;
-      MOE_CUDA(tc_gemm(kTcStore, b.x_s, Tp, d, w->Ws_gu, S, 2 * Hs, d, a, sms, st));
+      MOE_CUDA(tc_gemm(kTcStore, xs, Tp, d, w->Ws_gu, S, 2 * Hs, d, a, sms, st));
     }
     MOE_CUDA(launch_swiglu_from_au(b.au_s, nullptr, Tp, S, Hs, b.h_s, st));
     BwdArgs a = {};
@@ -937,7 +944,7 @@ extern "C" moe_status moe_layer_backward(const moe_config* cfg, const moe_weight
     a.ld_au = static_cast<long long>(S) * 2 * Hs;
     a.out_bf16 = static_cast<__nv_bfloat16*>(b.dA_s);
     a.ld_out = a.ld_au;
-    op = {b.dout_s, d, Tp, w->Ws_down, Hs, d, S};
+    op = {douts, d, Tp, w->Ws_down, Hs, d, S};
     MOE_CUDA(bwd_gemm(kBwdDH, op, a, sms, st));
     a.n_ntiles = d / 256;
     a.n_kblocks = S * 2 * Hs / 64;
@@ -959,7 +966,7 @@ extern "C" moe_status moe_layer_backward(const moe_config* cfg, const moe_weight
     g.out_f32 = dWs_down;
     g.ld_out = Hs;
     g.out_group_stride = static_cast<long long>(d) * Hs;
-    op = {b.dout_s, d, Tp, b.h_s, static_cast<long long>(S) * Hs, Tp, 1};
+    op = {douts, d, Tp, b.h_s, static_cast<long long>(S) * Hs, Tp, 1};
     MOE_CUDA(bwd_gemm(kBwdDWD, op, g, sms, st));
     g.n_mtiles = 2 * Hs / 256;
     g.n_ntiles = d / 256;
@@ -967,7 +974,7 @@ extern "C" moe_status moe_layer_backward(const moe_config* cfg, const moe_weight
     g.out_f32 = dWs_gu;
     g.ld_out = d;
     g.out_group_stride = 2ll * Hs * d;
-    op = {b.dA_s, static_cast<long long>(S) * 2 * Hs, Tp, b.x_s, d, Tp, 1};
+    op = {b.dA_s, static_cast<long long>(S) * 2 * Hs, Tp, xs, d, Tp, 1};
     MOE_CUDA(bwd_gemm(kBwdDWGU, op, g, sms, st));
   }
 
