@@ -222,6 +222,30 @@ def test_layer_full_size_sampled(moe, name):
     _layer_check(moe, name, tau=tau, tokens=_sample_tokens(cfg.T, 48))
 
 
+@pytest.mark.parametrize("E,k", [(256, 8), (64, 32)])
+def test_layer_max_experts_and_k(moe, E, k):
+    """The largest E (256: router split-K path, 257-entry group tables in the dispatch and both
+    GEMM kernels) and the largest k (32) the boundary takes, renormalised gates and a shared
+    expert; every token against the oracle."""
+    from dataclasses import replace
+    cfg = replace(gen.CONFIGS["qwen3_30b_a3b"], name=f"e{E}k{k}", T=600, d=256, E=E, k=k, H=128,
+                  n_shared=1, H_shared=128, router_bias="none")
+    inp = harness.condition(cfg, gen.make_inputs(cfg))
+    C = moe.Config.from_workload(cfg)
+    w, x, r = moe.upload(C, inp)
+    lay = moe.Layer(C, w)
+    idx = torch.empty((C.T, C.k), dtype=torch.int32, device=x.device)
+    out = lay(x, r, math.nan, topk_idx_out=idx)
+    torch.cuda.synchronize()
+    ref = orc.layer_forward(inp["x"], inp["W_r"], inp["bias"], inp["W_gu"], inp["W_down"],
+                            inp["Ws_gu"], inp["Ws_down"], cfg.k, cfg.gating,
+                            residual_mode=C.residual, residual=inp["residual"], tau=None,
+                            tokens=np.arange(C.T))
+    np.testing.assert_array_equal(_np(idx), ref["idx"])
+    assert harness.max_rel_err(_np(out), ref["out"]) <= harness.tolerance(cfg)
+    _status_ok(moe)
+
+
 @pytest.mark.parametrize("T", [1, 2, 127, 129, 777])
 def test_layer_ragged_token_counts(moe, T):
     _layer_check(moe, "dsv2_lite", T=T)
