@@ -145,6 +145,8 @@ __device__ __forceinline__ int total_tiles(const TcGemmArgs& a) {
 }
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+// SiLU with the approximate divide (bf16 output: its 2-ulp error is far below the rounding)
+__device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -214,6 +216,57 @@ __device__ __forceinline__ void ffn_epilogue(const TcGemmArgs& args, const TileI
           dst[v] = make_uint4(p[4 * v], p[4 * v + 1], p[4 * v + 2], p[4 * v + 3]);
       }
     }
+  }
+}
+
+// Epilogue of a full 32-row quarter of a pair tile (warp quarter q) through TMA: per
+// 32-column chunk each thread writes its row's 64 bytes into a {32, 32} bf16 box in shared
+// memory (64-byte swizzle: the row's four 16-byte pieces rotated by (row / 2) mod 4, so a
+// quarter-warp's stores hit distinct banks) and one thread stores the box.  Two boxes per
+// warp alternate; `nstore` counts the warp's stores.
+template <int MODE>
+__device__ __forceinline__ void ffn_epilogue_tma(const TcGemmArgs& args, const TileInfo& t,
+                                                 uint32_t col0, int q, int lane, uint8_t* stage,
+                                                 const CUtensorMap* tmO, uint32_t& nstore) {
+  const int row = t.row0 + 32 * q;
+  const int sw = (lane >> 1) & 3;
+  constexpr int NCH = MODE == kSwiGLU ? 4 : 8;
+  const int col_base = MODE == kSwiGLU ? t.nt * (BN / 2) : t.nt * BN;
+#pragma unroll 1
+  for (int c = 0; c < NCH; ++c) {
+    uint32_t p[16];
+    if (MODE == kSwiGLU) {
+      uint32_t g[32], u[32];
+      ptx::tmem_ld_32x32b_x32(col0 + c * 32, g);
+      ptx::tmem_ld_32x32b_x32(col0 + BN / 2 + c * 32, u);
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        p[i] = pack_bf16x2(silu_fast(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]),
+                           silu_fast(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]));
+    } else {
+      uint32_t v[32];
+      ptx::tmem_ld_32x32b_x32(col0 + c * 32, v);
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        p[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+    }
+    if (lane == 0) ptx::bulk_wait_read1();  // the box written two stores ago has been read
+    __syncwarp();
+    uint8_t* box = stage + (nstore & 1u) * (32 * 32 * 2);
+    uint8_t* mine = box + lane * 64;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      *reinterpret_cast<uint4*>(mine + ((j ^ sw) << 4)) =
+          make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+    ptx::fence_proxy_async_smem_cta();
+    __syncwarp();
+    if (lane == 0) {
+      ptx::tma_store_2d(tmO, ptx::smem_u32(box), col_base + c * 32, row);
+      ptx::bulk_commit();
+    }
+    ++nstore;
   }
 }
 
@@ -559,7 +612,11 @@ constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = (BN / 2) * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int SHARED_BYTES = 4096;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + SHARED_BYTES;
+// per epilogue warp: two {32 columns, 32 rows} bf16 TMA store boxes of 2 KB (64-byte swizzle)
+constexpr int OUT_BOX_BYTES = 32 * 32 * 2;
+constexpr int OUT_STAGE_BYTES = 4 * 2 * OUT_BOX_BYTES;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + SHARED_BYTES + OUT_STAGE_BYTES;
+static_assert((STAGES * STAGE_BYTES + SHARED_BYTES) % 1024 == 0, "output boxes 1024-byte aligned");
 constexpr int PAIR_GROUP = M_GROUP / 2;
 constexpr int TAIL_ROWS = BM / 2;  // token rows a CTA loads for a tail tile (box height)
 constexpr int TAIL_W_ROWS = 16;    // hidden units per gate (or up) run of a kSwiGLU tail
@@ -671,7 +728,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                              const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmA64,
-                             const __grid_constant__ CUtensorMap tmW5, const TcGemmArgs args) {
+                             const __grid_constant__ CUtensorMap tmW5,
+                             const __grid_constant__ CUtensorMap tmO, const TcGemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -700,6 +758,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::prefetch_tmap(&tmB);
     ptx::prefetch_tmap(&tmA64);
     ptx::prefetch_tmap(&tmW5);
+    ptx::prefetch_tmap(&tmO);
   }
   if (warp == 1) {
     ptx::tmem_alloc_pair(ptx::smem_u32(&sh->tmem_base), TMEM_COLS);
@@ -840,6 +899,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int q = warp & 3;
     const int r = q * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    // full quarters store through TMA boxes, except a down projection with remapped rows
+    uint8_t* out_stage = smem + pr::STAGES * pr::STAGE_BYTES + pr::SHARED_BYTES +
+                         (warp - 2) * 2 * pr::OUT_BOX_BYTES;
+    const bool tma_out = MODE == kSwiGLU || args.out_rowmap == nullptr;
+    uint32_t nstore = 0;
     int local = 0;
     for (int tile = cluster; tile < n_tiles; tile += n_clusters, ++local) {
       const int acc = local & 1;
@@ -848,6 +912,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::tc_fence_after();
       const TileInfo t = pr::tile_info(args, sh, tile, rank);
       if (t.tail) tail_epilogue<MODE>(args, t, lane_addr + acc * BN, q, lane, rank);
+      else if (tma_out && 32 * q + 32 <= t.nrows)
+        ffn_epilogue_tma<MODE>(args, t, lane_addr + acc * BN, q, lane, out_stage, &tmO, nstore);
       else ffn_epilogue<MODE>(args, t, lane_addr + acc * BN, r, r < t.nrows);
       ptx::tc_fence_before();
       __syncwarp();
@@ -857,6 +923,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         else ptx::mbar_arrive_cluster(ptx::mapa(e, 0));
       }
     }
+    if (lane == 0) ptx::bulk_wait0();  // this warp's output stores are performed
+    __syncwarp();
   }
 
   pdl_trigger();
@@ -917,9 +985,23 @@ static bool make_gate_up_map(CUtensorMap* m, const void* base, uint64_t K, uint6
   return r == CUDA_SUCCESS;
 }
 
+// bf16 output [rows][inner] for TMA stores of {32, 32} boxes, 64-byte swizzle
+static bool make_out_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int MODE>
 static cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& a64,
-                               const CUtensorMap& w5, const TcGemmArgs& args, int num_sms,
+                               const CUtensorMap& w5, const CUtensorMap& o, const TcGemmArgs& args,
+                               int num_sms,
                                cudaStream_t stream) {
   static bool attr_set[64] = {};
   static int max_clusters[64] = {};
@@ -965,7 +1047,7 @@ static cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<MODE>, a, b, a64, w5, args);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<MODE>, a, b, a64, w5, o, args);
 }
 
 template <int MODE>
@@ -1004,9 +1086,16 @@ cudaError_t tc_gemm(int mode, const void* A, long long a_rows, int K, const void
     return cudaErrorInvalidValue;
   if (mode == tc::kSwiGLU && !tc::make_gate_up_map(&mw5, B, b_cols, args.b_up_offset, b_slices))
     return cudaErrorInvalidValue;
+  // the output [a_rows][ld_out] bf16, stored in {32, 32} boxes by the full-quarter epilogue
+  CUtensorMap mo = ma;
+  if (pair && !tc::make_out_map(&mo, args.out, static_cast<uint64_t>(args.ld_out),
+                                static_cast<uint64_t>(a_rows)))
+    return cudaErrorInvalidValue;
   switch (mode) {
-    case tc::kSwiGLU: return tc::launch_pair<tc::kSwiGLU>(ma, mb, ma64, mw5, args, grid, stream);
-    case tc::kStore: return tc::launch_pair<tc::kStore>(ma, mb, ma64, mw5, args, grid, stream);
+    case tc::kSwiGLU:
+      return tc::launch_pair<tc::kSwiGLU>(ma, mb, ma64, mw5, mo, args, grid, stream);
+    case tc::kStore:
+      return tc::launch_pair<tc::kStore>(ma, mb, ma64, mw5, mo, args, grid, stream);
     case tc::kSimBits: return tc::launch<tc::kSimBits>(ma, mb, args, grid, stream);
     case tc::kRouter: return tc::launch<tc::kRouter>(ma, mb, args, grid, stream);
   }
