@@ -256,7 +256,6 @@ template <int MODE>
 __device__ __forceinline__ void epilogue(const BwdArgs& a, const Tile& t, uint32_t col0, int r,
                                          float* stage, const CUtensorMap* tmO) {
   const int NCOL = t.ncols;
-  const bool valid = r < t.nrows;
   if (MODE == kBwdDH) {
     // dh for hidden units [n0, n0 + 128) of this warp's 32 rows; AU = [a | u] per slice.
     // Per 32-column chunk the warp brings a and u of its 32 rows into shared memory with
