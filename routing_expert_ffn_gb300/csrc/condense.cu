@@ -21,7 +21,8 @@
 //                   among the representatives chosen before its group is its
 //                   answer (they all precede the group's own); only rows with none
 //                   are resolved in order against the group's new representatives,
-//                   on one 32-bit word.
+//                   on one 32-bit word.  Fifteen warps search a group's older words
+//                   while the group before it is being resolved.
 // The decision cos >= tau is taken in fp32.
 #include "common.cuh"
 #include "kernels.h"
@@ -29,7 +30,8 @@
 namespace moe {
 namespace {
 
-constexpr int kScanThreads = 128;     // warp 0 scans, warps 1-3 stage bit rows
+constexpr int kScanThreads = 512;     // warp 0 resolves groups, the other warps stage and search ahead
+constexpr int kScanHelpers = kScanThreads / 32 - 1;
 constexpr int kMaxBucketRows = 65536;
 constexpr int kMaxWords = kMaxBucketRows / 32;
 constexpr int kScanBufWords = 12288;  // one of two staging buffers (48 KB)
@@ -152,9 +154,10 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// One CTA per bucket.  Warps 1-3 stage the bit rows of the next chunk of rows
+// One CTA per bucket.  Warps 1-15 stage the bit rows of the next chunk of rows
 // into one of two buffers (row pitch odd, so 32 rows at the same word offset sit
-// in distinct banks) while warp 0 scans the current chunk 32 rows at a time.
+// in distinct banks) and search the current chunk's rows one 32-row group ahead
+// of warp 0, which resolves the groups in order.
 // Buckets whose 32-row group does not fit a buffer (more than 12256 rows) take
 // the row-by-row walk over staged rows instead.
 __global__ void __launch_bounds__(kScanThreads)
@@ -178,67 +181,104 @@ __global__ void __launch_bounds__(kScanThreads)
   const int pitch = W | 1;
   int reps = 0;
   if (32 * pitch <= kScanBufWords) {
+    // Per 32-row group G (rows 32G .. 32G + 31 of the bucket) a row's lowest
+    // candidate among the representatives chosen before the group lies in R's words
+    // 0 .. G-1.  Words 0 .. G-2 are final once group G-2 is resolved, so the helper
+    // warps search them one group ahead (an equal share of the words each, the lowest
+    // hit per row merged by a shared-memory minimum) while warp 0 resolves group G-1;
+    // warp 0 then checks only word G-1 for group G.
+    __shared__ int best[2][32];  // per look-ahead group and row: lowest hit, INT_MAX for none
+    if (threadIdx.x < 64) best[threadIdx.x >> 5][threadIdx.x & 31] = INT_MAX;
     const int rows_chunk = 32 * (kScanBufWords / (32 * pitch));
     const int n_chunks = (n + rows_chunk - 1) / rows_chunk;
-    // rows [c * rows_chunk, ...) of chunk c: row li needs words 0 .. li / 32 only;
-    // the copies are asynchronous and waited for once, before the chunk's barrier
-    auto stage_chunk = [&](int c, unsigned* dst) {
-      const int r0 = c * rows_chunk;
-      const int rows = min(rows_chunk, n - r0);
-      for (int rr = warp - 1; rr < rows; rr += 3) {
-        const int li = r0 + rr;
-        const unsigned* src = B + static_cast<long long>(li) * W;
-        unsigned* d = dst + rr * pitch;
-        for (int w = lane; w <= (li >> 5); w += 32) cp_async4(d + w, src + w);
+    // rows [r0 + g0, r0 + g0 + cnt) of the chunk starting at row r0, into dst: row li
+    // needs words 0 .. li / 32 only; the copies are asynchronous and waited for once,
+    // before the chunk's last barrier
+    auto stage_rows = [&](int r0, int g0, int cnt, unsigned* dst) {
+      int rr = g0 + warp - 1;
+      const unsigned* src = B + static_cast<long long>(r0 + rr) * W;
+      unsigned* d = dst + rr * pitch;
+      for (; rr < g0 + cnt; rr += kScanHelpers, src += kScanHelpers * W, d += kScanHelpers * pitch) {
+        const int top = (r0 + rr) >> 5;
+        for (int w = lane; w <= top; w += 32) cp_async4(d + w, src + w);
       }
-      cp_async_wait_all();
     };
-    if (warp != 0) stage_chunk(0, buf);
+    if (warp != 0) {
+      stage_rows(0, 0, min(rows_chunk, n), buf);
+      cp_async_wait_all();
+    }
     __syncthreads();
     for (int c = 0; c < n_chunks; ++c) {
       const unsigned* cur = buf + (c & 1) * kScanBufWords;
-      if (warp != 0) {
-        if (c + 1 < n_chunks) stage_chunk(c + 1, buf + ((c + 1) & 1) * kScanBufWords);
-      } else {
-        const int r0 = c * rows_chunk;
-        const int rows = min(rows_chunk, n - r0);
-        for (int g0 = 0; g0 < rows; g0 += 32) {
-          const int i0 = r0 + g0;  // a multiple of 32: the group's columns are word i0 / 32
+      const int r0 = c * rows_chunk;
+      const int rows = min(rows_chunk, n - r0);
+      const int ng = (rows + 31) >> 5;
+      // the next chunk (there is one only after a full chunk, so it has at most ng
+      // groups) is staged one group per iteration
+      const int rows_next = c + 1 < n_chunks ? min(rows_chunk, n - r0 - rows_chunk) : 0;
+      unsigned* nxt = buf + ((c + 1) & 1) * kScanBufWords;
+      // iteration j: the helpers stage the next chunk's group j and search group j's
+      // old words, warp 0 resolves group j - 1; every thread runs ng + 1 iterations and
+      // one barrier in each
+      for (int j = 0; j <= ng; ++j) {
+        if (warp != 0) {
+          if (32 * j < rows_next) stage_rows(r0 + rows_chunk, 32 * j, min(32, rows_next - 32 * j), nxt);
+          if (j < ng) {
+            const int g0 = 32 * j;
+            const int G = (r0 + g0) >> 5;
+            const int nw = max(G - 1, 0);
+            const int h = warp - 1;
+            const int wb = (h * nw) / kScanHelpers, we = ((h + 1) * nw) / kScanHelpers;
+            int hit = -1;
+            if (g0 + lane < rows) {
+              const unsigned* row = cur + (g0 + lane) * pitch;
+              // eight words per step: the loads of a step do not wait on each other
+              for (int w = wb; w < we; w += 8) {
+                unsigned m[8], any = 0u;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                  m[q] = (w + q < we) ? (row[w + q] & R[w + q]) : 0u;
+                  any |= m[q];
+                }
+                if (any) {
+                  int q = 7;
+                  unsigned mq = m[7];
+#pragma unroll
+                  for (int u = 6; u >= 0; --u)
+                    if (m[u]) q = u, mq = m[u];
+                  hit = ((w + q) << 5) + __ffs(mq) - 1;
+                  break;
+                }
+              }
+            }
+            if (hit >= 0) atomicMin(&best[j & 1][lane], hit);
+          }
+        } else if (j > 0) {
+          const int g0 = 32 * (j - 1);
+          const int i0 = r0 + g0;  // a multiple of 32: the group's columns are word G
+          const int G = i0 >> 5;
           const int li = i0 + lane;
           const bool live = g0 + lane < rows;
           const unsigned* row = cur + (g0 + lane) * pitch;
-          const int nw_old = i0 >> 5;
-          int old_hit = -1;  // lowest representative chosen before the group with A[li][r]
-          if (live) {
-            // eight words per step: the loads of a step do not wait on each other
-            for (int w = 0; w < nw_old; w += 8) {
-              unsigned m[8], any = 0u;
-#pragma unroll
-              for (int q = 0; q < 8; ++q) {
-                m[q] = (w + q < nw_old) ? (row[w + q] & R[w + q]) : 0u;
-                any |= m[q];
-              }
-              if (any) {
-                int q = 7;
-                unsigned mq = m[7];
-#pragma unroll
-                for (int u = 6; u >= 0; --u)
-                  if (m[u]) q = u, mq = m[u];
-                old_hit = ((w + q) << 5) + __ffs(mq) - 1;
-                break;
-              }
-            }
+          int old_hit = best[(j - 1) & 1][lane];
+          best[(j - 1) & 1][lane] = INT_MAX;  // ready for group j + 1's search
+          if (old_hit == INT_MAX) old_hit = -1;
+          if (live && old_hit < 0 && G >= 1) {
+            const unsigned m = row[G - 1] & R[G - 1];
+            if (m) old_hit = ((G - 1) << 5) + __ffs(m) - 1;
           }
           // similarities to the group's earlier rows (A holds only columns below the row)
-          const unsigned inw = live ? (row[nw_old] & ((1u << lane) - 1u)) : 0u;
+          const unsigned inw = live ? (row[G] & ((1u << lane) - 1u)) : 0u;
           const unsigned open = __ballot_sync(0xffffffffu, live && old_hit < 0);
-          unsigned fresh = 0u;  // the group's new representatives, in order
-          unsigned ib[32];      // every row's in-group word, fetched before the ordered pass
-#pragma unroll
-          for (int b = 0; b < 32; ++b) ib[b] = __shfl_sync(0xffffffffu, inw, b);
-#pragma unroll
-          for (int b = 0; b < 32; ++b)
-            if (((open >> b) & 1u) && !(ib[b] & fresh)) fresh |= 1u << b;
+          // an open row with no open row before it in its word is a new representative;
+          // the others are decided in order against the representatives before them
+          const unsigned dep = __ballot_sync(0xffffffffu, ((open >> lane) & 1u) && (inw & open));
+          unsigned fresh = open & ~dep;
+          for (unsigned dd = dep; dd; dd &= dd - 1u) {
+            const int b = __ffs(dd) - 1;
+            const unsigned wb = __shfl_sync(0xffffffffu, inw, b);
+            if (!(wb & fresh)) fresh |= 1u << b;
+          }
           if (live) {
             int rp;
             if (old_hit >= 0) rp = old_hit;
@@ -247,10 +287,11 @@ __global__ void __launch_bounds__(kScanThreads)
             rep_of[off + li] = off + rp;
           }
           reps += __popc(fresh);
-          if (lane == 0) R[nw_old] = fresh;
-          __syncwarp();
+          if (lane == 0) R[G] = fresh;
         }
+        __syncthreads();
       }
+      if (warp != 0) cp_async_wait_all();
       __syncthreads();
     }
   } else {
