@@ -409,6 +409,45 @@ def test_condense_duplicates_wide_buckets(moe, sizes):
     _status_ok(moe)
 
 
+def test_condense_ragged_buckets(moe):
+    """Empty, single-row and ragged buckets around the scan's 32-row groups and 160-row chunks.
+
+    Half the rows repeat rows of a small pool, the rest are drawn fresh; at tau = 1 every
+    row's representative is the first identical row of its bucket (closed form: distinct
+    random rows are far from cosine 1).
+    """
+    rng = np.random.default_rng(11)
+    d = 256
+    sizes = [0, 1, 31, 32, 33, 0, 161, 353, 2049]
+    pool = gen.round_to_bf16(rng.standard_normal((24, d)).astype(np.float32))
+    rows, expect, distinct = [], [], 0
+    base = 0
+    for n in sizes:
+        first = {}
+        for s in range(n):
+            if rng.random() < 0.5:
+                key, v = int(rng.integers(0, len(pool))), None
+            else:
+                key, v = ("fresh", base + s), gen.round_to_bf16(rng.standard_normal(d).astype(np.float32))
+            rows.append(pool[key] if v is None else v)
+            expect.append(base + first.setdefault(key, s))
+        distinct += len(first)
+        base += n
+    rows = np.stack(rows)
+    P = len(rows)
+    C = moe.Config(T=P, d=d, E=len(sizes), k=1, H=128, n_shared=0, H_shared=0, dtype="bf16",
+                   gating="softmax_topk", residual="none")
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    x_perm = torch.from_numpy(rows).to(device="cuda", dtype=torch.bfloat16)
+    rep_of, n_rep, ncond = moe.condense(C, x_perm, torch.from_numpy(offsets).cuda(), 1.0)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(_np(rep_of)[:P], np.array(expect))
+    per_bucket = [len(set(expect[offsets[e]:offsets[e + 1]])) for e in range(len(sizes))]
+    np.testing.assert_array_equal(_np(n_rep)[: len(sizes)], per_bucket)
+    assert int(ncond.item()) == P - distinct
+    _status_ok(moe)
+
+
 def test_condense_tau_above_one_is_identity(moe):
     cfg, inp, C, w, x, r = _setup(moe, "luffy_condense", T=2048)
     _, idx, _ = moe.route(C, x, w.W_r, w.router_bias)
