@@ -43,10 +43,11 @@
  *     access and return instead of faulting or hanging.
  *   - Outputs may not alias inputs, except that `out` may alias `residual`.
  *   - Sizes: T >= 0 tokens (T == 0 is a no-op), d model dim, E <= 256 routed
- *     experts, 1 <= k <= E, H expert hidden, n_shared shared experts of
- *     hidden H_shared.  bf16 layers need d % 256 == 0, H % 128 == 0 and
- *     H_shared % 128 == 0 (tensor-core tiles); fp32 layers need d % 4 == 0
- *     and H % 4 == 0.
+ *     experts, 1 <= k <= min(E, 32), H expert hidden, n_shared shared experts
+ *     of hidden H_shared (outside these: MOE_ERR_INVALID_ARG).  T * k <= 2^30.
+ *     bf16 layers need d % 256 == 0, H % 128 == 0 and H_shared % 128 == 0
+ *     (tensor-core tiles); fp32 layers need d % 64 == 0, H % 64 == 0 and
+ *     H_shared % 64 == 0.  Otherwise MOE_ERR_UNSUPPORTED.
  */
 #ifndef MOE_H_
 #define MOE_H_
@@ -180,7 +181,8 @@ moe_status moe_dispatch_static_scratch(const moe_config* cfg, const void* x,
                                        moe_stream_t stream);
 
 /* ---------------------------------------------------------------- condensation
- * Luffy token condensation inside each expert bucket (bf16 layers).  Walking a
+ * Luffy token condensation inside each expert bucket (bf16 layers with
+ * T * k <= 65536 when tau <= 1, else MOE_ERR_UNSUPPORTED).  Walking a
  * bucket in slot order with the set R of representatives, slot j is condensed
  * onto the earliest r in R with cos(x_perm[j], x_perm[r]) >= tau, else j joins
  * R.  Bitwise-identical rows have similarity 1; a zero row is otherwise
@@ -227,7 +229,8 @@ moe_status moe_combine(const moe_config* cfg, const void* y_perm, const void* sh
 /* ---------------------------------------------------------------- whole layer
  * route -> dispatch -> [condense if tau <= 1] -> expert FFN -> combine, all on
  * `stream`, no host synchronisation, intermediates in `ws`.
- *   x [T, d] act (in)  residual [T, d] act or NULL (in)  tau: <= 1 condenses, > 1 or NaN does not
+ *   x [T, d] act (in)  residual [T, d] act or NULL (in)  tau: <= 1 condenses (limits as
+ *     moe_condense), > 1 or NaN does not
  *   out [T, d] act (out)
  *   topk_idx_out [T, k] int32 or NULL (out)  n_condensed_out [1] int32 or NULL (out)
  *   ws: moe_workspace_size(cfg, tau <= 1) bytes                                 */

@@ -58,6 +58,8 @@ def _cfg(L, **kw):
     (dict(k=9), 1), (dict(k=0), 1), (dict(E=300, k=2), 1), (dict(T=-1), 1), (dict(d=0), 1),
     (dict(d=200), 2), (dict(H=100), 2), (dict(n_shared=1, H_shared=64), 2),
     (dict(dtype="f32", d=96), 2), (dict(n_shared=1, H_shared=0), 1),
+    (dict(E=64, k=33), 1), (dict(T=(1 << 27) + 1, E=16, k=8), 2),
+    (dict(dtype="f32", H=96), 2), (dict(dtype="f32", n_shared=1, H_shared=96), 2),
 ])
 def test_route_rejects_bad_configs(L, kw, code):
     c = _cfg(L, **kw)
@@ -108,6 +110,24 @@ def test_workspace_checks(L):
     r = lib.moe_expert_ffn(ctypes.byref(cs), ctypes.byref(w), FAKE, FAKE, None, FAKE, FAKE, FAKE,
                            FAKE, 1 << 40, None)
     assert r == 1
+
+
+def test_condensation_limits(L):
+    """Condensation takes bf16 layers with at most 65536 routed pairs (checked on the host)."""
+    lib = L.lib()
+    w = L.moe_weights(FAKE, None, FAKE, FAKE, None, None)
+    cbig = _cfg(L, T=32769)  # k = 2: 65538 pairs
+    r = lib.moe_condense(ctypes.byref(cbig), FAKE, FAKE, 0.9, FAKE, FAKE, FAKE, FAKE, 1 << 40, None)
+    assert r == 2
+    r = lib.moe_layer_forward(ctypes.byref(cbig), ctypes.byref(w), FAKE, None, 0.9, FAKE,
+                              None, None, FAKE, 1 << 40, None)
+    assert r == 2
+    r = lib.moe_layer_forward_ex(ctypes.byref(cbig), ctypes.byref(w), FAKE, None, 0.9, FAKE, None,
+                                 None, None, FAKE, 1 << 40, None, None)
+    assert r == 2
+    c32 = _cfg(L, dtype="f32")
+    r = lib.moe_condense(ctypes.byref(c32), FAKE, FAKE, 0.9, FAKE, FAKE, FAKE, FAKE, 1 << 40, None)
+    assert r == 2
 
 
 def test_layer_forward_ex_argument_checks(L):
