@@ -42,6 +42,8 @@
  *     word that moe_get_device_status reads; the kernels then skip the bad
  *     access and return instead of faulting or hanging.
  *   - Outputs may not alias inputs, except that `out` may alias `residual`.
+ *   - Host threads may call concurrently (each with its own outputs and
+ *     workspace): the one-time set-up per device is guarded by a lock.
  *   - Sizes: T >= 0 tokens (T == 0 is a no-op), d model dim, E <= 256 routed
  *     experts, 1 <= k <= min(E, 32), H expert hidden, n_shared shared experts
  *     of hidden H_shared (outside these: MOE_ERR_INVALID_ARG).  T * k <= 2^30.
@@ -169,8 +171,9 @@ moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* top
  *     every GPU that loads the library until the process exits.  The scratch
  *     needed is 8 * E * ceil(T / 128) bytes; larger shapes return
  *     MOE_ERR_WORKSPACE before anything is launched.
- *   - The first call on a device looks up the array's device address (with
- *     that device current); make that first call before any stream capture.
+ *   - The first call of any entry point on a device looks up the array's
+ *     device address (with that device current); make that first call
+ *     before any stream capture.
  *   - Every call shares the array and it keeps the last call's contents
  *     (nothing in it has to start at zero: each call writes every entry it
  *     reads).  Calls whose kernels overlap on the GPU -- on two streams, or

@@ -5,9 +5,37 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "../../include/moe.h"
 
 namespace moe {
+
+// One-time per-device set-up on the host (function attributes, occupancy queries,
+// symbol addresses), safe for callers on several host threads.  The first caller on
+// a device runs init() under one library-wide lock; the flag is then published with
+// release order and read with acquire order, so a caller that finds it set also sees
+// everything init() wrote.  A failed init() leaves the flag clear (the next call
+// retries).  Devices at or above N are not cached: init() runs on every call.
+inline std::mutex& setup_mutex() {
+  static std::mutex m;
+  return m;
+}
+template <int N>
+struct OncePerDevice {
+  std::atomic<bool> done[N] = {};
+  template <class F>
+  cudaError_t run(int dev, F&& init) {
+    if (dev < 0 || dev >= N) return init();
+    if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(setup_mutex());
+    if (done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+    const cudaError_t e = init();
+    if (e == cudaSuccess) done[dev].store(true, std::memory_order_release);
+    return e;
+  }
+};
 
 // Status codes recorded on the device (a per-device word; see moe_api.cu).
 // The first condition wins; later ones are dropped until the host reads it.

@@ -492,15 +492,14 @@ cudaError_t launch_condense(const __nv_bfloat16* x_perm, const int32_t* offsets,
   if (err != cudaSuccess) return err;
   const size_t smem = sizeof(unsigned) * (kMaxWords + 2 * kScanBufWords);
   // the shared-memory limit is a per-device attribute of the function
-  static bool attr_set[64] = {};
+  static OncePerDevice<64> once;
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 64 || !attr_set[dev]) {
-    err = cudaFuncSetAttribute(greedy_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
-    if (dev < 64) attr_set[dev] = true;
-  }
+  err = once.run(dev, [&]() {
+    return cudaFuncSetAttribute(greedy_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(smem));
+  });
+  if (err != cudaSuccess) return err;
   greedy_scan_kernel<<<E, kScanThreads, smem, stream>>>(s.bits, s.bits_base, offsets, rep_of,
                                                         n_rep, status);
   condensed_count_kernel<<<1, 32, 0, stream>>>(offsets, n_rep, E, n_condensed);

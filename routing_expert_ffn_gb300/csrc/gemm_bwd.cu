@@ -587,15 +587,16 @@ __global__ void __launch_bounds__(bw::NUM_THREADS, 1)
 namespace {
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  // looked up once (a function-local static is initialised once, even with concurrent callers)
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return nullptr;
+  }();
   return fn;
 }
 
@@ -629,11 +630,11 @@ bool make_out_map(CUtensorMap* m, float* base, uint64_t inner, uint64_t rows) {
 template <int MODE>
 cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
                    const BwdArgs& args, int num_sms, cudaStream_t stream) {
-  static bool attr_set[64] = {};
+  static OncePerDevice<64> once;
   static int max_clusters[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
+  const cudaError_t set_up = once.run(dev, [&]() -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(bwd_gemm_pair_kernel<MODE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          bw::SMEM_BYTES);
@@ -652,9 +653,10 @@ cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorM
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, bwd_gemm_pair_kernel<MODE>, &q) != cudaSuccess || n <= 0)
       n = num_sms / 2;
-    max_clusters[dev] = n;
-    attr_set[dev] = true;
-  }
+    if (dev < 64) max_clusters[dev] = n;
+    return cudaSuccess;
+  });
+  if (set_up != cudaSuccess) return set_up;
   int clusters = num_sms / 2;
   if (dev < 64 && max_clusters[dev] < clusters) clusters = max_clusters[dev];
   cudaLaunchConfig_t cfg = {};

@@ -937,15 +937,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // ---------------------------------------------------------------- host side
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  // looked up once (a function-local static is initialised once, even with concurrent callers)
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return nullptr;
+  }();
   return fn;
 }
 
@@ -1003,12 +1004,12 @@ static cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const
                                const CUtensorMap& w5, const CUtensorMap& o, const TcGemmArgs& args,
                                int num_sms,
                                cudaStream_t stream) {
-  static bool attr_set[64] = {};
+  static OncePerDevice<64> once;
   static int max_clusters[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   cudaLaunchConfig_t cfg = {};
-  if (dev < 64 && !attr_set[dev]) {
+  const cudaError_t set_up = once.run(dev, [&]() -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<MODE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          pr::SMEM_BYTES);
@@ -1028,9 +1029,10 @@ static cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const
     if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<MODE>, &cfg) != cudaSuccess ||
         n <= 0)
       n = num_sms / 2;
-    max_clusters[dev] = n;
-    attr_set[dev] = true;
-  }
+    if (dev < 64) max_clusters[dev] = n;
+    return cudaSuccess;
+  });
+  if (set_up != cudaSuccess) return set_up;
   const int clusters = dev < 64 ? (max_clusters[dev] < num_sms / 2 ? max_clusters[dev] : num_sms / 2)
                                 : num_sms / 2;
   cfg = cudaLaunchConfig_t{};
@@ -1053,15 +1055,14 @@ static cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const
 template <int MODE>
 static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const TcGemmArgs& args,
                           int grid, cudaStream_t stream) {
-  static bool attr_set[64] = {};
+  static OncePerDevice<64> once;
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
+  const cudaError_t e = once.run(dev, [&]() {
+    return cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  });
+  if (e != cudaSuccess) return e;
   return launch_pdl(grouped_gemm_kernel<MODE>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, stream, a,
                     b, args);
 }

@@ -11,31 +11,42 @@ namespace moe {
 // One status word per device, shared by every call on that device.
 static __device__ unsigned g_status_word;
 
+// Scratch of moe_dispatch_static_scratch (the one entry point without a
+// workspace): a file-scope device array, so every GPU that loads the library
+// holds these bytes until the process exits.
+constexpr size_t kStaticDispatchScratchBytes = size_t(1) << 20;  // 1 MiB
+static __device__ __align__(256) unsigned char g_dispatch_scratch[kStaticDispatchScratchBytes];
+
 namespace {
 
 constexpr int kMaxDevices = 64;
 
+// Device addresses of the two file-scope arrays (in host code their names are only
+// host-side stand-ins, never device addresses) and the SM count.
 struct DeviceInfo {
-  bool ready = false;
   int num_sms = 0;
   unsigned* status = nullptr;
+  void* dispatch_scratch = nullptr;
 };
 DeviceInfo g_dev[kMaxDevices];
+OncePerDevice<kMaxDevices> g_dev_once;
 
 // Per-device set-up, done on the first call made with that device current.
 DeviceInfo* device_info() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   DeviceInfo& d = g_dev[dev];
-  if (!d.ready) {
-    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return nullptr;
+  const cudaError_t e = g_dev_once.run(dev, [&]() -> cudaError_t {
+    cudaError_t r = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (r != cudaSuccess) return r;
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    if ((r = cudaGetSymbolAddress(&p, g_status_word)) != cudaSuccess) return r;
     d.status = static_cast<unsigned*>(p);
-    d.ready = true;
-  }
-  return &d;
+    if ((r = cudaGetSymbolAddress(&p, g_dispatch_scratch)) != cudaSuccess) return r;
+    d.dispatch_scratch = p;
+    return cudaSuccess;
+  });
+  return e == cudaSuccess ? &d : nullptr;
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -996,18 +1007,7 @@ extern "C" moe_status moe_layer_backward(const moe_config* cfg, const moe_weight
 
 // ------------------------------------------------------------------ dispatch without a workspace
 // For callers that cannot allocate device memory: the dispatch scratch lives
-// in this file-scope device array instead of a caller workspace.  Every GPU
-// that loads the library holds these bytes until the process exits.
-namespace moe {
-namespace {
-constexpr size_t kStaticDispatchScratchBytes = size_t(1) << 20;  // 1 MiB
-static __device__ __align__(256) unsigned char g_dispatch_scratch[kStaticDispatchScratchBytes];
-// Device address of g_dispatch_scratch, looked up once per device.  In host
-// code the array's name is only a host-side stand-in, never a device address.
-void* g_dispatch_scratch_addr[kMaxDevices] = {};
-}  // namespace
-}  // namespace moe
-
+// in the file-scope device array g_dispatch_scratch instead of a caller workspace.
 extern "C" moe_status moe_dispatch_static_scratch(const moe_config* cfg, const void* x,
                                                   const int32_t* topk_idx, int32_t* counts,
                                                   int32_t* offsets, int32_t* perm,
@@ -1028,15 +1028,8 @@ extern "C" moe_status moe_dispatch_static_scratch(const moe_config* cfg, const v
     return MOE_ERR_WORKSPACE;
   DeviceInfo* di = device_info();
   if (!di) return MOE_ERR_CUDA;
-  int dev = 0;
-  MOE_CUDA(cudaGetDevice(&dev));
-  if (!g_dispatch_scratch_addr[dev]) {
-    void* p = nullptr;
-    MOE_CUDA(cudaGetSymbolAddress(&p, g_dispatch_scratch));
-    g_dispatch_scratch_addr[dev] = p;
-  }
   MOE_CUDA(launch_dispatch(cfg->act_dtype, x, topk_idx, cfg->T, cfg->d, cfg->E, cfg->k, counts,
-                           offsets, perm, slot_of, x_perm, g_dispatch_scratch_addr[dev],
+                           offsets, perm, slot_of, x_perm, di->dispatch_scratch,
                            di->status, reinterpret_cast<cudaStream_t>(stream)));
   return MOE_OK;
 }
