@@ -286,6 +286,10 @@ __device__ int block_scan_smem(int* a, int n, int* wsum /* 33 ints */) {
 // counts and offsets -- this replaces a separate scan launch.  Otherwise blk
 // is already the exclusive prefix.
 constexpr int kRowChunk = 8;
+// Largest count table the scatter scans in shared memory: its dynamic shared memory
+// (4 bytes per entry) plus the static wsum[33] must stay within the 48 KB a launch may
+// use without opting in to more.
+constexpr int kScatterScanMaxEntries = (48 * 1024 - 33 * static_cast<int>(sizeof(int))) / 4;
 template <typename T, bool SCAN>
 __global__ void __launch_bounds__(256)
     scatter_rows_kernel(const T* __restrict__ x, const int32_t* __restrict__ idx,
@@ -539,7 +543,7 @@ cudaError_t launch_dispatch_auto(int act_dtype, const void* x, const int32_t* to
                                static_cast<int>(P), E, n_blk, local_rank, blk, status);
   if (err != cudaSuccess) return err;
   const long long table = static_cast<long long>(E) * n_blk;
-  const bool scan_in_smem = table <= 12288;  // 48 KB of shared memory per CTA
+  const bool scan_in_smem = table <= kScatterScanMaxEntries;
   if (!scan_in_smem) {
     err = launch_pdl(dispatch_block_scan_kernel, dim3(1), dim3(1024), 0, stream, blk, E, n_blk,
                      counts, offsets);
