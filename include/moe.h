@@ -46,7 +46,8 @@
  *     workspace): the one-time set-up per device is guarded by a lock.
  *   - Sizes: T >= 0 tokens (T == 0 is a no-op), d model dim, E <= 256 routed
  *     experts, 1 <= k <= min(E, 32), H expert hidden, n_shared shared experts
- *     of hidden H_shared (outside these: MOE_ERR_INVALID_ARG).  T * k <= 2^30.
+ *     of hidden H_shared (outside these: MOE_ERR_INVALID_ARG).  T * k <= 2^24
+ *     routed pairs per call (else MOE_ERR_UNSUPPORTED).
  *     bf16 layers need d % 256 == 0, H % 128 == 0 and H_shared % 128 == 0
  *     (tensor-core tiles); fp32 layers need d % 64 == 0, H % 64 == 0 and
  *     H_shared % 64 == 0.  Otherwise MOE_ERR_UNSUPPORTED.

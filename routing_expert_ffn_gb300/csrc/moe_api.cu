@@ -63,7 +63,9 @@ moe_status check_cfg(const moe_config* c) {
     return MOE_ERR_INVALID_ARG;
   if (c->residual < MOE_RES_NONE || c->residual > MOE_RES_INPUT_PLUS_EXTERNAL)
     return MOE_ERR_INVALID_ARG;
-  if (static_cast<long long>(c->T) * c->k > (1ll << 30)) return MOE_ERR_UNSUPPORTED;
+  // At most 2^24 routed pairs per call: the grouped GEMM packs an expert's 256-row pair
+  // count into 16 bits, so no expert may hold 2^24 rows or more.
+  if (static_cast<long long>(c->T) * c->k > (1ll << 24)) return MOE_ERR_UNSUPPORTED;
   if (c->act_dtype == MOE_BF16) {
     if (c->d % 256 || c->H % 128 || (c->n_shared > 0 && c->H_shared % 128))
       return MOE_ERR_UNSUPPORTED;

@@ -58,13 +58,22 @@ def _cfg(L, **kw):
     (dict(k=9), 1), (dict(k=0), 1), (dict(E=300, k=2), 1), (dict(T=-1), 1), (dict(d=0), 1),
     (dict(d=200), 2), (dict(H=100), 2), (dict(n_shared=1, H_shared=64), 2),
     (dict(dtype="f32", d=96), 2), (dict(n_shared=1, H_shared=0), 1),
-    (dict(E=64, k=33), 1), (dict(T=(1 << 27) + 1, E=16, k=8), 2),
+    (dict(E=64, k=33), 1), (dict(T=(1 << 27) + 1, E=16, k=8), 2), (dict(T=(1 << 21) + 1, k=8), 2),
     (dict(dtype="f32", H=96), 2), (dict(dtype="f32", n_shared=1, H_shared=96), 2),
 ])
 def test_route_rejects_bad_configs(L, kw, code):
     c = _cfg(L, **kw)
     r = L.lib().moe_route(ctypes.byref(c), FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, 1 << 40, None)
     assert r == code
+
+
+def test_pair_limit_boundary(L):
+    """2^24 routed pairs are accepted (the workspace query answers), one token more is not."""
+    lib = L.lib()
+    ok = _cfg(L, T=1 << 21, E=16, k=8)
+    over = _cfg(L, T=(1 << 21) + 1, E=16, k=8)
+    assert lib.moe_dispatch_workspace_size(ctypes.byref(ok)) > 0
+    assert lib.moe_dispatch_workspace_size(ctypes.byref(over)) == 0
 
 
 def test_route_rejects_null_and_misaligned(L):
