@@ -36,3 +36,17 @@ def test_reference_arm_other_ranks_do_no_work():
     r = _run({"RANK": "1", "WORLD_SIZE": "2"})
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+def test_launch_count_claim_matches_the_launch_lists():
+    """gpu_launches per step, as the committed ncu launch lists count them: 12 launches per
+    DeepSeek-V2-Lite forward (router 3, dispatch 2, m-tile tables 2, GEMMs 4, combine 1) and
+    17 per condensing Luffy-shaped forward."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    from routing_expert_ffn_gb300 import inputs as gen
+    assert bench.launches_per_step(gen.CONFIGS["dsv2_lite"], False) == 12
+    assert bench.launches_per_step(gen.CONFIGS["luffy_condense"], True) == 17
+    # 64 tokens: FMA router (logits + top-k), no weight split
+    assert bench.launches_per_step(gen.CONFIGS["dsv2_lite_decode"], False) == 11
