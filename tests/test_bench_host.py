@@ -1,4 +1,5 @@
-"""bench.py --impl reference on the host: one JSON line from rank 0, nothing from other ranks."""
+"""bench.py host logic: the reference arm (one JSON line from rank 0, nothing from other
+ranks) and the per-step launch count it claims."""
 from __future__ import annotations
 
 import json
