@@ -91,36 +91,6 @@ def test_dispatch_full_size(moe, name):
     _status_ok(moe)
 
 
-@pytest.mark.parametrize("E,T,k", [(256, 8192, 8), (256, 50000, 1), (256, 49152, 1),
-                                   (215, 58000, 1)])
-def test_dispatch_large_rank_tables(moe, E, T, k):
-    """(expert, 1024-pair block) count tables of 16384, 12544 and 12288 entries take the
-    separate one-CTA table scan; 12255 entries (E = 215, 57 blocks), the most the scatter
-    scans in shared memory within 48 KB, take the fused scan.  Skewed expert choices leave
-    empty buckets; everything bit for bit."""
-    d = 256
-    rng = np.random.default_rng(T + k)
-    pop = np.log(np.arange(1, E + 1) ** -1.1)[rng.permutation(E)]
-    pop[rng.choice(E, 5, replace=False)] = -np.inf  # never chosen: empty buckets
-    # k distinct experts per token, drawn with a Zipf-like popularity
-    keys = pop[None, :] + rng.gumbel(size=(T, E))
-    idx_np = np.argsort(-keys, axis=1)[:, :k].astype(np.int32)
-    C = moe.Config(T=T, d=d, E=E, k=k, H=128, n_shared=0, H_shared=0, dtype="bf16",
-                   gating="softmax_topk", residual="none")
-    rows = gen.round_to_bf16(rng.standard_normal((T, d)).astype(np.float32))
-    x = torch.from_numpy(rows).to(device="cuda", dtype=torch.bfloat16)
-    out = moe.dispatch(C, x, torch.from_numpy(idx_np).cuda())
-    torch.cuda.synchronize()
-    counts, offsets, perm, slot_of = orc.dispatch(idx_np, E)
-    assert (counts == 0).any()
-    np.testing.assert_array_equal(_np(out["counts"]), counts)
-    np.testing.assert_array_equal(_np(out["offsets"]), offsets)
-    np.testing.assert_array_equal(_np(out["perm"])[: T * k], perm)
-    np.testing.assert_array_equal(_np(out["slot_of"]), slot_of)
-    assert torch.equal(out["x_perm"][: T * k], x.index_select(0, out["perm"][: T * k].long()))
-    _status_ok(moe)
-
-
 def test_dispatch_empty_buckets_and_skew(moe):
     cfg, inp, C, w, x, r = _setup(moe, "qwen3_30b_a3b")
     _, idx, _ = moe.route(C, x, w.W_r, w.router_bias)
@@ -497,3 +467,34 @@ def test_condensed_layer_small(moe):
     cfg = gen.CONFIGS["luffy_condense"]
     for tau in cfg.taus:
         _layer_check(moe, "luffy_condense", T=SMALL_T["luffy_condense"], tau=tau)
+
+
+# ------------------------------------------------------------------ limits of the boundary
+@pytest.mark.parametrize("E,T,k", [(256, 8192, 8), (256, 50000, 1), (256, 49152, 1),
+                                   (215, 58000, 1)])
+def test_dispatch_large_rank_tables(moe, E, T, k):
+    """(expert, 1024-pair block) count tables of 16384, 12544 and 12288 entries take the
+    separate one-CTA table scan; 12255 entries (E = 215, 57 blocks), the most the scatter
+    scans in shared memory within 48 KB, take the fused scan.  Skewed expert choices leave
+    empty buckets; everything bit for bit."""
+    d = 256
+    rng = np.random.default_rng(T + k)
+    pop = np.log(np.arange(1, E + 1) ** -1.1)[rng.permutation(E)]
+    pop[rng.choice(E, 5, replace=False)] = -np.inf  # never chosen: empty buckets
+    # k distinct experts per token, drawn with a Zipf-like popularity
+    keys = pop[None, :] + rng.gumbel(size=(T, E))
+    idx_np = np.argsort(-keys, axis=1)[:, :k].astype(np.int32)
+    C = moe.Config(T=T, d=d, E=E, k=k, H=128, n_shared=0, H_shared=0, dtype="bf16",
+                   gating="softmax_topk", residual="none")
+    rows = gen.round_to_bf16(rng.standard_normal((T, d)).astype(np.float32))
+    x = torch.from_numpy(rows).to(device="cuda", dtype=torch.bfloat16)
+    out = moe.dispatch(C, x, torch.from_numpy(idx_np).cuda())
+    torch.cuda.synchronize()
+    counts, offsets, perm, slot_of = orc.dispatch(idx_np, E)
+    assert (counts == 0).any()
+    np.testing.assert_array_equal(_np(out["counts"]), counts)
+    np.testing.assert_array_equal(_np(out["offsets"]), offsets)
+    np.testing.assert_array_equal(_np(out["perm"])[: T * k], perm)
+    np.testing.assert_array_equal(_np(out["slot_of"]), slot_of)
+    assert torch.equal(out["x_perm"][: T * k], x.index_select(0, out["perm"][: T * k].long()))
+    _status_ok(moe)
