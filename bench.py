@@ -6,11 +6,15 @@
 A step is one moe_layer_forward_ex call (router -> dispatch -> [condensation] ->
 routed experts -> combine, with the shared experts on a second stream beside
 dispatch and the routed experts) over one batch of T synthetic tokens already
-resident in HBM; the single-stream moe_layer_forward is timed beside it.  Default workload: the DeepSeek-V2-Lite-shaped bf16 layer (T=4096,
-d=2048, 64 experts top-6, hidden 1408, 2 shared experts).  Inputs and weights
-are seeded synthetic draws (routing_expert_ffn_gb300.inputs); the weights
-(1.1 GB) exceed L2 and L2 is additionally flushed (a 256 MB write) between
-timed steps, outside the timed events.
+resident in HBM; the single-stream moe_layer_forward is timed beside it.
+Default workload: the largest layer of the five, the Llama-4-Scout-shaped bf16
+layer with FarSkip-Collective wiring (T=8192, d=5120, 16 experts top-1 sigmoid,
+hidden 8192, 1 shared expert of hidden 8192, external attention-partial
+residual); --workload names any other.  Inputs and weights are seeded synthetic
+draws (routing_expert_ffn_gb300.inputs); the weights exceed L2 and L2 is
+additionally flushed (a 256 MB write) between timed steps, outside the timed
+events.  Besides the K timed steps, a steady region replays the same step for
+at least one second (and at least 200 steps) with its own clock samples.
 
 Under torchrun each rank runs an independent replica on its own GPU (weak
 scaling, no data-path collective); the reported time is the max over ranks.
@@ -149,8 +153,8 @@ def launches_per_step(cfg, condense: bool) -> int:
     # logits and the top-k; fp32 layers and small batches run FMA logits and the top-k
     n = 3 if cfg.dtype == "bf16" and cfg.T > 256 else 2
     # dispatch: block ranks and row scatter; the (expert, 1024-pair block) count table is
-    # scanned inside the scatter up to 12255 entries, by a launch of its own above that
-    n += 2 + (cfg.E * -(-(cfg.T * cfg.k) // 1024) > 12255)
+    # scanned inside the scatter up to 8192 entries, by a launch of its own above that
+    n += 2 + (cfg.E * -(-(cfg.T * cfg.k) // 1024) > 8192)
     if condense:
         n += 6  # row stats, m-tiles, tile list, similarity GEMM, greedy scan, count
         n += 3  # compact reps, m-tiles over representatives, gather representative rows
@@ -234,16 +238,20 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     def layer_step():
         layer(x, r, tau, out=out, n_condensed_out=ncond, partial_out=part, aux_stream=aux)
 
-    def timed(g) -> float:
+    def timed_each(g, n) -> list:
+        """Per-step device ms of n replays, L2 flushed before each (outside the events)."""
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-        for i in range(args.steps):
+               for _ in range(n)]
+        for i in range(n):
             flush.zero_()
             evs[i][0].record(stream)
             g.replay()
             evs[i][1].record(stream)
         torch.cuda.synchronize()
-        return sum(a.elapsed_time(b) for a, b in evs) / args.steps
+        return [a.elapsed_time(b) for a, b in evs]
+
+    def timed(g) -> float:
+        return sum(timed_each(g, args.steps)) / args.steps
 
     graph = capture(torch, layer_step)
     for _ in range(args.warmup):
@@ -262,6 +270,25 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     clocks = sampler.stop()
     barrier()
     ms = max_over_ranks(ms, world, dev)
+
+    # Steady region: the same step replayed for >= 1 s of device time (and >= 200 steps),
+    # so that a box's clock behaviour and run-to-run noise can be told apart from a change.
+    n_steady = max(200, int(math.ceil(1000.0 / max(ms, 1e-3))))
+    sampler2 = ClockSampler(local_rank)
+    barrier()
+    torch.cuda.synchronize()
+    sampler2.start()
+    per = timed_each(graph, n_steady)
+    clocks2 = sampler2.stop()
+    barrier()
+    med = statistics.median(per)
+    steady = {"steps": n_steady, "device_s": sum(per) / 1e3, "median_ms": med,
+              "p10_ms": sorted(per)[len(per) // 10], "p90_ms": sorted(per)[(9 * len(per)) // 10],
+              "median_tokens_per_s": job_tokens_per_s(C.T, world, max_over_ranks(med, world, dev)),
+              "clocks": clocks2}
+    if clocks2.get("sm_mhz") and clocks2.get("sm_max_mhz"):
+        # the step time scaled to the maximum SM clock (time x median MHz / max MHz)
+        steady["median_ms_at_max_clock"] = med * clocks2["sm_mhz"] / clocks2["sm_max_mhz"]
 
     # For comparison: the same layer as one moe_layer_forward call on a single stream.
     g_serial = capture(torch, lambda: layer(x, r, tau, out=out, n_condensed_out=ncond))
@@ -369,6 +396,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         "condensed": n_condensed,
         "gpu_launches": launches_per_step(C, condense) * args.steps,
         "clocks": clocks,
+        "steady": steady,
         "e2e": e2e,
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -621,7 +649,13 @@ def run_reference(args, rank: int) -> None:
     from routing_expert_ffn_gb300 import inputs as gen
     cfg = gen.CONFIGS[args.workload]
     inp64 = _as_f64(gen.make_inputs(cfg))
-    T_s = min(cfg.T, args.reference_tokens)
+    # Each step is a bounded token sample, sized from one 32-token call so that the whole
+    # run (warm-up and timed steps) takes about --reference-seconds of host time.
+    t0 = time.perf_counter()
+    _oracle_call(orc, cfg, inp64, min(cfg.T, 32))
+    per_token = (time.perf_counter() - t0) / min(cfg.T, 32)
+    per_step = args.reference_seconds / (args.warmup + args.steps)
+    T_s = int(max(16, min(cfg.T, args.reference_tokens, per_step / max(per_token, 1e-9))))
     times = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
@@ -648,11 +682,14 @@ def main() -> None:
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="dsv2_lite")
+    ap.add_argument("--workload", default="llama4_scout_farskip")
     ap.add_argument("--no-backward", action="store_true", help="skip timing the layer backward")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--reference-tokens", type=int, default=1024)
+    ap.add_argument("--reference-tokens", type=int, default=1024,
+                    help="most tokens per reference step")
+    ap.add_argument("--reference-seconds", type=float, default=150.0,
+                    help="host time the whole reference run aims at")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -152,9 +152,9 @@ moe_status moe_route(const moe_config* cfg, const void* x, const float* W_r, con
  * routed to e in ascending token order; buckets are laid end to end.
  *   topk_idx [T, k] int32   (in)   entries outside [0, E) are skipped and flagged
  *   counts   [E] int32      (out)  tokens per expert
- *   offsets  [E+1] int32    (out)  exclusive prefix of counts; offsets[E] = T*k
+ *   offsets  [E+1] int32    (out)  exclusive prefix of counts; offsets[E] = T*k minus skipped entries
  *   perm     [T*k] int32    (out)  slot -> token
- *   slot_of  [T, k] int32   (out)  (token, j) -> slot
+ *   slot_of  [T, k] int32   (out)  (token, j) -> slot; -1 for a skipped entry
  *   x_perm   [T*k, d] act   (out)  x_perm[s] = x[perm[s]]
  *   ws       moe_dispatch_workspace_size(cfg) bytes of scratch              */
 size_t moe_dispatch_workspace_size(const moe_config* cfg);

@@ -9,10 +9,11 @@
 // expert and the residual base (Eq. 6 with its o_0 term, referee minor 1).
 //
 // Two index paths give the same slots.  The one the ABI calls ranks pairs in
-// parallel blocks of 256 (warp match + popc, block prefix), scans the
-// (expert, block) counts in one CTA, and scatters rows pair by pair.  The
-// chunked path (per-chunk counts, scan over (expert, chunk), in-chunk ranks by
-// one warp, slot-driven row gather) serves the no-workspace entry point.  Ranks come from a
+// parallel blocks of 1024 (warp match + popc, block prefix), scans the
+// (expert, block) counts (inside the scatter's CTAs when the table is small,
+// else in one CTA of its own), and scatters rows token by token.  The chunked
+// path (per-chunk counts, scan over (expert, chunk), in-chunk ranks by one
+// warp, slot-driven row gather) serves the no-workspace entry point.  Ranks come from a
 // warp match + popc in pair order, so the permutation is the same on every
 // run; the combine sums in a fixed order.
 #include "common.cuh"
@@ -50,41 +51,6 @@ __global__ void __launch_bounds__(256)
     chunk_counts[static_cast<long long>(e) * n_chunks + c] = cnt[e];
 }
 
-// One CTA: expert totals, offsets, and the first slot of every (expert, chunk).
-__global__ void __launch_bounds__(256)
-    dispatch_scan_kernel(const int32_t* __restrict__ chunk_counts, int E, int n_chunks,
-                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-                         int32_t* __restrict__ chunk_base) {
-  __shared__ int s_cnt[256];
-  __shared__ int s_off[257];
-  const int e = threadIdx.x;
-  if (e < E) {
-    int tot = 0;
-    for (int c = 0; c < n_chunks; ++c) tot += chunk_counts[static_cast<long long>(e) * n_chunks + c];
-    s_cnt[e] = tot;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int run = 0;
-    for (int i = 0; i < E; ++i) {
-      s_off[i] = run;
-      run += s_cnt[i];
-    }
-    s_off[E] = run;
-  }
-  __syncthreads();
-  if (e < E) {
-    counts[e] = s_cnt[e];
-    offsets[e] = s_off[e];
-    int run = s_off[e];
-    for (int c = 0; c < n_chunks; ++c) {
-      chunk_base[static_cast<long long>(e) * n_chunks + c] = run;
-      run += chunk_counts[static_cast<long long>(e) * n_chunks + c];
-    }
-  }
-  if (threadIdx.x == 0) offsets[E] = s_off[E];
-}
-
 // One CTA per chunk: all threads stage the chunk's expert ids in shared
 // memory, then warp 0 walks the pairs in (token, j) order, 32 at a time; lanes
 // holding the same expert get consecutive slots in lane order.
@@ -115,11 +81,12 @@ __global__ void __launch_bounds__(kScatterThreads)
       if (e < 0 || e >= E) e = -1;
     }
     const unsigned peers = __match_any_sync(0xffffffffu, e);
-    int slot = 0;
     if (e >= 0) {
-      slot = base[e] + __popc(peers & lt);
+      const int slot = base[e] + __popc(peers & lt);
       perm[slot] = static_cast<int32_t>(p / k);
       slot_of[p] = slot;
+    } else if (i < n) {
+      slot_of[p] = -1;  // out-of-range expert (flagged by the histogram): no slot
     }
     __syncwarp();
     if (e >= 0 && lane == 31 - __clz(peers)) base[e] += __popc(peers);
@@ -175,86 +142,57 @@ __global__ void __launch_bounds__(kLocalPairs)
   if (p < P) local_rank[p] = e >= 0 ? wh(warp, e) + r : -1;
 }
 
-// One CTA: blk <- exclusive prefix of blk (expert-major), counts, offsets.
-// The table goes through shared memory in coalesced pieces of kScanPiece
-// entries; each thread scans 8 consecutive entries of a piece.
+// One CTA: out <- exclusive prefix of the (expert, block) count table in (expert-major,
+// so expert e's slots start at offsets[e] and inside e block b's pairs follow blocks < b),
+// plus counts and offsets.  out may be in (each piece is read before it is written).
+// The table goes through shared memory in coalesced pieces of kScanPiece entries, each
+// scanned by block_scan_smem and offset by the total of the pieces before it.  An empty
+// table (n_blk = 0) gives zeros.
 constexpr int kScanPiece = 8192;
+__device__ int block_scan_smem(int* a, int n, int* wsum);
 __global__ void __launch_bounds__(1024)
-    dispatch_block_scan_kernel(int32_t* __restrict__ blk, int E, int n_blk,
+    dispatch_block_scan_kernel(const int32_t* in, int32_t* out, int E, int n_blk,
                                int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
   __shared__ int piece[kScanPiece];
-  __shared__ int warp_sum[32];
-  __shared__ int carry;
+  __shared__ int wsum[33];
   const long long N = static_cast<long long>(E) * n_blk;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   pdl_trigger();
   pdl_wait();
-  if (threadIdx.x == 0) carry = 0;
+  int carry = 0;
   for (long long base = 0; base < N; base += kScanPiece) {
     const int n = static_cast<int>(min(static_cast<long long>(kScanPiece), N - base));
+    for (int i = threadIdx.x; i < n; i += blockDim.x) piece[i] = in[base + i];
     __syncthreads();
-    for (int i = threadIdx.x; i < n; i += blockDim.x) piece[i] = blk[base + i];
-    __syncthreads();
-    const int a = threadIdx.x * 8;
-    int v[8], mine = 0;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      v[u] = a + u < n ? piece[a + u] : 0;
-      mine += v[u];
-    }
-    int incl = mine;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    if (lane == 31) warp_sum[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-      const int w = warp_sum[lane];
-      int wi = w;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, wi, o);
-        if (lane >= o) wi += y;
-      }
-      warp_sum[lane] = wi - w;
-    }
-    __syncthreads();
-    int run = carry + warp_sum[warp] + incl - mine;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      if (a + u < n) piece[a + u] = run;
-      run += v[u];
-    }
-    __syncthreads();
-    if (threadIdx.x == blockDim.x - 1) carry = run;  // the last thread's run is the total so far
-    for (int i = threadIdx.x; i < n; i += blockDim.x) blk[base + i] = piece[i];
+    const int total = block_scan_smem(piece, n, wsum);  // ends with a barrier
+    for (int i = threadIdx.x; i < n; i += blockDim.x) out[base + i] = carry + piece[i];
+    carry += total;
+    __syncthreads();  // the piece is rewritten by the next iteration
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) offsets[e] = blk[static_cast<long long>(e) * n_blk];
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    offsets[e] = n_blk > 0 ? out[static_cast<long long>(e) * n_blk] : 0;
   if (threadIdx.x == 0) offsets[E] = carry;
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) counts[e] = offsets[e + 1] - offsets[e];
 }
 
-// Exclusive prefix of a[0..n) in shared memory by the whole CTA; returns the total.
+// Exclusive prefix of a[0..n) in shared memory by the whole CTA (blockDim a multiple of
+// 32, at most 1024); returns the total.  Warp w owns the contiguous chunk
+// [w C, w C + C) with C a multiple of 32 and reads it 32 consecutive entries at a time
+// (one bank per lane, no conflicts): first the chunk's sum, then, after a scan of the
+// warp sums, a shuffle scan of each 32-entry step carried along the chunk.
 __device__ int block_scan_smem(int* a, int n, int* wsum /* 33 ints */) {
-  const int nt = blockDim.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int seg = (n + nt - 1) / nt;
-  const int lo = min(n, t * seg), hi = min(n, lo + seg);
-  int mine = 0;
-  for (int i = lo; i < hi; ++i) mine += a[i];
-  int incl = mine;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int C = ((n + nw - 1) / nw + 31) & ~31;
+  const int lo = min(n, warp * C), hi = min(n, lo + C);
+  int part = 0;
+  for (int i = lo + lane; i < hi; i += 32) part += a[i];
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) wsum[warp] = incl;
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+  if (lane == 0) wsum[warp] = part;
   __syncthreads();
   if (warp == 0) {
-    const int v = lane < (nt >> 5) ? wsum[lane] : 0;
+    const int v = lane < nw ? wsum[lane] : 0;
     int wi = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -265,11 +203,18 @@ __device__ int block_scan_smem(int* a, int n, int* wsum /* 33 ints */) {
     if (lane == 31) wsum[32] = wi;
   }
   __syncthreads();
-  int run = wsum[warp] + incl - mine;
-  for (int i = lo; i < hi; ++i) {
-    const int c = a[i];
-    a[i] = run;
-    run += c;
+  int carry = wsum[warp];
+  for (int i0 = lo; i0 < hi; i0 += 32) {
+    const int i = i0 + lane;
+    const int v = i < hi ? a[i] : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (i < hi) a[i] = carry + incl - v;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
   }
   __syncthreads();
   return wsum[32];
@@ -286,10 +231,12 @@ __device__ int block_scan_smem(int* a, int n, int* wsum /* 33 ints */) {
 // counts and offsets -- this replaces a separate scan launch.  Otherwise blk
 // is already the exclusive prefix.
 constexpr int kRowChunk = 8;
-// Largest count table the scatter scans in shared memory: its dynamic shared memory
-// (4 bytes per entry) plus the static wsum[33] must stay within the 48 KB a launch may
-// use without opting in to more.
-constexpr int kScatterScanMaxEntries = (48 * 1024 - 33 * static_cast<int>(sizeof(int))) / 4;
+// Largest count table the scatter scans in shared memory (32 KB of dynamic shared memory,
+// 4 bytes per entry).  Larger tables take the one-CTA scan: every scatter CTA would
+// otherwise re-read and re-scan a table that long.  scatter_scan_limit() checks at
+// set-up that this, plus the kernel's static shared memory and the dynamic region's
+// alignment, fits what a launch may use without opting in.
+constexpr int kScatterScanMaxEntries = 8192;
 template <typename T, bool SCAN>
 __global__ void __launch_bounds__(256)
     scatter_rows_kernel(const T* __restrict__ x, const int32_t* __restrict__ idx,
@@ -510,8 +457,8 @@ cudaError_t launch_dispatch(int act_dtype, const void* x, const int32_t* topk_id
     dispatch_hist_kernel<<<n_chunks, 256, 0, stream>>>(topk_idx, T, E, k, n_chunks, chunk_counts,
                                                        status);
   }
-  dispatch_scan_kernel<<<1, 256, 0, stream>>>(chunk_counts, E, n_chunks, counts, offsets,
-                                              chunk_base);
+  dispatch_block_scan_kernel<<<1, 1024, 0, stream>>>(chunk_counts, chunk_base, E, n_chunks, counts,
+                                                      offsets);
   if (T == 0) return cudaGetLastError();
   dispatch_scatter_kernel<<<n_chunks, kScatterThreads, 0, stream>>>(topk_idx, T, E, k, n_chunks, chunk_base,
                                                        perm, slot_of);
@@ -525,6 +472,40 @@ size_t dispatch_auto_scratch_bytes(int T, int k, int E) {
   const size_t n_blk = (P + kLocalPairs - 1) / kLocalPairs;
   return ((P * sizeof(int32_t) + 255) & ~size_t(255)) + n_blk * E * sizeof(int32_t);
 }
+
+namespace {
+// Largest (expert, block) table the scatter scans in its own shared memory on the current
+// device: kScatterScanMaxEntries, unless the scatter's static shared memory plus the
+// alignment of the dynamic region leave less than that within the per-launch default
+// (0: every table takes the one-CTA scan).
+int scatter_scan_limit() {
+  static OncePerDevice<64> once;
+  static int limit[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  int lim = 0;
+  const cudaError_t e = once.run(dev, [&]() -> cudaError_t {
+    int per_block = 0;
+    cudaError_t r = cudaDeviceGetAttribute(&per_block, cudaDevAttrMaxSharedMemoryPerBlock, dev);
+    if (r != cudaSuccess) return r;
+    cudaFuncAttributes fa_f, fa_b;
+    if ((r = cudaFuncGetAttributes(&fa_f, scatter_rows_kernel<float, true>)) != cudaSuccess) return r;
+    if ((r = cudaFuncGetAttributes(&fa_b, scatter_rows_kernel<__nv_bfloat16, true>)) != cudaSuccess)
+      return r;
+    const size_t stat = fa_f.sharedSizeBytes > fa_b.sharedSizeBytes ? fa_f.sharedSizeBytes
+                                                                    : fa_b.sharedSizeBytes;
+    // static bytes rounded up to 128, plus 128 bytes for the dynamic region's alignment
+    const long long room = static_cast<long long>(per_block) -
+                           static_cast<long long>((stat + 127) / 128 * 128) - 128;
+    const long long fit = room > 0 ? room / static_cast<long long>(sizeof(int)) : 0;
+    lim = static_cast<int>(fit < kScatterScanMaxEntries ? fit : kScatterScanMaxEntries);
+    if (dev < 64) limit[dev] = lim;
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return 0;
+  return dev < 64 ? limit[dev] : lim;
+}
+}  // namespace
 
 cudaError_t launch_dispatch_auto(int act_dtype, const void* x, const int32_t* topk_idx, int T,
                                  int d, int E, int k, int32_t* counts, int32_t* offsets,
@@ -543,10 +524,10 @@ cudaError_t launch_dispatch_auto(int act_dtype, const void* x, const int32_t* to
                                static_cast<int>(P), E, n_blk, local_rank, blk, status);
   if (err != cudaSuccess) return err;
   const long long table = static_cast<long long>(E) * n_blk;
-  const bool scan_in_smem = table <= kScatterScanMaxEntries;
+  const bool scan_in_smem = table <= scatter_scan_limit();
   if (!scan_in_smem) {
-    err = launch_pdl(dispatch_block_scan_kernel, dim3(1), dim3(1024), 0, stream, blk, E, n_blk,
-                     counts, offsets);
+    err = launch_pdl(dispatch_block_scan_kernel, dim3(1), dim3(1024), 0, stream,
+                     static_cast<const int32_t*>(blk), blk, E, n_blk, counts, offsets);
     if (err != cudaSuccess) return err;
   }
   const long long want = (static_cast<long long>(T) + 7) / 8;  // one warp per token

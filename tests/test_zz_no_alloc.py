@@ -50,6 +50,30 @@ def test_static_scratch_dispatch_matches_workspace_dispatch(moe, T, d, E, k):
 
 
 @pytest.mark.gpu
+def test_static_scratch_dispatch_skips_out_of_range_expert(moe):
+    """One routed pair names an expert outside [0, E): both entry points give it no slot
+    (slot_of -1), leave it out of every bucket, and flag it in the device status word."""
+    C, x, idx = _inputs(moe, 1000, 256, 8, 2, seed=11)
+    moe.get_device_status()  # start from a clear status word
+    bad = idx.clone()
+    bad[517, 1] = C.E + 3
+    ref = moe.dispatch(C, x, bad)
+    torch.cuda.synchronize()
+    assert moe.get_device_status() == 6  # MOE_ERR_DEVICE_INDEX
+    for call in range(2):
+        got = moe.dispatch_static_scratch(C, x, bad)
+        torch.cuda.synchronize()
+        assert moe.get_device_status() == 6, call
+        n = int(ref["offsets"][-1].item())
+        assert n == C.T * C.k - 1
+        assert int(got["slot_of"][517, 1].item()) == -1
+        for key in ("counts", "offsets", "slot_of"):
+            assert torch.equal(got[key], ref[key]), (call, key)
+        assert torch.equal(got["perm"][:n], ref["perm"][:n]), call
+        assert torch.equal(got["x_perm"][:n], ref["x_perm"][:n]), call
+
+
+@pytest.mark.gpu
 def test_static_scratch_dispatch_refuses_oversized_shapes(moe):
     # 8 * E * ceil(T / 128) bytes of scratch; E = 256, T = 70000 needs more than 1 MiB
     C = moe.Config(T=70000, d=256, E=256, k=2, H=128, dtype="bf16")
