@@ -205,6 +205,75 @@ def condense(x_perm, offsets, tau):
     return rep_of
 
 
+def condense_with_history(x_perm, offsets, perm, tau, s1, s2, history=None):
+    """Condensation that reuses the previous block's similarity of a token pair.
+
+    Luffy review: the fast similarity measurement "uses expert activation and
+    historical similarity to skip most pair-wise comparisons" ("What carries the
+    argument"); the ledger's free parameters S1 and S2 (e.g. 0.8 and 0.2) decide
+    which pairs are classified similar or dissimilar without a cosine, and its
+    domain assumption is that historical similarity persists across consecutive
+    blocks (Figure 7).
+
+    Reading (the pages give no more): the history is a set of token pairs, each
+    with a class, carried from one block (one call) to the next and keyed by the
+    two token indices, so it does not depend on which buckets the tokens share.
+    At this block every pair of slots in one bucket (expert activation: only
+    co-routed tokens are compared) is decided as follows, for the token pair
+    (u, t) of its two slots:
+
+    * the pair is in the history: its class decides (similar = the pair counts
+      as sim >= tau; dissimilar = it does not), no cosine is taken;
+    * otherwise: sim(x_u, x_t) >= tau, with sim as in ``cosine_similarity_matrix``,
+      decided in float32.
+
+    The greedy representative walk is then the one of ``condense_bucket`` on
+    these decisions.  The history handed to the next block holds exactly the
+    pairs compared at this block: a pair decided by its history keeps its class;
+    a pair with a cosine gets class similar if float32(sim) >= float32(s1),
+    dissimilar if float32(sim) <= float32(s2), and no entry otherwise.  Pairs not
+    compared at this block (no shared bucket) are not carried on.
+
+    history: dict {(u, t): bool} with u < t token indices, True = similar; None
+    or {} for the first block.  Returns (rep_of [P], new_history dict).
+    """
+    P = int(offsets[-1])
+    rep_of = np.arange(P, dtype=np.int64)
+    hist = {} if history is None else history
+    new_hist: dict = {}
+    tau32, s1_32, s2_32 = np.float32(tau), np.float32(s1), np.float32(s2)
+    perm = np.asarray(perm)
+    for e in range(len(offsets) - 1):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        n = b - a
+        if n == 0:
+            continue
+        S32 = cosine_similarity_matrix(x_perm[a:b]).astype(np.float32)
+        toks = perm[a:b]
+        similar = np.zeros((n, n), dtype=bool)
+        for i in range(n):
+            for j in range(i):
+                u, t = sorted((int(toks[j]), int(toks[i])))
+                if (u, t) in hist:
+                    cls = bool(hist[(u, t)])
+                    similar[i, j] = cls
+                    new_hist[(u, t)] = cls
+                else:
+                    similar[i, j] = bool(S32[i, j] >= tau32)
+                    if S32[i, j] >= s1_32:
+                        new_hist[(u, t)] = True
+                    elif S32[i, j] <= s2_32:
+                        new_hist[(u, t)] = False
+        reps: list[int] = []
+        for i in range(n):
+            hit = next((r for r in reps if similar[i, r]), None)
+            if hit is None:
+                reps.append(i)
+            else:
+                rep_of[a + i] = a + hit
+    return rep_of, new_hist
+
+
 def adaptive_tau(l_norm):
     """Luffy's adaptive condensation threshold h_t = 1 / (1 + exp(l_norm)).
 

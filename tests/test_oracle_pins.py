@@ -524,3 +524,87 @@ def test_backward_dense_case_matches_autograd():
     np.testing.assert_allclose(g["dW_gu"].sum(axis=0), wg.grad.numpy(), rtol=1e-9, atol=1e-11)
     np.testing.assert_allclose(g["dW_down"].sum(axis=0), wd.grad.numpy(), rtol=1e-9, atol=1e-11)
     np.testing.assert_allclose(g["dW_r"], 0.0, atol=1e-9)
+
+
+# ------------------------------------------------------------------ condensation with history
+def _history_block(angles, buckets):
+    """x_perm, offsets, perm of one block whose buckets list token indices in slot order."""
+    rows = harness.angle_rows(angles, [1.0] * len(angles))
+    perm = np.array([t for b in buckets for t in b], dtype=np.int64)
+    offsets = np.concatenate([[0], np.cumsum([len(b) for b in buckets])]).astype(np.int64)
+    return rows[perm], offsets, perm
+
+
+def test_condense_history_golden_two_blocks():
+    g = _golden("condense_history.json")
+    for c in g["cases"]:
+        hist = None
+        for bi, blk in enumerate(c["blocks"]):
+            xp, offsets, perm = _history_block(blk["angles"], blk["buckets"])
+            rep_of, hist = orc.condense_with_history(xp, offsets, perm, g["tau"], g["s1"], g["s2"], hist)
+            got = [[int(perm[rep_of[s]]) for s in range(offsets[e], offsets[e + 1])]
+                   for e in range(len(blk["buckets"]))]
+            assert got == blk["rep"], (c["name"], bi)
+            want = {(u, t): cls for u, t, cls in blk["history"]}
+            assert hist == want, (c["name"], bi)
+
+
+def test_condense_history_disabled_is_plain_condensation():
+    """S1 > 1 and S2 < -1 classify nothing, so every block is plain condensation and the
+    history stays empty; an empty history with S1 = 0.8, S2 = 0.2 also leaves the first
+    block's assignment unchanged."""
+    cfg, inp = harness.workload("luffy_condense", T=512)
+    _, idx, _ = orc.route(inp["x"], inp["W_r"], inp["bias"], cfg.k, cfg.gating)
+    _, offsets, perm, _ = orc.dispatch(idx, cfg.E)
+    xp = inp["x"][perm]
+    plain = orc.condense(xp, offsets, 0.95)
+    rep, hist = orc.condense_with_history(xp, offsets, perm, 0.95, 2.0, -2.0, None)
+    np.testing.assert_array_equal(rep, plain)
+    assert hist == {}
+    rep2, hist2 = orc.condense_with_history(xp, offsets, perm, 0.95, 2.0, -2.0, hist)
+    np.testing.assert_array_equal(rep2, plain)
+    rep3, hist3 = orc.condense_with_history(xp, offsets, perm, 0.95, 0.8, 0.2, {})
+    np.testing.assert_array_equal(rep3, plain)
+    assert len(hist3) > 0
+
+
+def test_condense_history_classes_of_first_block():
+    """From an empty history the classes are exactly the co-routed pairs whose cosine (here
+    from the 2-D angle difference, not from the oracle's similarity matrix) is >= S1 or <= S2."""
+    rng = np.random.default_rng(3)
+    angles = rng.uniform(0, 360, size=24)
+    buckets = [sorted(rng.choice(24, size=9, replace=False).tolist()) for _ in range(3)]
+    xp, offsets, perm = _history_block(angles, buckets)
+    _, hist = orc.condense_with_history(xp, offsets, perm, 0.95, 0.8, 0.2, None)
+    want = {}
+    for b in buckets:
+        for i in range(len(b)):
+            for j in range(i):
+                c = math.cos(math.radians(angles[b[i]] - angles[b[j]]))
+                if abs(c - 0.8) < 1e-6 or abs(c - 0.2) < 1e-6:
+                    continue
+                if c >= 0.8:
+                    want[(b[j], b[i])] = True
+                elif c <= 0.2:
+                    want[(b[j], b[i])] = False
+    assert hist == want
+
+
+def test_condense_history_repeated_block_keeps_assignment():
+    """The same block twice (same rows, same buckets).  On this workload every co-routed
+    cosine lies below S2 or at or above tau (i.i.d. rows are near orthogonal, copies of a
+    centroid near 1; checked here), so each class the first block records says what the
+    cosine says: the second block repeats the assignment and its history is the first's."""
+    cfg, inp = harness.workload("luffy_condense", T=512)
+    _, idx, _ = orc.route(inp["x"], inp["W_r"], inp["bias"], cfg.k, cfg.gating)
+    _, offsets, perm, _ = orc.dispatch(idx, cfg.E)
+    xp = inp["x"][perm]
+    for e in range(cfg.E):
+        S = orc.cosine_similarity_matrix(xp[offsets[e]:offsets[e + 1]])
+        low = S[np.tril_indices(len(S), -1)]
+        assert np.all((low <= 0.2) | (low >= 0.95))
+    rep1, h1 = orc.condense_with_history(xp, offsets, perm, 0.95, 0.8, 0.2, None)
+    rep2, h2 = orc.condense_with_history(xp, offsets, perm, 0.95, 0.8, 0.2, h1)
+    np.testing.assert_array_equal(rep1, rep2)
+    assert h1 == h2
+    np.testing.assert_array_equal(rep1, orc.condense(xp, offsets, 0.95))
