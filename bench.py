@@ -153,8 +153,8 @@ def launches_per_step(cfg, condense: bool) -> int:
     # logits and the top-k; fp32 layers and small batches run FMA logits and the top-k
     n = 3 if cfg.dtype == "bf16" and cfg.T > 256 else 2
     # dispatch: block ranks and row scatter; the (expert, 1024-pair block) count table is
-    # scanned inside the scatter up to 8192 entries, by a launch of its own above that
-    n += 2 + (cfg.E * -(-(cfg.T * cfg.k) // 1024) > 8192)
+    # scanned inside the scatter up to 2048 entries, by a launch of its own above that
+    n += 2 + (cfg.E * -(-(cfg.T * cfg.k) // 1024) > 2048)
     if condense:
         n += 6  # row stats, m-tiles, tile list, similarity GEMM, greedy scan, count
         n += 3  # compact reps, m-tiles over representatives, gather representative rows
@@ -208,7 +208,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     dev = torch.device("cuda", local_rank)
     moe_build.build()
     moe.lib()
-    cfg = gen.CONFIGS[args.workload]
+    cfg = workload_config(args)
     inp = gen.make_inputs(cfg)
     C = moe.Config.from_workload(cfg)
     w, x, r = moe.upload(C, inp, device=dev)
@@ -362,7 +362,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
                     "peak_source": f"{peak_src} HBM copy", "bytes": wk["ffn_bytes"],
                     "active_experts": active}
     roofline["frac"] = roofline["achieved"] / roofline["peak"]
-    roofline["traffic"] = GEMM_DRAM_BYTES.get(cfg.name)
+    reduced = bool(args.tokens or args.experts)
+    roofline["traffic"] = None if reduced else GEMM_DRAM_BYTES.get(cfg.name)
     disp_gbs = wk["dispatch_bytes"] / (phases["T_dispatch_ms"] / 1e3) / 1e9
     comb_gbs = wk["combine_bytes"] / (phases["T_combine_ms"] / 1e3) / 1e9
     line = {
@@ -634,6 +635,19 @@ def cpu_baseline(cfg, inp, target_s: float = 12.0) -> dict:
                       f"({dt:.1f} s); weights pre-cast to float64"}
 
 
+def workload_config(args):
+    """The named workload, with --tokens / --experts overriding T and E (smaller cases of the
+    same kernels for profiler captures; the bench line then names the reduced shape)."""
+    from dataclasses import replace
+    from routing_expert_ffn_gb300 import inputs as gen
+    cfg = gen.CONFIGS[args.workload]
+    if args.tokens:
+        cfg = replace(cfg, T=args.tokens)
+    if args.experts:
+        cfg = replace(cfg, E=args.experts)
+    return cfg
+
+
 def workload_desc(cfg) -> str:
     """The workload named by its shape (the same string in both arms' config)."""
     tau = cfg.taus[0] if cfg.taus else math.nan
@@ -647,7 +661,7 @@ def run_reference(args, rank: int) -> None:
         return
     from oracle import moe_oracle as orc
     from routing_expert_ffn_gb300 import inputs as gen
-    cfg = gen.CONFIGS[args.workload]
+    cfg = workload_config(args)
     inp64 = _as_f64(gen.make_inputs(cfg))
     # Each step is a bounded token sample, sized from one 32-token call so that the whole
     # run (warm-up and timed steps) takes about --reference-seconds of host time.
@@ -683,6 +697,8 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama4_scout_farskip")
+    ap.add_argument("--tokens", type=int, default=0, help="override the workload's T")
+    ap.add_argument("--experts", type=int, default=0, help="override the workload's E")
     ap.add_argument("--no-backward", action="store_true", help="skip timing the layer backward")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

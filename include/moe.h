@@ -200,6 +200,39 @@ moe_status moe_condense(const moe_config* cfg, const void* x_perm, const int32_t
                         int32_t* rep_of, int32_t* n_rep, int32_t* n_condensed,
                         void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* ---------------------------------------------------------------- condensation with history
+ * Luffy's fast similarity measurement (Luffy review, "What carries the argument": expert
+ * activation and historical similarity skip most pair-wise comparisons; ledger free
+ * parameters S1, S2 classify pairs similar or dissimilar without a cosine; domain
+ * assumption that historical similarity persists across consecutive blocks).
+ * As moe_condense, except that a pair of slots in one bucket whose two TOKENS were
+ * compared at the previous call and got a class there is decided by that class, with no
+ * cosine.  Every pair compared at this call goes to hist_out: an inherited class is kept;
+ * a pair decided by its cosine gets "similar" if cos >= s1, "dissimilar" if cos <= s2
+ * (similar wins if both hold), else no class.  Pairs whose tokens share no bucket at this
+ * call are not carried on.  The decisions cos >= tau, >= s1, <= s2 are taken in fp32.
+ * Gram tiles (128 x 256 slot pairs) in which every pair has a class get no tensor-core
+ * work; n_cos_tiles counts the tiles that did.
+ *   perm [T*k], slot_of [T, k] int32 (in, from moe_dispatch of this call)
+ *   hist_in   (in) a record written by an earlier call with the same T, k and E, or NULL
+ *             (first block).  A record of another shape or never written counts as empty.
+ *   hist_out  (out) moe_condense_history_bytes(cfg) bytes; must not overlap hist_in.
+ *   n_cos_tiles [1] int32 (out, nullable)
+ * Same limits and workspace as moe_condense (tau <= 1 required: MOE_ERR_INVALID_ARG else).
+ * History record layout (byte offsets from the record's start; each array starts on a
+ * 256-byte boundary after the previous one):
+ *   int32 header[5] = {0x48697374, T, k, E, T*k} at 0; int32 offsets[E+1] at 256;
+ *   int32 slot_of[T*k]; int64 bits_base[E]; uint32 known[(T*k) * ceil(T*k/32)];
+ *   uint32 similar[same].  Bucket e's local rows i < n_e (slot offsets[e] + i) are rows of
+ *   ceil(n_e/32) words from word bits_base[e]; bit b of word w of row i is the pair
+ *   (i, 32w + b) for 32w + b < i: known = it has a class, similar = the class.       */
+size_t moe_condense_history_bytes(const moe_config* cfg);
+moe_status moe_condense_hist(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
+                             const int32_t* perm, const int32_t* slot_of, float tau, float s1,
+                             float s2, const void* hist_in, void* hist_out, int32_t* rep_of,
+                             int32_t* n_rep, int32_t* n_condensed, int32_t* n_cos_tiles,
+                             void* ws, size_t ws_bytes, moe_stream_t stream);
+
 /* ---------------------------------------------------------------- expert FFN
  * T_routed of FarSkip Eq. 9: y[s] = W_down,e (SiLU(W_gate,e x_perm[s]) * (W_up,e x_perm[s]))
  * for every slot s of bucket e.  bf16 layers run on tcgen05 tensor cores

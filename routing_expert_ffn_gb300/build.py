@@ -5,6 +5,11 @@
 Objects go to routing_expert_ffn_gb300/_build/, the library to
 routing_expert_ffn_gb300/libmoe.so.  A translation unit is recompiled when it
 or any header under csrc/ or include/ is newer than its object.
+
+build(fault=True) builds the fault-injection test variant instead: the same sources with
+-DMOE_FAULT_INJECTION (bounded waits give up after 50 ms, and moe_test_drop_gemm_loads
+makes the GEMM's loads never arrive), into _build_fault/ and libmoe_fault.so.  Only the
+timeout test loads it.
 """
 from __future__ import annotations
 
@@ -21,6 +26,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe.so")
+BUILD_FAULT = os.path.join(PKG, "_build_fault")
+LIB_FAULT = os.path.join(PKG, "libmoe_fault.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I" + os.path.join(ROOT, "include")]
@@ -39,7 +46,10 @@ def _headers_mtime() -> float:
     return max((os.path.getmtime(h) for h in hs), default=0.0)
 
 
-def build(verbose_ptxas: bool = False, force: bool = False) -> str:
+def build(verbose_ptxas: bool = False, force: bool = False, fault: bool = False) -> str:
+    BUILD = BUILD_FAULT if fault else globals()["BUILD"]
+    LIB = LIB_FAULT if fault else globals()["LIB"]
+    extra = ["-DMOE_FAULT_INJECTION"] if fault else []
     os.makedirs(BUILD, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     hdr_t = _headers_mtime()
@@ -50,7 +60,7 @@ def build(verbose_ptxas: bool = False, force: bool = False) -> str:
         if (not force and os.path.exists(obj) and os.path.getmtime(obj) >= os.path.getmtime(src)
                 and os.path.getmtime(obj) >= hdr_t and not verbose_ptxas):
             return obj, ""
-        cmd = [cc, *ARCH, *FLAGS, "-c", src, "-o", obj]
+        cmd = [cc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
         if verbose_ptxas:
             cmd += ["-Xptxas", "-v"]
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -76,5 +86,6 @@ if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("--verbose-ptxas", action="store_true")
     ap.add_argument("--force", action="store_true")
+    ap.add_argument("--fault", action="store_true", help="the fault-injection test variant")
     a = ap.parse_args()
-    print(build(a.verbose_ptxas, a.force))
+    print(build(a.verbose_ptxas, a.force, a.fault))

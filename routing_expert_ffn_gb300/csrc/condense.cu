@@ -403,6 +403,147 @@ __global__ void __launch_bounds__(1024)
   if (threadIdx.x == 0) rep_counts[e] = base - s_base;
 }
 
+// Expert (bucket) of a slot of the record: the largest e with off[e] <= s < off[e + 1];
+// -1 if s is out of range.
+__device__ __forceinline__ int bucket_of(const int* off, int E, int s) {
+  if (s < 0 || s >= off[E]) return -1;
+  int lo = 0, hi = E;  // off[lo] <= s < off[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (off[mid] <= s) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// Historical similarity: for every tile of the Gram tile list, each pair (li, lj), lj < li,
+// of bucket e's slots takes the class its two tokens got at the previous call, found in the
+// previous record's bucket that held both (their previous slots si > sj, both in it; a pair
+// of tokens that shared two buckets got the same class in each).  Writes, in the bits layout
+// of this call, known / simc (the inherited classes) and the bits themselves (= simc; the
+// similarity GEMM rewrites the bits of tiles with unclassified pairs), and lists the tiles
+// with an unclassified pair for the GEMM.  One CTA per tile (grid-stride), 8 warps; a warp
+// takes a row and a 32-column chunk at a time, a lane one pair.
+constexpr int kLookupThreads = 256;
+__global__ void __launch_bounds__(kLookupThreads)
+    hist_lookup_kernel(const int2* __restrict__ tile_list, const int32_t* __restrict__ n_list,
+                       const int4* __restrict__ mt_info, const int32_t* __restrict__ offsets,
+                       const int32_t* __restrict__ perm, int T, int k, int E,
+                       const long long* __restrict__ bits_base, HistView prev,
+                       unsigned* __restrict__ known_out, unsigned* __restrict__ simc_out,
+                       unsigned* __restrict__ bits, int2* __restrict__ cos_list,
+                       int32_t* __restrict__ n_cos) {
+  extern __shared__ int hsm[];
+  int* poff = hsm;                      // [E + 1] previous offsets
+  int* col_e = poff + (E + 1);          // [256][k] previous bucket of each column token's pairs
+  int* col_s = col_e + kTcTileN * k;    // [256][k] and their slots
+  int* row_e = col_s + kTcTileN * k;    // [128][k]
+  int* row_s = row_e + kMTile * k;      // [128][k]
+  __shared__ int s_unknown;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int P = T * k;
+  const bool have = prev.header[0] == kHistMagic && prev.header[1] == T && prev.header[2] == k &&
+                    prev.header[3] == E && prev.header[4] == P;
+  if (have)
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) poff[i] = prev.offsets[i];
+  const int n_tiles = *n_list;
+  for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    const int2 tl = tile_list[tile];
+    const int4 m = mt_info[tl.x];
+    const int e = m.x, row0 = m.y, nrows = m.z, gbase = m.w;
+    const int n_e = offsets[e + 1] - offsets[e];
+    const int W = (n_e + 31) >> 5;
+    const int lj0 = tl.y * kTcTileN;
+    const int li0 = row0 - gbase;
+    if (threadIdx.x == 0) s_unknown = 0;
+    __syncthreads();  // poff staged; the previous tile's reads of the tables are done
+    if (have) {
+      for (int q = threadIdx.x; q < kTcTileN * k; q += blockDim.x) {
+        const int c = q / k, a = q - c * k;
+        int pe = -1, ps = -1;
+        if (lj0 + c < n_e) {
+          const int tok = perm[gbase + lj0 + c];
+          if (tok >= 0 && tok < T) {
+            ps = prev.slot_of[static_cast<long long>(tok) * k + a];
+            pe = bucket_of(poff, E, ps);
+          }
+        }
+        col_e[q] = pe;
+        col_s[q] = ps;
+      }
+      for (int q = threadIdx.x; q < kMTile * k; q += blockDim.x) {
+        const int rr = q / k, a = q - rr * k;
+        int pe = -1, ps = -1;
+        if (rr < nrows) {
+          const int tok = perm[row0 + rr];
+          if (tok >= 0 && tok < T) {
+            ps = prev.slot_of[static_cast<long long>(tok) * k + a];
+            pe = bucket_of(poff, E, ps);
+          }
+        }
+        row_e[q] = pe;
+        row_s[q] = ps;
+      }
+    }
+    __syncthreads();
+    bool unknown = false;
+    for (int rr = warp; rr < nrows; rr += kLookupThreads / 32) {
+      const int li = li0 + rr;
+      const long long wrow = bits_base[e] + static_cast<long long>(li) * W;
+      for (int ch = 0; ch < kTcTileN / 32; ++ch) {
+        const int ljb = lj0 + ch * 32;
+        if (ljb >= li) break;
+        const int c = ch * 32 + lane;
+        const bool in = ljb + lane < li;
+        bool kn = false, sm = false;
+        if (in && have) {
+          for (int a = 0; a < k && !kn; ++a) {
+            const int ea = row_e[rr * k + a];
+            if (ea < 0) continue;
+            for (int b = 0; b < k; ++b) {
+              if (col_e[c * k + b] != ea) continue;
+              const int o = poff[ea];
+              const int ne = poff[ea + 1] - o;
+              const int pi = row_s[rr * k + a] - o, pj = col_s[c * k + b] - o;
+              if (pj >= 0 && pj < pi && pi < ne) {
+                const long long widx = prev.bits_base[ea] +
+                                       static_cast<long long>(pi) * ((ne + 31) >> 5) + (pj >> 5);
+                const unsigned bit = 1u << (pj & 31);
+                kn = (prev.known[widx] & bit) != 0u;
+                sm = kn && (prev.simc[widx] & bit) != 0u;
+              }
+              break;
+            }
+          }
+        }
+        const unsigned kw = __ballot_sync(0xffffffffu, in && kn);
+        const unsigned sw = __ballot_sync(0xffffffffu, in && sm);
+        const unsigned iw = __ballot_sync(0xffffffffu, in);
+        if (kw != iw) unknown = true;
+        if (lane == 0) {
+          const long long widx = wrow + (ljb >> 5);
+          known_out[widx] = kw;
+          simc_out[widx] = sw;
+          bits[widx] = sw;
+        }
+      }
+    }
+    if (unknown && lane == 0) s_unknown = 1;
+    __syncthreads();
+    if (threadIdx.x == 0 && s_unknown) cos_list[atomicAdd(n_cos, 1)] = tl;
+  }
+}
+
+// Record header: magic, T, k, E, P.
+__global__ void hist_header_kernel(int32_t* header, int T, int k, int E) {
+  if (threadIdx.x == 0) {
+    header[0] = kHistMagic;
+    header[1] = T;
+    header[2] = k;
+    header[3] = E;
+    header[4] = T * k;
+  }
+}
+
 struct CondenseScratch {
   float* norm;
   unsigned long long* hash;
@@ -412,6 +553,8 @@ struct CondenseScratch {
   int32_t* n_list;
   long long* bits_base;
   unsigned* bits;
+  int2* cos_list;   // history: tiles with an unclassified pair
+  int32_t* n_cos;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -434,6 +577,8 @@ size_t carve(void* base, int P, int E, CondenseScratch* s) {
   const size_t o_nl = take(sizeof(int32_t));
   const size_t o_bb = take(sizeof(long long) * E);
   const size_t o_bits = take(sizeof(unsigned) * max_words);
+  const size_t o_cl = take(sizeof(int2) * max_tiles);
+  const size_t o_nc = take(sizeof(int32_t));
   if (s && base) {
     char* b = static_cast<char*>(base);
     s->norm = reinterpret_cast<float*>(b + o_norm);
@@ -444,6 +589,29 @@ size_t carve(void* base, int P, int E, CondenseScratch* s) {
     s->n_list = reinterpret_cast<int32_t*>(b + o_nl);
     s->bits_base = reinterpret_cast<long long*>(b + o_bb);
     s->bits = reinterpret_cast<unsigned*>(b + o_bits);
+    s->cos_list = reinterpret_cast<int2*>(b + o_cl);
+    s->n_cos = reinterpret_cast<int32_t*>(b + o_nc);
+  }
+  return o;
+}
+
+size_t hist_layout(int T, int k, int E, size_t* at /* 6 offsets or NULL */) {
+  const long long P = static_cast<long long>(T) * k;
+  const size_t words = static_cast<size_t>(P) * static_cast<size_t>((P + 31) / 32);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t a = o;
+    o = align256(o + bytes);
+    return a;
+  };
+  const size_t a0 = take(sizeof(int32_t) * 5);
+  const size_t a1 = take(sizeof(int32_t) * (E + 1));
+  const size_t a2 = take(sizeof(int32_t) * static_cast<size_t>(P));
+  const size_t a3 = take(sizeof(long long) * E);
+  const size_t a4 = take(sizeof(unsigned) * words);
+  const size_t a5 = take(sizeof(unsigned) * words);
+  if (at) {
+    at[0] = a0; at[1] = a1; at[2] = a2; at[3] = a3; at[4] = a4; at[5] = a5;
   }
   return o;
 }
@@ -452,13 +620,72 @@ size_t carve(void* base, int P, int E, CondenseScratch* s) {
 
 size_t condense_scratch_bytes(int T, int k, int E) { return carve(nullptr, T * k, E, nullptr); }
 
+size_t hist_record_bytes(int T, int k, int E) { return hist_layout(T, k, E, nullptr); }
+
+HistView hist_view(const void* base, int T, int k, int E) {
+  size_t at[6];
+  hist_layout(T, k, E, at);
+  char* b = static_cast<char*>(const_cast<void*>(base));
+  HistView v;
+  v.header = reinterpret_cast<int32_t*>(b + at[0]);
+  v.offsets = reinterpret_cast<int32_t*>(b + at[1]);
+  v.slot_of = reinterpret_cast<int32_t*>(b + at[2]);
+  v.bits_base = reinterpret_cast<long long*>(b + at[3]);
+  v.known = reinterpret_cast<unsigned*>(b + at[4]);
+  v.simc = reinterpret_cast<unsigned*>(b + at[5]);
+  return v;
+}
+
+namespace {
+cudaError_t condense_pipeline(const __nv_bfloat16* x_perm, const int32_t* offsets, int P, int d,
+                              int E, float tau, const HistArgs* h, int num_sms, int32_t* rep_of,
+                              int32_t* n_rep, int32_t* n_condensed, void* scratch,
+                              unsigned* status, cudaStream_t stream);
+}  // namespace
+
 cudaError_t launch_condense(const __nv_bfloat16* x_perm, const int32_t* offsets, int P, int d,
                             int E, float tau, int num_sms, int32_t* rep_of, int32_t* n_rep,
                             int32_t* n_condensed, void* scratch, unsigned* status,
                             cudaStream_t stream) {
+  return condense_pipeline(x_perm, offsets, P, d, E, tau, nullptr, num_sms, rep_of, n_rep,
+                           n_condensed, scratch, status, stream);
+}
+
+cudaError_t launch_condense_hist(const __nv_bfloat16* x_perm, const int32_t* offsets, int P, int d,
+                                 int E, float tau, const HistArgs& h, int num_sms,
+                                 int32_t* rep_of, int32_t* n_rep, int32_t* n_condensed,
+                                 void* scratch, unsigned* status, cudaStream_t stream) {
+  return condense_pipeline(x_perm, offsets, P, d, E, tau, &h, num_sms, rep_of, n_rep,
+                           n_condensed, scratch, status, stream);
+}
+
+namespace {
+cudaError_t condense_pipeline(const __nv_bfloat16* x_perm, const int32_t* offsets, int P, int d,
+                              int E, float tau, const HistArgs* h, int num_sms, int32_t* rep_of,
+                              int32_t* n_rep, int32_t* n_condensed, void* scratch,
+                              unsigned* status, cudaStream_t stream) {
+  HistView out = {};
+  if (h) {
+    // the record's header, offsets and slots; its bits_base is written by the tile list
+    out = hist_view(h->hist_out, h->T, h->k, E);
+    hist_header_kernel<<<1, 32, 0, stream>>>(out.header, h->T, h->k, E);
+    cudaError_t e = cudaMemcpyAsync(out.offsets, offsets, sizeof(int32_t) * (E + 1),
+                                    cudaMemcpyDeviceToDevice, stream);
+    if (e == cudaSuccess && P > 0)
+      e = cudaMemcpyAsync(out.slot_of, h->slot_of, sizeof(int32_t) * P, cudaMemcpyDeviceToDevice,
+                          stream);
+    if (e == cudaSuccess && h->n_cos_tiles)
+      e = cudaMemsetAsync(h->n_cos_tiles, 0, sizeof(int32_t), stream);
+    if (e != cudaSuccess) return e;
+  }
   if (!(tau <= 1.0f) || P == 0) {
     identity_reps_kernel<<<max(1, min(ceil_div(P, 256), 1024)), 256, 0, stream>>>(
         offsets, E, P, rep_of, n_rep, n_condensed);
+    if (h) {
+      // no pair was compared: every bucket's planes are empty
+      cudaError_t e = cudaMemsetAsync(out.bits_base, 0, sizeof(long long) * E, stream);
+      if (e != cudaSuccess) return e;
+    }
     return cudaGetLastError();
   }
   CondenseScratch s;
@@ -468,14 +695,53 @@ cudaError_t launch_condense(const __nv_bfloat16* x_perm, const int32_t* offsets,
   cudaError_t err = launch_build_mtiles(nullptr, offsets, 0, E, nullptr, s.mt_info,
                                         s.group_mt_begin, stream);
   if (err != cudaSuccess) return err;
+  long long* bits_base = h ? out.bits_base : s.bits_base;
   sim_tiles_kernel<<<1, 256, 0, stream>>>(s.mt_info, s.group_mt_begin, offsets, E, s.tile_list,
-                                          s.n_list, s.bits_base);
+                                          s.n_list, bits_base);
+  const int2* gemm_list = s.tile_list;
+  const int32_t* gemm_n = s.n_list;
+  int hist_mode = 0;
+  if (h && h->hist_in) {
+    // the previous call's classes: tiles whose pairs all have one skip the GEMM
+    cudaError_t e = cudaMemsetAsync(s.n_cos, 0, sizeof(int32_t), stream);
+    if (e != cudaSuccess) return e;
+    const HistView prev = hist_view(h->hist_in, h->T, h->k, E);
+    const size_t smem = sizeof(int) * ((E + 1) + 2 * (kTcTileN + kMTile) * h->k);
+    static OncePerDevice<64> once_l;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    e = once_l.run(dev, [&]() {
+      // the largest table: E = 256, k = 32
+      return cudaFuncSetAttribute(hist_lookup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(sizeof(int) * (257 + 2 * (kTcTileN + kMTile) * 32)));
+    });
+    if (e != cudaSuccess) return e;
+    const int max_tiles = max_mtiles(P, E) * ((P + kTcTileN - 1) / kTcTileN);
+    hist_lookup_kernel<<<max(1, min(max_tiles, 4 * num_sms)), kLookupThreads, smem, stream>>>(
+        s.tile_list, s.n_list, s.mt_info, offsets, h->perm, h->T, h->k, E, bits_base, prev,
+        out.known, out.simc, s.bits, s.cos_list, s.n_cos);
+    gemm_list = s.cos_list;
+    gemm_n = s.n_cos;
+    hist_mode = 2;
+  } else if (h) {
+    hist_mode = 1;
+  }
+  if (h && h->n_cos_tiles) {
+    cudaError_t e = cudaMemcpyAsync(h->n_cos_tiles, gemm_n, sizeof(int32_t),
+                                    cudaMemcpyDeviceToDevice, stream);
+    if (e != cudaSuccess) return e;
+  }
   TcGemmArgs a = {};
   a.mt_info = s.mt_info;
   a.group_mt_begin = s.group_mt_begin;
   a.n_groups = E;
-  a.tile_list = s.tile_list;
-  a.n_list = s.n_list;
+  a.tile_list = gemm_list;
+  a.n_list = gemm_n;
+  a.hist_mode = hist_mode;
+  a.hknown = out.known;
+  a.hsimc = out.simc;
+  a.s1 = h ? h->s1 : 2.0f;
+  a.s2 = h ? h->s2 : -2.0f;
   a.n_kblocks = d / kTcTileK;
   a.kb_per_slice = a.n_kblocks;
   a.nt_per_slice = 1;
@@ -484,7 +750,7 @@ cudaError_t launch_condense(const __nv_bfloat16* x_perm, const int32_t* offsets,
   a.rows = x_perm;
   a.d = d;
   a.bucket_off = offsets;
-  a.bits_base = s.bits_base;
+  a.bits_base = bits_base;
   a.bits = s.bits;
   a.tau = tau;
   a.status = status;
@@ -500,11 +766,12 @@ cudaError_t launch_condense(const __nv_bfloat16* x_perm, const int32_t* offsets,
                                 static_cast<int>(smem));
   });
   if (err != cudaSuccess) return err;
-  greedy_scan_kernel<<<E, kScanThreads, smem, stream>>>(s.bits, s.bits_base, offsets, rep_of,
+  greedy_scan_kernel<<<E, kScanThreads, smem, stream>>>(s.bits, bits_base, offsets, rep_of,
                                                         n_rep, status);
   condensed_count_kernel<<<1, 32, 0, stream>>>(offsets, n_rep, E, n_condensed);
   return cudaGetLastError();
 }
+}  // namespace
 
 cudaError_t launch_compact_reps(const int32_t* rep_of, const int32_t* offsets, int P, int E,
                                 int32_t* rep_rows, int32_t* rep_counts, cudaStream_t stream) {

@@ -150,10 +150,11 @@ __global__ void __launch_bounds__(kLocalPairs)
 // table (n_blk = 0) gives zeros.
 constexpr int kScanPiece = 8192;
 __device__ int block_scan_smem(int* a, int n, int* wsum);
+__device__ __forceinline__ int pad32(int i);
 __global__ void __launch_bounds__(1024)
     dispatch_block_scan_kernel(const int32_t* in, int32_t* out, int E, int n_blk,
                                int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
-  __shared__ int piece[kScanPiece];
+  __shared__ int piece[kScanPiece + kScanPiece / 32 + 1];  // padded (pad32)
   __shared__ int wsum[33];
   const long long N = static_cast<long long>(E) * n_blk;
   pdl_trigger();
@@ -161,10 +162,10 @@ __global__ void __launch_bounds__(1024)
   int carry = 0;
   for (long long base = 0; base < N; base += kScanPiece) {
     const int n = static_cast<int>(min(static_cast<long long>(kScanPiece), N - base));
-    for (int i = threadIdx.x; i < n; i += blockDim.x) piece[i] = in[base + i];
+    for (int i = threadIdx.x; i < n; i += blockDim.x) piece[pad32(i)] = in[base + i];
     __syncthreads();
     const int total = block_scan_smem(piece, n, wsum);  // ends with a barrier
-    for (int i = threadIdx.x; i < n; i += blockDim.x) out[base + i] = carry + piece[i];
+    for (int i = threadIdx.x; i < n; i += blockDim.x) out[base + i] = carry + piece[pad32(i)];
     carry += total;
     __syncthreads();  // the piece is rewritten by the next iteration
   }
@@ -176,23 +177,32 @@ __global__ void __launch_bounds__(1024)
   for (int e = threadIdx.x; e < E; e += blockDim.x) counts[e] = offsets[e + 1] - offsets[e];
 }
 
-// Exclusive prefix of a[0..n) in shared memory by the whole CTA (blockDim a multiple of
-// 32, at most 1024); returns the total.  Warp w owns the contiguous chunk
-// [w C, w C + C) with C a multiple of 32 and reads it 32 consecutive entries at a time
-// (one bank per lane, no conflicts): first the chunk's sum, then, after a scan of the
-// warp sums, a shuffle scan of each 32-entry step carried along the chunk.
+// Shared-memory tables that block_scan_smem scans are stored padded: entry i at pad32(i),
+// one spare word after every 32, so that threads reading consecutive segments of any
+// length hit distinct banks (a segment of 32 per thread would otherwise put a whole warp
+// on one bank).  A padded table of n entries takes pad32(n) + 1 words.
+__device__ __forceinline__ int pad32(int i) { return i + (i >> 5); }
+
+// Exclusive prefix of the padded table a[0..n) by the whole CTA (blockDim a multiple of 32,
+// at most 1024); returns the total.  Each thread sums a contiguous segment, the segment
+// sums are scanned across the warp (shuffles) and the warps (shared memory), and each
+// thread rewrites its segment.
 __device__ int block_scan_smem(int* a, int n, int* wsum /* 33 ints */) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const int C = ((n + nw - 1) / nw + 31) & ~31;
-  const int lo = min(n, warp * C), hi = min(n, lo + C);
-  int part = 0;
-  for (int i = lo + lane; i < hi; i += 32) part += a[i];
+  const int nt = blockDim.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int seg = (n + nt - 1) / nt;
+  const int lo = min(n, t * seg), hi = min(n, lo + seg);
+  int mine = 0;
+  for (int i = lo; i < hi; ++i) mine += a[pad32(i)];
+  int incl = mine;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-  if (lane == 0) wsum[warp] = part;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    const int v = lane < nw ? wsum[lane] : 0;
+    const int v = lane < (nt >> 5) ? wsum[lane] : 0;
     int wi = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -203,18 +213,11 @@ __device__ int block_scan_smem(int* a, int n, int* wsum /* 33 ints */) {
     if (lane == 31) wsum[32] = wi;
   }
   __syncthreads();
-  int carry = wsum[warp];
-  for (int i0 = lo; i0 < hi; i0 += 32) {
-    const int i = i0 + lane;
-    const int v = i < hi ? a[i] : 0;
-    int incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    if (i < hi) a[i] = carry + incl - v;
-    carry += __shfl_sync(0xffffffffu, incl, 31);
+  int run = wsum[warp] + incl - mine;
+  for (int i = lo; i < hi; ++i) {
+    const int c = a[pad32(i)];
+    a[pad32(i)] = run;
+    run += c;
   }
   __syncthreads();
   return wsum[32];
@@ -231,12 +234,13 @@ __device__ int block_scan_smem(int* a, int n, int* wsum /* 33 ints */) {
 // counts and offsets -- this replaces a separate scan launch.  Otherwise blk
 // is already the exclusive prefix.
 constexpr int kRowChunk = 8;
-// Largest count table the scatter scans in shared memory (32 KB of dynamic shared memory,
-// 4 bytes per entry).  Larger tables take the one-CTA scan: every scatter CTA would
-// otherwise re-read and re-scan a table that long.  scatter_scan_limit() checks at
-// set-up that this, plus the kernel's static shared memory and the dynamic region's
-// alignment, fits what a launch may use without opting in.
-constexpr int kScatterScanMaxEntries = 8192;
+// Largest count table the scatter scans in shared memory (8.3 KB of dynamic shared memory:
+// 4 bytes per entry, padded by one word in 32).  Larger tables take the one-CTA scan: every
+// scatter CTA would otherwise re-read and re-scan a table that long (measured on the
+// Qwen3-30B-A3B-shaped layer's 8192-entry table: 71.5 us fused, 60.5 us with the one-CTA scan).
+// scatter_scan_limit() checks at set-up that this, plus the kernel's static shared memory and
+// the dynamic region's alignment, fits what a launch may use without opting in.
+constexpr int kScatterScanMaxEntries = 2048;
 template <typename T, bool SCAN>
 __global__ void __launch_bounds__(256)
     scatter_rows_kernel(const T* __restrict__ x, const int32_t* __restrict__ idx,
@@ -252,40 +256,52 @@ __global__ void __launch_bounds__(256)
   __shared__ int wsum[33];
   pdl_trigger();
   pdl_wait();
-  const int32_t* base_tab = blk;
-  if (SCAN) {
-    const int N = E * n_blk;
-    for (int i = threadIdx.x; i < N; i += blockDim.x) tab[i] = blk[i];
-    __syncthreads();
-    const int total = block_scan_smem(tab, N, wsum);
-    if (blockIdx.x == 0) {
-      for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        const int o = tab[e * n_blk];
-        offsets[e] = o;
-        counts[e] = (e + 1 < E ? tab[(e + 1) * n_blk] : total) - o;
-      }
-      if (threadIdx.x == 0) offsets[E] = total;
-    }
-    base_tab = tab;
-  }
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int lane = threadIdx.x & 31;
-  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T_tok; t += warps) {
-    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<long long>(t) * d);
-    // the row's first chunk does not depend on the routing: start reading it now
-    uint4 r[kRowChunk];
+  int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  // The first token's row chunk and its routing are loaded before the table scan, so
+  // their latency overlaps it; each later token's are loaded at the end of the previous
+  // token's iteration.
+  uint4 r[kRowChunk];
+  int e = -1, lr = -1;
+  auto load_token = [&](int tok) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<long long>(tok) * d);
 #pragma unroll
     for (int u = 0; u < kRowChunk; ++u) {
       const int v = u * 32 + lane;
       if (v < nv) r[u] = src[v];
     }
+    e = -1;
+    lr = -1;
+    if (lane < k) {
+      const int p = tok * k + lane;
+      e = idx[p];
+      lr = local_rank[p];
+    }
+  };
+  if (t < T_tok) load_token(t);
+  if (SCAN) {
+    const int N = E * n_blk;
+    for (int i = threadIdx.x; i < N; i += blockDim.x) tab[pad32(i)] = blk[i];
+    __syncthreads();
+    const int total = block_scan_smem(tab, N, wsum);
+    if (blockIdx.x == 0) {
+      for (int ee = threadIdx.x; ee < E; ee += blockDim.x) {
+        const int o = tab[pad32(ee * n_blk)];
+        offsets[ee] = o;
+        counts[ee] = (ee + 1 < E ? tab[pad32((ee + 1) * n_blk)] : total) - o;
+      }
+      if (threadIdx.x == 0) offsets[E] = total;
+    }
+  }
+  for (; t < T_tok; t += warps) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<long long>(t) * d);
     int slot = -1;
     if (lane < k) {
       const int p = t * k + lane;
-      const int e = idx[p];
-      const int lr = local_rank[p];
       if (e >= 0 && e < E && lr >= 0) {
-        slot = base_tab[static_cast<long long>(e) * n_blk + p / kLocalPairs] + lr;
+        const int ti = e * n_blk + p / kLocalPairs;
+        slot = (SCAN ? tab[pad32(ti)] : blk[ti]) + lr;
         if (slot >= P) {
           record_status(status, MOE_ERR_DEVICE_INDEX);
           slot = -1;
@@ -313,6 +329,7 @@ __global__ void __launch_bounds__(256)
         }
       }
     }
+    if (t + warps < T_tok) load_token(t + warps);
   }
 }
 
@@ -342,21 +359,62 @@ __global__ void __launch_bounds__(256)
 // out[t] = r[t] + shared[t] + sum_j g[t,j] * y[rep(slot_of[t,j])], fp32 accumulate.
 // partial (nullable): p[t] = r[t] + shared[t], the same fp32 sum before the
 // routed terms, rounded once.
-// One CTA per token, one 16-byte vector per thread (blockDim = d / V), so every
-// load of a thread is issued before its single store.
+// One CTA per token, one 16-byte vector per thread (blockDim = d / V).  The loads that do
+// not depend on the routing (residual base, shared output) are issued before the token's
+// slots and gates are fetched, so the CTA pays one memory round trip before its routed-row
+// loads instead of two.  inputs_ready: x and residual are complete before this kernel
+// starts (the layer's own chain guarantees it: the kernel before this one triggers its
+// dependents only after its own wait), so they are read before the programmatic-launch
+// wait and overlap the previous kernel's tail.
 template <typename T>
 __global__ void __launch_bounds__(1024)
     combine_kernel(const T* __restrict__ y, const T* __restrict__ shared_out,
                    const int32_t* __restrict__ slot_of, const int32_t* __restrict__ rep_of,
                    const float* __restrict__ gate, const T* __restrict__ x,
                    const T* residual, int residual_mode, T* out, T* __restrict__ partial, int d,
-                   int k, int P, unsigned* status) {
+                   int k, int P, int inputs_ready, unsigned* status) {
   constexpr int V = Act<T>::kVec;
   __shared__ long long s_row[32];
   __shared__ float s_g[32];
   const int t = blockIdx.x;
+  const int v = threadIdx.x;  // this thread's 16-byte vector of the row
+  const bool act = v < d / V;
+  const long long rowoff = static_cast<long long>(t) * d + static_cast<long long>(v) * V;
+  const bool use_x = residual_mode == MOE_RES_INPUT || residual_mode == MOE_RES_INPUT_PLUS_EXTERNAL;
+  const bool use_r =
+      residual_mode == MOE_RES_EXTERNAL || residual_mode == MOE_RES_INPUT_PLUS_EXTERNAL;
+  float acc[V], tmp[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) acc[i] = 0.f;
   pdl_trigger();
+  if (inputs_ready && act) {
+    if (use_x) {
+      load_vec_f32<T>(x + rowoff, tmp);
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[i] += tmp[i];
+    }
+    if (use_r) {
+      load_vec_f32<T>(residual + rowoff, tmp);
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[i] += tmp[i];
+    }
+  }
   pdl_wait();
+  if (!inputs_ready && act) {
+    if (use_x) {
+      load_vec_f32<T>(x + rowoff, tmp);
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[i] += tmp[i];
+    }
+    if (use_r) {
+      load_vec_f32<T>(residual + rowoff, tmp);
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[i] += tmp[i];
+    }
+  }
+  // the shared output's load is in flight while the slots are fetched
+  uint4 sh = make_uint4(0u, 0u, 0u, 0u);
+  if (shared_out && act) sh = *reinterpret_cast<const uint4*>(shared_out + rowoff);
   if (threadIdx.x < k) {
     int s = slot_of[static_cast<long long>(t) * k + threadIdx.x];
     if (s >= 0 && s < P && rep_of) s = rep_of[s];
@@ -370,37 +428,22 @@ __global__ void __launch_bounds__(1024)
     s_g[threadIdx.x] = g;
   }
   __syncthreads();
-  const long long rowoff = static_cast<long long>(t) * d;
-  for (int v = threadIdx.x; v < d / V; v += blockDim.x) {
-    float acc[V], tmp[V];
+  if (!act) return;
+  if (shared_out) {
+    load_vec_f32<T>(reinterpret_cast<const T*>(&sh), tmp);
 #pragma unroll
-    for (int i = 0; i < V; ++i) acc[i] = 0.f;
-    if (residual_mode == MOE_RES_INPUT || residual_mode == MOE_RES_INPUT_PLUS_EXTERNAL) {
-      load_vec_f32<T>(x + rowoff + v * V, tmp);
-#pragma unroll
-      for (int i = 0; i < V; ++i) acc[i] += tmp[i];
-    }
-    if (residual_mode == MOE_RES_EXTERNAL || residual_mode == MOE_RES_INPUT_PLUS_EXTERNAL) {
-      load_vec_f32<T>(residual + rowoff + v * V, tmp);
-#pragma unroll
-      for (int i = 0; i < V; ++i) acc[i] += tmp[i];
-    }
-    if (shared_out) {
-      load_vec_f32<T>(shared_out + rowoff + v * V, tmp);
-#pragma unroll
-      for (int i = 0; i < V; ++i) acc[i] += tmp[i];
-    }
-    if (partial) store_vec_f32<T>(partial + rowoff + v * V, acc);
-    // branch-free over the k routed rows (unrolled, so several row loads are in flight)
-#pragma unroll 4
-    for (int j = 0; j < k; ++j) {
-      const float g = s_g[j];
-      load_vec_f32<T>(y + s_row[j] * d + v * V, tmp);
-#pragma unroll
-      for (int i = 0; i < V; ++i) acc[i] = fmaf(g, tmp[i], acc[i]);
-    }
-    store_vec_f32<T>(out + rowoff + v * V, acc);
+    for (int i = 0; i < V; ++i) acc[i] += tmp[i];
   }
+  if (partial) store_vec_f32<T>(partial + rowoff, acc);
+  // branch-free over the k routed rows (unrolled, so several row loads are in flight)
+#pragma unroll 4
+  for (int j = 0; j < k; ++j) {
+    const float g = s_g[j];
+    load_vec_f32<T>(y + s_row[j] * d + static_cast<long long>(v) * V, tmp);
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[i] = fmaf(g, tmp[i], acc[i]);
+  }
+  store_vec_f32<T>(out + rowoff, acc);
 }
 
 __global__ void __launch_bounds__(256)
@@ -497,7 +540,9 @@ int scatter_scan_limit() {
     // static bytes rounded up to 128, plus 128 bytes for the dynamic region's alignment
     const long long room = static_cast<long long>(per_block) -
                            static_cast<long long>((stat + 127) / 128 * 128) - 128;
-    const long long fit = room > 0 ? room / static_cast<long long>(sizeof(int)) : 0;
+    // a padded table of n entries takes n + n / 32 + 1 words
+    const long long words = room > 0 ? room / static_cast<long long>(sizeof(int)) : 0;
+    const long long fit = words > 1 ? (words - 1) * 32 / 33 : 0;
     lim = static_cast<int>(fit < kScatterScanMaxEntries ? fit : kScatterScanMaxEntries);
     if (dev < 64) limit[dev] = lim;
     return cudaSuccess;
@@ -532,7 +577,7 @@ cudaError_t launch_dispatch_auto(int act_dtype, const void* x, const int32_t* to
   }
   const long long want = (static_cast<long long>(T) + 7) / 8;  // one warp per token
   const int blocks = static_cast<int>(want < 8ll * num_sms ? want : 8ll * num_sms);
-  const size_t smem = scan_in_smem ? sizeof(int) * table : 0;
+  const size_t smem = scan_in_smem ? sizeof(int) * (table + table / 32 + 1) : 0;
   if (act_dtype == MOE_F32) {
     const float* xf = static_cast<const float*>(x);
     float* xp = static_cast<float*>(x_perm);
@@ -577,23 +622,25 @@ cudaError_t launch_combine(int act_dtype, const void* y_perm, const void* shared
                            const int32_t* slot_of, const int32_t* rep_of, const float* topk_gate,
                            const void* x, const void* residual, int residual_mode, void* out, int T,
                            int d, int k, int P, unsigned* status, cudaStream_t stream,
-                           void* partial) {
+                           void* partial, bool inputs_ready) {
   if (T == 0) return cudaSuccess;
   const int vec = act_dtype == MOE_F32 ? 4 : 8;
   const int threads = min(1024, max(32, ceil_div(d / vec, 32) * 32));
+  const int ready = inputs_ready ? 1 : 0;
   if (act_dtype == MOE_F32)
     return launch_pdl(combine_kernel<float>, dim3(T), dim3(threads), 0, stream,
                       static_cast<const float*>(y_perm), static_cast<const float*>(shared_out),
                       slot_of, rep_of, topk_gate, static_cast<const float*>(x),
                       static_cast<const float*>(residual), residual_mode,
-                      static_cast<float*>(out), static_cast<float*>(partial), d, k, P, status);
+                      static_cast<float*>(out), static_cast<float*>(partial), d, k, P, ready,
+                      status);
   return launch_pdl(combine_kernel<__nv_bfloat16>, dim3(T), dim3(threads), 0, stream,
                     static_cast<const __nv_bfloat16*>(y_perm),
                     static_cast<const __nv_bfloat16*>(shared_out), slot_of, rep_of, topk_gate,
                     static_cast<const __nv_bfloat16*>(x),
                     static_cast<const __nv_bfloat16*>(residual), residual_mode,
                     static_cast<__nv_bfloat16*>(out), static_cast<__nv_bfloat16*>(partial), d, k,
-                    P, status);
+                    P, ready, status);
 }
 
 cudaError_t launch_build_mtiles(const int32_t* counts, const int32_t* offsets_in, int fixed_rows,

@@ -43,6 +43,18 @@
 namespace moe {
 namespace tc {
 
+#ifdef MOE_FAULT_INJECTION
+// Test build only: when set, the pair kernel's producers issue no TMA loads (the expected
+// bytes never arrive), so the MMA warp's bounded wait on the full barrier runs out and the
+// call ends with MOE_ERR_TIMEOUT in the device status word.
+__device__ int g_fault_drop_loads = 0;
+__device__ __forceinline__ bool fault_drop_loads() {
+  return *reinterpret_cast<volatile int*>(&g_fault_drop_loads) != 0;
+}
+#else
+__device__ __forceinline__ bool fault_drop_loads() { return false; }
+#endif
+
 constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
@@ -521,7 +533,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       } else {
         // Gram tile of bucket `slice`: row slot i = row0 + r, column slot j = gbase + nt*256 + c.
         // cos(x_i, x_j) = D[i][j] / (|x_i| |x_j|), taken as D * (1/|x_i|) * (1/|x_j|) in fp32,
-        // clamped to [-1, 1]; a zero row is dissimilar unless the rows are identical.
+        // clamped to [-1, 1]; a zero row has similarity 0 to every row it is not identical
+        // to, and identical rows have similarity exactly 1.  Bits: sim >= tau (the decision),
+        // and with history sim >= s1 / sim <= s2 (the classes handed to the next call).
         const int e = t.slice;
         const int n_e = args.bucket_off[e + 1] - args.bucket_off[e];
         const int W = (n_e + 31) >> 5;
@@ -531,7 +545,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const float inv_ni = ni > 0.f ? 1.0f / ni : 0.f;
         const unsigned long long hi = valid ? args.row_hash[i] : 0ull;
         const uint32_t hi_lo = static_cast<uint32_t>(hi);
-        unsigned* brow = args.bits + args.bits_base[e] + static_cast<long long>(li) * W;
+        const long long wrow = args.bits_base[e] + static_cast<long long>(li) * W;
+        unsigned* brow = args.bits + wrow;
+        const int hmode = args.hist_mode;
 #pragma unroll 1
         for (int c = 0; c < 8; ++c) {
           uint32_t v[32];
@@ -547,15 +563,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t hj_lo_l =
               col_in ? static_cast<uint32_t>(args.row_hash[t.gbase + lj0 + lane]) : 0u;
           const int n_in = min(32, li - lj0);  // columns of this chunk below row li
-          uint32_t word = 0, same_hash = 0;
+          uint32_t word = 0, w1 = 0, w2 = 0, same_hash = 0;
 #pragma unroll
           for (int b = 0; b < 32; ++b) {
             const float inv_nj = __shfl_sync(0xffffffffu, inv_nj_l, b);
             const uint32_t hj_lo = __shfl_sync(0xffffffffu, hj_lo_l, b);
-            const float s =
-                fminf(fmaxf(__uint_as_float(v[b]) * inv_ni * inv_nj, -1.f), 1.f);
-            const bool in = b < n_in;
-            word |= static_cast<uint32_t>(in && inv_ni > 0.f && inv_nj > 0.f && s >= args.tau) << b;
+            const float s = (inv_ni > 0.f && inv_nj > 0.f)
+                                ? fminf(fmaxf(__uint_as_float(v[b]) * inv_ni * inv_nj, -1.f), 1.f)
+                                : 0.f;
+            const uint32_t in = b < n_in ? 1u : 0u;
+            word |= (in & static_cast<uint32_t>(s >= args.tau)) << b;
+            w1 |= (in & static_cast<uint32_t>(s >= args.s1)) << b;
+            w2 |= (in & static_cast<uint32_t>(s <= args.s2)) << b;
             same_hash |= static_cast<uint32_t>(in && hj_lo == hi_lo) << b;
           }
           // identical rows: similarity exactly 1 (full hash, then the rows themselves)
@@ -563,9 +582,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int b = __ffs(same_hash) - 1;
             same_hash &= same_hash - 1;
             const int j = t.gbase + lj0 + b;
-            if (args.row_hash[j] == hi && rows_identical(args.rows, args.d, i, j)) word |= 1u << b;
+            if (args.row_hash[j] == hi && rows_identical(args.rows, args.d, i, j)) {
+              const uint32_t m = 1u << b;
+              word = 1.0f >= args.tau ? (word | m) : (word & ~m);
+              w1 = 1.0f >= args.s1 ? (w1 | m) : (w1 & ~m);
+              w2 = 1.0f <= args.s2 ? (w2 | m) : (w2 & ~m);
+            }
           }
-          if (valid && lj0 < li) brow[lj0 >> 5] = word;
+          if (valid && lj0 < li) {
+            if (hmode == 0) {
+              brow[lj0 >> 5] = word;
+            } else {
+              const long long widx = wrow + (lj0 >> 5);
+              uint32_t kw = 0, sw = 0;
+              if (hmode == 2) {
+                kw = args.hknown[widx];
+                sw = args.hsimc[widx];
+              }
+              // a pair with a class is decided by it; the others by their cosine, and get
+              // a class from it (similar first)
+              brow[lj0 >> 5] = (kw & sw) | (~kw & word);
+              args.hknown[widx] = kw | (~kw & (w1 | w2));
+              args.hsimc[widx] = (kw & sw) | (~kw & w1);
+            }
+          }
         }
       }
       ptx::tc_fence_before();
@@ -829,8 +869,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t sa = smem0 + stage * pr::STAGE_BYTES;
           if (rank == 0)
             ptx::mbar_arrive_expect_tx(full, t.tail ? pr::TAIL_TX : 2 * pr::STAGE_BYTES);
-          pr::issue_kblock<MODE>(args, &tmA, &tmB, &tmA64, &tmW5, t, kb, rank, full, sa,
-                                 sa + pr::A_BYTES);
+          if (!fault_drop_loads())
+            pr::issue_kblock<MODE>(args, &tmA, &tmB, &tmA64, &tmW5, t, kb, rank, full, sa,
+                                   sa + pr::A_BYTES);
         }
         __syncwarp();
         if (++stage == pr::STAGES) stage = 0, phase ^= 1u;
@@ -1068,6 +1109,14 @@ static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const TcGe
 }
 
 }  // namespace tc
+
+#ifdef MOE_FAULT_INJECTION
+// Test build only: switch the dropped loads on (1) or off (0) on the current device.
+extern "C" int moe_test_drop_gemm_loads(int on) {
+  const int v = on ? 1 : 0;
+  return cudaMemcpyToSymbol(tc::g_fault_drop_loads, &v, sizeof(v)) == cudaSuccess ? 0 : 4;
+}
+#endif
 
 cudaError_t tc_gemm(int mode, const void* A, long long a_rows, int K, const void* B,
                     int b_slices, int b_rows, int b_cols, const TcGemmArgs& args_in, int grid,

@@ -53,11 +53,14 @@ cudaError_t launch_gather_rows(int act_dtype, const void* src, int src_rows, con
                                const int* n_rows_dev, int max_rows, int d, void* dst,
                                unsigned* status, cudaStream_t stream);
 // partial (nullable): also writes p = r + shared_out, the sum before the routed terms.
+// inputs_ready: x and residual were complete before the previous kernel on the stream
+// started (true only inside the layer's own launch chain); they are then read before the
+// programmatic-launch wait.
 cudaError_t launch_combine(int act_dtype, const void* y_perm, const void* shared_out,
                            const int32_t* slot_of, const int32_t* rep_of, const float* topk_gate,
                            const void* x, const void* residual, int residual_mode, void* out, int T,
                            int d, int k, int P, unsigned* status, cudaStream_t stream,
-                           void* partial = nullptr);
+                           void* partial = nullptr, bool inputs_ready = false);
 
 // ------------------------------------------------------------------ m-tile tables
 // Groups of rows (experts, buckets, or one group of fixed_rows rows when counts
@@ -99,6 +102,13 @@ struct TcGemmArgs {
   const long long* bits_base;  // [E] first word of bucket e's bit matrix
   unsigned* bits;
   float tau;
+  // kSimBits with history: 0 none; 1 record the classes (cos >= s1 similar, <= s2
+  // dissimilar) into hknown / hsimc (bits layout); 2 also merge the classes the history
+  // lookup already wrote there: a pair with a class keeps it and decides its bit
+  int hist_mode;
+  unsigned* hknown;
+  unsigned* hsimc;
+  float s1, s2;
   unsigned* status;
   // kRouter: D = x . [W1|W2|W3] over a K range of 3*d (the three bf16 terms of W_r)
   int router_n;        // N of the MMA = E rounded up to 32
@@ -202,6 +212,32 @@ cudaError_t launch_condense(const __nv_bfloat16* x_perm, const int32_t* offsets,
                             int E, float tau, int num_sms, int32_t* rep_of, int32_t* n_rep,
                             int32_t* n_condensed, void* scratch, unsigned* status,
                             cudaStream_t stream);
+// Condensation with the previous call's pair classes (Luffy's historical similarity).
+// The record layout is the one include/moe.h documents for moe_condense_hist.
+constexpr int kHistMagic = 0x48697374;
+struct HistView {
+  int32_t* header;       // {magic, T, k, E, P}
+  int32_t* offsets;      // [E+1]
+  int32_t* slot_of;      // [T*k]
+  long long* bits_base;  // [E]
+  unsigned* known;       // [P * ceil(P/32)]
+  unsigned* simc;        // [P * ceil(P/32)]
+};
+size_t hist_record_bytes(int T, int k, int E);
+HistView hist_view(const void* base, int T, int k, int E);
+struct HistArgs {
+  const int32_t* perm;     // [T*k] slot -> token, this call
+  const int32_t* slot_of;  // [T, k] this call
+  int T, k;
+  float s1, s2;
+  const void* hist_in;     // nullable
+  void* hist_out;
+  int32_t* n_cos_tiles;    // nullable
+};
+cudaError_t launch_condense_hist(const __nv_bfloat16* x_perm, const int32_t* offsets, int P, int d,
+                                 int E, float tau, const HistArgs& h, int num_sms,
+                                 int32_t* rep_of, int32_t* n_rep, int32_t* n_condensed,
+                                 void* scratch, unsigned* status, cudaStream_t stream);
 // Representative rows compacted bucket by bucket: rep_rows[c] = slot of the c-th
 // representative, rep_counts[e] = representatives of bucket e.
 cudaError_t launch_compact_reps(const int32_t* rep_of, const int32_t* offsets, int P, int E,

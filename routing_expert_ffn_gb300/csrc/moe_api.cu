@@ -467,6 +467,61 @@ moe_status moe_condense(const moe_config* cfg, const void* x_perm, const int32_t
   return MOE_OK;
 }
 
+size_t moe_condense_history_bytes(const moe_config* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return 0;
+  return hist_record_bytes(cfg->T, cfg->k, cfg->E);
+}
+
+moe_status moe_condense_hist(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
+                             const int32_t* perm, const int32_t* slot_of, float tau, float s1,
+                             float s2, const void* hist_in, void* hist_out, int32_t* rep_of,
+                             int32_t* n_rep, int32_t* n_condensed, int32_t* n_cos_tiles,
+                             void* ws, size_t ws_bytes, moe_stream_t stream) {
+  moe_status s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!(tau <= 1.0f) || s1 != s1 || s2 != s2) return MOE_ERR_INVALID_ARG;
+  if (cfg->act_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  const long long P = static_cast<long long>(cfg->T) * cfg->k;
+  if (P > 65536) return MOE_ERR_UNSUPPORTED;
+  MOE_PTR(offsets);
+  MOE_PTR(n_rep);
+  MOE_PTR(n_condensed);
+  MOE_OPT_PTR(n_cos_tiles);
+  MOE_OPT_PTR(hist_in);
+  MOE_PTR(hist_out);
+  if (P > 0) {
+    MOE_PTR(x_perm);
+    MOE_PTR(rep_of);
+    MOE_PTR(perm);
+    MOE_PTR(slot_of);
+  }
+  const size_t rec = hist_record_bytes(cfg->T, cfg->k, cfg->E);
+  if (hist_in) {
+    const char* a = static_cast<const char*>(hist_in);
+    const char* b = static_cast<const char*>(hist_out);
+    MOE_REQUIRE(a + rec <= b || b + rec <= a, MOE_ERR_INVALID_ARG);
+  }
+  MOE_PTR(ws);
+  MOE_REQUIRE(ws_bytes >= moe_condense_workspace_size(cfg), MOE_ERR_WORKSPACE);
+  DeviceInfo* di = device_info();
+  if (!di) return MOE_ERR_CUDA;
+  HistArgs h;
+  h.perm = perm;
+  h.slot_of = slot_of;
+  h.T = cfg->T;
+  h.k = cfg->k;
+  h.s1 = s1;
+  h.s2 = s2;
+  h.hist_in = hist_in;
+  h.hist_out = hist_out;
+  h.n_cos_tiles = n_cos_tiles;
+  MOE_CUDA(launch_condense_hist(static_cast<const __nv_bfloat16*>(x_perm), offsets,
+                                static_cast<int>(P), cfg->d, cfg->E, tau, h, di->num_sms, rep_of,
+                                n_rep, n_condensed, ws, di->status,
+                                reinterpret_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
 size_t moe_expert_ffn_workspace_size(const moe_config* cfg, int with_condensation) {
   if (check_cfg(cfg) != MOE_OK) return 0;
   return carve_ffn(cfg, with_condensation != 0, nullptr, nullptr);
@@ -617,9 +672,13 @@ moe_status layer_forward_impl(const moe_config* cfg, const moe_weights* w, const
     s = run_shared_ffn(cfg, w, x, L.shared_out, fs, di, st);
     if (s != MOE_OK) return s;
   }
+  // The kernel before the combine (a down-projection GEMM) triggers its dependents only
+  // after its own wait, and the router waited for the caller's work before reading x, so
+  // x and residual are complete whenever the combine starts.
   MOE_CUDA(launch_combine(cfg->act_dtype, L.y_perm, cfg->n_shared > 0 ? L.shared_out : nullptr,
                           L.slot_of, rep_of, L.gate, x, residual, cfg->residual, out, cfg->T,
-                          cfg->d, cfg->k, static_cast<int>(P), di->status, st, partial_out));
+                          cfg->d, cfg->k, static_cast<int>(P), di->status, st, partial_out,
+                          /*inputs_ready=*/true));
   return MOE_OK;
 }
 

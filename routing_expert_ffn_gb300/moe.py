@@ -33,7 +33,7 @@ EXPORTED = ("moe_status_string", "moe_adaptive_tau", "moe_get_device_status",
             "moe_condense", "moe_expert_ffn_workspace_size", "moe_expert_ffn", "moe_combine",
             "moe_workspace_size", "moe_layer_forward", "moe_layer_forward_ex",
             "moe_dispatch_static_scratch", "moe_layer_backward_workspace_size",
-            "moe_layer_backward")
+            "moe_layer_backward", "moe_condense_history_bytes", "moe_condense_hist")
 
 
 class MoEError(RuntimeError):
@@ -63,10 +63,17 @@ def lib() -> ctypes.CDLL:
     global _lib
     if _lib is not None:
         return _lib
-    if not os.path.exists(LIB_PATH):
-        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+    _lib = load_library(LIB_PATH)
+    return _lib
+
+
+def load_library(path: str) -> ctypes.CDLL:
+    """A build of the library at `path` with the C ABI's signatures set (lib() loads the
+    product library; the timeout test loads the fault-injection build this way)."""
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with "
                            "`python -m routing_expert_ffn_gb300.build`")
-    L = ctypes.CDLL(LIB_PATH)
+    L = ctypes.CDLL(path)
     P, S, I, F = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_float
     CFG, W = ctypes.POINTER(moe_config), ctypes.POINTER(moe_weights)
     sig = {
@@ -79,6 +86,8 @@ def lib() -> ctypes.CDLL:
         "moe_dispatch": (I, [CFG, P, P, P, P, P, P, P, P, S, P]),
         "moe_condense_workspace_size": (S, [CFG]),
         "moe_condense": (I, [CFG, P, P, F, P, P, P, P, S, P]),
+        "moe_condense_history_bytes": (S, [CFG]),
+        "moe_condense_hist": (I, [CFG, P, P, P, P, F, F, F, P, P, P, P, P, P, P, S, P]),
         "moe_expert_ffn_workspace_size": (S, [CFG, I]),
         "moe_expert_ffn": (I, [CFG, W, P, P, P, P, P, P, P, S, P]),
         "moe_combine": (I, [CFG, P, P, P, P, P, P, P, P, P]),
@@ -93,7 +102,6 @@ def lib() -> ctypes.CDLL:
         fn = getattr(L, name)
         fn.restype = res
         fn.argtypes = args
-    _lib = L
     return L
 
 
@@ -225,6 +233,33 @@ def dispatch_static_scratch(cfg: Config, x, topk_idx, stream=None) -> dict:
         _ptr(out["perm"]), _ptr(out["slot_of"]), _ptr(out["x_perm"]), _stream(stream)),
         "moe_dispatch_static_scratch")
     return out
+
+
+def condense_history_bytes(cfg: Config) -> int:
+    return int(lib().moe_condense_history_bytes(ctypes.byref(cfg.c())))
+
+
+def condense_hist(cfg: Config, x_perm, offsets, perm, slot_of, tau: float, s1: float, s2: float,
+                  hist_in=None, hist_out=None, stream=None):
+    """Condensation with the previous call's pair classes.  hist_in / hist_out are uint8
+    device tensors of condense_history_bytes(cfg) bytes (hist_out is allocated when None).
+    Returns (rep_of, n_rep, n_condensed, n_cos_tiles, hist_out)."""
+    dev = x_perm.device
+    c = cfg.c()
+    P = cfg.T * cfg.k
+    rep_of = _empty((max(P, 1),), torch.int32, dev)
+    n_rep = _empty((cfg.E,), torch.int32, dev)
+    n_cond = _empty((1,), torch.int32, dev)
+    n_cos = _empty((1,), torch.int32, dev)
+    if hist_out is None:
+        hist_out = torch.empty(condense_history_bytes(cfg), dtype=torch.uint8, device=dev)
+    n = lib().moe_condense_workspace_size(ctypes.byref(c))
+    ws = _workspace(n, dev)
+    _check(lib().moe_condense_hist(ctypes.byref(c), _ptr(x_perm), _ptr(offsets), _ptr(perm),
+                                   _ptr(slot_of), tau, s1, s2, _ptr(hist_in), _ptr(hist_out),
+                                   _ptr(rep_of), _ptr(n_rep), _ptr(n_cond), _ptr(n_cos), _ptr(ws),
+                                   n, _stream(stream)), "moe_condense_hist")
+    return rep_of, n_rep, n_cond, n_cos, hist_out
 
 
 def condense(cfg: Config, x_perm, offsets, tau: float, stream=None):

@@ -470,13 +470,14 @@ def test_condensed_layer_small(moe):
 
 
 # ------------------------------------------------------------------ limits of the boundary
-@pytest.mark.parametrize("E,T,k", [(128, 65536, 1), (128, 65535, 1), (129, 65536, 1),
-                                   (256, 8192, 8), (256, 50000, 1), (215, 58000, 1)])
+@pytest.mark.parametrize("E,T,k", [(128, 16384, 1), (128, 16383, 1), (129, 16384, 1),
+                                   (128, 65536, 1), (256, 8192, 8), (256, 50000, 1),
+                                   (215, 58000, 1)])
 def test_dispatch_large_rank_tables(moe, E, T, k):
     """The scatter scans the (expert, 1024-pair block) count table in its own shared memory
-    up to 8192 entries: E = 128 with 64 blocks is exactly that limit (and 65535 tokens a
-    ragged last block under it).  E = 129 with 64 blocks (8256 entries) is one expert past
-    it, and 16384, 12544 and 12255 entries lie further past; those take the separate
+    up to 2048 entries: E = 128 with 16 blocks is exactly that limit (and 16383 tokens a
+    ragged last block under it).  E = 129 with 16 blocks (2064 entries) is one expert past
+    it, and 8192, 16384, 12544 and 12255 entries lie further past; those take the separate
     one-CTA table scan.  Skewed expert choices leave empty buckets; everything bit for bit."""
     d = 256
     rng = np.random.default_rng(T + k)
