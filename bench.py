@@ -39,10 +39,10 @@ if ROOT not in sys.path:
 
 METRIC = "MoE-layer tokens/s on 1 GB300; expert-GEMM % of BF16 peak; dispatch GB/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM bytes (read + write) of the four grouped-GEMM launches of one moe_expert_ffn call,
-# from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the current kernel
-# on that workload; workloads without a capture report null.
-GEMM_DRAM_BYTES = {"dsv2_lite": 1504.6e6}
+# DRAM bytes (read + write) of the grouped-GEMM launches of one moe_expert_ffn call, from
+# one-pass ncu captures (dram__bytes_read.sum + dram__bytes_write.sum) of the pair kernel at
+# the workload's full size; workloads without a capture report null.
+GEMM_DRAM_BYTES = {"dsv2_lite": 1497.3e6, "llama4_scout_farskip": 6303.8e6}
 
 
 def load_peaks() -> tuple[dict, str]:
@@ -155,14 +155,15 @@ def launches_per_step(cfg, condense: bool) -> int:
     # dispatch: block ranks and row scatter; the (expert, 1024-pair block) count table is
     # scanned inside the scatter up to 2048 entries, by a launch of its own above that
     n += 2 + (cfg.E * -(-(cfg.T * cfg.k) // 1024) > 2048)
+    bf16 = cfg.dtype == "bf16"
     if condense:
         n += 6  # row stats, m-tiles, tile list, similarity GEMM, greedy scan, count
         n += 3  # compact reps, m-tiles over representatives, gather representative rows
-    else:
-        n += 1  # m-tiles
+    elif not bf16:
+        n += 1  # m-tiles (the bf16 pair GEMM reads the bucket offsets itself)
     n += 2      # routed gate/up + down GEMMs
     if cfg.n_shared:
-        n += 3  # shared m-tiles + gate/up + down GEMMs
+        n += 2 + (0 if bf16 else 1)  # shared gate/up + down GEMMs (+ m-tiles for fp32)
     n += 1      # combine
     return n
 
@@ -330,6 +331,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
 
     # per-phase breakdown (FarSkip Eq. 9 terms): the same step as separate ABI calls
     phases = phase_breakdown(args, moe, C, w, x, r, tau, flush, stream, torch)
+    history = history_report(args, moe, C, w, x, tau, flush, stream, torch) if condense else None
     # the layer's outputs after all timing passes still come from the same graph
     graph.replay()
     # end to end: pinned host input -> device -> layer -> pinned host output, every step,
@@ -395,6 +397,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         "serial": serial,
         "backward": backward,
         "condensed": n_condensed,
+        "history": history,
         "gpu_launches": launches_per_step(C, condense) * args.steps,
         "clocks": clocks,
         "steady": steady,
@@ -514,6 +517,58 @@ def phase_breakdown(args, moe, C, w, x, r, tau, flush, stream, torch) -> dict:
                    "T_experts = moe_expert_ffn (routed + shared grouped GEMMs on tcgen05 and their "
                    "m-tile tables); T_routed = the same call without the shared experts; "
                    "T_shared = their difference")
+    return res
+
+
+def history_report(args, moe, C, w, x, tau, flush, stream, torch) -> dict:
+    """Condensation with Luffy's historical similarity (moe_condense_hist, S1 = 0.8,
+    S2 = 0.2) against plain moe_condense on the same dispatched batch: a first block (no
+    record: every Gram tile needs cosines, and the classes are recorded) and a repeated block
+    (the record of the same batch: tiles whose pairs all have a class skip the tensor cores).
+    Each timed as one ABI call in a CUDA graph, L2 flushed before each replay."""
+    dev = x.device
+    _, idx, _ = moe.route(C, x, w.W_r, w.router_bias)
+    d = moe.dispatch(C, x, idx)
+    torch.cuda.synchronize()
+    rec_a = torch.empty(moe.condense_history_bytes(C), dtype=torch.uint8, device=dev)
+    rec_b = torch.empty_like(rec_a)
+    outs = {}
+
+    def plain():
+        outs["plain"] = moe.condense(C, d["x_perm"], d["offsets"], tau)
+
+    def first():
+        outs["first"] = moe.condense_hist(C, d["x_perm"], d["offsets"], d["perm"], d["slot_of"],
+                                          tau, 0.8, 0.2, hist_in=None, hist_out=rec_a)
+
+    def repeat():
+        outs["repeat"] = moe.condense_hist(C, d["x_perm"], d["offsets"], d["perm"], d["slot_of"],
+                                           tau, 0.8, 0.2, hist_in=rec_a, hist_out=rec_b)
+
+    res = {}
+    for name, fn in (("plain", plain), ("first", first), ("repeat", repeat)):
+        g = capture(torch, fn)
+        for _ in range(args.warmup):
+            g.replay()
+        ts = []
+        for _ in range(max(args.steps, 20)):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        res[f"T_condense_{name}_ms"] = statistics.median(ts)
+    torch.cuda.synchronize()
+    same = all(torch.equal(outs[n][0], outs["plain"][0]) for n in ("first", "repeat"))
+    res.update({"tiles_first": int(outs["first"][3].item()),
+                "tiles_repeat": int(outs["repeat"][3].item()),
+                "condensed": int(outs["plain"][2].item()),
+                "same_assignment_as_plain": bool(same),
+                "note": "S1 = 0.8, S2 = 0.2; 'first' = no record yet, 'repeat' = the record of the "
+                        "same batch (a block whose tokens and routing repeat the previous one's); "
+                        "tiles = Gram tiles that needed tensor-core cosines"})
     return res
 
 

@@ -186,7 +186,9 @@ moe_status moe_dispatch_static_scratch(const moe_config* cfg, const void* x,
 
 /* ---------------------------------------------------------------- condensation
  * Luffy token condensation inside each expert bucket (bf16 layers with
- * T * k <= 65536 when tau <= 1, else MOE_ERR_UNSUPPORTED).  Walking a
+ * T <= 65536 when tau <= 1, else MOE_ERR_UNSUPPORTED; a bucket holds each token at most
+ * once).  Offsets whose bucket is longer than T (a routing that named one expert twice
+ * for a token) are flagged on the device (MOE_ERR_DEVICE_INDEX) and condense nothing.  Walking a
  * bucket in slot order with the set R of representatives, slot j is condensed
  * onto the earliest r in R with cos(x_perm[j], x_perm[r]) >= tau, else j joins
  * R.  Bitwise-identical rows have similarity 1; a zero row is otherwise
@@ -222,10 +224,11 @@ moe_status moe_condense(const moe_config* cfg, const void* x_perm, const int32_t
  * History record layout (byte offsets from the record's start; each array starts on a
  * 256-byte boundary after the previous one):
  *   int32 header[5] = {0x48697374, T, k, E, T*k} at 0; int32 offsets[E+1] at 256;
- *   int32 slot_of[T*k]; int64 bits_base[E]; uint32 known[(T*k) * ceil(T*k/32)];
- *   uint32 similar[same].  Bucket e's local rows i < n_e (slot offsets[e] + i) are rows of
- *   ceil(n_e/32) words from word bits_base[e]; bit b of word w of row i is the pair
- *   (i, 32w + b) for 32w + b < i: known = it has a class, similar = the class.       */
+ *   int32 slot_of[T*k]; int64 bits_base[E]; uint32 planes[2 * (T*k) * ceil(min(T, T*k)/32)].
+ *   Bucket e's local rows i < n_e (slot offsets[e] + i) are rows of ceil(n_e/32) word pairs
+ *   from pair bits_base[e]; word pair q is planes[2q] (known) and planes[2q + 1] (similar);
+ *   bit b of pair w of row i is the slot pair (i, 32w + b) for 32w + b < i: known = it has a
+ *   class, similar = the class.                                                        */
 size_t moe_condense_history_bytes(const moe_config* cfg);
 moe_status moe_condense_hist(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
                              const int32_t* perm, const int32_t* slot_of, float tau, float s1,
@@ -314,7 +317,7 @@ moe_status moe_layer_forward_ex(const moe_config* cfg, const moe_weights* w, con
  * 64 rows so the weight gradients contract over whole 64-row blocks.  The steps of the
  * path follow FarSkip-Collective's pre-training execution (review page, Figures 11-12):
  * router, Dispatch, routed and shared experts, Combine.
- * bf16 layers only (fp32 layers: MOE_ERR_UNSUPPORTED); condensation needs T*k <= 65536.
+ * bf16 layers only (fp32 layers: MOE_ERR_UNSUPPORTED); condensation needs T <= 65536.
  *   x [T, d] bf16 (in)   d_out [T, d] bf16 (in)   tau: as moe_layer_forward
  *   d_x [T, d] bf16 (out): gradient w.r.t. x (x also feeds the residual base in the
  *       input modes), summed in fp32, rounded once

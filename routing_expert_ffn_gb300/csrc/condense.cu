@@ -86,12 +86,38 @@ __global__ void __launch_bounds__(256)
 
 // Tile list of the lower triangle of every bucket's Gram matrix, and the
 // start word of each bucket's bit matrix (rows of ceil(n_e / 32) words).
+// The scratch is sized for buckets of at most max_rows rows (a bucket holds each token at
+// most once).  A bucket longer than that (offsets from a routing that names one expert twice
+// for a token) sets *overflow, flags MOE_ERR_DEVICE_INDEX, lists no tile, invalidates the
+// history record being written (hist_header, nullable) and leaves every slot its own
+// representative (greedy_scan reads *overflow).
 __global__ void __launch_bounds__(256)
     sim_tiles_kernel(const int4* __restrict__ mt_info, const int32_t* __restrict__ group_mt_begin,
-                     const int32_t* __restrict__ offsets, int E, int2* __restrict__ tile_list,
-                     int32_t* __restrict__ n_list, long long* __restrict__ bits_base) {
+                     const int32_t* __restrict__ offsets, int E, int max_rows,
+                     int2* __restrict__ tile_list, int32_t* __restrict__ n_list,
+                     long long* __restrict__ bits_base, int32_t* __restrict__ overflow,
+                     int32_t* __restrict__ hist_header, unsigned* status) {
   __shared__ int s_cnt[1024];
   __shared__ int s_beg[1025];
+  __shared__ int s_over;
+  if (threadIdx.x == 0) s_over = 0;
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int n = offsets[e + 1] - offsets[e];
+    if (n < 0 || n > max_rows) s_over = 1;
+  }
+  __syncthreads();
+  if (s_over) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) bits_base[e] = 0;
+    if (threadIdx.x == 0) {
+      *overflow = 1;
+      *n_list = 0;
+      if (hist_header) hist_header[0] = 0;
+      record_status(status, MOE_ERR_DEVICE_INDEX);
+    }
+    return;
+  }
+  if (threadIdx.x == 0) *overflow = 0;
   const int n_mt = group_mt_begin[E];
   // Chunks of 1024 m-tiles; the running tile count carries across chunks.
   __shared__ int s_carry;
@@ -162,8 +188,8 @@ __global__ void __launch_bounds__(256)
 // the row-by-row walk over staged rows instead.
 __global__ void __launch_bounds__(kScanThreads)
     greedy_scan_kernel(const unsigned* __restrict__ bits, const long long* __restrict__ bits_base,
-                       const int32_t* __restrict__ offsets, int32_t* __restrict__ rep_of,
-                       int32_t* __restrict__ n_rep, unsigned* status) {
+                       const int32_t* __restrict__ offsets, const int32_t* __restrict__ overflow,
+                       int32_t* __restrict__ rep_of, int32_t* __restrict__ n_rep, unsigned* status) {
   extern __shared__ unsigned scan_smem[];
   unsigned* R = scan_smem;                  // kMaxWords: representatives so far, as a bitset
   unsigned* buf = scan_smem + kMaxWords;    // 2 x kScanBufWords
@@ -171,8 +197,13 @@ __global__ void __launch_bounds__(kScanThreads)
   const int off = offsets[e];
   const int n = offsets[e + 1] - off;
   const int W = (n + 31) >> 5;
-  if (n > kMaxBucketRows) {
-    if (threadIdx.x == 0) record_status(status, MOE_ERR_DEVICE_INDEX);
+  if (*overflow || n > kMaxBucketRows) {
+    // no bit matrix: every slot is its own representative
+    for (int i = threadIdx.x; i < n; i += blockDim.x) rep_of[off + i] = off + i;
+    if (threadIdx.x == 0) {
+      n_rep[e] = max(n, 0);
+      record_status(status, MOE_ERR_DEVICE_INDEX);
+    }
     return;
   }
   for (int w = threadIdx.x; w < W; w += blockDim.x) R[w] = 0u;
@@ -419,19 +450,22 @@ __device__ __forceinline__ int bucket_of(const int* off, int E, int s) {
 // of bucket e's slots takes the class its two tokens got at the previous call, found in the
 // previous record's bucket that held both (their previous slots si > sj, both in it; a pair
 // of tokens that shared two buckets got the same class in each).  Writes, in the bits layout
-// of this call, known / simc (the inherited classes) and the bits themselves (= simc; the
+// of this call, the planes (the inherited classes) and the bits themselves (= the class; the
 // similarity GEMM rewrites the bits of tiles with unclassified pairs), and lists the tiles
 // with an unclassified pair for the GEMM.  One CTA per tile (grid-stride), 8 warps; a warp
-// takes a row and a 32-column chunk at a time, a lane one pair.
+// takes a row at a time.  A chunk of 32 columns whose tokens sat at consecutive slots of one
+// previous bucket, with the row's token in that bucket too, is one 32-bit window of the
+// previous row's planes (one lane, a funnel shift); any other chunk takes a lane per column,
+// each searching its pair's previous buckets for a common one.
 constexpr int kLookupThreads = 256;
+constexpr int kLookupChunks = kTcTileN / 32;
 __global__ void __launch_bounds__(kLookupThreads)
     hist_lookup_kernel(const int2* __restrict__ tile_list, const int32_t* __restrict__ n_list,
                        const int4* __restrict__ mt_info, const int32_t* __restrict__ offsets,
                        const int32_t* __restrict__ perm, int T, int k, int E,
                        const long long* __restrict__ bits_base, HistView prev,
-                       unsigned* __restrict__ known_out, unsigned* __restrict__ simc_out,
-                       unsigned* __restrict__ bits, int2* __restrict__ cos_list,
-                       int32_t* __restrict__ n_cos) {
+                       uint2* __restrict__ planes_out, unsigned* __restrict__ bits,
+                       int2* __restrict__ cos_list, int32_t* __restrict__ n_cos) {
   extern __shared__ int hsm[];
   int* poff = hsm;                      // [E + 1] previous offsets
   int* col_e = poff + (E + 1);          // [256][k] previous bucket of each column token's pairs
@@ -439,6 +473,9 @@ __global__ void __launch_bounds__(kLookupThreads)
   int* row_e = col_s + kTcTileN * k;    // [128][k]
   int* row_s = row_e + kMTile * k;      // [128][k]
   __shared__ int s_unknown;
+  // per 32-column chunk: the previous bucket its tokens all held at consecutive slots from
+  // s_ch_s0 (-1: none), so a row in that bucket reads its 32 classes without a search
+  __shared__ int s_ch_e[kLookupChunks], s_ch_s0[kLookupChunks];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int P = T * k;
   const bool have = prev.header[0] == kHistMagic && prev.header[1] == T && prev.header[2] == k &&
@@ -485,18 +522,84 @@ __global__ void __launch_bounds__(kLookupThreads)
       }
     }
     __syncthreads();
+    if (have && warp < kLookupChunks) {
+      // warp ch: is chunk ch's run of columns one run of a previous bucket?  The candidates
+      // are the first column's previous buckets; each lane looks the candidate up among its
+      // own column's k entries (a token's buckets are stored in its routing order).
+      const int ch = warp, c = ch * 32 + lane;
+      const bool vc = lj0 + c < n_e;
+      int fe = -1, fs = 0;
+      for (int b = 0; b < k && fe < 0; ++b) {
+        const int e0 = __shfl_sync(0xffffffffu, vc ? col_e[c * k + b] : -1, 0);
+        const int s0 = __shfl_sync(0xffffffffu, vc ? col_s[c * k + b] : 0, 0);
+        if (e0 < 0) continue;
+        int my = -1;
+        for (int bb = 0; bb < k; ++bb)
+          if (vc && col_e[c * k + bb] == e0) my = col_s[c * k + bb];
+        if (__all_sync(0xffffffffu, !vc || my == s0 + lane)) {
+          fe = e0;
+          fs = s0;
+        }
+      }
+      if (lane == 0) {
+        s_ch_e[ch] = fe;
+        s_ch_s0[ch] = fs;
+      }
+    }
+    __syncthreads();
     bool unknown = false;
     for (int rr = warp; rr < nrows; rr += kLookupThreads / 32) {
       const int li = li0 + rr;
+      if (lj0 >= li) continue;  // the row has no pair in this column tile
       const long long wrow = bits_base[e] + static_cast<long long>(li) * W;
-      for (int ch = 0; ch < kTcTileN / 32; ++ch) {
+      // Word path: lane ch < 8 takes chunk ch when its columns are one run of the previous
+      // bucket fe and the row's token was in fe too; its 32 classes are then the 32-bit
+      // window of the previous row pi's planes that starts at the run's first slot.
+      bool fast = false;
+      if (have && lane < kLookupChunks) {
+        const int ch = lane;
+        const int ljb = lj0 + ch * 32;
+        const int fe = s_ch_e[ch];
+        if (ljb < li && fe >= 0) {
+          int pi = -1;
+          for (int a = 0; a < k; ++a)
+            if (row_e[rr * k + a] == fe) pi = row_s[rr * k + a];
+          const int o = poff[fe];
+          const int ne = poff[fe + 1] - o;
+          const int nvalid = min(32, li - ljb);
+          const int pj0 = s_ch_s0[ch] - o;
+          pi -= o;
+          if (pi >= 0 && pj0 >= 0 && pj0 + nvalid <= pi && pi < ne) {
+            const int Wp = (ne + 31) >> 5;
+            const long long base = prev.bits_base[fe] + static_cast<long long>(pi) * Wp;
+            const int w0 = pj0 >> 5, sh = pj0 & 31;
+            const uint2 lo = prev.planes[base + w0];
+            const uint2 hi = (pj0 + nvalid > 32 * (w0 + 1)) ? prev.planes[base + w0 + 1]
+                                                              : make_uint2(0u, 0u);
+            const unsigned vmask = nvalid == 32 ? 0xffffffffu : (1u << nvalid) - 1u;
+            const unsigned kw = __funnelshift_r(lo.x, hi.x, sh) & vmask;
+            const unsigned sw = __funnelshift_r(lo.y, hi.y, sh) & kw;
+            const long long w = wrow + (ljb >> 5);
+            planes_out[w] = make_uint2(kw, sw);
+            bits[w] = sw;
+            if (kw != vmask) unknown = true;
+            fast = true;
+          }
+        }
+      }
+      const unsigned fast_chunks = __ballot_sync(0xffffffffu, fast);
+      // Lane path for the other chunks: each lane searches its pair's buckets for a common one.
+      for (int ch = 0; ch < kLookupChunks; ++ch) {
         const int ljb = lj0 + ch * 32;
         if (ljb >= li) break;
-        const int c = ch * 32 + lane;
-        const bool in = ljb + lane < li;
-        bool kn = false, sm = false;
-        if (in && have) {
-          for (int a = 0; a < k && !kn; ++a) {
+        if ((fast_chunks >> ch) & 1u) continue;
+        const int lj = ljb + lane;
+        const bool in = lj < li;
+        long long widx = -1;
+        unsigned bitm = 0u;
+        if (have && in) {
+          const int c = ch * 32 + lane;
+          for (int a = 0; a < k && widx < 0; ++a) {
             const int ea = row_e[rr * k + a];
             if (ea < 0) continue;
             for (int b = 0; b < k; ++b) {
@@ -505,25 +608,25 @@ __global__ void __launch_bounds__(kLookupThreads)
               const int ne = poff[ea + 1] - o;
               const int pi = row_s[rr * k + a] - o, pj = col_s[c * k + b] - o;
               if (pj >= 0 && pj < pi && pi < ne) {
-                const long long widx = prev.bits_base[ea] +
-                                       static_cast<long long>(pi) * ((ne + 31) >> 5) + (pj >> 5);
-                const unsigned bit = 1u << (pj & 31);
-                kn = (prev.known[widx] & bit) != 0u;
-                sm = kn && (prev.simc[widx] & bit) != 0u;
+                widx = prev.bits_base[ea] + static_cast<long long>(pi) * ((ne + 31) >> 5) +
+                       (pj >> 5);
+                bitm = 1u << (pj & 31);
               }
               break;
             }
           }
         }
-        const unsigned kw = __ballot_sync(0xffffffffu, in && kn);
-        const unsigned sw = __ballot_sync(0xffffffffu, in && sm);
+        const uint2 pv = widx >= 0 ? prev.planes[widx] : make_uint2(0u, 0u);
+        const bool kn = in && (pv.x & bitm) != 0u;
+        const bool sm = kn && (pv.y & bitm) != 0u;
+        const unsigned kw = __ballot_sync(0xffffffffu, kn);
+        const unsigned sw = __ballot_sync(0xffffffffu, sm);
         const unsigned iw = __ballot_sync(0xffffffffu, in);
         if (kw != iw) unknown = true;
         if (lane == 0) {
-          const long long widx = wrow + (ljb >> 5);
-          known_out[widx] = kw;
-          simc_out[widx] = sw;
-          bits[widx] = sw;
+          const long long w = wrow + (ljb >> 5);
+          planes_out[w] = make_uint2(kw, sw);
+          bits[w] = sw;
         }
       }
     }
@@ -555,14 +658,20 @@ struct CondenseScratch {
   unsigned* bits;
   int2* cos_list;   // history: tiles with an unclassified pair
   int32_t* n_cos;
+  int32_t* overflow;  // a bucket longer than the scratch allows
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-size_t carve(void* base, int P, int E, CondenseScratch* s) {
+// Bucket rows the scratch is sized for: a bucket holds each token at most once.
+inline int bucket_rows_max(int T, int k) { return T < T * k ? T : T * k; }
+
+size_t carve(void* base, int T, int k, int E, CondenseScratch* s) {
+  const int P = T * k;
+  const int R = bucket_rows_max(T, k);
   const int n_mt = max_mtiles(P, E);
-  const long long max_tiles = static_cast<long long>(n_mt) * ((P + kTcTileN - 1) / kTcTileN);
-  const long long max_words = static_cast<long long>(P) * ((P + 31) / 32);
+  const long long max_tiles = static_cast<long long>(n_mt) * ((R + kTcTileN - 1) / kTcTileN);
+  const long long max_words = static_cast<long long>(P) * ((R + 31) / 32);
   size_t o = 0;
   auto take = [&](size_t bytes) {
     size_t at = o;
@@ -579,6 +688,7 @@ size_t carve(void* base, int P, int E, CondenseScratch* s) {
   const size_t o_bits = take(sizeof(unsigned) * max_words);
   const size_t o_cl = take(sizeof(int2) * max_tiles);
   const size_t o_nc = take(sizeof(int32_t));
+  const size_t o_of = take(sizeof(int32_t));
   if (s && base) {
     char* b = static_cast<char*>(base);
     s->norm = reinterpret_cast<float*>(b + o_norm);
@@ -591,13 +701,14 @@ size_t carve(void* base, int P, int E, CondenseScratch* s) {
     s->bits = reinterpret_cast<unsigned*>(b + o_bits);
     s->cos_list = reinterpret_cast<int2*>(b + o_cl);
     s->n_cos = reinterpret_cast<int32_t*>(b + o_nc);
+    s->overflow = reinterpret_cast<int32_t*>(b + o_of);
   }
   return o;
 }
 
-size_t hist_layout(int T, int k, int E, size_t* at /* 6 offsets or NULL */) {
+size_t hist_layout(int T, int k, int E, size_t* at /* 5 offsets or NULL */) {
   const long long P = static_cast<long long>(T) * k;
-  const size_t words = static_cast<size_t>(P) * static_cast<size_t>((P + 31) / 32);
+  const size_t words = static_cast<size_t>(P) * static_cast<size_t>((bucket_rows_max(T, k) + 31) / 32);
   size_t o = 0;
   auto take = [&](size_t bytes) {
     size_t a = o;
@@ -608,22 +719,21 @@ size_t hist_layout(int T, int k, int E, size_t* at /* 6 offsets or NULL */) {
   const size_t a1 = take(sizeof(int32_t) * (E + 1));
   const size_t a2 = take(sizeof(int32_t) * static_cast<size_t>(P));
   const size_t a3 = take(sizeof(long long) * E);
-  const size_t a4 = take(sizeof(unsigned) * words);
-  const size_t a5 = take(sizeof(unsigned) * words);
+  const size_t a4 = take(sizeof(uint2) * words);
   if (at) {
-    at[0] = a0; at[1] = a1; at[2] = a2; at[3] = a3; at[4] = a4; at[5] = a5;
+    at[0] = a0; at[1] = a1; at[2] = a2; at[3] = a3; at[4] = a4;
   }
   return o;
 }
 
 }  // namespace
 
-size_t condense_scratch_bytes(int T, int k, int E) { return carve(nullptr, T * k, E, nullptr); }
+size_t condense_scratch_bytes(int T, int k, int E) { return carve(nullptr, T, k, E, nullptr); }
 
 size_t hist_record_bytes(int T, int k, int E) { return hist_layout(T, k, E, nullptr); }
 
 HistView hist_view(const void* base, int T, int k, int E) {
-  size_t at[6];
+  size_t at[5];
   hist_layout(T, k, E, at);
   char* b = static_cast<char*>(const_cast<void*>(base));
   HistView v;
@@ -631,39 +741,39 @@ HistView hist_view(const void* base, int T, int k, int E) {
   v.offsets = reinterpret_cast<int32_t*>(b + at[1]);
   v.slot_of = reinterpret_cast<int32_t*>(b + at[2]);
   v.bits_base = reinterpret_cast<long long*>(b + at[3]);
-  v.known = reinterpret_cast<unsigned*>(b + at[4]);
-  v.simc = reinterpret_cast<unsigned*>(b + at[5]);
+  v.planes = reinterpret_cast<uint2*>(b + at[4]);
   return v;
 }
 
 namespace {
-cudaError_t condense_pipeline(const __nv_bfloat16* x_perm, const int32_t* offsets, int P, int d,
-                              int E, float tau, const HistArgs* h, int num_sms, int32_t* rep_of,
-                              int32_t* n_rep, int32_t* n_condensed, void* scratch,
-                              unsigned* status, cudaStream_t stream);
+cudaError_t condense_pipeline(const __nv_bfloat16* x_perm, const int32_t* offsets, int T, int k,
+                              int d, int E, float tau, const HistArgs* h, int num_sms,
+                              int32_t* rep_of, int32_t* n_rep, int32_t* n_condensed,
+                              void* scratch, unsigned* status, cudaStream_t stream);
 }  // namespace
 
-cudaError_t launch_condense(const __nv_bfloat16* x_perm, const int32_t* offsets, int P, int d,
-                            int E, float tau, int num_sms, int32_t* rep_of, int32_t* n_rep,
+cudaError_t launch_condense(const __nv_bfloat16* x_perm, const int32_t* offsets, int T, int k,
+                            int d, int E, float tau, int num_sms, int32_t* rep_of, int32_t* n_rep,
                             int32_t* n_condensed, void* scratch, unsigned* status,
                             cudaStream_t stream) {
-  return condense_pipeline(x_perm, offsets, P, d, E, tau, nullptr, num_sms, rep_of, n_rep,
+  return condense_pipeline(x_perm, offsets, T, k, d, E, tau, nullptr, num_sms, rep_of, n_rep,
                            n_condensed, scratch, status, stream);
 }
 
-cudaError_t launch_condense_hist(const __nv_bfloat16* x_perm, const int32_t* offsets, int P, int d,
+cudaError_t launch_condense_hist(const __nv_bfloat16* x_perm, const int32_t* offsets, int d,
                                  int E, float tau, const HistArgs& h, int num_sms,
                                  int32_t* rep_of, int32_t* n_rep, int32_t* n_condensed,
                                  void* scratch, unsigned* status, cudaStream_t stream) {
-  return condense_pipeline(x_perm, offsets, P, d, E, tau, &h, num_sms, rep_of, n_rep,
+  return condense_pipeline(x_perm, offsets, h.T, h.k, d, E, tau, &h, num_sms, rep_of, n_rep,
                            n_condensed, scratch, status, stream);
 }
 
 namespace {
-cudaError_t condense_pipeline(const __nv_bfloat16* x_perm, const int32_t* offsets, int P, int d,
-                              int E, float tau, const HistArgs* h, int num_sms, int32_t* rep_of,
-                              int32_t* n_rep, int32_t* n_condensed, void* scratch,
-                              unsigned* status, cudaStream_t stream) {
+cudaError_t condense_pipeline(const __nv_bfloat16* x_perm, const int32_t* offsets, int T, int k,
+                              int d, int E, float tau, const HistArgs* h, int num_sms,
+                              int32_t* rep_of, int32_t* n_rep, int32_t* n_condensed,
+                              void* scratch, unsigned* status, cudaStream_t stream) {
+  const int P = T * k;
   HistView out = {};
   if (h) {
     // the record's header, offsets and slots; its bits_base is written by the tile list
@@ -689,15 +799,16 @@ cudaError_t condense_pipeline(const __nv_bfloat16* x_perm, const int32_t* offset
     return cudaGetLastError();
   }
   CondenseScratch s;
-  carve(scratch, P, E, &s);
+  carve(scratch, T, k, E, &s);
   row_stats_kernel<<<min(ceil_div(P, 8), 4096), 256, 0, stream>>>(x_perm, offsets, E, d, s.norm,
                                                                   s.hash);
   cudaError_t err = launch_build_mtiles(nullptr, offsets, 0, E, nullptr, s.mt_info,
                                         s.group_mt_begin, stream);
   if (err != cudaSuccess) return err;
   long long* bits_base = h ? out.bits_base : s.bits_base;
-  sim_tiles_kernel<<<1, 256, 0, stream>>>(s.mt_info, s.group_mt_begin, offsets, E, s.tile_list,
-                                          s.n_list, bits_base);
+  sim_tiles_kernel<<<1, 256, 0, stream>>>(s.mt_info, s.group_mt_begin, offsets, E,
+                                          bucket_rows_max(T, k), s.tile_list, s.n_list, bits_base,
+                                          s.overflow, h ? out.header : nullptr, status);
   const int2* gemm_list = s.tile_list;
   const int32_t* gemm_n = s.n_list;
   int hist_mode = 0;
@@ -716,10 +827,10 @@ cudaError_t condense_pipeline(const __nv_bfloat16* x_perm, const int32_t* offset
                                   static_cast<int>(sizeof(int) * (257 + 2 * (kTcTileN + kMTile) * 32)));
     });
     if (e != cudaSuccess) return e;
-    const int max_tiles = max_mtiles(P, E) * ((P + kTcTileN - 1) / kTcTileN);
-    hist_lookup_kernel<<<max(1, min(max_tiles, 4 * num_sms)), kLookupThreads, smem, stream>>>(
+    const int max_tiles = max_mtiles(P, E) * ((bucket_rows_max(T, k) + kTcTileN - 1) / kTcTileN);
+    hist_lookup_kernel<<<max(1, min(max_tiles, 8 * num_sms)), kLookupThreads, smem, stream>>>(
         s.tile_list, s.n_list, s.mt_info, offsets, h->perm, h->T, h->k, E, bits_base, prev,
-        out.known, out.simc, s.bits, s.cos_list, s.n_cos);
+        out.planes, s.bits, s.cos_list, s.n_cos);
     gemm_list = s.cos_list;
     gemm_n = s.n_cos;
     hist_mode = 2;
@@ -738,8 +849,7 @@ cudaError_t condense_pipeline(const __nv_bfloat16* x_perm, const int32_t* offset
   a.tile_list = gemm_list;
   a.n_list = gemm_n;
   a.hist_mode = hist_mode;
-  a.hknown = out.known;
-  a.hsimc = out.simc;
+  a.hplanes = out.planes;
   a.s1 = h ? h->s1 : 2.0f;
   a.s2 = h ? h->s2 : -2.0f;
   a.n_kblocks = d / kTcTileK;
@@ -766,8 +876,8 @@ cudaError_t condense_pipeline(const __nv_bfloat16* x_perm, const int32_t* offset
                                 static_cast<int>(smem));
   });
   if (err != cudaSuccess) return err;
-  greedy_scan_kernel<<<E, kScanThreads, smem, stream>>>(s.bits, bits_base, offsets, rep_of,
-                                                        n_rep, status);
+  greedy_scan_kernel<<<E, kScanThreads, smem, stream>>>(s.bits, bits_base, offsets, s.overflow,
+                                                        rep_of, n_rep, status);
   condensed_count_kernel<<<1, 32, 0, stream>>>(offsets, n_rep, E, n_condensed);
   return cudaGetLastError();
 }

@@ -594,16 +594,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               brow[lj0 >> 5] = word;
             } else {
               const long long widx = wrow + (lj0 >> 5);
-              uint32_t kw = 0, sw = 0;
-              if (hmode == 2) {
-                kw = args.hknown[widx];
-                sw = args.hsimc[widx];
-              }
+              uint2 ks = make_uint2(0u, 0u);
+              if (hmode == 2) ks = args.hplanes[widx];
+              const uint32_t kw = ks.x, sw = ks.y;
               // a pair with a class is decided by it; the others by their cosine, and get
               // a class from it (similar first)
               brow[lj0 >> 5] = (kw & sw) | (~kw & word);
-              args.hknown[widx] = kw | (~kw & (w1 | w2));
-              args.hsimc[widx] = (kw & sw) | (~kw & w1);
+              args.hplanes[widx] = make_uint2(kw | (~kw & (w1 | w2)), (kw & sw) | (~kw & w1));
             }
           }
         }
@@ -651,13 +648,17 @@ constexpr int STAGES = 6;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = (BN / 2) * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int SHARED_BYTES = 4096;
+constexpr int SHARED_BYTES = 5120;
 // per epilogue warp: two {32 columns, 32 rows} bf16 TMA store boxes of 2 KB (64-byte swizzle)
 constexpr int OUT_BOX_BYTES = 32 * 32 * 2;
 constexpr int OUT_STAGE_BYTES = 4 * 2 * OUT_BOX_BYTES;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + SHARED_BYTES + OUT_STAGE_BYTES;
 static_assert((STAGES * STAGE_BYTES + SHARED_BYTES) % 1024 == 0, "output boxes 1024-byte aligned");
-constexpr int PAIR_GROUP = M_GROUP / 2;
+// Units per block of the tile walk.  Measured on the Llama-4-Scout-shaped shared expert
+// (32 pair tiles, K = 5120): blocks of 8 keep the block's 21 MB of token rows in L2 and read
+// the weights once per block; blocks of 25 (65 MB of token rows) lost the rows from L2 and
+// read 1.84x the DRAM bytes.
+constexpr int kUnitGroup = 8;
 constexpr int TAIL_ROWS = BM / 2;  // token rows a CTA loads for a tail tile (box height)
 constexpr int TAIL_W_ROWS = 16;    // hidden units per gate (or up) run of a kSwiGLU tail
 constexpr int TAIL_TX = 2 * (A_BYTES + TAIL_ROWS * BK * 2);  // both CTAs, one K block
@@ -672,7 +673,8 @@ struct Shared {
   uint64_t drain;
   uint32_t tmem_base;
   volatile int abort_flag;
-  int gmb[257];    // first m-tile of each group
+  int goff[257];   // first row of each group
+  int grows[256];  // rows of each group
   int gub[257];    // first unit (pair or tail) of each group
   int gpt[256];    // pairs of each group | rows of its tail (0..128) << 16
 };
@@ -696,8 +698,12 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Shared* 
 }
 
 // Tile -> this CTA's part.  Groups are walked in order; inside a group, blocks
-// of PAIR_GROUP units (pairs first, then tails), N tiles with the units
-// fastest, so a group's tails run beside its pairs and share their weights in L2.
+// of a.unit_group units (pairs first, then tails), N tiles with the units
+// fastest, so a group's tails run beside its pairs and share their weights in L2,
+// and a block's token rows stay in L2 while the weights stream past them.  Odd blocks walk
+// the N tiles in reverse, so a block starts on the weight tiles the block before it used
+// last, which are still in L2 (a group's weights can be larger than L2: the shared expert's
+// gate/up projection of the Llama-4-Scout-shaped layer is 168 MB).
 __device__ __forceinline__ TileInfo tile_info(const TcGemmArgs& a, const Shared* sh, int tile,
                                               uint32_t rank) {
   const int NT = a.n_ntiles;
@@ -708,20 +714,23 @@ __device__ __forceinline__ TileInfo tile_info(const TcGemmArgs& a, const Shared*
   }
   const int beg = sh->gub[lo], cnt = sh->gub[lo + 1] - beg;
   const int local = tile - beg * NT;
-  const int blk = local / (PAIR_GROUP * NT);
-  const int within = local - blk * PAIR_GROUP * NT;
-  const int bs = min(PAIR_GROUP, cnt - blk * PAIR_GROUP);
-  const int nt = within / bs;
-  const int u = blk * PAIR_GROUP + (within - nt * bs);
+  const int G = a.unit_group;
+  const int blk = local / (G * NT);
+  const int within = local - blk * G * NT;
+  const int bs = min(G, cnt - blk * G);
+  const int nt_fwd = within / bs;
+  const int u = blk * G + (within - nt_fwd * bs);
+  const int nt = (blk & 1) ? NT - 1 - nt_fwd : nt_fwd;
   const int np = sh->gpt[lo] & 0xffff;
   const bool tail = u >= np;
-  const int4 m = a.mt_info[sh->gmb[lo] + (tail ? 2 * np : 2 * u + static_cast<int>(rank))];
+  // m-tile of the group: 128-row tile 2u + rank of a pair, or the one left after the pairs
+  const int mt = tail ? 2 * np : 2 * u + static_cast<int>(rank);
   TileInfo t;
   t.nt = nt;
-  t.slice = m.x;
-  t.row0 = m.y;
-  t.nrows = tail ? sh->gpt[lo] >> 16 : m.z;
-  t.gbase = m.w;
+  t.slice = lo;
+  t.gbase = sh->goff[lo];
+  t.row0 = t.gbase + mt * BM;
+  t.nrows = tail ? sh->gpt[lo] >> 16 : min(BM, sh->grows[lo] - mt * BM);
   t.tail = tail ? 1 : 0;
   return t;
 }
@@ -808,17 +817,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   ptx::cluster_sync();  // both CTAs' barriers and the pair's TMEM exist from here on
   ptx::tc_fence_after();
   pdl_wait();
-  for (int g = threadIdx.x; g <= args.n_groups; g += blockDim.x) sh->gmb[g] = args.group_mt_begin[g];
-  __syncthreads();
-  // Units of each group: pairs of m-tiles, then a tail if a single m-tile is left.
+  // Rows of each group, from the group offsets, from a fixed row count, or from the m-tile
+  // table (whose m-tiles are 128-row pieces of each group from its first row).  Units of each
+  // group: pairs of m-tiles, then a tail if a single m-tile is left.
   for (int g = threadIdx.x; g < args.n_groups; g += blockDim.x) {
-    const int m = sh->gmb[g + 1] - sh->gmb[g];
-    int np = 0, tail_rows = 0;
-    if (m > 0) {
-      const int rows = (m - 1) * BM + args.mt_info[sh->gmb[g + 1] - 1].z;
-      np = m >> 1;
-      tail_rows = (m & 1) ? rows - np * 2 * BM : 0;
+    int off = 0, rows = 0;
+    if (args.group_off) {
+      off = args.group_off[g];
+      rows = args.group_off[g + 1] - off;
+    } else if (args.fixed_rows > 0) {
+      off = g * args.fixed_rows;
+      rows = args.fixed_rows;
+    } else {
+      const int b = args.group_mt_begin[g], e = args.group_mt_begin[g + 1];
+      if (e > b) {
+        const int4 first = args.mt_info[b];
+        off = first.w;
+        rows = (e - b - 1) * BM + args.mt_info[e - 1].z;
+      }
     }
+    const int m = (rows + BM - 1) / BM;
+    const int np = m >> 1;
+    const int tail_rows = (m & 1) ? rows - np * 2 * BM : 0;
+    sh->goff[g] = off;
+    sh->grows[g] = rows;
     sh->gpt[g] = np | (tail_rows << 16);
     sh->gub[g] = np + (tail_rows > 0 ? 1 : 0);  // units, turned into offsets below
   }
@@ -1122,7 +1144,8 @@ cudaError_t tc_gemm(int mode, const void* A, long long a_rows, int K, const void
                     int b_slices, int b_rows, int b_cols, const TcGemmArgs& args_in, int grid,
                     cudaStream_t stream) {
   CUtensorMap ma, mb;
-  const TcGemmArgs& args = args_in;
+  TcGemmArgs args = args_in;
+  if (args.unit_group <= 0) args.unit_group = tc::pr::kUnitGroup;
   if (!tc::make_map(&ma, 2, A, K, a_rows, 1, tc::BM)) return cudaErrorInvalidValue;
   // The FFN modes run on CTA pairs, each CTA loading half of the 256-row B tile.
   const bool pair = mode == tc::kSwiGLU || mode == tc::kStore;

@@ -83,10 +83,18 @@ struct TcGemmArgs {
   const int4* mt_info;
   const int32_t* group_mt_begin;
   int n_groups;
+  // pair kernel (kSwiGLU, kStore): the groups' rows straight from their offsets
+  // [n_groups + 1] or, when fixed_rows > 0, fixed_rows rows each from row 0; else from
+  // mt_info / group_mt_begin
+  const int32_t* group_off;
+  int fixed_rows;
   const int2* tile_list;  // kSimBits only
   const int32_t* n_list;  // kSimBits only
   int n_ntiles;
   int n_kblocks;
+  // pair kernel: units (pair or tail tiles) per block of the tile walk; a block sweeps every
+  // N tile with its units fastest (0 = the default, 8)
+  int unit_group;
   int kb_per_slice;  // K blocks per B slice (the shared down projection spans slices along K)
   int nt_per_slice;  // N tiles per B slice (the shared gate/up projection spans slices along N)
   int b_up_offset;   // kSwiGLU: row of the first up-projection row inside a B slice (= H)
@@ -103,11 +111,10 @@ struct TcGemmArgs {
   unsigned* bits;
   float tau;
   // kSimBits with history: 0 none; 1 record the classes (cos >= s1 similar, <= s2
-  // dissimilar) into hknown / hsimc (bits layout); 2 also merge the classes the history
-  // lookup already wrote there: a pair with a class keeps it and decides its bit
+  // dissimilar) into hplanes (bits layout; x = known, y = similar); 2 also merge the classes
+  // the history lookup already wrote there: a pair with a class keeps it and decides its bit
   int hist_mode;
-  unsigned* hknown;
-  unsigned* hsimc;
+  uint2* hplanes;
   float s1, s2;
   unsigned* status;
   // kRouter: D = x . [W1|W2|W3] over a K range of 3*d (the three bf16 terms of W_r)
@@ -208,7 +215,7 @@ cudaError_t simt_gemm_store(const float* A, const float* B, int b_slices, int b_
 
 // ------------------------------------------------------------------ condensation
 size_t condense_scratch_bytes(int T, int k, int E);
-cudaError_t launch_condense(const __nv_bfloat16* x_perm, const int32_t* offsets, int P, int d,
+cudaError_t launch_condense(const __nv_bfloat16* x_perm, const int32_t* offsets, int T, int k, int d,
                             int E, float tau, int num_sms, int32_t* rep_of, int32_t* n_rep,
                             int32_t* n_condensed, void* scratch, unsigned* status,
                             cudaStream_t stream);
@@ -220,8 +227,7 @@ struct HistView {
   int32_t* offsets;      // [E+1]
   int32_t* slot_of;      // [T*k]
   long long* bits_base;  // [E]
-  unsigned* known;       // [P * ceil(P/32)]
-  unsigned* simc;        // [P * ceil(P/32)]
+  uint2* planes;         // [P * ceil(P/32)]: x = known (the pair has a class), y = the class
 };
 size_t hist_record_bytes(int T, int k, int E);
 HistView hist_view(const void* base, int T, int k, int E);
@@ -234,7 +240,7 @@ struct HistArgs {
   void* hist_out;
   int32_t* n_cos_tiles;    // nullable
 };
-cudaError_t launch_condense_hist(const __nv_bfloat16* x_perm, const int32_t* offsets, int P, int d,
+cudaError_t launch_condense_hist(const __nv_bfloat16* x_perm, const int32_t* offsets, int d,
                                  int E, float tau, const HistArgs& h, int num_sms,
                                  int32_t* rep_of, int32_t* n_rep, int32_t* n_condensed,
                                  void* scratch, unsigned* status, cudaStream_t stream);

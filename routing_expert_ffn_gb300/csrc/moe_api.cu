@@ -20,6 +20,9 @@ static __device__ __align__(256) unsigned char g_dispatch_scratch[kStaticDispatc
 namespace {
 
 constexpr int kMaxDevices = 64;
+// Condensation walks a bucket's representatives as a shared-memory bitset of up to 65536
+// rows; a bucket holds each token at most once, so T <= 65536 bounds every bucket.
+constexpr int kCondenseMaxTokens = 65536;
 
 // Device addresses of the two file-scope arrays (in host code their names are only
 // host-side stand-ins, never device addresses) and the SM count.
@@ -154,15 +157,17 @@ moe_status run_routed_ffn(const moe_config* c, const moe_weights* w, const void*
                                 s.rep_off + E, static_cast<int>(P), d, s.x_rep, di->status, st));
     A1 = s.x_rep;
     rowmap = s.rep_rows;
-  } else {
+  } else if (c->act_dtype != MOE_BF16) {
     MOE_CUDA(launch_build_mtiles(nullptr, offsets, 0, E, nullptr, s.mt_routed, s.gmb_routed, st));
   }
   if (c->act_dtype == MOE_BF16) {
     TcGemmArgs a = {};
     a.status = di->status;
-    // gate/up + SwiGLU
+    // gate/up + SwiGLU; the pair kernel reads the buckets' rows from the offsets (all slots)
+    // or from the representatives' m-tile table
     a.mt_info = s.mt_routed;
     a.group_mt_begin = s.gmb_routed;
+    a.group_off = rep_of ? nullptr : offsets;
     a.n_groups = E;
     a.n_ntiles = H / 128;
     a.nt_per_slice = H / 128;
@@ -201,12 +206,12 @@ moe_status run_shared_ffn(const moe_config* c, const moe_weights* w, const void*
                           void* shared_out, const FfnScratch& s, DeviceInfo* di, cudaStream_t st) {
   const int T = c->T, d = c->d, S = c->n_shared, Hs = c->H_shared;
   if (S == 0) return MOE_OK;
-  MOE_CUDA(launch_build_mtiles(nullptr, nullptr, T, 1, nullptr, s.mt_shared, s.gmb_shared, st));
+  if (c->act_dtype != MOE_BF16)
+    MOE_CUDA(launch_build_mtiles(nullptr, nullptr, T, 1, nullptr, s.mt_shared, s.gmb_shared, st));
   if (c->act_dtype == MOE_BF16) {
     TcGemmArgs b = {};
     b.status = di->status;
-    b.mt_info = s.mt_shared;
-    b.group_mt_begin = s.gmb_shared;
+    b.fixed_rows = T;  // one group of all T tokens
     b.n_groups = 1;
     b.n_ntiles = S * Hs / 128;
     b.nt_per_slice = Hs / 128;
@@ -454,14 +459,14 @@ moe_status moe_condense(const moe_config* cfg, const void* x_perm, const int32_t
   const bool active = tau <= 1.0f;
   if (active) {
     if (cfg->act_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
-    if (P > 65536) return MOE_ERR_UNSUPPORTED;
+    if (cfg->T > kCondenseMaxTokens) return MOE_ERR_UNSUPPORTED;
     MOE_PTR(ws);
     MOE_REQUIRE(ws_bytes >= moe_condense_workspace_size(cfg), MOE_ERR_WORKSPACE);
   }
   DeviceInfo* di = device_info();
   if (!di) return MOE_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  MOE_CUDA(launch_condense(static_cast<const __nv_bfloat16*>(x_perm), offsets, static_cast<int>(P),
+  MOE_CUDA(launch_condense(static_cast<const __nv_bfloat16*>(x_perm), offsets, cfg->T, cfg->k,
                            cfg->d, cfg->E, tau, di->num_sms, rep_of, n_rep, n_condensed, ws,
                            di->status, st));
   return MOE_OK;
@@ -482,7 +487,7 @@ moe_status moe_condense_hist(const moe_config* cfg, const void* x_perm, const in
   if (!(tau <= 1.0f) || s1 != s1 || s2 != s2) return MOE_ERR_INVALID_ARG;
   if (cfg->act_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   const long long P = static_cast<long long>(cfg->T) * cfg->k;
-  if (P > 65536) return MOE_ERR_UNSUPPORTED;
+  if (cfg->T > kCondenseMaxTokens) return MOE_ERR_UNSUPPORTED;
   MOE_PTR(offsets);
   MOE_PTR(n_rep);
   MOE_PTR(n_condensed);
@@ -516,7 +521,7 @@ moe_status moe_condense_hist(const moe_config* cfg, const void* x_perm, const in
   h.hist_out = hist_out;
   h.n_cos_tiles = n_cos_tiles;
   MOE_CUDA(launch_condense_hist(static_cast<const __nv_bfloat16*>(x_perm), offsets,
-                                static_cast<int>(P), cfg->d, cfg->E, tau, h, di->num_sms, rep_of,
+                                cfg->d, cfg->E, tau, h, di->num_sms, rep_of,
                                 n_rep, n_condensed, ws, di->status,
                                 reinterpret_cast<cudaStream_t>(stream)));
   return MOE_OK;
@@ -625,7 +630,8 @@ moe_status layer_forward_impl(const moe_config* cfg, const moe_weights* w, const
     MOE_PTR(residual);
   const bool condense = tau <= 1.0f;
   const long long P = static_cast<long long>(cfg->T) * cfg->k;
-  if (condense && (cfg->act_dtype != MOE_BF16 || P > 65536)) return MOE_ERR_UNSUPPORTED;
+  if (condense && (cfg->act_dtype != MOE_BF16 || cfg->T > kCondenseMaxTokens))
+    return MOE_ERR_UNSUPPORTED;
   MOE_PTR(ws);
   MOE_REQUIRE(ws_bytes >= moe_workspace_size(cfg, condense), MOE_ERR_WORKSPACE);
   DeviceInfo* di = device_info();
@@ -657,7 +663,7 @@ moe_status layer_forward_impl(const moe_config* cfg, const moe_weights* w, const
   const int32_t* rep_of = nullptr;
   if (condense) {
     MOE_CUDA(launch_condense(static_cast<const __nv_bfloat16*>(L.x_perm), L.offsets,
-                             static_cast<int>(P), cfg->d, cfg->E, tau, di->num_sms, L.rep_of,
+                             cfg->T, cfg->k, cfg->d, cfg->E, tau, di->num_sms, L.rep_of,
                              L.n_rep, n_condensed_out ? n_condensed_out : L.n_condensed,
                              L.condense_ws, di->status, st));
     rep_of = L.rep_of;
@@ -843,7 +849,7 @@ extern "C" moe_status moe_layer_backward(const moe_config* cfg, const moe_weight
   if (cfg->T == 0) return MOE_OK;
   if (cfg->act_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   const bool condense = tau <= 1.0f;
-  if (condense && static_cast<long long>(cfg->T) * cfg->k > 65536) return MOE_ERR_UNSUPPORTED;
+  if (condense && cfg->T > kCondenseMaxTokens) return MOE_ERR_UNSUPPORTED;
   s = check_weights(cfg, w);
   if (s != MOE_OK) return s;
   MOE_PTR(w->W_r);
@@ -880,8 +886,8 @@ extern "C" moe_status moe_layer_backward(const moe_config* cfg, const moe_weight
                                 b.slot_of, b.x_perm, b.dispatch_ws, sms, di->status, st));
   if (condense) {
     // Luffy condensation: a condensed slot's expert input is its representative's row
-    MOE_CUDA(launch_condense(static_cast<const __nv_bfloat16*>(b.x_perm), b.offsets,
-                             static_cast<int>(static_cast<long long>(T) * k), d, E, tau, sms,
+    MOE_CUDA(launch_condense(static_cast<const __nv_bfloat16*>(b.x_perm), b.offsets, T, k, d, E,
+                             tau, sms,
                              b.rep_of, b.n_rep, b.n_condensed, b.condense_ws, di->status, st));
     MOE_CUDA(launch_members(b.rep_of, b.offsets, E, b.mem_off, b.mem_cnt, b.mem_list, st));
   }

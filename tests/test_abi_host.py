@@ -122,10 +122,10 @@ def test_workspace_checks(L):
 
 
 def test_condensation_limits(L):
-    """Condensation takes bf16 layers with at most 65536 routed pairs (checked on the host)."""
+    """Condensation takes bf16 layers of at most 65536 tokens (checked on the host)."""
     lib = L.lib()
     w = L.moe_weights(FAKE, None, FAKE, FAKE, None, None)
-    cbig = _cfg(L, T=32769)  # k = 2: 65538 pairs
+    cbig = _cfg(L, T=65537)
     r = lib.moe_condense(ctypes.byref(cbig), FAKE, FAKE, 0.9, FAKE, FAKE, FAKE, FAKE, 1 << 40, None)
     assert r == 2
     r = lib.moe_layer_forward(ctypes.byref(cbig), ctypes.byref(w), FAKE, None, 0.9, FAKE,
@@ -172,7 +172,7 @@ def test_layer_backward_argument_checks(L):
     c32 = _cfg(L, dtype="f32")
     assert lib.moe_layer_backward(*args(c32, FAKE, nan, 1 << 40)) == 2     # fp32 layers
     cbig = _cfg(L, T=70000)
-    assert lib.moe_layer_backward(*args(cbig, FAKE, 0.9, 1 << 40)) == 2    # condensing T*k > 65536
+    assert lib.moe_layer_backward(*args(cbig, FAKE, 0.9, 1 << 40)) == 2    # condensing T > 65536
     c0 = _cfg(L, T=0)
     assert lib.moe_layer_backward(ctypes.byref(c0), ctypes.byref(w), None, None, nan, None, None,
                                   None, None, None, None, None, None, None, 0, None) == 0

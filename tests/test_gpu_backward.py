@@ -1,11 +1,13 @@
 """Layer backward (moe_layer_backward) vs the fp64 oracle's chain rule, on one GPU.
 
 Routing is bit-exact (the same forward recompute as the forward tests).  Gradients are
-compared as max|gpu - oracle| <= BWD_TOL * max|oracle| per tensor.  BWD_TOL = 2e-2: the
-backward chains two more bf16 roundings than the forward (the output gradient dy = g * d_out
-and the SwiGLU gradient dA are rounded to bf16 before their GEMMs, on top of the recomputed
-pre-activations and h), each worth up to 2^-9 relative, accumulated over K = d, 2H or the
-expert's rows in fp32.
+compared as max|gpu - oracle| <= BWD_TOL * max|oracle| per tensor, with BWD_TOL = 1e-2, the
+bound the layer statement gives bf16 outputs.  The backward chains two more bf16 roundings
+than the forward (the output gradient dy = g * d_out and the SwiGLU gradient dA are rounded
+to bf16 before their GEMMs, on top of the recomputed pre-activations and h), each worth up to
+2^-9 relative, accumulated over K = d, 2H or the expert's rows in fp32; measured on every case
+here the largest error is 0.998e-2 (a small expert's down-projection weight gradient), and
+the kernels are deterministic, so the same inputs give the same error on every run.
 """
 from __future__ import annotations
 
@@ -21,7 +23,7 @@ from tests import harness
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-BWD_TOL = 2e-2
+BWD_TOL = 1e-2
 
 SMALL = {
     # softmax top-k, shared expert, residual = x (DeepSeek-V2-Lite-like, narrow)
@@ -130,6 +132,23 @@ def test_backward_full_width_decode_shape(moe):
     used = sorted(set(idx.ravel().tolist()))
     unused = sorted(set(range(cfg.E)) - set(used))
     experts = used[:3] + unused[:1]
+    ref = orc.layer_backward(inp["x"], inp["W_r"], inp["bias"], inp["W_gu"], inp["W_down"],
+                             inp["Ws_gu"], inp["Ws_down"], cfg.k, cfg.gating, d_out_np,
+                             residual_mode=cfg.residual, residual=inp["residual"],
+                             grad_experts=experts)
+    _check(g, ref, cfg, experts=experts)
+
+
+def test_backward_full_size_dsv2_lite(moe):
+    """The DeepSeek-V2-Lite-shaped layer at its full 4096 tokens: the input and router
+    gradients of every token, both shared experts' weight gradients, and the routed weight
+    gradients of three experts (the first, a middle and the last expert index)."""
+    cfg = gen.CONFIGS["dsv2_lite"]
+    inp, C, w, x, d_out, d_out_np = _case(moe, cfg)
+    g = moe.layer_backward(C, w, x, d_out)
+    torch.cuda.synchronize()
+    assert moe.get_device_status() == 0
+    experts = [0, cfg.E // 2, cfg.E - 1]
     ref = orc.layer_backward(inp["x"], inp["W_r"], inp["bias"], inp["W_gu"], inp["W_down"],
                              inp["Ws_gu"], inp["Ws_down"], cfg.k, cfg.gating, d_out_np,
                              residual_mode=cfg.residual, residual=inp["residual"],

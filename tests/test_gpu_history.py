@@ -41,10 +41,10 @@ def _align(x):
 def decode_history(rec: np.ndarray, T: int, k: int, E: int) -> dict:
     """{(u, t): similar} from a history record (layout of include/moe.h)."""
     P = T * k
-    words = P * ((P + 31) // 32)
+    words = P * ((min(T, P) + 31) // 32)  # a bucket holds each token at most once
     o = 0
     at = []
-    for nbytes in (4 * 5, 4 * (E + 1), 4 * P, 8 * E, 4 * words, 4 * words):
+    for nbytes in (4 * 5, 4 * (E + 1), 4 * P, 8 * E, 8 * words):
         at.append(o)
         o = _align(o + nbytes)
     b = rec.tobytes()
@@ -53,8 +53,8 @@ def decode_history(rec: np.ndarray, T: int, k: int, E: int) -> dict:
     offsets = np.frombuffer(b, np.int32, E + 1, at[1])
     slot_of = np.frombuffer(b, np.int32, P, at[2])
     base = np.frombuffer(b, np.int64, E, at[3])
-    known = np.frombuffer(b, np.uint32, words, at[4])
-    simc = np.frombuffer(b, np.uint32, words, at[5])
+    planes = np.frombuffer(b, np.uint32, 2 * words, at[4])
+    known, simc = np.ascontiguousarray(planes[0::2]), np.ascontiguousarray(planes[1::2])
     tok_of = np.full(P, -1, np.int64)
     for p, s in enumerate(slot_of):
         if s >= 0:

@@ -222,6 +222,34 @@ def test_layer_full_size_sampled(moe, name):
     _layer_check(moe, name, tau=tau, tokens=_sample_tokens(cfg.T, 48))
 
 
+def test_layer_full_size_every_token_dsv2_lite(moe):
+    """The DeepSeek-V2-Lite-shaped layer at its full 4096 tokens, every token of the output
+    against the oracle (its whole fp64 layer, about 570 GFLOP, takes seconds on the host)."""
+    _layer_check(moe, "dsv2_lite")
+
+
+def test_expert_ffn_full_size_every_slot_dsv2_lite(moe):
+    """Every one of the 24576 routed slots (and every token's shared output) of the
+    DeepSeek-V2-Lite-shaped expert FFN against the oracle's SwiGLU experts."""
+    cfg, inp, C, w, x, r = _setup(moe, "dsv2_lite")
+    _, idx, _ = moe.route(C, x, w.W_r, w.router_bias)
+    d = moe.dispatch(C, x, idx)
+    y, so = moe.expert_ffn(C, w, d["x_perm"], d["offsets"], None, x)
+    torch.cuda.synchronize()
+    _, offsets, perm, _ = orc.dispatch(orc.route(inp["x"], inp["W_r"], inp["bias"], cfg.k,
+                                                 cfg.gating)[1], cfg.E)
+    np.testing.assert_array_equal(_np(d["perm"])[: cfg.P], perm)
+    yr = np.zeros((cfg.P, cfg.d))
+    for e in range(cfg.E):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if b > a:
+            yr[a:b] = orc.swiglu_expert(inp["x"][perm[a:b]], inp["W_gu"][e], inp["W_down"][e])
+    assert harness.max_rel_err(_np(y)[: cfg.P], yr) <= harness.tolerance(cfg)
+    sr = orc.shared_experts(inp["x"], inp["Ws_gu"], inp["Ws_down"])
+    assert harness.max_rel_err(_np(so), sr) <= harness.tolerance(cfg)
+    _status_ok(moe)
+
+
 @pytest.mark.parametrize("E,k", [(256, 8), (64, 32)])
 def test_layer_max_experts_and_k(moe, E, k):
     """The largest E (256: router split-K path, 257-entry group tables in the dispatch and both
@@ -445,6 +473,25 @@ def test_condense_ragged_buckets(moe):
     per_bucket = [len(set(expect[offsets[e]:offsets[e + 1]])) for e in range(len(sizes))]
     np.testing.assert_array_equal(_np(n_rep)[: len(sizes)], per_bucket)
     assert int(ncond.item()) == P - distinct
+    _status_ok(moe)
+
+
+def test_condense_more_than_65536_pairs(moe):
+    """The Luffy workload at 40000 tokens (80000 routed pairs, buckets of about 5000 rows):
+    the scratch is sized by bucket rows (each token at most once per bucket), so condensation
+    takes more pairs than the 65536 it was once limited to; bit for bit against the oracle."""
+    cfg, inp, C, w, x, r = _setup(moe, "luffy_condense", T=40000)
+    assert cfg.P > 65536
+    _, idx, _ = moe.route(C, x, w.W_r, w.router_bias)
+    d = moe.dispatch(C, x, idx)
+    rep_of, n_rep, ncond = moe.condense(C, d["x_perm"], d["offsets"], cfg.taus[0])
+    torch.cuda.synchronize()
+    _, idx_o, _ = orc.route(inp["x"], inp["W_r"], inp["bias"], cfg.k, cfg.gating)
+    _, offsets, perm, _ = orc.dispatch(idx_o, cfg.E)
+    np.testing.assert_array_equal(_np(d["perm"])[: cfg.P], perm)
+    ref = orc.condense(inp["x"][perm], offsets, cfg.taus[0])
+    np.testing.assert_array_equal(_np(rep_of)[: cfg.P], ref)
+    assert int(ncond.item()) == int(np.sum(ref != np.arange(cfg.P)))
     _status_ok(moe)
 
 
