@@ -314,10 +314,14 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         ms_b = max_over_ranks(timed(g_bwd), world, dev)
         wkb = work(C)
         b_flops = 2.0 * wkb["ffn_flops"]  # input and weight gradients: 12 d H per pair (+ shared)
+        peak_b = float(load_peaks()[0].get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
         backward = {"ms_per_step": ms_b, "tokens_per_s": job_tokens_per_s(C.T, world, ms_b),
                     "algorithmic_TFLOP_s": b_flops / (ms_b / 1e3) / 1e12,
-                    "frac_of_bf16_peak": b_flops / (ms_b / 1e3) / 1e12 /
-                    float(load_peaks()[0].get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])),
+                    "frac_of_bf16_peak": b_flops / (ms_b / 1e3) / 1e12 / peak_b,
+                    # the call also recomputes the forward's expert GEMMs (6 d H per pair and
+                    # per token and shared expert): the tensor work it actually does
+                    "frac_of_bf16_peak_with_recompute":
+                        (b_flops + wkb["ffn_flops"]) / (ms_b / 1e3) / 1e12 / peak_b,
                     "path": "moe_layer_backward (forward recomputed inside), CUDA graph",
                     "flops_note": "12 d H per routed pair + 12 d H_shared per token and shared "
                                   "expert; the recompute of the forward (6 d H per pair) is not counted"}
