@@ -189,6 +189,7 @@ __global__ void __launch_bounds__(256)
 __global__ void __launch_bounds__(kScanThreads)
     greedy_scan_kernel(const unsigned* __restrict__ bits, const long long* __restrict__ bits_base,
                        const int32_t* __restrict__ offsets, const int32_t* __restrict__ overflow,
+                       const int32_t* __restrict__ unresolved, const int32_t* __restrict__ nrep_fast,
                        int32_t* __restrict__ rep_of, int32_t* __restrict__ n_rep, unsigned* status) {
   extern __shared__ unsigned scan_smem[];
   unsigned* R = scan_smem;                  // kMaxWords: representatives so far, as a bitset
@@ -197,6 +198,11 @@ __global__ void __launch_bounds__(kScanThreads)
   const int off = offsets[e];
   const int n = offsets[e + 1] - off;
   const int W = (n + 31) >> 5;
+  if (!*overflow && unresolved[e] == 0) {
+    // resolve_kernel decided every row of the bucket
+    if (threadIdx.x == 0) n_rep[e] = nrep_fast[e];
+    return;
+  }
   if (*overflow || n > kMaxBucketRows) {
     // no bit matrix: every slot is its own representative
     for (int i = threadIdx.x; i < n; i += blockDim.x) rep_of[off + i] = off + i;
@@ -369,6 +375,83 @@ __global__ void __launch_bounds__(kScanThreads)
     }
   }
   if (threadIdx.x == 0) n_rep[e] = reps;
+}
+
+// Rows decided without the walk.  For slot s (local row li of bucket e) let C be the rows
+// before li that its bits mark similar.  first_hit_kernel writes first[s] = min C (local),
+// or -1 when C is empty.  resolve_kernel then decides two kinds of row exactly as the walk
+// would: C empty -> a representative; m = min C with no similar row before it (m is then a
+// representative, and the earliest candidate) -> condensed onto m.  Any other row is left to
+// the walk: a bucket with such a row counts it in unresolved[e] and greedy_scan_kernel walks
+// that bucket; the other buckets are complete (n_rep from nrep_fast).  One warp per row.
+__global__ void __launch_bounds__(256)
+    first_hit_kernel(const unsigned* __restrict__ bits, const long long* __restrict__ bits_base,
+                     const int32_t* __restrict__ offsets, int E, const int32_t* __restrict__ overflow,
+                     int32_t* __restrict__ first, int32_t* __restrict__ unresolved,
+                     int32_t* __restrict__ nrep_fast) {
+  __shared__ int off[257];
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) off[i] = offsets[i];
+  if (blockIdx.x == 0)
+    for (int e = threadIdx.x; e < E; e += blockDim.x) unresolved[e] = nrep_fast[e] = 0;
+  __syncthreads();
+  if (*overflow) return;
+  const int n_rows = off[E];
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int sl = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; sl < n_rows; sl += warps) {
+    int lo = 0, hi = E;  // off[lo] <= sl < off[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (off[mid] <= sl) lo = mid; else hi = mid;
+    }
+    const int e = lo, li = sl - off[e], n_e = off[e + 1] - off[e];
+    const int W = (n_e + 31) >> 5;
+    const unsigned* row = bits + bits_base[e] + static_cast<long long>(li) * W;
+    const int nw = (li + 31) >> 5;  // words holding columns < li
+    int hit = -1;
+    for (int w0 = 0; w0 < nw && hit < 0; w0 += 32) {
+      const int w = w0 + lane;
+      unsigned m = 0u;
+      if (w < nw) {
+        m = row[w];
+        if (w == nw - 1 && (li & 31)) m &= (1u << (li & 31)) - 1u;  // only columns < li
+      }
+      const unsigned any = __ballot_sync(0xffffffffu, m != 0u);
+      if (any) {
+        const int src = __ffs(any) - 1;
+        const unsigned mw = __shfl_sync(0xffffffffu, m, src);
+        hit = (w0 + src) * 32 + __ffs(mw) - 1;
+      }
+    }
+    if (lane == 0) first[sl] = hit;
+  }
+}
+
+__global__ void __launch_bounds__(256)
+    resolve_kernel(const int32_t* __restrict__ first, const int32_t* __restrict__ offsets, int E,
+                   const int32_t* __restrict__ overflow, int32_t* __restrict__ rep_of,
+                   int32_t* __restrict__ unresolved, int32_t* __restrict__ nrep_fast) {
+  __shared__ int off[257];
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) off[i] = offsets[i];
+  __syncthreads();
+  if (*overflow) return;
+  const int n_rows = off[E];
+  for (int sl = blockIdx.x * blockDim.x + threadIdx.x; sl < n_rows; sl += gridDim.x * blockDim.x) {
+    int lo = 0, hi = E;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (off[mid] <= sl) lo = mid; else hi = mid;
+    }
+    const int f = first[sl];
+    if (f < 0) {
+      rep_of[sl] = sl;
+      atomicAdd(&nrep_fast[lo], 1);
+    } else if (first[off[lo] + f] < 0) {
+      rep_of[sl] = off[lo] + f;
+    } else {
+      atomicAdd(&unresolved[lo], 1);
+    }
+  }
 }
 
 // n_condensed = (number of slots) - sum of representatives.
@@ -659,6 +742,9 @@ struct CondenseScratch {
   int2* cos_list;   // history: tiles with an unclassified pair
   int32_t* n_cos;
   int32_t* overflow;  // a bucket longer than the scratch allows
+  int32_t* first;       // [P] earliest similar row before each row (local), -1 none
+  int32_t* unresolved;  // [E] rows the walk has to decide
+  int32_t* nrep_fast;   // [E] representatives found without the walk
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -689,6 +775,9 @@ size_t carve(void* base, int T, int k, int E, CondenseScratch* s) {
   const size_t o_cl = take(sizeof(int2) * max_tiles);
   const size_t o_nc = take(sizeof(int32_t));
   const size_t o_of = take(sizeof(int32_t));
+  const size_t o_fi = take(sizeof(int32_t) * P);
+  const size_t o_un = take(sizeof(int32_t) * E);
+  const size_t o_nf = take(sizeof(int32_t) * E);
   if (s && base) {
     char* b = static_cast<char*>(base);
     s->norm = reinterpret_cast<float*>(b + o_norm);
@@ -702,6 +791,9 @@ size_t carve(void* base, int T, int k, int E, CondenseScratch* s) {
     s->cos_list = reinterpret_cast<int2*>(b + o_cl);
     s->n_cos = reinterpret_cast<int32_t*>(b + o_nc);
     s->overflow = reinterpret_cast<int32_t*>(b + o_of);
+    s->first = reinterpret_cast<int32_t*>(b + o_fi);
+    s->unresolved = reinterpret_cast<int32_t*>(b + o_un);
+    s->nrep_fast = reinterpret_cast<int32_t*>(b + o_nf);
   }
   return o;
 }
@@ -876,8 +968,13 @@ cudaError_t condense_pipeline(const __nv_bfloat16* x_perm, const int32_t* offset
                                 static_cast<int>(smem));
   });
   if (err != cudaSuccess) return err;
+  first_hit_kernel<<<max(1, min(ceil_div(P, 8), 8 * num_sms)), 256, 0, stream>>>(
+      s.bits, bits_base, offsets, E, s.overflow, s.first, s.unresolved, s.nrep_fast);
+  resolve_kernel<<<max(1, min(ceil_div(P, 256), 4 * num_sms)), 256, 0, stream>>>(
+      s.first, offsets, E, s.overflow, rep_of, s.unresolved, s.nrep_fast);
   greedy_scan_kernel<<<E, kScanThreads, smem, stream>>>(s.bits, bits_base, offsets, s.overflow,
-                                                        rep_of, n_rep, status);
+                                                        s.unresolved, s.nrep_fast, rep_of, n_rep,
+                                                        status);
   condensed_count_kernel<<<1, 32, 0, stream>>>(offsets, n_rep, E, n_condensed);
   return cudaGetLastError();
 }

@@ -476,6 +476,58 @@ def test_condense_ragged_buckets(moe):
     _status_ok(moe)
 
 
+def test_condense_chains_take_the_walk(moe):
+    """Buckets where rows are decided in parallel and buckets that need the greedy walk.
+
+    Chain buckets: runs of 45 rows 7 degrees apart on a circle, each run in its own plane of
+    two coordinates (so rows of different runs are orthogonal), tau = cos 20 degrees: each row
+    is similar to the two rows before it, and the earliest similar row of a row is then often
+    itself condensed (no chaining through condensed rows), which only the walk decides.  Their
+    sizes sit around the walk's 32-row groups and staged chunks.  Other buckets hold exact
+    duplicates only (decided without the walk) or nothing.  Bit for bit against the oracle on
+    the same stored rows; every similarity is at least 2e-3 from tau."""
+    d = 256
+    tau = math.cos(math.radians(20.0))
+    sizes = [40, 0, 300, 1000, 7, 64, 2100]
+    chains = {0, 2, 3, 5, 6}
+    rng = np.random.default_rng(5)
+    pool = gen.round_to_bf16(rng.standard_normal((8, d)).astype(np.float32))
+    blocks = []
+    for b, n in enumerate(sizes):
+        if b in chains:
+            rows = np.zeros((n, d), np.float32)
+            i = np.arange(n)
+            ang = np.radians(7.0 * (i % 45) + 3.0 * b)
+            plane = i // 45
+            rows[i, 2 * plane], rows[i, 2 * plane + 1] = np.cos(ang), np.sin(ang)
+        else:
+            rows = pool[rng.integers(0, len(pool), size=n)]
+        blocks.append(gen.round_to_bf16(rows))
+    rows = np.concatenate(blocks)
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    for b, n in enumerate(sizes):
+        if b in chains and n:
+            S = orc.cosine_similarity_matrix(rows[offsets[b]:offsets[b + 1]])
+            assert np.min(np.abs(S[np.tril_indices(n, -1)] - tau)) > 2e-3
+    ref = orc.condense(rows, offsets, tau)
+    walked = [b for b in chains if sizes[b] and np.any(
+        (ref[offsets[b]:offsets[b + 1]] != np.arange(offsets[b], offsets[b + 1])))]
+    assert walked  # chains condense rows
+    P = len(rows)
+    C = moe.Config(T=P, d=d, E=len(sizes), k=1, H=128, n_shared=0, H_shared=0, dtype="bf16",
+                   gating="softmax_topk", residual="none")
+    x_perm = torch.from_numpy(rows).to(device="cuda", dtype=torch.bfloat16)
+    rep_of, n_rep, ncond = moe.condense(C, x_perm, torch.from_numpy(offsets.astype(np.int32)).cuda(),
+                                        tau)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(_np(rep_of)[:P], ref)
+    per_bucket = [int(np.sum(ref[offsets[b]:offsets[b + 1]] == np.arange(offsets[b], offsets[b + 1])))
+                  for b in range(len(sizes))]
+    np.testing.assert_array_equal(_np(n_rep)[: len(sizes)], per_bucket)
+    assert int(ncond.item()) == P - sum(per_bucket)
+    _status_ok(moe)
+
+
 def test_condense_more_than_65536_pairs(moe):
     """The Luffy workload at 40000 tokens (80000 routed pairs, buckets of about 5000 rows):
     the scratch is sized by bucket rows (each token at most once per bucket), so condensation
