@@ -488,6 +488,12 @@ def phase_breakdown(args, moe, C, w, x, r, tau, flush, stream, torch) -> dict:
                                     p(ws_f), nf_r, s), "expert_ffn (routed only)")
 
     fns = [ph_route, ph_dispatch, ph_condense, ph_ffn, ph_combine, ph_routed_only]
+    names = ["T_gate_ms", "T_dispatch_ms", "T_condense_ms", "T_experts_ms", "T_combine_ms",
+             "T_routed_ms"]
+    inside = phases_inside_graph(args, torch, fns[:5], fns[5], names, flush, stream,
+                                 skip=None if condense else ph_condense)
+    if inside is not None:
+        return inside
     graphs = [capture(torch, f) if (f is not ph_condense or condense) else None for f in fns]
 
     def step(evs):
@@ -510,8 +516,6 @@ def phase_breakdown(args, moe, C, w, x, r, tau, flush, stream, torch) -> dict:
         step(evs)
         all_evs.append(evs)
     torch.cuda.synchronize()
-    names = ["T_gate_ms", "T_dispatch_ms", "T_condense_ms", "T_experts_ms", "T_combine_ms",
-             "T_routed_ms"]
     res = {n: 0.0 for n in names}
     for evs in all_evs:
         for i, n in enumerate(names):
@@ -521,6 +525,93 @@ def phase_breakdown(args, moe, C, w, x, r, tau, flush, stream, torch) -> dict:
                    "T_experts = moe_expert_ffn (routed + shared grouped GEMMs on tcgen05 and their "
                    "m-tile tables); T_routed = the same call without the shared experts; "
                    "T_shared = their difference")
+    return res
+
+
+def _external_event_record():
+    """cuEventRecordWithFlags(event, stream, CU_EVENT_RECORD_EXTERNAL) from the driver library:
+    recorded while a stream is being captured, it becomes an event-record node of the graph,
+    whose timestamp can be read after each replay.  None if the driver call is unavailable."""
+    try:
+        cu = ctypes.CDLL("libcuda.so.1")
+        f = cu.cuEventRecordWithFlags
+    except (OSError, AttributeError):
+        return None
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+    f.restype = ctypes.c_int
+    return lambda ev, st: f(ctypes.c_void_p(ev.cuda_event), ctypes.c_void_p(st.cuda_stream), 1)
+
+
+def phases_inside_graph(args, torch, step_fns, routed_fn, names, flush, stream, skip=None):
+    """Phase times from events recorded inside the captured graph of the whole step (one graph:
+    event, phase, event, phase, ...; the routed-only call in a graph of its own, after an L2
+    flush), so that each phase's events bracket its own kernels and not the graph's launch.
+    Returns None (the caller then times one graph per phase) if the events cannot be recorded
+    into a graph."""
+    rec = _external_event_record()
+    if rec is None:
+        return None
+    cap = torch.cuda.Stream()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(step_fns) + 3)]
+    for e in evs:
+        e.record(stream)  # creates the events
+    torch.cuda.synchronize()
+    if not all(getattr(e, "cuda_event", 0) for e in evs):
+        return None
+    ok = [True]
+
+    def record(e):
+        if rec(e, torch.cuda.current_stream()) != 0:
+            ok[0] = False
+
+    def whole():
+        record(evs[0])
+        for i, f in enumerate(step_fns):
+            if f is not skip:
+                f()
+            record(evs[i + 1])
+
+    def routed():
+        record(evs[-2])
+        routed_fn()
+        record(evs[-1])
+
+    try:
+        for f in step_fns + [routed_fn]:  # every ABI call once outside the capture
+            if f is not skip:
+                f()
+        torch.cuda.synchronize()
+        graphs = []
+        for fn in (whole, routed):
+            g = torch.cuda.CUDAGraph()
+            cap.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.graph(g, stream=cap):
+                fn()
+            graphs.append(g)
+        torch.cuda.synchronize()
+    except Exception:  # the capture could not record the events: time one graph per phase
+        return None
+    if not ok[0]:
+        return None
+    res = {n: 0.0 for n in names}
+    n_step = max(args.steps, 1)
+    for it in range(max(1, args.warmup) + n_step):
+        flush.zero_()
+        graphs[0].replay()
+        flush.zero_()
+        graphs[1].replay()
+        torch.cuda.synchronize()
+        if it < max(1, args.warmup):
+            continue
+        for i in range(len(step_fns)):
+            res[names[i]] += evs[i].elapsed_time(evs[i + 1]) / n_step
+        res[names[-1]] += evs[-2].elapsed_time(evs[-1]) / n_step
+    res["T_shared_ms"] = max(0.0, res["T_experts_ms"] - res["T_routed_ms"])
+    res["note"] = ("the step's ABI calls captured as one CUDA graph with event-record nodes between "
+                   "them (the events bracket each phase's own kernels, not the graph launch), "
+                   "replayed after an L2 flush; T_experts = moe_expert_ffn (routed + shared grouped "
+                   "GEMMs on tcgen05); T_routed = the same call without the shared experts, in a "
+                   "graph of its own after another flush; T_shared = their difference")
     return res
 
 
