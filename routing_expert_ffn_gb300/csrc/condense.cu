@@ -85,7 +85,9 @@ __global__ void __launch_bounds__(256)
 }
 
 // Tile list of the lower triangle of every bucket's Gram matrix, and the
-// start word of each bucket's bit matrix (rows of ceil(n_e / 32) words).
+// start word of each bucket's bit matrix (rows of ceil(n_e / 32) words).  A tile is
+// 256 rows (a pair of the bucket's m-tiles, run on a CTA pair) by 256 columns:
+// {first m-tile, column tile | (1 << 16) when the bucket holds the pair's second m-tile}.
 // The scratch is sized for buckets of at most max_rows rows (a bucket holds each token at
 // most once).  A bucket longer than that (offsets from a routing that names one expert twice
 // for a token) sets *overflow, flags MOE_ERR_DEVICE_INDEX, lists no tile, invalidates the
@@ -99,6 +101,7 @@ __global__ void __launch_bounds__(256)
                      int32_t* __restrict__ hist_header, unsigned* status) {
   __shared__ int s_cnt[1024];
   __shared__ int s_beg[1025];
+  __shared__ int s_second[1024];
   __shared__ int s_over;
   if (threadIdx.x == 0) s_over = 0;
   __syncthreads();
@@ -126,13 +129,19 @@ __global__ void __launch_bounds__(256)
   for (int c0 = 0; c0 < n_mt; c0 += 1024) {
     for (int i = threadIdx.x; i < 1024; i += blockDim.x) {
       const int m = c0 + i;
-      int cnt = 0;
+      int cnt = 0, second = 0;
       if (m < n_mt) {
         const int4 t = mt_info[m];
-        const int li_end = t.y - t.w + t.z;  // one past the last local row of the tile
-        cnt = (li_end + kTcTileN - 1) / kTcTileN;
+        const int mb = group_mt_begin[t.x], me = group_mt_begin[t.x + 1];
+        if (((m - mb) & 1) == 0) {  // the first m-tile of a pair
+          second = m + 1 < me ? 1 : 0;
+          const int4 u = second ? mt_info[m + 1] : t;
+          const int li_end = u.y - u.w + u.z;  // one past the last local row of the pair
+          cnt = (li_end + kTcTileN - 1) / kTcTileN;
+        }
       }
       s_cnt[i] = cnt;
+      s_second[i] = second;
     }
     __syncthreads();
     {
@@ -163,7 +172,8 @@ __global__ void __launch_bounds__(256)
     }
     __syncthreads();
     for (int i = threadIdx.x; i < 1024; i += blockDim.x) {
-      for (int j = 0; j < s_cnt[i]; ++j) tile_list[s_beg[i] + j] = make_int2(c0 + i, j);
+      for (int j = 0; j < s_cnt[i]; ++j)
+        tile_list[s_beg[i] + j] = make_int2(c0 + i, j | (s_second[i] << 16));
     }
     __syncthreads();
     if (threadIdx.x == 0) s_carry = s_beg[1024];
@@ -535,8 +545,8 @@ __device__ __forceinline__ int bucket_of(const int* off, int E, int s) {
 // of tokens that shared two buckets got the same class in each).  Writes, in the bits layout
 // of this call, the planes (the inherited classes) and the bits themselves (= the class; the
 // similarity GEMM rewrites the bits of tiles with unclassified pairs), and lists the tiles
-// with an unclassified pair for the GEMM.  One CTA per tile (grid-stride), 8 warps; a warp
-// takes a row at a time.  A chunk of 32 columns whose tokens sat at consecutive slots of one
+// with an unclassified pair for the GEMM.  One CTA per tile of up to 256 rows (grid-stride),
+// 8 warps; a warp takes a row at a time.  A chunk of 32 columns whose tokens sat at consecutive slots of one
 // previous bucket, with the row's token in that bucket too, is one 32-bit window of the
 // previous row's planes (one lane, a funnel shift); any other chunk takes a lane per column,
 // each searching its pair's previous buckets for a common one.
@@ -553,8 +563,8 @@ __global__ void __launch_bounds__(kLookupThreads)
   int* poff = hsm;                      // [E + 1] previous offsets
   int* col_e = poff + (E + 1);          // [256][k] previous bucket of each column token's pairs
   int* col_s = col_e + kTcTileN * k;    // [256][k] and their slots
-  int* row_e = col_s + kTcTileN * k;    // [128][k]
-  int* row_s = row_e + kMTile * k;      // [128][k]
+  int* row_e = col_s + kTcTileN * k;    // [256][k] the same for the tile's row tokens
+  int* row_s = row_e + 2 * kMTile * k;  // [256][k]
   __shared__ int s_unknown;
   // per 32-column chunk: the previous bucket its tokens all held at consecutive slots from
   // s_ch_s0 (-1: none), so a row in that bucket reads its 32 classes without a search
@@ -569,10 +579,12 @@ __global__ void __launch_bounds__(kLookupThreads)
   for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
     const int2 tl = tile_list[tile];
     const int4 m = mt_info[tl.x];
-    const int e = m.x, row0 = m.y, nrows = m.z, gbase = m.w;
+    // the pair's m-tiles are consecutive 128-row pieces of the bucket: rows row0 .. + nrows
+    const int e = m.x, row0 = m.y, gbase = m.w;
+    const int nrows = m.z + (((tl.y >> 16) & 1) ? mt_info[tl.x + 1].z : 0);
     const int n_e = offsets[e + 1] - offsets[e];
     const int W = (n_e + 31) >> 5;
-    const int lj0 = tl.y * kTcTileN;
+    const int lj0 = (tl.y & 0xffff) * kTcTileN;
     const int li0 = row0 - gbase;
     if (threadIdx.x == 0) s_unknown = 0;
     __syncthreads();  // poff staged; the previous tile's reads of the tables are done
@@ -590,7 +602,7 @@ __global__ void __launch_bounds__(kLookupThreads)
         col_e[q] = pe;
         col_s[q] = ps;
       }
-      for (int q = threadIdx.x; q < kMTile * k; q += blockDim.x) {
+      for (int q = threadIdx.x; q < 2 * kMTile * k; q += blockDim.x) {
         const int rr = q / k, a = q - rr * k;
         int pe = -1, ps = -1;
         if (rr < nrows) {
@@ -909,14 +921,14 @@ cudaError_t condense_pipeline(const __nv_bfloat16* x_perm, const int32_t* offset
     cudaError_t e = cudaMemsetAsync(s.n_cos, 0, sizeof(int32_t), stream);
     if (e != cudaSuccess) return e;
     const HistView prev = hist_view(h->hist_in, h->T, h->k, E);
-    const size_t smem = sizeof(int) * ((E + 1) + 2 * (kTcTileN + kMTile) * h->k);
+    const size_t smem = sizeof(int) * ((E + 1) + 2 * (kTcTileN + 2 * kMTile) * h->k);
     static OncePerDevice<64> once_l;
     int dev = 0;
     cudaGetDevice(&dev);
     e = once_l.run(dev, [&]() {
       // the largest table: E = 256, k = 32
       return cudaFuncSetAttribute(hist_lookup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  static_cast<int>(sizeof(int) * (257 + 2 * (kTcTileN + kMTile) * 32)));
+                                  static_cast<int>(sizeof(int) * (257 + 2 * (kTcTileN + 2 * kMTile) * 32)));
     });
     if (e != cudaSuccess) return e;
     const int max_tiles = max_mtiles(P, E) * ((bucket_rows_max(T, k) + kTcTileN - 1) / kTcTileN);

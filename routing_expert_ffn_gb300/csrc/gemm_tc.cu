@@ -15,8 +15,8 @@
 //            hidden units, so one accumulator holds gate|up; the epilogue writes
 //            h = SiLU(gate) * up (bf16) -- the gate/up half of a SwiGLU expert.
 //   kStore   writes D (bf16), optionally to a remapped output row.
-//   kSimBits condensation: D is a tile of the bucket's Gram matrix; the
-//            epilogue turns cos(x_i, x_j) >= tau, j < i, into bits.
+//   kSimBits condensation (CTA pairs): D is a 256 x 256 tile of the bucket's Gram matrix;
+//            the epilogue turns cos(x_i, x_j) >= tau, j < i, into bits.
 //   kRouter  router logits: B is the fp32 router weight split exactly into
 //            three bf16 terms; the K loop runs over the three terms, split
 //            across CTAs, and the epilogue writes fp32 partial sums (N = E
@@ -28,7 +28,7 @@
 // groups in order; inside a group it walks blocks of up to 16 m-tiles, and
 // inside a block the N tiles with the m-tiles fastest, so CTAs running at the
 // same time share B tiles (weights) and A tiles (tokens) through L2.
-// kSimBits reads an explicit (m-tile, column tile) list.
+// kSimBits reads an explicit list of (pair of m-tiles, column tile).
 //
 // Every wait is bounded; on timeout the CTA records MOE_ERR_TIMEOUT, stops
 // issuing work, drains what it issued, frees TMEM and returns.
@@ -119,11 +119,7 @@ __device__ __forceinline__ TileInfo tile_info(const TcGemmArgs& a, const int* gm
     t.gbase = 0;
     return t;
   }
-  if (MODE == kSimBits) {
-    int2 e = a.tile_list[tile];
-    mt = e.x;
-    nt = e.y;
-  } else {
+  {
     const int NT = a.n_ntiles;
     int lo = 0, hi = a.n_groups;  // largest g with begin[g] * NT <= tile
     while (hi - lo > 1) {
@@ -151,7 +147,6 @@ __device__ __forceinline__ TileInfo tile_info(const TcGemmArgs& a, const int* gm
 
 template <int MODE>
 __device__ __forceinline__ int total_tiles(const TcGemmArgs& a) {
-  if (MODE == kSimBits) return *a.n_list;
   if (MODE == kRouter) return ((a.n_rows + BM - 1) / BM) * a.n_ntiles;
   return a.group_mt_begin[a.n_groups] * a.n_ntiles;
 }
@@ -337,6 +332,138 @@ __device__ __forceinline__ void tail_epilogue(const TcGemmArgs& args, const Tile
   }
 }
 
+// Operands of one Gram tile's epilogue that do not depend on the accumulator: the lane's
+// row's inverse norm and hash (registers), and the 256 columns' {inverse norm, low hash
+// word} (the warp's shared-memory slice, read by every lane as broadcasts).  Loaded before
+// the wait on the accumulator, so their latency runs under the tile's MMAs.
+struct SimOperands {
+  float inv_ni;
+  unsigned long long hi;
+  float2* col;  // [256] shared: {1 / |x_j|, low word of x_j's hash as bits}
+};
+
+__device__ __forceinline__ void sim_prefetch(const TcGemmArgs& args, const TileInfo& t, int r,
+                                             int lane, SimOperands& o) {
+  const int e = t.slice;
+  const int n_e = args.bucket_off[e + 1] - args.bucket_off[e];
+  const bool valid = r < t.nrows;
+  const float ni = valid ? args.norm[t.row0 + r] : 0.f;
+  o.inv_ni = ni > 0.f ? 1.0f / ni : 0.f;
+  o.hi = valid ? args.row_hash[t.row0 + r] : 0ull;
+  float nj[BN / 32];
+  uint32_t hj[BN / 32];
+#pragma unroll
+  for (int c = 0; c < BN / 32; ++c) {
+    const int lj = t.nt * BN + c * 32 + lane;
+    const bool col_in = lj < n_e;
+    nj[c] = col_in ? args.norm[t.gbase + lj] : 0.f;
+    hj[c] = col_in ? static_cast<uint32_t>(args.row_hash[t.gbase + lj]) : 0u;
+  }
+  __syncwarp();  // every lane is done with the previous tile's columns
+#pragma unroll
+  for (int c = 0; c < BN / 32; ++c)
+    o.col[c * 32 + lane] = make_float2(nj[c] > 0.f ? 1.0f / nj[c] : 0.f, __uint_as_float(hj[c]));
+  __syncwarp();
+}
+
+// Epilogue of one Gram tile of the similarity GEMM for one TMEM lane: row slot i = row0 + r
+// of bucket e (valid: r < nrows), column slots j = gbase + nt * 256 + c, c < 256.
+__device__ __forceinline__ void sim_epilogue(const TcGemmArgs& args, const TileInfo& t,
+                                             const SimOperands& o, uint32_t col0, int r,
+                                             int lane) {
+  // cos(x_i, x_j) = D[i][j] / (|x_i| |x_j|), taken as (D * (1/|x_i|)) * (1/|x_j|) in fp32,
+  // clamped to [-1, 1]; a zero row has similarity 0 to every row it is not identical
+  // to (its D and its inverse norm are 0), and identical rows have similarity exactly 1.
+  // Bits: sim >= tau (the decision), and with history sim >= s1 / sim <= s2 (the classes
+  // handed to the next call).  Without history only the decision is formed: the clamp is
+  // then folded into it (tau <= 1 on this path, so min(s, 1) >= tau is s >= tau, and
+  // max(s, -1) >= tau is s >= tau or tau <= -1).
+  const int e = t.slice, gbase = t.gbase, nt = t.nt;
+  const bool valid = r < t.nrows;
+  const int n_e = args.bucket_off[e + 1] - args.bucket_off[e];
+  const int W = (n_e + 31) >> 5;
+  const int i = t.row0 + r;
+  const int li = i - gbase;
+  const float inv_ni = o.inv_ni;
+  const unsigned long long hi = o.hi;
+  const uint32_t hi_lo = static_cast<uint32_t>(hi);
+  const long long wrow = args.bits_base[e] + static_cast<long long>(li) * W;
+  unsigned* brow = args.bits + wrow;
+  const int hmode = args.hist_mode;
+  const float tau = args.tau;
+  const bool all_similar = tau <= -1.f;
+  const float4* col4 = reinterpret_cast<const float4*>(o.col);
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    const int lj0 = nt * BN + c * 32;
+    // a chunk that lies above every row of this warp's quarter holds no bit
+    if (!__any_sync(0xffffffffu, valid && lj0 < li)) continue;
+    uint32_t v[32];
+    ptx::tmem_ld_32x32b_x32(col0 + c * 32, v);
+    ptx::tmem_ld_wait();
+    const int n_in = li - lj0;  // columns of this chunk below row li
+    const uint32_t in_mask = n_in >= 32 ? 0xffffffffu : n_in <= 0 ? 0u : (1u << n_in) - 1u;
+    uint32_t word = 0, w1 = 0, w2 = 0, same_hash = 0;
+    if (hmode == 0) {
+#pragma unroll
+      for (int b = 0; b < 32; b += 2) {
+        const float4 q = col4[c * 16 + (b >> 1)];  // columns b, b + 1 (a broadcast)
+        const float s0 = __uint_as_float(v[b]) * inv_ni * q.x;
+        const float s1 = __uint_as_float(v[b + 1]) * inv_ni * q.z;
+        word |= (static_cast<uint32_t>(s0 >= tau) << b) | (static_cast<uint32_t>(s1 >= tau) << (b + 1));
+        same_hash |= (static_cast<uint32_t>(__float_as_uint(q.y) == hi_lo) << b) |
+                     (static_cast<uint32_t>(__float_as_uint(q.w) == hi_lo) << (b + 1));
+      }
+      if (all_similar) word = 0xffffffffu;
+    } else {
+#pragma unroll
+      for (int b = 0; b < 32; b += 2) {
+        const float4 q = col4[c * 16 + (b >> 1)];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float inv_nj = h ? q.z : q.x;
+          const uint32_t hj_lo = __float_as_uint(h ? q.w : q.y);
+          const float s = fminf(fmaxf(__uint_as_float(v[b + h]) * inv_ni * inv_nj, -1.f), 1.f);
+          word |= static_cast<uint32_t>(s >= tau) << (b + h);
+          w1 |= static_cast<uint32_t>(s >= args.s1) << (b + h);
+          w2 |= static_cast<uint32_t>(s <= args.s2) << (b + h);
+          same_hash |= static_cast<uint32_t>(hj_lo == hi_lo) << (b + h);
+        }
+      }
+    }
+    word &= in_mask;
+    w1 &= in_mask;
+    w2 &= in_mask;
+    same_hash &= in_mask;
+    // identical rows: similarity exactly 1 (full hash, then the rows themselves)
+    while (valid && same_hash) {
+      const int b = __ffs(same_hash) - 1;
+      same_hash &= same_hash - 1;
+      const int j = gbase + lj0 + b;
+      if (args.row_hash[j] == hi && rows_identical(args.rows, args.d, i, j)) {
+        const uint32_t m = 1u << b;
+        word = 1.0f >= tau ? (word | m) : (word & ~m);
+        w1 = 1.0f >= args.s1 ? (w1 | m) : (w1 & ~m);
+        w2 = 1.0f <= args.s2 ? (w2 | m) : (w2 & ~m);
+      }
+    }
+    if (valid && lj0 < li) {
+      if (hmode == 0) {
+        brow[lj0 >> 5] = word;
+      } else {
+        const long long widx = wrow + (lj0 >> 5);
+        uint2 ks = make_uint2(0u, 0u);
+        if (hmode == 2) ks = args.hplanes[widx];
+        const uint32_t kw = ks.x, sw = ks.y;
+        // a pair with a class is decided by it; the others by their cosine, and get
+        // a class from it (similar first)
+        brow[lj0 >> 5] = (kw & sw) | (~kw & word);
+        args.hplanes[widx] = make_uint2(kw | (~kw & (w1 | w2)), (kw & sw) | (~kw & w1));
+      }
+    }
+  }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -426,8 +553,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const int nslice = t.nt / args.nt_per_slice;
               const int n0 = (t.nt - nslice * args.nt_per_slice) * BN;
               ptx::tma_load_3d(sb, &tmB, full, kin, n0, t.slice + nslice + kslice);
-            } else {
-              ptx::tma_load_3d(sb, &tmB, full, kb * BK, t.gbase + t.nt * BN, 0);
             }
           }
         }
@@ -530,80 +655,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       } else if (MODE == kSwiGLU || MODE == kStore) {
         ffn_epilogue<MODE>(args, t, col0, r, valid);
-      } else {
-        // Gram tile of bucket `slice`: row slot i = row0 + r, column slot j = gbase + nt*256 + c.
-        // cos(x_i, x_j) = D[i][j] / (|x_i| |x_j|), taken as D * (1/|x_i|) * (1/|x_j|) in fp32,
-        // clamped to [-1, 1]; a zero row has similarity 0 to every row it is not identical
-        // to, and identical rows have similarity exactly 1.  Bits: sim >= tau (the decision),
-        // and with history sim >= s1 / sim <= s2 (the classes handed to the next call).
-        const int e = t.slice;
-        const int n_e = args.bucket_off[e + 1] - args.bucket_off[e];
-        const int W = (n_e + 31) >> 5;
-        const int i = t.row0 + r;
-        const int li = i - t.gbase;
-        const float ni = valid ? args.norm[i] : 0.f;
-        const float inv_ni = ni > 0.f ? 1.0f / ni : 0.f;
-        const unsigned long long hi = valid ? args.row_hash[i] : 0ull;
-        const uint32_t hi_lo = static_cast<uint32_t>(hi);
-        const long long wrow = args.bits_base[e] + static_cast<long long>(li) * W;
-        unsigned* brow = args.bits + wrow;
-        const int hmode = args.hist_mode;
-#pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          uint32_t v[32];
-          ptx::tmem_ld_32x32b_x32(col0 + c * 32, v);
-          ptx::tmem_ld_wait();
-          const int lj0 = t.nt * BN + c * 32;
-          // a chunk that lies above every row of this warp's quarter holds no bit
-          if (!__any_sync(0xffffffffu, valid && lj0 < li)) continue;
-          // lane b fetches column lj0 + b's norm and hash once; each row takes them by shuffle
-          const bool col_in = lj0 + lane < n_e;
-          const float nj_l = col_in ? args.norm[t.gbase + lj0 + lane] : 0.f;
-          const float inv_nj_l = nj_l > 0.f ? 1.0f / nj_l : 0.f;
-          const uint32_t hj_lo_l =
-              col_in ? static_cast<uint32_t>(args.row_hash[t.gbase + lj0 + lane]) : 0u;
-          const int n_in = min(32, li - lj0);  // columns of this chunk below row li
-          uint32_t word = 0, w1 = 0, w2 = 0, same_hash = 0;
-#pragma unroll
-          for (int b = 0; b < 32; ++b) {
-            const float inv_nj = __shfl_sync(0xffffffffu, inv_nj_l, b);
-            const uint32_t hj_lo = __shfl_sync(0xffffffffu, hj_lo_l, b);
-            const float s = (inv_ni > 0.f && inv_nj > 0.f)
-                                ? fminf(fmaxf(__uint_as_float(v[b]) * inv_ni * inv_nj, -1.f), 1.f)
-                                : 0.f;
-            const uint32_t in = b < n_in ? 1u : 0u;
-            word |= (in & static_cast<uint32_t>(s >= args.tau)) << b;
-            w1 |= (in & static_cast<uint32_t>(s >= args.s1)) << b;
-            w2 |= (in & static_cast<uint32_t>(s <= args.s2)) << b;
-            same_hash |= static_cast<uint32_t>(in && hj_lo == hi_lo) << b;
-          }
-          // identical rows: similarity exactly 1 (full hash, then the rows themselves)
-          while (valid && same_hash) {
-            const int b = __ffs(same_hash) - 1;
-            same_hash &= same_hash - 1;
-            const int j = t.gbase + lj0 + b;
-            if (args.row_hash[j] == hi && rows_identical(args.rows, args.d, i, j)) {
-              const uint32_t m = 1u << b;
-              word = 1.0f >= args.tau ? (word | m) : (word & ~m);
-              w1 = 1.0f >= args.s1 ? (w1 | m) : (w1 & ~m);
-              w2 = 1.0f <= args.s2 ? (w2 | m) : (w2 & ~m);
-            }
-          }
-          if (valid && lj0 < li) {
-            if (hmode == 0) {
-              brow[lj0 >> 5] = word;
-            } else {
-              const long long widx = wrow + (lj0 >> 5);
-              uint2 ks = make_uint2(0u, 0u);
-              if (hmode == 2) ks = args.hplanes[widx];
-              const uint32_t kw = ks.x, sw = ks.y;
-              // a pair with a class is decided by it; the others by their cosine, and get
-              // a class from it (similar first)
-              brow[lj0 >> 5] = (kw & sw) | (~kw & word);
-              args.hplanes[widx] = make_uint2(kw | (~kw & (w1 | w2)), (kw & sw) | (~kw & w1));
-            }
-          }
-        }
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -652,6 +703,7 @@ constexpr int SHARED_BYTES = 5120;
 // per epilogue warp: two {32 columns, 32 rows} bf16 TMA store boxes of 2 KB (64-byte swizzle)
 constexpr int OUT_BOX_BYTES = 32 * 32 * 2;
 constexpr int OUT_STAGE_BYTES = 4 * 2 * OUT_BOX_BYTES;
+static_assert(2 * BN * 4 <= 2 * OUT_BOX_BYTES, "a warp's similarity operands fit its staging area");
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + SHARED_BYTES + OUT_STAGE_BYTES;
 static_assert((STAGES * STAGE_BYTES + SHARED_BYTES) % 1024 == 0, "output boxes 1024-byte aligned");
 // Units per block of the tile walk.  Measured on the Llama-4-Scout-shaped shared expert
@@ -735,6 +787,31 @@ __device__ __forceinline__ TileInfo tile_info(const TcGemmArgs& a, const Shared*
   return t;
 }
 
+// Similarity tile -> this CTA's part: tile_list[tile] = {first m-tile of a pair of a bucket's
+// m-tiles, column tile | (1 << 16) when the pair's second m-tile is in the same bucket}.  CTA
+// rank r takes m-tile r of the pair (no rows when the bucket has only the first).
+__device__ __forceinline__ TileInfo sim_tile_info(const TcGemmArgs& a, int tile, uint32_t rank) {
+  const int2 e = a.tile_list[tile];
+  const int4 m0 = a.mt_info[e.x];
+  TileInfo t;
+  t.slice = m0.x;
+  t.gbase = m0.w;
+  t.nt = e.y & 0xffff;
+  t.tail = 0;
+  if (rank == 0) {
+    t.row0 = m0.y;
+    t.nrows = m0.z;
+  } else if ((e.y >> 16) & 1) {
+    const int4 m1 = a.mt_info[e.x + 1];
+    t.row0 = m1.y;
+    t.nrows = m1.z;
+  } else {
+    t.row0 = m0.y + BM;
+    t.nrows = 0;
+  }
+  return t;
+}
+
 // This CTA's loads of K block kb, completing on the leader's barrier `full`:
 // for a pair tile its A rows and its half of the B tile; for a tail tile its
 // 128 weight rows (into the A region) and its half of the tail's token rows
@@ -745,6 +822,13 @@ __device__ __forceinline__ void issue_kblock(const TcGemmArgs& args, const CUten
                                              const CUtensorMap* tmW5, const TileInfo& t, int kb,
                                              uint32_t rank, uint32_t full, uint32_t sa,
                                              uint32_t sb) {
+  if (MODE == kSimBits) {
+    // the bucket's rows: A = this CTA's 128 rows i, B = its half of the 256 column rows j
+    ptx::tma_load_2d_pair(sa, tmA, full, kb * BK, t.row0);
+    ptx::tma_load_3d_pair(sb, tmB, full, kb * BK,
+                          t.gbase + t.nt * BN + static_cast<int>(rank) * (BN / 2), 0);
+    return;
+  }
   const int kslice = kb / args.kb_per_slice;
   const int kin = (kb - kslice * args.kb_per_slice) * BK;
   const int nslice = t.nt / args.nt_per_slice;
@@ -819,8 +903,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   pdl_wait();
   // Rows of each group, from the group offsets, from a fixed row count, or from the m-tile
   // table (whose m-tiles are 128-row pieces of each group from its first row).  Units of each
-  // group: pairs of m-tiles, then a tail if a single m-tile is left.
-  for (int g = threadIdx.x; g < args.n_groups; g += blockDim.x) {
+  // group: pairs of m-tiles, then a tail if a single m-tile is left.  (The similarity tiles
+  // come from an explicit list instead.)
+  for (int g = threadIdx.x; MODE != kSimBits && g < args.n_groups; g += blockDim.x) {
     int off = 0, rows = 0;
     if (args.group_off) {
       off = args.group_off[g];
@@ -845,7 +930,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     sh->gub[g] = np + (tail_rows > 0 ? 1 : 0);  // units, turned into offsets below
   }
   __syncthreads();
-  if (warp == 0) {
+  if (MODE != kSimBits && warp == 0) {
     // exclusive scan of the unit counts, lane l owning groups [8 l, 8 l + 8)
     const int per = (args.n_groups + 31) >> 5;
     const int g0 = lane * per;
@@ -871,8 +956,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   __syncthreads();
   const uint32_t tmem_base = sh->tmem_base;
-  const int n_tiles = sh->gub[args.n_groups] * args.n_ntiles;
+  const int n_tiles = MODE == kSimBits ? *args.n_list : sh->gub[args.n_groups] * args.n_ntiles;
   const int cluster = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
+  auto tile_of = [&](int tile, uint32_t r) {
+    return MODE == kSimBits ? pr::sim_tile_info(args, tile, r) : pr::tile_info(args, sh, tile, r);
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
@@ -880,7 +968,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t phase = 0;
     bool ok = true;
     for (int tile = cluster; tile < n_tiles && ok; tile += n_clusters) {
-      const TileInfo t = pr::tile_info(args, sh, tile, rank);
+      const TileInfo t = tile_of(tile, rank);
       for (int kb = 0; kb < args.n_kblocks; ++kb) {
         if (!pr::wait_bar(ptx::smem_u32(&sh->empty[stage]), phase ^ 1u, sh, args.status)) {
           ok = false;
@@ -914,7 +1002,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int local = 0;
       bool ok = true;
       for (int tile = cluster; tile < n_tiles && ok; tile += n_clusters, ++local) {
-        const TileInfo t = pr::tile_info(args, sh, tile, 0);
+        const TileInfo t = tile_of(tile, 0);
         const uint32_t idesc =
             t.tail ? ptx::idesc_bf16_f32(2 * BM, (t.nrows + 15) & ~15) : idesc_pair;
         const int acc = local & 1;
@@ -971,10 +1059,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int tile = cluster; tile < n_tiles; tile += n_clusters, ++local) {
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
+      const TileInfo t = tile_of(tile, rank);
+      SimOperands so;
+      if (MODE == kSimBits) {
+        // the warp's output staging area is free in this mode
+        so.col = reinterpret_cast<float2*>(out_stage);
+        sim_prefetch(args, t, r, lane, so);
+      }
       if (!pr::wait_bar(ptx::smem_u32(&sh->tmem_full[acc]), acc_phase, sh, args.status)) break;
       ptx::tc_fence_after();
-      const TileInfo t = pr::tile_info(args, sh, tile, rank);
-      if (t.tail) tail_epilogue<MODE>(args, t, lane_addr + acc * BN, q, lane, rank);
+      if (MODE == kSimBits) sim_epilogue(args, t, so, lane_addr + acc * BN, r, lane);
+      else if (t.tail) tail_epilogue<MODE>(args, t, lane_addr + acc * BN, q, lane, rank);
       else if (tma_out && 32 * q + 32 <= t.nrows)
         ffn_epilogue_tma<MODE>(args, t, lane_addr + acc * BN, q, lane, out_stage, &tmO, nstore);
       else ffn_epilogue<MODE>(args, t, lane_addr + acc * BN, r, r < t.nrows);
@@ -1147,8 +1242,9 @@ cudaError_t tc_gemm(int mode, const void* A, long long a_rows, int K, const void
   TcGemmArgs args = args_in;
   if (args.unit_group <= 0) args.unit_group = tc::pr::kUnitGroup;
   if (!tc::make_map(&ma, 2, A, K, a_rows, 1, tc::BM)) return cudaErrorInvalidValue;
-  // The FFN modes run on CTA pairs, each CTA loading half of the 256-row B tile.
-  const bool pair = mode == tc::kSwiGLU || mode == tc::kStore;
+  // The FFN and similarity modes run on CTA pairs, each CTA loading half of the 256-row B tile.
+  const bool ffn = mode == tc::kSwiGLU || mode == tc::kStore;
+  const bool pair = ffn || mode == tc::kSimBits;
   const uint32_t box_rows = pair                  ? tc::BN / 2
                             : mode == tc::kRouter ? static_cast<uint32_t>(args.router_n)
                                                   : tc::BN;
@@ -1161,15 +1257,16 @@ cudaError_t tc_gemm(int mode, const void* A, long long a_rows, int K, const void
     return cudaErrorInvalidValue;
   // the output [a_rows][ld_out] bf16, stored in {32, 32} boxes by the full-quarter epilogue
   CUtensorMap mo = ma;
-  if (pair && !tc::make_out_map(&mo, args.out, static_cast<uint64_t>(args.ld_out),
-                                static_cast<uint64_t>(a_rows)))
+  if (ffn && !tc::make_out_map(&mo, args.out, static_cast<uint64_t>(args.ld_out),
+                               static_cast<uint64_t>(a_rows)))
     return cudaErrorInvalidValue;
   switch (mode) {
     case tc::kSwiGLU:
       return tc::launch_pair<tc::kSwiGLU>(ma, mb, ma64, mw5, mo, args, grid, stream);
     case tc::kStore:
       return tc::launch_pair<tc::kStore>(ma, mb, ma64, mw5, mo, args, grid, stream);
-    case tc::kSimBits: return tc::launch<tc::kSimBits>(ma, mb, args, grid, stream);
+    case tc::kSimBits:
+      return tc::launch_pair<tc::kSimBits>(ma, mb, ma64, mw5, mo, args, grid, stream);
     case tc::kRouter: return tc::launch<tc::kRouter>(ma, mb, args, grid, stream);
   }
   return cudaErrorInvalidValue;

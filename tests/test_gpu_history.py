@@ -174,6 +174,31 @@ def test_history_luffy_two_blocks(moe, scenario):
         hist_gpu = rec
 
 
+def test_history_top8_two_blocks(moe):
+    """The lookup searches each token pair's k previous buckets for a common one: top-8 of 16
+    experts (each token in half the buckets) on 512 tokens of the condensation workload; the
+    second block keeps the rows and draws a fresh top-8 per token (copies of one centroid
+    still route together), so pairs meet again in other buckets than before."""
+    from dataclasses import replace
+    base = gen.CONFIGS["luffy_condense"]
+    cfg = replace(base, name="luffy_top8", k=8)
+    inp = harness.condition(cfg, gen.make_inputs(cfg.with_tokens(512)))
+    cfg = cfg.with_tokens(512)
+    C = moe.Config.from_workload(cfg)
+    _, idx1, _ = orc.route(inp["x"], inp["W_r"], inp["bias"], cfg.k, cfg.gating)
+    idx2 = _luffy_block2_routing(cfg, inp["labels"], seed=21)
+    hist_gpu, hist_orc = None, None
+    for bi, idx in enumerate((idx1, idx2)):
+        counts, offsets, perm, slot_of = orc.dispatch(idx, cfg.E)
+        xp = inp["x"][perm]
+        rep_o, hist_orc = orc.condense_with_history(xp, offsets, perm, 0.95, 0.8, 0.2, hist_orc)
+        rep_g, n_cond, n_cos, rec = _gpu_block(moe, C, xp, offsets, perm, slot_of, 0.95, 0.8,
+                                               0.2, hist_gpu)
+        np.testing.assert_array_equal(rep_g[: cfg.P], rep_o)
+        assert decode_history(rec.cpu().numpy(), cfg.T, cfg.k, cfg.E) == hist_orc, bi
+        hist_gpu = rec
+
+
 def test_history_of_another_shape_is_ignored(moe):
     """A record written for another token count counts as no history: the call equals the
     first block's."""
