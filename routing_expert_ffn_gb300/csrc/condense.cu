@@ -48,26 +48,42 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// Per dispatched row: fp32 norm and a 64-bit content hash (a filter for identical rows,
+// which are then compared element by element).  One warp per row; a lane's vectors are
+// loaded kStatBatch at a time, so their loads are in flight together.
+constexpr int kStatBatch = 4;
 __global__ void __launch_bounds__(256)
     row_stats_kernel(const __nv_bfloat16* __restrict__ rows, const int32_t* __restrict__ offsets,
                      int E, int d, float* __restrict__ norm, unsigned long long* __restrict__ hash) {
+  pdl_trigger();
+  pdl_wait();
   const int n_rows = offsets[E];
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int lane = threadIdx.x & 31;
+  const int nv = d / 8;
   for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < n_rows; r += warps) {
     const uint4* p = reinterpret_cast<const uint4*>(rows + static_cast<long long>(r) * d);
     float ss = 0.f;
     unsigned long long h = 0x9E3779B97F4A7C15ull * (lane + 1);
-    for (int v = lane; v < d / 8; v += 32) {
-      uint4 q = p[v];
-      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    for (int v0 = 0; v0 < nv; v0 += 32 * kStatBatch) {
+      uint4 q[kStatBatch];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xFFFF0000u);
-        ss = fmaf(lo, lo, ss);
-        ss = fmaf(hi, hi, ss);
-        h = (h ^ w[i]) * 0x100000001B3ull;
-        h ^= h >> 29;
+      for (int u = 0; u < kStatBatch; ++u) {
+        const int v = v0 + u * 32 + lane;
+        q[u] = v < nv ? p[v] : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < kStatBatch; ++u) {
+        if (v0 + u * 32 + lane >= nv) break;
+        const uint32_t w[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xFFFF0000u);
+          ss = fmaf(lo, lo, ss);
+          ss = fmaf(hi, hi, ss);
+          h = (h ^ w[i]) * 0x100000001B3ull;
+          h ^= h >> 29;
+        }
       }
     }
 #pragma unroll
@@ -75,8 +91,8 @@ __global__ void __launch_bounds__(256)
       ss += __shfl_xor_sync(0xffffffffu, ss, off);
       h ^= __shfl_xor_sync(0xffffffffu, h, off) * 0xBF58476D1CE4E5B9ull;
     }
-    // The xor-butterfly above is symmetric in the lanes, so every lane holds
-    // the same values; lane 0 writes.
+    // Every lane holds the full sum of squares; lane 0's hash depends on every lane's
+    // words.  Lane 0 writes.
     if (lane == 0) {
       norm[r] = sqrtf(ss);
       hash[r] = h;
@@ -103,6 +119,8 @@ __global__ void __launch_bounds__(256)
   __shared__ int s_beg[1025];
   __shared__ int s_second[1024];
   __shared__ int s_over;
+  pdl_trigger();
+  pdl_wait();
   if (threadIdx.x == 0) s_over = 0;
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -196,11 +214,12 @@ __global__ void __launch_bounds__(256)
 // of warp 0, which resolves the groups in order.
 // Buckets whose 32-row group does not fit a buffer (more than 12256 rows) take
 // the row-by-row walk over staged rows instead.
-__global__ void __launch_bounds__(kScanThreads)
-    greedy_scan_kernel(const unsigned* __restrict__ bits, const long long* __restrict__ bits_base,
-                       const int32_t* __restrict__ offsets, const int32_t* __restrict__ overflow,
-                       const int32_t* __restrict__ unresolved, const int32_t* __restrict__ nrep_fast,
-                       int32_t* __restrict__ rep_of, int32_t* __restrict__ n_rep, unsigned* status) {
+// Returns the bucket's representative count (in thread 0).
+__device__ __forceinline__ int greedy_scan_bucket(
+    const unsigned* __restrict__ bits, const long long* __restrict__ bits_base,
+    const int32_t* __restrict__ offsets, const int32_t* __restrict__ overflow,
+    const int32_t* __restrict__ unresolved, const int32_t* __restrict__ nrep_fast,
+    int32_t* __restrict__ rep_of, unsigned* status) {
   extern __shared__ unsigned scan_smem[];
   unsigned* R = scan_smem;                  // kMaxWords: representatives so far, as a bitset
   unsigned* buf = scan_smem + kMaxWords;    // 2 x kScanBufWords
@@ -210,17 +229,13 @@ __global__ void __launch_bounds__(kScanThreads)
   const int W = (n + 31) >> 5;
   if (!*overflow && unresolved[e] == 0) {
     // resolve_kernel decided every row of the bucket
-    if (threadIdx.x == 0) n_rep[e] = nrep_fast[e];
-    return;
+    return nrep_fast[e];
   }
   if (*overflow || n > kMaxBucketRows) {
     // no bit matrix: every slot is its own representative
     for (int i = threadIdx.x; i < n; i += blockDim.x) rep_of[off + i] = off + i;
-    if (threadIdx.x == 0) {
-      n_rep[e] = max(n, 0);
-      record_status(status, MOE_ERR_DEVICE_INDEX);
-    }
-    return;
+    if (threadIdx.x == 0) record_status(status, MOE_ERR_DEVICE_INDEX);
+    return max(n, 0);
   }
   for (int w = threadIdx.x; w < W; w += blockDim.x) R[w] = 0u;
   const unsigned* B = bits + bits_base[e];
@@ -384,7 +399,34 @@ __global__ void __launch_bounds__(kScanThreads)
       }
     }
   }
-  if (threadIdx.x == 0) n_rep[e] = reps;
+  return reps;
+}
+
+// One CTA per bucket (see greedy_scan_bucket).  The last CTA to finish also writes
+// n_condensed = (number of slots) - (representatives of every bucket); *done counts the
+// finished CTAs (zeroed by first_hit_kernel, reset here for the next call).
+__global__ void __launch_bounds__(kScanThreads)
+    greedy_scan_kernel(const unsigned* __restrict__ bits, const long long* __restrict__ bits_base,
+                       const int32_t* __restrict__ offsets, const int32_t* __restrict__ overflow,
+                       const int32_t* __restrict__ unresolved, const int32_t* __restrict__ nrep_fast,
+                       int32_t* __restrict__ rep_of, int32_t* n_rep, int32_t* done,
+                       int32_t* __restrict__ n_condensed, unsigned* status) {
+  pdl_trigger();
+  pdl_wait();
+  const int reps =
+      greedy_scan_bucket(bits, bits_base, offsets, overflow, unresolved, nrep_fast, rep_of, status);
+  if (threadIdx.x == 0) {
+    n_rep[blockIdx.x] = reps;
+    __threadfence();
+    if (atomicAdd(done, 1) == static_cast<int>(gridDim.x) - 1) {
+      __threadfence();
+      const volatile int32_t* nr = n_rep;
+      int total = 0;
+      for (int e = 0; e < static_cast<int>(gridDim.x); ++e) total += nr[e];
+      *n_condensed = offsets[gridDim.x] - total;
+      *done = 0;
+    }
+  }
 }
 
 // Rows decided without the walk.  For slot s (local row li of bucket e) let C be the rows
@@ -398,11 +440,15 @@ __global__ void __launch_bounds__(256)
     first_hit_kernel(const unsigned* __restrict__ bits, const long long* __restrict__ bits_base,
                      const int32_t* __restrict__ offsets, int E, const int32_t* __restrict__ overflow,
                      int32_t* __restrict__ first, int32_t* __restrict__ unresolved,
-                     int32_t* __restrict__ nrep_fast) {
+                     int32_t* __restrict__ nrep_fast, int32_t* __restrict__ done) {
   __shared__ int off[257];
+  pdl_trigger();
+  pdl_wait();
   for (int i = threadIdx.x; i <= E; i += blockDim.x) off[i] = offsets[i];
-  if (blockIdx.x == 0)
+  if (blockIdx.x == 0) {
     for (int e = threadIdx.x; e < E; e += blockDim.x) unresolved[e] = nrep_fast[e] = 0;
+    if (threadIdx.x == 0) *done = 0;
+  }
   __syncthreads();
   if (*overflow) return;
   const int n_rows = off[E];
@@ -442,35 +488,44 @@ __global__ void __launch_bounds__(256)
                    const int32_t* __restrict__ overflow, int32_t* __restrict__ rep_of,
                    int32_t* __restrict__ unresolved, int32_t* __restrict__ nrep_fast) {
   __shared__ int off[257];
+  pdl_trigger();
+  pdl_wait();
   for (int i = threadIdx.x; i <= E; i += blockDim.x) off[i] = offsets[i];
   __syncthreads();
   if (*overflow) return;
   const int n_rows = off[E];
-  for (int sl = blockIdx.x * blockDim.x + threadIdx.x; sl < n_rows; sl += gridDim.x * blockDim.x) {
-    int lo = 0, hi = E;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (off[mid] <= sl) lo = mid; else hi = mid;
+  const int lane = threadIdx.x & 31;
+  const int stride = gridDim.x * blockDim.x;
+  // warp-uniform trip count; the per-bucket counts are summed over the warp's lanes of one
+  // bucket and added by one lane
+  for (int base = blockIdx.x * blockDim.x + (threadIdx.x & ~31); base < n_rows; base += stride) {
+    const int sl = base + lane;
+    int lo = -1;
+    bool is_rep = false, open = false;
+    if (sl < n_rows) {
+      lo = 0;
+      int hi = E;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (off[mid] <= sl) lo = mid; else hi = mid;
+      }
+      const int f = first[sl];
+      if (f < 0) {
+        rep_of[sl] = sl;
+        is_rep = true;
+      } else if (first[off[lo] + f] < 0) {
+        rep_of[sl] = off[lo] + f;
+      } else {
+        open = true;
+      }
     }
-    const int f = first[sl];
-    if (f < 0) {
-      rep_of[sl] = sl;
-      atomicAdd(&nrep_fast[lo], 1);
-    } else if (first[off[lo] + f] < 0) {
-      rep_of[sl] = off[lo] + f;
-    } else {
-      atomicAdd(&unresolved[lo], 1);
+    const unsigned peers = __match_any_sync(0xffffffffu, lo);
+    const int n_r = __popc(__ballot_sync(0xffffffffu, is_rep) & peers);
+    const int n_o = __popc(__ballot_sync(0xffffffffu, open) & peers);
+    if (lo >= 0 && lane == __ffs(peers) - 1) {
+      if (n_r) atomicAdd(&nrep_fast[lo], n_r);
+      if (n_o) atomicAdd(&unresolved[lo], n_o);
     }
-  }
-}
-
-// n_condensed = (number of slots) - sum of representatives.
-__global__ void condensed_count_kernel(const int32_t* offsets, const int32_t* n_rep, int E,
-                                       int32_t* n_condensed) {
-  if (threadIdx.x == 0) {
-    int reps = 0;
-    for (int e = 0; e < E; ++e) reps += n_rep[e];
-    *n_condensed = offsets[E] - reps;
   }
 }
 
@@ -487,28 +542,19 @@ __global__ void identity_reps_kernel(const int32_t* offsets, int E, int P, int32
   (void)P;
 }
 
-// One CTA per bucket: representatives of the bucket in slot order.
+// One CTA per bucket: the bucket's representatives in slot order, at the bucket's own
+// slots (rep_local[off_e + i] = slot of its i-th representative), and their count.  No CTA
+// needs another bucket's count: gather_reps_kernel places the lists one after another.
 __global__ void __launch_bounds__(1024)
     compact_reps_kernel(const int32_t* __restrict__ rep_of, const int32_t* __restrict__ offsets,
-                        int E, int32_t* __restrict__ rep_rows, int32_t* __restrict__ rep_counts) {
+                        int E, int32_t* __restrict__ rep_local, int32_t* __restrict__ rep_counts) {
   __shared__ int s_warp[32];
-  __shared__ int s_base;
+  pdl_trigger();
+  pdl_wait();
   const int e = blockIdx.x;
   const int off = offsets[e], n = offsets[e + 1] - off;
-  // first output position of this bucket = representatives of buckets < e
-  if (threadIdx.x == 0) s_base = 0;
-  __syncthreads();
-  {
-    int mine = 0;
-    for (int e2 = 0; e2 < e; ++e2) {
-      const int o = offsets[e2], m = offsets[e2 + 1] - o;
-      for (int s = threadIdx.x; s < m; s += blockDim.x) mine += rep_of[o + s] == o + s;
-    }
-    if (mine) atomicAdd(&s_base, mine);
-  }
-  __syncthreads();
-  int base = s_base;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int base = 0;
   for (int c0 = 0; c0 < n; c0 += blockDim.x) {
     const int s = c0 + threadIdx.x;
     const bool is_rep = s < n && rep_of[off + s] == off + s;
@@ -520,11 +566,48 @@ __global__ void __launch_bounds__(1024)
       if (w < warp) before += s_warp[w];
       total += s_warp[w];
     }
-    if (is_rep) rep_rows[base + before + __popc(b & ((1u << lane) - 1u))] = off + s;
+    if (is_rep) rep_local[off + base + before + __popc(b & ((1u << lane) - 1u))] = off + s;
     base += total;
     __syncthreads();
   }
-  if (threadIdx.x == 0) rep_counts[e] = base - s_base;
+  if (threadIdx.x == 0) rep_counts[e] = base;
+}
+
+// Row r of the compact representative list (r < rep_off[E], rep_off the exclusive prefix of
+// the per-bucket counts): bucket e with rep_off[e] <= r < rep_off[e + 1], slot
+// s = rep_local[offsets[e] + r - rep_off[e]]; writes rep_rows[r] = s and dst[r] = src[s].
+// One warp per row, 16-byte vectors.
+template <typename T>
+__global__ void __launch_bounds__(256)
+    gather_reps_kernel(const T* __restrict__ src, const int32_t* __restrict__ rep_local,
+                       const int32_t* __restrict__ offsets, const int32_t* __restrict__ rep_off,
+                       int E, int d, T* __restrict__ dst, int32_t* __restrict__ rep_rows) {
+  constexpr int V = Act<T>::kVec;
+  __shared__ int s_roff[257];
+  __shared__ int s_off[257];
+  pdl_trigger();
+  pdl_wait();
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) {
+    s_roff[i] = rep_off[i];
+    s_off[i] = offsets[i];
+  }
+  __syncthreads();
+  const int n_rows = s_roff[E];
+  const int nv = d / V;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < n_rows; r += warps) {
+    int lo = 0, hi = E;  // s_roff[lo] <= r < s_roff[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_roff[mid] <= r) lo = mid; else hi = mid;
+    }
+    const int s = rep_local[s_off[lo] + r - s_roff[lo]];
+    if (lane == 0) rep_rows[r] = s;
+    const uint4* a = reinterpret_cast<const uint4*>(src + static_cast<long long>(s) * d);
+    uint4* b = reinterpret_cast<uint4*>(dst + static_cast<long long>(r) * d);
+    for (int v = lane; v < nv; v += 32) b[v] = a[v];
+  }
 }
 
 // Expert (bucket) of a slot of the record: the largest e with off[e] <= s < off[e + 1];
@@ -754,6 +837,7 @@ struct CondenseScratch {
   int2* cos_list;   // history: tiles with an unclassified pair
   int32_t* n_cos;
   int32_t* overflow;  // a bucket longer than the scratch allows
+  int32_t* done;      // greedy-scan CTAs finished (the word after overflow)
   int32_t* first;       // [P] earliest similar row before each row (local), -1 none
   int32_t* unresolved;  // [E] rows the walk has to decide
   int32_t* nrep_fast;   // [E] representatives found without the walk
@@ -786,7 +870,7 @@ size_t carve(void* base, int T, int k, int E, CondenseScratch* s) {
   const size_t o_bits = take(sizeof(unsigned) * max_words);
   const size_t o_cl = take(sizeof(int2) * max_tiles);
   const size_t o_nc = take(sizeof(int32_t));
-  const size_t o_of = take(sizeof(int32_t));
+  const size_t o_of = take(sizeof(int32_t) * 2);
   const size_t o_fi = take(sizeof(int32_t) * P);
   const size_t o_un = take(sizeof(int32_t) * E);
   const size_t o_nf = take(sizeof(int32_t) * E);
@@ -803,6 +887,7 @@ size_t carve(void* base, int T, int k, int E, CondenseScratch* s) {
     s->cos_list = reinterpret_cast<int2*>(b + o_cl);
     s->n_cos = reinterpret_cast<int32_t*>(b + o_nc);
     s->overflow = reinterpret_cast<int32_t*>(b + o_of);
+    s->done = s->overflow + 1;
     s->first = reinterpret_cast<int32_t*>(b + o_fi);
     s->unresolved = reinterpret_cast<int32_t*>(b + o_un);
     s->nrep_fast = reinterpret_cast<int32_t*>(b + o_nf);
@@ -904,15 +989,17 @@ cudaError_t condense_pipeline(const __nv_bfloat16* x_perm, const int32_t* offset
   }
   CondenseScratch s;
   carve(scratch, T, k, E, &s);
-  row_stats_kernel<<<min(ceil_div(P, 8), 4096), 256, 0, stream>>>(x_perm, offsets, E, d, s.norm,
-                                                                  s.hash);
-  cudaError_t err = launch_build_mtiles(nullptr, offsets, 0, E, nullptr, s.mt_info,
-                                        s.group_mt_begin, stream);
+  cudaError_t err = launch_pdl(row_stats_kernel, dim3(min(ceil_div(P, 8), 4096)), dim3(256), 0,
+                               stream, x_perm, offsets, E, d, s.norm, s.hash);
+  if (err != cudaSuccess) return err;
+  err = launch_build_mtiles(nullptr, offsets, 0, E, nullptr, s.mt_info, s.group_mt_begin, stream);
   if (err != cudaSuccess) return err;
   long long* bits_base = h ? out.bits_base : s.bits_base;
-  sim_tiles_kernel<<<1, 256, 0, stream>>>(s.mt_info, s.group_mt_begin, offsets, E,
-                                          bucket_rows_max(T, k), s.tile_list, s.n_list, bits_base,
-                                          s.overflow, h ? out.header : nullptr, status);
+  err = launch_pdl(sim_tiles_kernel, dim3(1), dim3(256), 0, stream,
+                   static_cast<const int4*>(s.mt_info), static_cast<const int32_t*>(s.group_mt_begin),
+                   offsets, E, bucket_rows_max(T, k), s.tile_list, s.n_list, bits_base, s.overflow,
+                   h ? out.header : nullptr, status);
+  if (err != cudaSuccess) return err;
   const int2* gemm_list = s.tile_list;
   const int32_t* gemm_n = s.n_list;
   int hist_mode = 0;
@@ -980,22 +1067,49 @@ cudaError_t condense_pipeline(const __nv_bfloat16* x_perm, const int32_t* offset
                                 static_cast<int>(smem));
   });
   if (err != cudaSuccess) return err;
-  first_hit_kernel<<<max(1, min(ceil_div(P, 8), 8 * num_sms)), 256, 0, stream>>>(
-      s.bits, bits_base, offsets, E, s.overflow, s.first, s.unresolved, s.nrep_fast);
-  resolve_kernel<<<max(1, min(ceil_div(P, 256), 4 * num_sms)), 256, 0, stream>>>(
-      s.first, offsets, E, s.overflow, rep_of, s.unresolved, s.nrep_fast);
-  greedy_scan_kernel<<<E, kScanThreads, smem, stream>>>(s.bits, bits_base, offsets, s.overflow,
-                                                        s.unresolved, s.nrep_fast, rep_of, n_rep,
-                                                        status);
-  condensed_count_kernel<<<1, 32, 0, stream>>>(offsets, n_rep, E, n_condensed);
+  err = launch_pdl(first_hit_kernel, dim3(max(1, min(ceil_div(P, 8), 8 * num_sms))), dim3(256), 0,
+                   stream, static_cast<const unsigned*>(s.bits),
+                   static_cast<const long long*>(bits_base), offsets, E,
+                   static_cast<const int32_t*>(s.overflow), s.first, s.unresolved, s.nrep_fast,
+                   s.done);
+  if (err != cudaSuccess) return err;
+  err = launch_pdl(resolve_kernel, dim3(max(1, min(ceil_div(P, 256), 4 * num_sms))), dim3(256), 0,
+                   stream, static_cast<const int32_t*>(s.first), offsets, E,
+                   static_cast<const int32_t*>(s.overflow), rep_of, s.unresolved, s.nrep_fast);
+  if (err != cudaSuccess) return err;
+  err = launch_pdl(greedy_scan_kernel, dim3(E), dim3(kScanThreads), smem, stream,
+                   static_cast<const unsigned*>(s.bits), static_cast<const long long*>(bits_base),
+                   offsets, static_cast<const int32_t*>(s.overflow),
+                   static_cast<const int32_t*>(s.unresolved),
+                   static_cast<const int32_t*>(s.nrep_fast), rep_of, n_rep, s.done, n_condensed,
+                   status);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 }  // namespace
 
-cudaError_t launch_compact_reps(const int32_t* rep_of, const int32_t* offsets, int P, int E,
-                                int32_t* rep_rows, int32_t* rep_counts, cudaStream_t stream) {
-  (void)P;
-  compact_reps_kernel<<<E, 1024, 0, stream>>>(rep_of, offsets, E, rep_rows, rep_counts);
+cudaError_t launch_compact_reps(const int32_t* rep_of, const int32_t* offsets, int E,
+                                int32_t* rep_local, int32_t* rep_counts, cudaStream_t stream) {
+  const cudaError_t e = launch_pdl(compact_reps_kernel, dim3(E), dim3(1024), 0, stream, rep_of,
+                                   offsets, E, rep_local, rep_counts);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_reps(int act_dtype, const void* src, const int32_t* rep_local,
+                               const int32_t* offsets, const int32_t* rep_off, int E, int max_rows,
+                               int d, void* dst, int32_t* rep_rows, cudaStream_t stream) {
+  if (max_rows <= 0) return cudaSuccess;
+  const int blocks = min(ceil_div(max_rows, 8), 4096);
+  const cudaError_t e =
+      act_dtype == MOE_F32
+          ? launch_pdl(gather_reps_kernel<float>, dim3(blocks), dim3(256), 0, stream,
+                       static_cast<const float*>(src), rep_local, offsets, rep_off, E, d,
+                       static_cast<float*>(dst), rep_rows)
+          : launch_pdl(gather_reps_kernel<__nv_bfloat16>, dim3(blocks), dim3(256), 0, stream,
+                       static_cast<const __nv_bfloat16*>(src), rep_local, offsets, rep_off, E, d,
+                       static_cast<__nv_bfloat16*>(dst), rep_rows);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -340,6 +340,8 @@ __global__ void __launch_bounds__(256)
                        const int* __restrict__ n_rows_dev, int src_rows, int d,
                        T* __restrict__ dst, unsigned* status) {
   constexpr int V = Act<T>::kVec;
+  pdl_trigger();
+  pdl_wait();
   const int n_rows = *n_rows_dev;
   const int nv = d / V;
   const int warps = (gridDim.x * blockDim.x) >> 5;
@@ -607,14 +609,15 @@ cudaError_t launch_gather_rows(int act_dtype, const void* src, int src_rows, con
                                unsigned* status, cudaStream_t stream) {
   if (max_rows <= 0) return cudaSuccess;
   const int blocks = min(ceil_div(max_rows, 8), 4096);
-  if (act_dtype == MOE_F32)
-    gather_rows_kernel<float><<<blocks, 256, 0, stream>>>(
-        static_cast<const float*>(src), rows, n_rows_dev, src_rows, d, static_cast<float*>(dst),
-        status);
-  else
-    gather_rows_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(src), rows, n_rows_dev, src_rows, d,
-        static_cast<__nv_bfloat16*>(dst), status);
+  const cudaError_t e =
+      act_dtype == MOE_F32
+          ? launch_pdl(gather_rows_kernel<float>, dim3(blocks), dim3(256), 0, stream,
+                       static_cast<const float*>(src), rows, n_rows_dev, src_rows, d,
+                       static_cast<float*>(dst), status)
+          : launch_pdl(gather_rows_kernel<__nv_bfloat16>, dim3(blocks), dim3(256), 0, stream,
+                       static_cast<const __nv_bfloat16*>(src), rows, n_rows_dev, src_rows, d,
+                       static_cast<__nv_bfloat16*>(dst), status);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

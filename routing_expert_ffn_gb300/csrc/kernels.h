@@ -246,7 +246,14 @@ cudaError_t launch_condense_hist(const __nv_bfloat16* x_perm, const int32_t* off
                                  void* scratch, unsigned* status, cudaStream_t stream);
 // Representative rows compacted bucket by bucket: rep_rows[c] = slot of the c-th
 // representative, rep_counts[e] = representatives of bucket e.
-cudaError_t launch_compact_reps(const int32_t* rep_of, const int32_t* offsets, int P, int E,
-                                int32_t* rep_rows, int32_t* rep_counts, cudaStream_t stream);
+// Per bucket e: its representatives' slots in slot order at rep_local[offsets[e] ..], and
+// their count rep_counts[e].
+cudaError_t launch_compact_reps(const int32_t* rep_of, const int32_t* offsets, int E,
+                                int32_t* rep_local, int32_t* rep_counts, cudaStream_t stream);
+// The compact representative list: rows r < rep_off[E] (rep_off = exclusive prefix of the
+// counts), rep_rows[r] = slot, dst[r] = src[slot]; max_rows bounds the rows (sizes the grid).
+cudaError_t launch_gather_reps(int act_dtype, const void* src, const int32_t* rep_local,
+                               const int32_t* offsets, const int32_t* rep_off, int E, int max_rows,
+                               int d, void* dst, int32_t* rep_rows, cudaStream_t stream);
 
 }  // namespace moe

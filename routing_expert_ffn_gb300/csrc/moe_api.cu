@@ -110,7 +110,8 @@ struct FfnScratch {
   int32_t* gmb_shared;
   void* h;
   void* h_shared;
-  int32_t* rep_rows;
+  int32_t* rep_rows;   // compact list of the representatives' slots
+  int32_t* rep_local;  // the same per bucket, at the bucket's own slots
   int32_t* rep_counts;
   int32_t* rep_off;
   void* x_rep;
@@ -127,10 +128,11 @@ size_t carve_ffn(const moe_config* c, bool condense, void* ws, FfnScratch* s) {
   t.gmb_shared = cv.take<int32_t>(2);
   t.h = cv.take<char>(static_cast<size_t>(P) * c->H * ab);
   t.h_shared = cv.take<char>(static_cast<size_t>(c->T) * c->n_shared * c->H_shared * ab);
-  t.rep_rows = t.rep_counts = t.rep_off = nullptr;
+  t.rep_rows = t.rep_local = t.rep_counts = t.rep_off = nullptr;
   t.x_rep = nullptr;
   if (condense) {
     t.rep_rows = cv.take<int32_t>(P);
+    t.rep_local = cv.take<int32_t>(P);
     t.rep_counts = cv.take<int32_t>(c->E);
     t.rep_off = cv.take<int32_t>(c->E + 1);
     t.x_rep = cv.take<char>(static_cast<size_t>(P) * c->d * ab);
@@ -149,12 +151,11 @@ moe_status run_routed_ffn(const moe_config* c, const moe_weights* w, const void*
   const void* A1 = x_perm;
   const int32_t* rowmap = nullptr;
   if (rep_of) {
-    MOE_CUDA(launch_compact_reps(rep_of, offsets, static_cast<int>(P), E, s.rep_rows,
-                                 s.rep_counts, st));
+    MOE_CUDA(launch_compact_reps(rep_of, offsets, E, s.rep_local, s.rep_counts, st));
     MOE_CUDA(launch_build_mtiles(s.rep_counts, nullptr, 0, E, s.rep_off, s.mt_routed,
                                  s.gmb_routed, st));
-    MOE_CUDA(launch_gather_rows(c->act_dtype, x_perm, static_cast<int>(P), s.rep_rows,
-                                s.rep_off + E, static_cast<int>(P), d, s.x_rep, di->status, st));
+    MOE_CUDA(launch_gather_reps(c->act_dtype, x_perm, s.rep_local, offsets, s.rep_off, E,
+                                static_cast<int>(P), d, s.x_rep, s.rep_rows, st));
     A1 = s.x_rep;
     rowmap = s.rep_rows;
   } else if (c->act_dtype != MOE_BF16) {
