@@ -180,9 +180,10 @@ __global__ void __launch_bounds__(256)
       v[i] = -INFINITY;
     }
   }
+  // lane j < k keeps the j-th selection in registers
   unsigned taken = 0;
-  float sel_v[32];
-  int sel_i[32];
+  float my_v = -INFINITY;
+  int my_i = 0;
 #pragma unroll 1
   for (int j = 0; j < k; ++j) {
     float bv = -INFINITY;
@@ -206,14 +207,16 @@ __global__ void __launch_bounds__(256)
     }
     if (bi >= E) bi = 0;  // only reachable with NaN logits
     if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    sel_v[j] = bv;
-    sel_i[j] = bi;
+    if (lane == j) {
+      my_v = bv;
+      my_i = bi;
+    }
   }
-  float g[32];
+  float g;
   if (gating == MOE_GATE_SIGMOID_TOPK) {
-    for (int j = 0; j < k; ++j) g[j] = 1.f / (1.f + expf(-sel_v[j]));
+    g = 1.f / (1.f + expf(-my_v));
   } else {
-    const float m = sel_v[0];
+    const float m = __shfl_sync(0xffffffffu, my_v, 0);  // the largest logit
     float z = 0.f;
     if (gating == MOE_GATE_SOFTMAX_TOPK) {
 #pragma unroll
@@ -221,13 +224,15 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
     } else {
-      for (int j = 0; j < k; ++j) z += expf(sel_v[j] - m);
+      // the selected terms added in selection order
+      const float t = lane < k ? expf(my_v - m) : 0.f;
+      for (int j = 0; j < k; ++j) z += __shfl_sync(0xffffffffu, t, j);
     }
-    for (int j = 0; j < k; ++j) g[j] = expf(sel_v[j] - m) / z;
+    g = expf(my_v - m) / z;
   }
-  for (int j = lane; j < k; j += 32) {
-    topk_idx[static_cast<long long>(warp) * k + j] = sel_i[j];
-    topk_gate[static_cast<long long>(warp) * k + j] = g[j];
+  if (lane < k) {
+    topk_idx[static_cast<long long>(warp) * k + lane] = my_i;
+    topk_gate[static_cast<long long>(warp) * k + lane] = g;
   }
 }
 
