@@ -18,9 +18,11 @@
 //   kSimBits condensation (CTA pairs): D is a 256 x 256 tile of the bucket's Gram matrix;
 //            the epilogue turns cos(x_i, x_j) >= tau, j < i, into bits.
 //   kRouter  router logits: B is the fp32 router weight split exactly into
-//            three bf16 terms; the K loop runs over the three terms, split
-//            across CTAs, and the epilogue writes fp32 partial sums (N = E
-//            rounded up to 32).
+//            three bf16 terms.  With E up to 64 the terms sit side by side along N
+//            (N = 3 x E rounded up to 32): the K loop runs over d, split across CTAs,
+//            and the epilogue adds the three accumulators; otherwise the K loop runs
+//            over the three terms in turn (N = E rounded up to 32).  The epilogue
+//            writes fp32 partial sums.
 //
 // Tiles.  Rows are grouped (one group per expert / bucket); a group's rows are
 // cut into 128-row m-tiles (the last one ragged; rows past the group are
@@ -532,7 +534,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t sb = sa + A_BYTES;
           const int kslice = kb / args.kb_per_slice;
           const int kin = (kb - kslice * args.kb_per_slice) * BK;
-          if (MODE == kRouter) {
+          if (MODE == kRouter && args.router_stacked) {
+            // K block kb of this split: x once, the three terms' rows one after another
+            const int k0 = (t.nt * args.n_kblocks + kb) * BK;
+            ptx::mbar_arrive_expect_tx(full, A_BYTES + 3 * args.router_n * BK * 2);
+            ptx::tma_load_2d(sa, &tmA, full, k0, t.row0);
+#pragma unroll
+            for (int term = 0; term < 3; ++term)
+              ptx::tma_load_3d(sb + term * args.router_n * BK * 2, &tmB, full, k0, 0, term);
+          } else if (MODE == kRouter) {
             // K block kb of this split -> term (W1, W2 or W3) and K offset inside x
             const int g = t.nt * args.n_kblocks + kb;
             const int term = g / args.router_kbd;
@@ -574,7 +584,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    const uint32_t idesc = ptx::idesc_bf16_f32(BM, MODE == kRouter ? args.router_n : BN);
+    const uint32_t idesc = ptx::idesc_bf16_f32(
+        BM, MODE == kRouter ? (args.router_stacked ? 3 : 1) * args.router_n : BN);
     int stage = 0;
     uint32_t phase = 0;
     int local = 0;
@@ -644,6 +655,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int c = 0; c < args.router_n / 32; ++c) {
           uint32_t v[32];
           ptx::tmem_ld_32x32b_x32(col0 + c * 32, v);
+          if (args.router_stacked) {
+            // the three terms' accumulators, added in term order
+            uint32_t v1[32], v2[32];
+            ptx::tmem_ld_32x32b_x32(col0 + args.router_n + c * 32, v1);
+            ptx::tmem_ld_32x32b_x32(col0 + 2 * args.router_n + c * 32, v2);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              v[i] = __float_as_uint((__uint_as_float(v[i]) + __uint_as_float(v1[i])) +
+                                     __uint_as_float(v2[i]));
+          }
           ptx::tmem_ld_wait();
           if (valid) {
             float4* dst = reinterpret_cast<float4*>(prow + c * 32);

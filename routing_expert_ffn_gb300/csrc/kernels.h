@@ -15,7 +15,7 @@ cudaError_t launch_router_logits(int act_dtype, const void* x, const float* W_r,
 // bf16 layers: W_r [d,E] fp32 -> W3 [3][E_pad][d] bf16 with W_r = W1 + W2 + W3 exactly,
 // then the tcgen05 GEMM writes split-K partial logits.
 int router_n_pad(int E);
-int router_splits(int T, int d, int num_sms);
+int router_splits(int T, int d, int E, int num_sms);
 size_t router_scratch_bytes(int T, int d, int E, int num_sms);
 cudaError_t launch_router_tc(const void* x, const float* W_r, int T, int d, int E, int num_sms,
                              void* scratch, const float** part, int* n_split, int* ld,
@@ -120,6 +120,9 @@ struct TcGemmArgs {
   // kRouter: D = x . [W1|W2|W3] over a K range of 3*d (the three bf16 terms of W_r)
   int router_n;        // N of the MMA = E rounded up to 32
   int router_kbd;      // K blocks per term (d / 64)
+  // 1: the three terms side by side along N (B = [W1; W2; W3], 3 router_n rows): each x K
+  // block is loaded once, K runs over d, and the epilogue adds the three accumulators
+  int router_stacked;
   int n_rows;          // T
   float* part;         // [n_ntiles (K splits)][T][router_n] fp32 partial logits
 };

@@ -290,10 +290,13 @@ cudaError_t launch_router_topk(const float* part, int n_split, int ld, const flo
 
 int router_n_pad(int E) { return ceil_div(E, 32) * 32; }
 
-// K splits: the largest divisor of the 3d/64 K blocks that keeps the tile count
-// (m-tiles x splits) within one wave of CTAs.
-int router_splits(int T, int d, int num_sms) {
-  const int kb = 3 * (d / kTcTileK);
+// The three terms fit side by side in one MMA (N = 3 x E rounded up to 32, at most 256).
+static bool router_stacked(int E) { return 3 * router_n_pad(E) <= 256; }
+
+// K splits: the largest divisor of the K blocks (d/64 with the terms side by side, else
+// 3d/64) that keeps the tile count (m-tiles x splits) within one wave of CTAs.
+int router_splits(int T, int d, int E, int num_sms) {
+  const int kb = (router_stacked(E) ? 1 : 3) * (d / kTcTileK);
   const int mtiles = ceil_div(T, kMTile);
   const int target = max(1, num_sms / max(1, mtiles));
   int best = 1;
@@ -307,7 +310,8 @@ size_t router_scratch_bytes(int T, int d, int E, int num_sms) {
     return static_cast<size_t>(router_simt_splits(d)) * T * E * sizeof(float);
   const size_t n_pad = router_n_pad(E);
   const size_t w3 = (3 * n_pad * d * sizeof(__nv_bfloat16) + 255) & ~size_t(255);
-  const size_t part = static_cast<size_t>(router_splits(T, d, num_sms)) * T * n_pad * sizeof(float);
+  const size_t part =
+      static_cast<size_t>(router_splits(T, d, E, num_sms)) * T * n_pad * sizeof(float);
   return w3 + part;
 }
 
@@ -315,7 +319,8 @@ cudaError_t launch_router_tc(const void* x, const float* W_r, int T, int d, int 
                              void* scratch, const float** part_out, int* n_split, int* ld,
                              unsigned* status, cudaStream_t stream) {
   const int n_pad = router_n_pad(E);
-  const int splits = router_splits(T, d, num_sms);
+  const int splits = router_splits(T, d, E, num_sms);
+  const bool stacked = router_stacked(E);
   __nv_bfloat16* W3 = static_cast<__nv_bfloat16*>(scratch);
   float* part = reinterpret_cast<float*>(static_cast<char*>(scratch) +
                                          ((3 * static_cast<size_t>(n_pad) * d * 2 + 255) & ~size_t(255)));
@@ -326,7 +331,8 @@ cudaError_t launch_router_tc(const void* x, const float* W_r, int T, int d, int 
   if (err != cudaSuccess) return err;
   TcGemmArgs a = {};
   a.n_ntiles = splits;
-  a.n_kblocks = 3 * (d / kTcTileK) / splits;
+  a.n_kblocks = (stacked ? 1 : 3) * (d / kTcTileK) / splits;
+  a.router_stacked = stacked ? 1 : 0;
   a.kb_per_slice = a.n_kblocks;
   a.nt_per_slice = splits;
   a.router_n = n_pad;
