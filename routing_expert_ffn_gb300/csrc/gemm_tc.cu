@@ -656,15 +656,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint32_t v[32];
           ptx::tmem_ld_32x32b_x32(col0 + c * 32, v);
           if (args.router_stacked) {
-            // the three terms' accumulators, added in term order
+            // the three terms' accumulators, the two small ones added first
             uint32_t v1[32], v2[32];
             ptx::tmem_ld_32x32b_x32(col0 + args.router_n + c * 32, v1);
             ptx::tmem_ld_32x32b_x32(col0 + 2 * args.router_n + c * 32, v2);
             ptx::tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              v[i] = __float_as_uint((__uint_as_float(v[i]) + __uint_as_float(v1[i])) +
-                                     __uint_as_float(v2[i]));
+              v[i] = __float_as_uint(__uint_as_float(v[i]) +
+                                     (__uint_as_float(v1[i]) + __uint_as_float(v2[i])));
           }
           ptx::tmem_ld_wait();
           if (valid) {
