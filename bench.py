@@ -157,7 +157,9 @@ def launches_per_step(cfg, condense: bool) -> int:
     n += 2 + (cfg.E * -(-(cfg.T * cfg.k) // 1024) > 2048)
     bf16 = cfg.dtype == "bf16"
     if condense:
-        n += 7  # row stats, m-tiles, tile list, similarity GEMM, first hits, resolve, greedy scan
+        # m-tiles, tile list, similarity GEMM, first hits, resolve, greedy scan (the dispatch
+        # forms the row statistics of a condensing layer)
+        n += 6
         n += 3  # compact reps, m-tiles over representatives, gather representative rows
     elif not bf16:
         n += 1  # m-tiles (the bf16 pair GEMM reads the bucket offsets itself)

@@ -938,15 +938,16 @@ namespace {
 cudaError_t condense_pipeline(const __nv_bfloat16* x_perm, const int32_t* offsets, int T, int k,
                               int d, int E, float tau, const HistArgs* h, int num_sms,
                               int32_t* rep_of, int32_t* n_rep, int32_t* n_condensed,
-                              void* scratch, unsigned* status, cudaStream_t stream);
+                              void* scratch, unsigned* status, cudaStream_t stream,
+                              bool stats_ready);
 }  // namespace
 
 cudaError_t launch_condense(const __nv_bfloat16* x_perm, const int32_t* offsets, int T, int k,
                             int d, int E, float tau, int num_sms, int32_t* rep_of, int32_t* n_rep,
                             int32_t* n_condensed, void* scratch, unsigned* status,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, bool stats_ready) {
   return condense_pipeline(x_perm, offsets, T, k, d, E, tau, nullptr, num_sms, rep_of, n_rep,
-                           n_condensed, scratch, status, stream);
+                           n_condensed, scratch, status, stream, stats_ready);
 }
 
 cudaError_t launch_condense_hist(const __nv_bfloat16* x_perm, const int32_t* offsets, int d,
@@ -954,14 +955,23 @@ cudaError_t launch_condense_hist(const __nv_bfloat16* x_perm, const int32_t* off
                                  int32_t* rep_of, int32_t* n_rep, int32_t* n_condensed,
                                  void* scratch, unsigned* status, cudaStream_t stream) {
   return condense_pipeline(x_perm, offsets, h.T, h.k, d, E, tau, &h, num_sms, rep_of, n_rep,
-                           n_condensed, scratch, status, stream);
+                           n_condensed, scratch, status, stream, false);
+}
+
+void condense_stats_ptrs(void* scratch, int T, int k, int E, float** norm,
+                         unsigned long long** hash) {
+  CondenseScratch s;
+  carve(scratch, T, k, E, &s);
+  *norm = s.norm;
+  *hash = s.hash;
 }
 
 namespace {
 cudaError_t condense_pipeline(const __nv_bfloat16* x_perm, const int32_t* offsets, int T, int k,
                               int d, int E, float tau, const HistArgs* h, int num_sms,
                               int32_t* rep_of, int32_t* n_rep, int32_t* n_condensed,
-                              void* scratch, unsigned* status, cudaStream_t stream) {
+                              void* scratch, unsigned* status, cudaStream_t stream,
+                              bool stats_ready) {
   const int P = T * k;
   HistView out = {};
   if (h) {
@@ -989,9 +999,12 @@ cudaError_t condense_pipeline(const __nv_bfloat16* x_perm, const int32_t* offset
   }
   CondenseScratch s;
   carve(scratch, T, k, E, &s);
-  cudaError_t err = launch_pdl(row_stats_kernel, dim3(min(ceil_div(P, 8), 4096)), dim3(256), 0,
-                               stream, x_perm, offsets, E, d, s.norm, s.hash);
-  if (err != cudaSuccess) return err;
+  cudaError_t err = cudaSuccess;
+  if (!stats_ready) {
+    err = launch_pdl(row_stats_kernel, dim3(min(ceil_div(P, 8), 4096)), dim3(256), 0, stream,
+                     x_perm, offsets, E, d, s.norm, s.hash);
+    if (err != cudaSuccess) return err;
+  }
   err = launch_build_mtiles(nullptr, offsets, 0, E, nullptr, s.mt_info, s.group_mt_begin, stream);
   if (err != cudaSuccess) return err;
   long long* bits_base = h ? out.bits_base : s.bits_base;

@@ -241,13 +241,18 @@ constexpr int kRowChunk = 8;
 // scatter_scan_limit() checks at set-up that this, plus the kernel's static shared memory and
 // the dynamic region's alignment, fits what a launch may use without opting in.
 constexpr int kScatterScanMaxEntries = 2048;
-template <typename T, bool SCAN>
+// STATS (bf16 rows, for the condensation that follows in the same layer call): the warp also
+// forms the row's fp32 norm and 64-bit content hash while the row is in its registers, in the
+// same element order and with the same arithmetic as the condensation's own row statistics, and
+// writes them at each of the token's slots.
+template <typename T, bool SCAN, bool STATS>
 __global__ void __launch_bounds__(256)
     scatter_rows_kernel(const T* __restrict__ x, const int32_t* __restrict__ idx,
                         const int32_t* __restrict__ local_rank, const int32_t* __restrict__ blk,
                         int n_blk, int E, int T_tok, int k, int d, T* __restrict__ x_perm,
                         int32_t* __restrict__ perm, int32_t* __restrict__ slot_of,
                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                        float* __restrict__ norm_out, unsigned long long* __restrict__ hash_out,
                         unsigned* status) {
   constexpr int V = Act<T>::kVec;
   const int nv = d / V;
@@ -310,12 +315,29 @@ __global__ void __launch_bounds__(256)
       slot_of[p] = slot;
       if (slot >= 0) perm[slot] = t;
     }
+    float ss = 0.f;
+    unsigned long long h = 0x9E3779B97F4A7C15ull * (lane + 1);
     for (int v0 = 0; v0 < nv; v0 += 32 * kRowChunk) {
       if (v0 > 0) {
 #pragma unroll
         for (int u = 0; u < kRowChunk; ++u) {
           const int v = v0 + u * 32 + lane;
           if (v < nv) r[u] = src[v];
+        }
+      }
+      if (STATS) {
+#pragma unroll
+        for (int u = 0; u < kRowChunk; ++u) {
+          if (v0 + u * 32 + lane >= nv) break;
+          const uint32_t w[4] = {r[u].x, r[u].y, r[u].z, r[u].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xFFFF0000u);
+            ss = fmaf(lo, lo, ss);
+            ss = fmaf(hi, hi, ss);
+            h = (h ^ w[i]) * 0x100000001B3ull;
+            h ^= h >> 29;
+          }
         }
       }
       for (int j = 0; j < k; ++j) {
@@ -327,6 +349,19 @@ __global__ void __launch_bounds__(256)
           const int v = v0 + u * 32 + lane;
           if (v < nv) dst[v] = r[u];
         }
+      }
+    }
+    if (STATS) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        h ^= __shfl_xor_sync(0xffffffffu, h, off) * 0xBF58476D1CE4E5B9ull;
+      }
+      // every lane holds the sum of squares; lane 0's hash is the row's
+      const unsigned long long h0 = __shfl_sync(0xffffffffu, h, 0);
+      if (lane < k && slot >= 0) {
+        norm_out[slot] = sqrtf(ss);
+        hash_out[slot] = h0;
       }
     }
     if (t + warps < T_tok) load_token(t + warps);
@@ -534,11 +569,18 @@ int scatter_scan_limit() {
     cudaError_t r = cudaDeviceGetAttribute(&per_block, cudaDevAttrMaxSharedMemoryPerBlock, dev);
     if (r != cudaSuccess) return r;
     cudaFuncAttributes fa_f, fa_b;
-    if ((r = cudaFuncGetAttributes(&fa_f, scatter_rows_kernel<float, true>)) != cudaSuccess) return r;
-    if ((r = cudaFuncGetAttributes(&fa_b, scatter_rows_kernel<__nv_bfloat16, true>)) != cudaSuccess)
+    cudaFuncAttributes fa_s;
+    if ((r = cudaFuncGetAttributes(&fa_f, scatter_rows_kernel<float, true, false>)) != cudaSuccess)
       return r;
-    const size_t stat = fa_f.sharedSizeBytes > fa_b.sharedSizeBytes ? fa_f.sharedSizeBytes
-                                                                    : fa_b.sharedSizeBytes;
+    if ((r = cudaFuncGetAttributes(&fa_b, scatter_rows_kernel<__nv_bfloat16, true, false>)) !=
+        cudaSuccess)
+      return r;
+    if ((r = cudaFuncGetAttributes(&fa_s, scatter_rows_kernel<__nv_bfloat16, true, true>)) !=
+        cudaSuccess)
+      return r;
+    size_t stat = fa_f.sharedSizeBytes > fa_b.sharedSizeBytes ? fa_f.sharedSizeBytes
+                                                              : fa_b.sharedSizeBytes;
+    if (fa_s.sharedSizeBytes > stat) stat = fa_s.sharedSizeBytes;
     // static bytes rounded up to 128, plus 128 bytes for the dynamic region's alignment
     const long long room = static_cast<long long>(per_block) -
                            static_cast<long long>((stat + 127) / 128 * 128) - 128;
@@ -557,7 +599,8 @@ int scatter_scan_limit() {
 cudaError_t launch_dispatch_auto(int act_dtype, const void* x, const int32_t* topk_idx, int T,
                                  int d, int E, int k, int32_t* counts, int32_t* offsets,
                                  int32_t* perm, int32_t* slot_of, void* x_perm, void* scratch,
-                                 int num_sms, unsigned* status, cudaStream_t stream) {
+                                 int num_sms, unsigned* status, cudaStream_t stream,
+                                 float* norm_out, unsigned long long* hash_out) {
   const long long P = static_cast<long long>(T) * k;
   if (P == 0)
     return launch_dispatch(act_dtype, x, topk_idx, T, d, E, k, counts, offsets, perm, slot_of,
@@ -583,22 +626,27 @@ cudaError_t launch_dispatch_auto(int act_dtype, const void* x, const int32_t* to
   if (act_dtype == MOE_F32) {
     const float* xf = static_cast<const float*>(x);
     float* xp = static_cast<float*>(x_perm);
-    err = scan_in_smem ? launch_pdl(scatter_rows_kernel<float, true>, dim3(blocks), dim3(256), smem,
-                                    stream, xf, topk_idx, local_rank, blk, n_blk, E, T, k, d, xp,
-                                    perm, slot_of, counts, offsets, status)
-                       : launch_pdl(scatter_rows_kernel<float, false>, dim3(blocks), dim3(256), 0,
-                                    stream, xf, topk_idx, local_rank, blk, n_blk, E, T, k, d, xp,
-                                    perm, slot_of, counts, offsets, status);
+    err = scan_in_smem ? launch_pdl(scatter_rows_kernel<float, true, false>, dim3(blocks),
+                                    dim3(256), smem, stream, xf, topk_idx, local_rank, blk, n_blk,
+                                    E, T, k, d, xp, perm, slot_of, counts, offsets,
+                                    static_cast<float*>(nullptr),
+                                    static_cast<unsigned long long*>(nullptr), status)
+                       : launch_pdl(scatter_rows_kernel<float, false, false>, dim3(blocks),
+                                    dim3(256), 0, stream, xf, topk_idx, local_rank, blk, n_blk, E,
+                                    T, k, d, xp, perm, slot_of, counts, offsets,
+                                    static_cast<float*>(nullptr),
+                                    static_cast<unsigned long long*>(nullptr), status);
   } else {
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
     __nv_bfloat16* xp = static_cast<__nv_bfloat16*>(x_perm);
-    err = scan_in_smem
-              ? launch_pdl(scatter_rows_kernel<__nv_bfloat16, true>, dim3(blocks), dim3(256), smem,
-                           stream, xb, topk_idx, local_rank, blk, n_blk, E, T, k, d, xp, perm,
-                           slot_of, counts, offsets, status)
-              : launch_pdl(scatter_rows_kernel<__nv_bfloat16, false>, dim3(blocks), dim3(256), 0,
-                           stream, xb, topk_idx, local_rank, blk, n_blk, E, T, k, d, xp, perm,
-                           slot_of, counts, offsets, status);
+    const bool stats = norm_out != nullptr && hash_out != nullptr;
+    auto kern = scan_in_smem ? (stats ? scatter_rows_kernel<__nv_bfloat16, true, true>
+                                      : scatter_rows_kernel<__nv_bfloat16, true, false>)
+                             : (stats ? scatter_rows_kernel<__nv_bfloat16, false, true>
+                                      : scatter_rows_kernel<__nv_bfloat16, false, false>);
+    err = launch_pdl(kern, dim3(blocks), dim3(256), scan_in_smem ? smem : 0, stream, xb, topk_idx,
+                     local_rank, blk, n_blk, E, T, k, d, xp, perm, slot_of, counts, offsets,
+                     norm_out, hash_out, status);
   }
   if (err != cudaSuccess) return err;
   return cudaGetLastError();

@@ -44,10 +44,14 @@ cudaError_t launch_dispatch(int act_dtype, const void* x, const int32_t* topk_id
 // Same outputs as launch_dispatch, with ranks computed in parallel blocks of
 // 1024 pairs; scratch: dispatch_auto_scratch_bytes.
 size_t dispatch_auto_scratch_bytes(int T, int k, int E);
+// norm_out / hash_out (bf16 only, both or neither): also each slot's row norm and hash, as the
+// condensation's row statistics form them (condense_stats_ptrs gives where it reads them).
 cudaError_t launch_dispatch_auto(int act_dtype, const void* x, const int32_t* topk_idx, int T,
                                  int d, int E, int k, int32_t* counts, int32_t* offsets,
                                  int32_t* perm, int32_t* slot_of, void* x_perm, void* scratch,
-                                 int num_sms, unsigned* status, cudaStream_t stream);
+                                 int num_sms, unsigned* status, cudaStream_t stream,
+                                 float* norm_out = nullptr,
+                                 unsigned long long* hash_out = nullptr);
 // dst[r] = src[rows[r]] for r < *n_rows_dev (<= max_rows); rows outside [0, src_rows) are flagged.
 cudaError_t launch_gather_rows(int act_dtype, const void* src, int src_rows, const int32_t* rows,
                                const int* n_rows_dev, int max_rows, int d, void* dst,
@@ -218,10 +222,14 @@ cudaError_t simt_gemm_store(const float* A, const float* B, int b_slices, int b_
 
 // ------------------------------------------------------------------ condensation
 size_t condense_scratch_bytes(int T, int k, int E);
+// stats_ready: the slots' row norms and hashes are already at condense_stats_ptrs(scratch)
+// (written by the dispatch), so the row-statistics pass is skipped.
 cudaError_t launch_condense(const __nv_bfloat16* x_perm, const int32_t* offsets, int T, int k, int d,
                             int E, float tau, int num_sms, int32_t* rep_of, int32_t* n_rep,
                             int32_t* n_condensed, void* scratch, unsigned* status,
-                            cudaStream_t stream);
+                            cudaStream_t stream, bool stats_ready = false);
+void condense_stats_ptrs(void* scratch, int T, int k, int E, float** norm,
+                         unsigned long long** hash);
 // Condensation with the previous call's pair classes (Luffy's historical similarity).
 // The record layout is the one include/moe.h documents for moe_condense_hist.
 constexpr int kHistMagic = 0x48697374;

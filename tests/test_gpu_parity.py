@@ -73,6 +73,27 @@ def test_router_full_size(moe, name):
     _status_ok(moe)
 
 
+@pytest.mark.parametrize("E", [8, 33, 64, 65, 96])
+def test_router_terms_side_by_side_boundary(moe, E):
+    """Up to E = 64 the tensor-core router puts the three bf16 terms of W_r side by side
+    along N (N = 3 x E rounded up to 32, at most 256) and splits K over d; above that the
+    terms follow one another along K.  Both sides of the boundary, 1000 tokens (a ragged
+    last m-tile), every token against the oracle."""
+    from dataclasses import replace
+    cfg = replace(gen.CONFIGS["qwen3_30b_a3b"], name=f"router{E}", T=1000, d=512, E=E, k=2, H=128,
+                  n_shared=1, H_shared=128, router_bias="none")
+    inp = harness.condition(cfg, gen.make_inputs(cfg))
+    C = moe.Config.from_workload(cfg)
+    w, x, r = moe.upload(C, inp)
+    logits, idx, gate = moe.route(C, x, w.W_r, w.router_bias)
+    torch.cuda.synchronize()
+    l_ref, idx_ref, g_ref = orc.route(inp["x"], inp["W_r"], inp["bias"], cfg.k, cfg.gating)
+    np.testing.assert_array_equal(_np(idx), idx_ref)
+    assert harness.max_rel_err(_np(logits), l_ref) < 5e-5
+    np.testing.assert_allclose(_np(gate), g_ref, rtol=2e-5, atol=1e-7)
+    _status_ok(moe)
+
+
 # ------------------------------------------------------------------ dispatch
 @pytest.mark.parametrize("name", NAMES)
 def test_dispatch_full_size(moe, name):
