@@ -157,9 +157,10 @@ def launches_per_step(cfg, condense: bool) -> int:
     n += 2 + (cfg.E * -(-(cfg.T * cfg.k) // 1024) > 2048)
     bf16 = cfg.dtype == "bf16"
     if condense:
-        # m-tiles, tile list, similarity GEMM, first hits, resolve, greedy scan (the dispatch
-        # forms the row statistics of a condensing layer)
-        n += 6
+        # m-tiles, tile list, similarity GEMM (its epilogue also finds each row's earliest
+        # similar row), resolve, greedy scan (the dispatch forms the row statistics of a
+        # condensing layer)
+        n += 5
         n += 3  # compact reps, m-tiles over representatives, gather representative rows
     elif not bf16:
         n += 1  # m-tiles (the bf16 pair GEMM reads the bucket offsets itself)

@@ -49,12 +49,13 @@ __device__ __forceinline__ void cp_async_wait_all() {
 }
 
 // Per dispatched row: fp32 norm and a 64-bit content hash (a filter for identical rows,
-// which are then compared element by element).  One warp per row; a lane's vectors are
+// which are then compared element by element); resets the row's earliest-similar-row entry.  One warp per row; a lane's vectors are
 // loaded kStatBatch at a time, so their loads are in flight together.
 constexpr int kStatBatch = 4;
 __global__ void __launch_bounds__(256)
     row_stats_kernel(const __nv_bfloat16* __restrict__ rows, const int32_t* __restrict__ offsets,
-                     int E, int d, float* __restrict__ norm, unsigned long long* __restrict__ hash) {
+                     int E, int d, float* __restrict__ norm, unsigned long long* __restrict__ hash,
+                     int32_t* __restrict__ first) {
   pdl_trigger();
   pdl_wait();
   const int n_rows = offsets[E];
@@ -96,6 +97,7 @@ __global__ void __launch_bounds__(256)
     if (lane == 0) {
       norm[r] = sqrtf(ss);
       hash[r] = h;
+      first[r] = kNoHit;  // lowered by the similarity tiles
     }
   }
 }
@@ -114,14 +116,21 @@ __global__ void __launch_bounds__(256)
                      const int32_t* __restrict__ offsets, int E, int max_rows,
                      int2* __restrict__ tile_list, int32_t* __restrict__ n_list,
                      long long* __restrict__ bits_base, int32_t* __restrict__ overflow,
-                     int32_t* __restrict__ hist_header, unsigned* status) {
+                     int32_t* __restrict__ hist_header, int32_t* __restrict__ unresolved,
+                     int32_t* __restrict__ nrep_fast, int32_t* __restrict__ done,
+                     unsigned* status) {
   __shared__ int s_cnt[1024];
   __shared__ int s_beg[1025];
   __shared__ int s_second[1024];
   __shared__ int s_over;
   pdl_trigger();
   pdl_wait();
-  if (threadIdx.x == 0) s_over = 0;
+  // the counts the resolve pass and the walk add up
+  for (int e = threadIdx.x; e < E; e += blockDim.x) unresolved[e] = nrep_fast[e] = 0;
+  if (threadIdx.x == 0) {
+    *done = 0;
+    s_over = 0;
+  }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     const int n = offsets[e + 1] - offsets[e];
@@ -404,7 +413,7 @@ __device__ __forceinline__ int greedy_scan_bucket(
 
 // One CTA per bucket (see greedy_scan_bucket).  The last CTA to finish also writes
 // n_condensed = (number of slots) - (representatives of every bucket); *done counts the
-// finished CTAs (zeroed by first_hit_kernel, reset here for the next call).
+// finished CTAs (zeroed by sim_tiles_kernel, reset here for the next call).
 __global__ void __launch_bounds__(kScanThreads)
     greedy_scan_kernel(const unsigned* __restrict__ bits, const long long* __restrict__ bits_base,
                        const int32_t* __restrict__ offsets, const int32_t* __restrict__ overflow,
@@ -430,59 +439,13 @@ __global__ void __launch_bounds__(kScanThreads)
 }
 
 // Rows decided without the walk.  For slot s (local row li of bucket e) let C be the rows
-// before li that its bits mark similar.  first_hit_kernel writes first[s] = min C (local),
-// or -1 when C is empty.  resolve_kernel then decides two kinds of row exactly as the walk
-// would: C empty -> a representative; m = min C with no similar row before it (m is then a
-// representative, and the earliest candidate) -> condensed onto m.  Any other row is left to
-// the walk: a bucket with such a row counts it in unresolved[e] and greedy_scan_kernel walks
-// that bucket; the other buckets are complete (n_rep from nrep_fast).  One warp per row.
-__global__ void __launch_bounds__(256)
-    first_hit_kernel(const unsigned* __restrict__ bits, const long long* __restrict__ bits_base,
-                     const int32_t* __restrict__ offsets, int E, const int32_t* __restrict__ overflow,
-                     int32_t* __restrict__ first, int32_t* __restrict__ unresolved,
-                     int32_t* __restrict__ nrep_fast, int32_t* __restrict__ done) {
-  __shared__ int off[257];
-  pdl_trigger();
-  pdl_wait();
-  for (int i = threadIdx.x; i <= E; i += blockDim.x) off[i] = offsets[i];
-  if (blockIdx.x == 0) {
-    for (int e = threadIdx.x; e < E; e += blockDim.x) unresolved[e] = nrep_fast[e] = 0;
-    if (threadIdx.x == 0) *done = 0;
-  }
-  __syncthreads();
-  if (*overflow) return;
-  const int n_rows = off[E];
-  const int lane = threadIdx.x & 31;
-  const int warps = (gridDim.x * blockDim.x) >> 5;
-  for (int sl = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; sl < n_rows; sl += warps) {
-    int lo = 0, hi = E;  // off[lo] <= sl < off[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (off[mid] <= sl) lo = mid; else hi = mid;
-    }
-    const int e = lo, li = sl - off[e], n_e = off[e + 1] - off[e];
-    const int W = (n_e + 31) >> 5;
-    const unsigned* row = bits + bits_base[e] + static_cast<long long>(li) * W;
-    const int nw = (li + 31) >> 5;  // words holding columns < li
-    int hit = -1;
-    for (int w0 = 0; w0 < nw && hit < 0; w0 += 32) {
-      const int w = w0 + lane;
-      unsigned m = 0u;
-      if (w < nw) {
-        m = row[w];
-        if (w == nw - 1 && (li & 31)) m &= (1u << (li & 31)) - 1u;  // only columns < li
-      }
-      const unsigned any = __ballot_sync(0xffffffffu, m != 0u);
-      if (any) {
-        const int src = __ffs(any) - 1;
-        const unsigned mw = __shfl_sync(0xffffffffu, m, src);
-        hit = (w0 + src) * 32 + __ffs(mw) - 1;
-      }
-    }
-    if (lane == 0) first[sl] = hit;
-  }
-}
-
+// before li that its bits mark similar.  first[s] = min C (local), or kNoHit when C is empty:
+// the similarity GEMM's epilogue and the history lookup lower it with atomicMin as they write
+// the bits.  resolve_kernel then decides two kinds of row exactly as the walk would: C empty ->
+// a representative; m = min C with no similar row before it (m is then a representative, and
+// the earliest candidate) -> condensed onto m.  Any other row is left to the walk: a bucket
+// with such a row counts it in unresolved[e] and greedy_scan_kernel walks that bucket; the
+// other buckets are complete (n_rep from nrep_fast).
 __global__ void __launch_bounds__(256)
     resolve_kernel(const int32_t* __restrict__ first, const int32_t* __restrict__ offsets, int E,
                    const int32_t* __restrict__ overflow, int32_t* __restrict__ rep_of,
@@ -510,10 +473,10 @@ __global__ void __launch_bounds__(256)
         if (off[mid] <= sl) lo = mid; else hi = mid;
       }
       const int f = first[sl];
-      if (f < 0) {
+      if (f == kNoHit) {
         rep_of[sl] = sl;
         is_rep = true;
-      } else if (first[off[lo] + f] < 0) {
+      } else if (first[off[lo] + f] == kNoHit) {
         rep_of[sl] = off[lo] + f;
       } else {
         open = true;
@@ -641,7 +604,8 @@ __global__ void __launch_bounds__(kLookupThreads)
                        const int32_t* __restrict__ perm, int T, int k, int E,
                        const long long* __restrict__ bits_base, HistView prev,
                        uint2* __restrict__ planes_out, unsigned* __restrict__ bits,
-                       int2* __restrict__ cos_list, int32_t* __restrict__ n_cos) {
+                       int32_t* __restrict__ first, int2* __restrict__ cos_list,
+                       int32_t* __restrict__ n_cos) {
   extern __shared__ int hsm[];
   int* poff = hsm;                      // [E + 1] previous offsets
   int* col_e = poff + (E + 1);          // [256][k] previous bucket of each column token's pairs
@@ -760,6 +724,7 @@ __global__ void __launch_bounds__(kLookupThreads)
             const long long w = wrow + (ljb >> 5);
             planes_out[w] = make_uint2(kw, sw);
             bits[w] = sw;
+            if (sw) atomicMin(&first[row0 + rr], ljb + __ffs(sw) - 1);
             if (kw != vmask) unknown = true;
             fast = true;
           }
@@ -805,6 +770,7 @@ __global__ void __launch_bounds__(kLookupThreads)
           const long long w = wrow + (ljb >> 5);
           planes_out[w] = make_uint2(kw, sw);
           bits[w] = sw;
+          if (sw) atomicMin(&first[row0 + rr], ljb + __ffs(sw) - 1);
         }
       }
     }
@@ -958,12 +924,10 @@ cudaError_t launch_condense_hist(const __nv_bfloat16* x_perm, const int32_t* off
                            n_condensed, scratch, status, stream, false);
 }
 
-void condense_stats_ptrs(void* scratch, int T, int k, int E, float** norm,
-                         unsigned long long** hash) {
+RowStatsOut condense_stats_ptrs(void* scratch, int T, int k, int E) {
   CondenseScratch s;
   carve(scratch, T, k, E, &s);
-  *norm = s.norm;
-  *hash = s.hash;
+  return RowStatsOut{s.norm, s.hash, s.first};
 }
 
 namespace {
@@ -1002,7 +966,7 @@ cudaError_t condense_pipeline(const __nv_bfloat16* x_perm, const int32_t* offset
   cudaError_t err = cudaSuccess;
   if (!stats_ready) {
     err = launch_pdl(row_stats_kernel, dim3(min(ceil_div(P, 8), 4096)), dim3(256), 0, stream,
-                     x_perm, offsets, E, d, s.norm, s.hash);
+                     x_perm, offsets, E, d, s.norm, s.hash, s.first);
     if (err != cudaSuccess) return err;
   }
   err = launch_build_mtiles(nullptr, offsets, 0, E, nullptr, s.mt_info, s.group_mt_begin, stream);
@@ -1011,7 +975,7 @@ cudaError_t condense_pipeline(const __nv_bfloat16* x_perm, const int32_t* offset
   err = launch_pdl(sim_tiles_kernel, dim3(1), dim3(256), 0, stream,
                    static_cast<const int4*>(s.mt_info), static_cast<const int32_t*>(s.group_mt_begin),
                    offsets, E, bucket_rows_max(T, k), s.tile_list, s.n_list, bits_base, s.overflow,
-                   h ? out.header : nullptr, status);
+                   h ? out.header : nullptr, s.unresolved, s.nrep_fast, s.done, status);
   if (err != cudaSuccess) return err;
   const int2* gemm_list = s.tile_list;
   const int32_t* gemm_n = s.n_list;
@@ -1034,7 +998,7 @@ cudaError_t condense_pipeline(const __nv_bfloat16* x_perm, const int32_t* offset
     const int max_tiles = max_mtiles(P, E) * ((bucket_rows_max(T, k) + kTcTileN - 1) / kTcTileN);
     hist_lookup_kernel<<<max(1, min(max_tiles, 8 * num_sms)), kLookupThreads, smem, stream>>>(
         s.tile_list, s.n_list, s.mt_info, offsets, h->perm, h->T, h->k, E, bits_base, prev,
-        out.planes, s.bits, s.cos_list, s.n_cos);
+        out.planes, s.bits, s.first, s.cos_list, s.n_cos);
     gemm_list = s.cos_list;
     gemm_n = s.n_cos;
     hist_mode = 2;
@@ -1067,6 +1031,7 @@ cudaError_t condense_pipeline(const __nv_bfloat16* x_perm, const int32_t* offset
   a.bits_base = bits_base;
   a.bits = s.bits;
   a.tau = tau;
+  a.first = s.first;
   a.status = status;
   err = tc_gemm(kTcSimBits, x_perm, P, d, x_perm, 1, P, d, a, num_sms, stream);
   if (err != cudaSuccess) return err;
@@ -1079,12 +1044,6 @@ cudaError_t condense_pipeline(const __nv_bfloat16* x_perm, const int32_t* offset
     return cudaFuncSetAttribute(greedy_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(smem));
   });
-  if (err != cudaSuccess) return err;
-  err = launch_pdl(first_hit_kernel, dim3(max(1, min(ceil_div(P, 8), 8 * num_sms))), dim3(256), 0,
-                   stream, static_cast<const unsigned*>(s.bits),
-                   static_cast<const long long*>(bits_base), offsets, E,
-                   static_cast<const int32_t*>(s.overflow), s.first, s.unresolved, s.nrep_fast,
-                   s.done);
   if (err != cudaSuccess) return err;
   err = launch_pdl(resolve_kernel, dim3(max(1, min(ceil_div(P, 256), 4 * num_sms))), dim3(256), 0,
                    stream, static_cast<const int32_t*>(s.first), offsets, E,

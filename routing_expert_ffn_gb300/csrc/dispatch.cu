@@ -244,7 +244,7 @@ constexpr int kScatterScanMaxEntries = 2048;
 // STATS (bf16 rows, for the condensation that follows in the same layer call): the warp also
 // forms the row's fp32 norm and 64-bit content hash while the row is in its registers, in the
 // same element order and with the same arithmetic as the condensation's own row statistics, and
-// writes them at each of the token's slots.
+// writes them at each of the token's slots (and resets the slot's earliest-similar-row entry).
 template <typename T, bool SCAN, bool STATS>
 __global__ void __launch_bounds__(256)
     scatter_rows_kernel(const T* __restrict__ x, const int32_t* __restrict__ idx,
@@ -252,8 +252,7 @@ __global__ void __launch_bounds__(256)
                         int n_blk, int E, int T_tok, int k, int d, T* __restrict__ x_perm,
                         int32_t* __restrict__ perm, int32_t* __restrict__ slot_of,
                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-                        float* __restrict__ norm_out, unsigned long long* __restrict__ hash_out,
-                        unsigned* status) {
+                        RowStatsOut stats, unsigned* status) {
   constexpr int V = Act<T>::kVec;
   const int nv = d / V;
   const int P = T_tok * k;
@@ -360,8 +359,9 @@ __global__ void __launch_bounds__(256)
       // every lane holds the sum of squares; lane 0's hash is the row's
       const unsigned long long h0 = __shfl_sync(0xffffffffu, h, 0);
       if (lane < k && slot >= 0) {
-        norm_out[slot] = sqrtf(ss);
-        hash_out[slot] = h0;
+        stats.norm[slot] = sqrtf(ss);
+        stats.hash[slot] = h0;
+        stats.first[slot] = kNoHit;
       }
     }
     if (t + warps < T_tok) load_token(t + warps);
@@ -600,7 +600,7 @@ cudaError_t launch_dispatch_auto(int act_dtype, const void* x, const int32_t* to
                                  int d, int E, int k, int32_t* counts, int32_t* offsets,
                                  int32_t* perm, int32_t* slot_of, void* x_perm, void* scratch,
                                  int num_sms, unsigned* status, cudaStream_t stream,
-                                 float* norm_out, unsigned long long* hash_out) {
+                                 const RowStatsOut* stats) {
   const long long P = static_cast<long long>(T) * k;
   if (P == 0)
     return launch_dispatch(act_dtype, x, topk_idx, T, d, E, k, counts, offsets, perm, slot_of,
@@ -628,25 +628,23 @@ cudaError_t launch_dispatch_auto(int act_dtype, const void* x, const int32_t* to
     float* xp = static_cast<float*>(x_perm);
     err = scan_in_smem ? launch_pdl(scatter_rows_kernel<float, true, false>, dim3(blocks),
                                     dim3(256), smem, stream, xf, topk_idx, local_rank, blk, n_blk,
-                                    E, T, k, d, xp, perm, slot_of, counts, offsets,
-                                    static_cast<float*>(nullptr),
-                                    static_cast<unsigned long long*>(nullptr), status)
+                                    E, T, k, d, xp, perm, slot_of, counts, offsets, RowStatsOut{},
+                                    status)
                        : launch_pdl(scatter_rows_kernel<float, false, false>, dim3(blocks),
                                     dim3(256), 0, stream, xf, topk_idx, local_rank, blk, n_blk, E,
-                                    T, k, d, xp, perm, slot_of, counts, offsets,
-                                    static_cast<float*>(nullptr),
-                                    static_cast<unsigned long long*>(nullptr), status);
+                                    T, k, d, xp, perm, slot_of, counts, offsets, RowStatsOut{},
+                                    status);
   } else {
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
     __nv_bfloat16* xp = static_cast<__nv_bfloat16*>(x_perm);
-    const bool stats = norm_out != nullptr && hash_out != nullptr;
-    auto kern = scan_in_smem ? (stats ? scatter_rows_kernel<__nv_bfloat16, true, true>
-                                      : scatter_rows_kernel<__nv_bfloat16, true, false>)
-                             : (stats ? scatter_rows_kernel<__nv_bfloat16, false, true>
-                                      : scatter_rows_kernel<__nv_bfloat16, false, false>);
+    const bool st = stats != nullptr;
+    auto kern = scan_in_smem ? (st ? scatter_rows_kernel<__nv_bfloat16, true, true>
+                                   : scatter_rows_kernel<__nv_bfloat16, true, false>)
+                             : (st ? scatter_rows_kernel<__nv_bfloat16, false, true>
+                                   : scatter_rows_kernel<__nv_bfloat16, false, false>);
     err = launch_pdl(kern, dim3(blocks), dim3(256), scan_in_smem ? smem : 0, stream, xb, topk_idx,
                      local_rank, blk, n_blk, E, T, k, d, xp, perm, slot_of, counts, offsets,
-                     norm_out, hash_out, status);
+                     st ? *stats : RowStatsOut{}, status);
   }
   if (err != cudaSuccess) return err;
   return cudaGetLastError();

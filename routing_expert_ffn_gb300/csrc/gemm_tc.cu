@@ -369,7 +369,8 @@ __device__ __forceinline__ void sim_prefetch(const TcGemmArgs& args, const TileI
 }
 
 // Epilogue of one Gram tile of the similarity GEMM for one TMEM lane: row slot i = row0 + r
-// of bucket e (valid: r < nrows), column slots j = gbase + nt * 256 + c, c < 256.
+// of bucket e (valid: r < nrows), column slots j = gbase + nt * 256 + c, c < 256.  Writes
+// the row's bit words of the tile and lowers first[i] to its earliest similar column.
 __device__ __forceinline__ void sim_epilogue(const TcGemmArgs& args, const TileInfo& t,
                                              const SimOperands& o, uint32_t col0, int r,
                                              int lane) {
@@ -395,6 +396,7 @@ __device__ __forceinline__ void sim_epilogue(const TcGemmArgs& args, const TileI
   const float tau = args.tau;
   const bool all_similar = tau <= -1.f;
   const float4* col4 = reinterpret_cast<const float4*>(o.col);
+  int hit = -1;  // earliest similar column of this tile (local index)
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
     const int lj0 = nt * BN + c * 32;
@@ -450,20 +452,23 @@ __device__ __forceinline__ void sim_epilogue(const TcGemmArgs& args, const TileI
       }
     }
     if (valid && lj0 < li) {
-      if (hmode == 0) {
-        brow[lj0 >> 5] = word;
-      } else {
+      uint32_t wout = word;
+      if (hmode != 0) {
         const long long widx = wrow + (lj0 >> 5);
         uint2 ks = make_uint2(0u, 0u);
         if (hmode == 2) ks = args.hplanes[widx];
         const uint32_t kw = ks.x, sw = ks.y;
         // a pair with a class is decided by it; the others by their cosine, and get
         // a class from it (similar first)
-        brow[lj0 >> 5] = (kw & sw) | (~kw & word);
+        wout = (kw & sw) | (~kw & word);
         args.hplanes[widx] = make_uint2(kw | (~kw & (w1 | w2)), (kw & sw) | (~kw & w1));
       }
+      brow[lj0 >> 5] = wout;
+      // the chunks run in column order: the first set bit is the tile's earliest similar row
+      if (hit < 0 && wout) hit = lj0 + __ffs(wout) - 1;
     }
   }
+  if (hit >= 0) atomicMin(&args.first[i], hit);
 }
 
 template <int MODE>

@@ -44,14 +44,21 @@ cudaError_t launch_dispatch(int act_dtype, const void* x, const int32_t* topk_id
 // Same outputs as launch_dispatch, with ranks computed in parallel blocks of
 // 1024 pairs; scratch: dispatch_auto_scratch_bytes.
 size_t dispatch_auto_scratch_bytes(int T, int k, int E);
-// norm_out / hash_out (bf16 only, both or neither): also each slot's row norm and hash, as the
-// condensation's row statistics form them (condense_stats_ptrs gives where it reads them).
+// Condensation row statistics at the slots (bf16 only): norm and hash as the condensation's
+// row-statistics pass forms them, and the earliest-similar-row entry reset to kNoHit.
+struct RowStatsOut {
+  float* norm;
+  unsigned long long* hash;
+  int32_t* first;
+};
+constexpr int32_t kNoHit = 0x7fffffff;
+// stats (nullable): the dispatch also writes each slot's row statistics (condense_stats_ptrs
+// gives where the condensation reads them).
 cudaError_t launch_dispatch_auto(int act_dtype, const void* x, const int32_t* topk_idx, int T,
                                  int d, int E, int k, int32_t* counts, int32_t* offsets,
                                  int32_t* perm, int32_t* slot_of, void* x_perm, void* scratch,
                                  int num_sms, unsigned* status, cudaStream_t stream,
-                                 float* norm_out = nullptr,
-                                 unsigned long long* hash_out = nullptr);
+                                 const RowStatsOut* stats = nullptr);
 // dst[r] = src[rows[r]] for r < *n_rows_dev (<= max_rows); rows outside [0, src_rows) are flagged.
 cudaError_t launch_gather_rows(int act_dtype, const void* src, int src_rows, const int32_t* rows,
                                const int* n_rows_dev, int max_rows, int d, void* dst,
@@ -120,6 +127,9 @@ struct TcGemmArgs {
   int hist_mode;
   uint2* hplanes;
   float s1, s2;
+  // kSimBits: earliest similar earlier row of each row (local index), lowered by atomicMin
+  // from every tile (kNoHit: none yet)
+  int32_t* first;
   unsigned* status;
   // kRouter: D = x . [W1|W2|W3] over a K range of 3*d (the three bf16 terms of W_r)
   int router_n;        // N of the MMA = E rounded up to 32
@@ -228,8 +238,7 @@ cudaError_t launch_condense(const __nv_bfloat16* x_perm, const int32_t* offsets,
                             int E, float tau, int num_sms, int32_t* rep_of, int32_t* n_rep,
                             int32_t* n_condensed, void* scratch, unsigned* status,
                             cudaStream_t stream, bool stats_ready = false);
-void condense_stats_ptrs(void* scratch, int T, int k, int E, float** norm,
-                         unsigned long long** hash);
+RowStatsOut condense_stats_ptrs(void* scratch, int T, int k, int E);
 // Condensation with the previous call's pair classes (Luffy's historical similarity).
 // The record layout is the one include/moe.h documents for moe_condense_hist.
 constexpr int kHistMagic = 0x48697374;

@@ -660,19 +660,18 @@ moe_status layer_forward_impl(const moe_config* cfg, const moe_weights* w, const
   }
   // a condensing layer has the dispatch form the slots' row norms and hashes as it moves the
   // rows, where the condensation reads them
-  float* stat_norm = nullptr;
-  unsigned long long* stat_hash = nullptr;
-  if (condense && cfg->T * cfg->k > 0)
-    condense_stats_ptrs(L.condense_ws, cfg->T, cfg->k, cfg->E, &stat_norm, &stat_hash);
+  const bool stats = condense && cfg->T * cfg->k > 0;
+  RowStatsOut rs = {};
+  if (stats) rs = condense_stats_ptrs(L.condense_ws, cfg->T, cfg->k, cfg->E);
   MOE_CUDA(launch_dispatch_auto(cfg->act_dtype, x, idx, cfg->T, cfg->d, cfg->E, cfg->k,
                                 L.counts, L.offsets, L.perm, L.slot_of, L.x_perm, L.dispatch_ws,
-                                di->num_sms, di->status, st, stat_norm, stat_hash));
+                                di->num_sms, di->status, st, stats ? &rs : nullptr));
   const int32_t* rep_of = nullptr;
   if (condense) {
     MOE_CUDA(launch_condense(static_cast<const __nv_bfloat16*>(L.x_perm), L.offsets,
                              cfg->T, cfg->k, cfg->d, cfg->E, tau, di->num_sms, L.rep_of,
                              L.n_rep, n_condensed_out ? n_condensed_out : L.n_condensed,
-                             L.condense_ws, di->status, st, stat_norm != nullptr));
+                             L.condense_ws, di->status, st, stats));
     rep_of = L.rep_of;
   } else if (n_condensed_out) {
     MOE_CUDA(cudaMemsetAsync(n_condensed_out, 0, sizeof(int32_t), st));
@@ -889,17 +888,17 @@ extern "C" moe_status moe_layer_backward(const moe_config* cfg, const moe_weight
   // forward recompute: routing, dispatch, padded slot space, [a | u], h, y
   s = run_router(cfg, x, w->W_r, w->router_bias, b.logits, b.idx, b.gate, b.route_ws, di, st);
   if (s != MOE_OK) return s;
-  float* stat_norm = nullptr;
-  unsigned long long* stat_hash = nullptr;
-  if (condense && T * k > 0) condense_stats_ptrs(b.condense_ws, T, k, E, &stat_norm, &stat_hash);
+  const bool stats = condense && T * k > 0;
+  RowStatsOut rs = {};
+  if (stats) rs = condense_stats_ptrs(b.condense_ws, T, k, E);
   MOE_CUDA(launch_dispatch_auto(cfg->act_dtype, x, b.idx, T, d, E, k, b.counts, b.offsets, b.perm,
-                                b.slot_of, b.x_perm, b.dispatch_ws, sms, di->status, st, stat_norm,
-                                stat_hash));
+                                b.slot_of, b.x_perm, b.dispatch_ws, sms, di->status, st,
+                                stats ? &rs : nullptr));
   if (condense) {
     // Luffy condensation: a condensed slot's expert input is its representative's row
     MOE_CUDA(launch_condense(static_cast<const __nv_bfloat16*>(b.x_perm), b.offsets, T, k, d, E,
                              tau, sms, b.rep_of, b.n_rep, b.n_condensed, b.condense_ws, di->status,
-                             st, stat_norm != nullptr));
+                             st, stats));
     MOE_CUDA(launch_members(b.rep_of, b.offsets, E, b.mem_off, b.mem_cnt, b.mem_list, st));
   }
   MOE_CUDA(launch_pad_counts(b.counts, E, b.pcounts, st));

@@ -43,10 +43,10 @@ def test_launch_count_claim_matches_the_launch_lists():
     """gpu_launches per step, as the committed ncu launch lists count them: 10 launches per
     DeepSeek-V2-Lite or Llama-4-Scout forward (router 3, dispatch 2, GEMMs 4, combine 1; the
     bf16 pair GEMM reads the bucket offsets itself), 9 per Qwen3-30B-A3B forward (its
-    8192-entry dispatch count table takes a scan launch of its own; no shared expert) and 17
-    per condensing Luffy-shaped forward (condensation 6: m-tiles, tile list, similarity GEMM,
-    first hits, resolve, greedy scan with the condensed count; the dispatch forms the row
-    statistics)."""
+    8192-entry dispatch count table takes a scan launch of its own; no shared expert) and 16
+    per condensing Luffy-shaped forward (condensation 5: m-tiles, tile list, similarity GEMM
+    with each row's earliest similar row, resolve, greedy scan with the condensed count; the
+    dispatch forms the row statistics)."""
     import sys
     sys.path.insert(0, ROOT)
     import bench
@@ -54,6 +54,6 @@ def test_launch_count_claim_matches_the_launch_lists():
     assert bench.launches_per_step(gen.CONFIGS["dsv2_lite"], False) == 10
     assert bench.launches_per_step(gen.CONFIGS["llama4_scout_farskip"], False) == 10
     assert bench.launches_per_step(gen.CONFIGS["qwen3_30b_a3b"], False) == 9
-    assert bench.launches_per_step(gen.CONFIGS["luffy_condense"], True) == 17
+    assert bench.launches_per_step(gen.CONFIGS["luffy_condense"], True) == 16
     # 64 tokens: FMA router (logits + top-k), no weight split
     assert bench.launches_per_step(gen.CONFIGS["dsv2_lite_decode"], False) == 9
