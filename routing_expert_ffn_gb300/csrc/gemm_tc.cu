@@ -722,10 +722,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 //           one TMA box of a 5-D view of the gate/up weights.
 //   kStore  tail A rows: the same 128 weight rows the CTA loads as B in a pair tile.
 namespace pr {
-constexpr int STAGES = 6;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = (BN / 2) * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+// A ring stage holds KSUB consecutive 64-deep K blocks (each laid out as A then B, as one
+// 32 KB block): the MMA issuer waits once and commits once per stage, for 4 x KSUB MMAs.
+constexpr int KSUB = 2;
+constexpr int SUB_BYTES = A_BYTES + B_BYTES;
+constexpr int STAGE_BYTES = KSUB * SUB_BYTES;
+constexpr int STAGES = 6 / KSUB;
 constexpr int SHARED_BYTES = 5120;
 // per epilogue warp: two {32 columns, 32 rows} bf16 TMA store boxes of 2 KB (64-byte swizzle)
 constexpr int OUT_BOX_BYTES = 32 * 32 * 2;
@@ -996,19 +1000,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool ok = true;
     for (int tile = cluster; tile < n_tiles && ok; tile += n_clusters) {
       const TileInfo t = tile_of(tile, rank);
-      for (int kb = 0; kb < args.n_kblocks; ++kb) {
+      for (int kb0 = 0; kb0 < args.n_kblocks; kb0 += pr::KSUB) {
+        const int nsub = min(pr::KSUB, args.n_kblocks - kb0);
         if (!pr::wait_bar(ptx::smem_u32(&sh->empty[stage]), phase ^ 1u, sh, args.status)) {
           ok = false;
           break;
         }
         if (lane == 0) {
           const uint32_t full = ptx::smem_u32(&sh->full[stage]) & ptx::kLeaderMask;
-          const uint32_t sa = smem0 + stage * pr::STAGE_BYTES;
+          const uint32_t sbase = smem0 + stage * pr::STAGE_BYTES;
           if (rank == 0)
-            ptx::mbar_arrive_expect_tx(full, t.tail ? pr::TAIL_TX : 2 * pr::STAGE_BYTES);
+            ptx::mbar_arrive_expect_tx(full, nsub * (t.tail ? pr::TAIL_TX : 2 * pr::SUB_BYTES));
           if (!fault_drop_loads())
-            pr::issue_kblock<MODE>(args, &tmA, &tmB, &tmA64, &tmW5, t, kb, rank, full, sa,
-                                   sa + pr::A_BYTES);
+            for (int u = 0; u < nsub; ++u) {
+              const uint32_t sa = sbase + u * pr::SUB_BYTES;
+              pr::issue_kblock<MODE>(args, &tmA, &tmB, &tmA64, &tmW5, t, kb0 + u, rank, full, sa,
+                                     sa + pr::A_BYTES);
+            }
         }
         __syncwarp();
         if (++stage == pr::STAGES) stage = 0, phase ^= 1u;
@@ -1040,20 +1048,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < args.n_kblocks; ++kb) {
+        for (int kb0 = 0; kb0 < args.n_kblocks; kb0 += pr::KSUB) {
+          const int nsub = min(pr::KSUB, args.n_kblocks - kb0);
           if (!pr::wait_bar(ptx::smem_u32(&sh->full[stage]), phase, sh, args.status)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
           if (lane == 0) {
-            const uint32_t sa = smem0 + stage * pr::STAGE_BYTES;
-            const uint64_t adesc = ptx::sw128_kmajor_desc(sa);
-            const uint64_t bdesc = ptx::sw128_kmajor_desc(sa + pr::A_BYTES);
+            for (int u = 0; u < nsub; ++u) {
+              const uint32_t sa = smem0 + stage * pr::STAGE_BYTES + u * pr::SUB_BYTES;
+              const uint64_t adesc = ptx::sw128_kmajor_desc(sa);
+              const uint64_t bdesc = ptx::sw128_kmajor_desc(sa + pr::A_BYTES);
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk)
-              ptx::umma_bf16_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc,
-                                  (kb > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < BK / 16; ++kk)
+                ptx::umma_bf16_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc,
+                                    (kb0 + u > 0 || kk > 0) ? 1u : 0u);
+            }
             ptx::umma_commit_pair(ptx::smem_u32(&sh->empty[stage]), 0x3);
           }
           __syncwarp();
