@@ -37,10 +37,14 @@ namespace moe {
 namespace bw {
 
 constexpr int BK = 64;
-constexpr int STAGES = 6;
 constexpr int A_BYTES = 128 * BK * 2;  // 16 KB
 constexpr int B_BYTES = 128 * BK * 2;  // 16 KB (N = 256); N = 128 uses half
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+// A ring stage holds KSUB consecutive K blocks (each A then B, 32 KB): the MMA issuer waits
+// once and commits once per stage.
+constexpr int KSUB = 2;
+constexpr int SUB_BYTES = A_BYTES + B_BYTES;
+constexpr int STAGE_BYTES = KSUB * SUB_BYTES;
+constexpr int STAGES = 6 / KSUB;
 constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 512;
 // per epilogue warp: 32 x 33 fp32 (gradient chunks) or two 32 x 40 bf16 tiles (kBwdDH)
@@ -473,16 +477,19 @@ __global__ void __launch_bounds__(bw::NUM_THREADS, 1)
     for (int tile = cluster; tile < n_tiles && ok; tile += n_clusters) {
       const Tile t = tile_info<MODE>(args, sh, tile, rank);
       const uint32_t TX = 2u * static_cast<uint32_t>(A_BYTES + (t.ncols / 2) * BK * 2);
-      for (int kb = 0; kb < t.n_kb; ++kb) {
+      for (int kb0 = 0; kb0 < t.n_kb; kb0 += KSUB) {
+        const int nsub = min(KSUB, t.n_kb - kb0);
         if (!wait_bar(ptx::smem_u32(&sh->empty[stage]), phase ^ 1u, sh, args.status)) {
           ok = false;
           break;
         }
         if (lane == 0) {
           const uint32_t full = ptx::smem_u32(&sh->full[stage]) & ptx::kLeaderMask;
-          const uint32_t sa = smem0 + stage * STAGE_BYTES;
-          if (rank == 0) ptx::mbar_arrive_expect_tx(full, TX);
-          bw::issue_kblock<MODE>(args, &tmA, &tmB, t, kb, rank, full, sa, sa + A_BYTES);
+          if (rank == 0) ptx::mbar_arrive_expect_tx(full, static_cast<uint32_t>(nsub) * TX);
+          for (int u = 0; u < nsub; ++u) {
+            const uint32_t sa = smem0 + stage * STAGE_BYTES + u * SUB_BYTES;
+            bw::issue_kblock<MODE>(args, &tmA, &tmB, t, kb0 + u, rank, full, sa, sa + A_BYTES);
+          }
         }
         __syncwarp();
         if (++stage == STAGES) stage = 0, phase ^= 1u;
@@ -515,20 +522,23 @@ __global__ void __launch_bounds__(bw::NUM_THREADS, 1)
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * 256;
-        for (int kb = 0; kb < t.n_kb; ++kb) {
+        for (int kb0 = 0; kb0 < t.n_kb; kb0 += KSUB) {
+          const int nsub = min(KSUB, t.n_kb - kb0);
           if (!wait_bar(ptx::smem_u32(&sh->full[stage]), phase, sh, args.status)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
           if (lane == 0) {
-            const uint32_t sa = smem0 + stage * STAGE_BYTES;
-            const uint64_t adesc = bw::desc(sa, a_lbo);
-            const uint64_t bdesc = bw::desc(sa + A_BYTES, 8192u);
+            for (int u = 0; u < nsub; ++u) {
+              const uint32_t sa = smem0 + stage * STAGE_BYTES + u * SUB_BYTES;
+              const uint64_t adesc = bw::desc(sa, a_lbo);
+              const uint64_t bdesc = bw::desc(sa + A_BYTES, 8192u);
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk)
-              ptx::umma_bf16_pair(d_tmem, adesc + a_step * kk, bdesc + b_step * kk, idesc,
-                                  (kb > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < BK / 16; ++kk)
+                ptx::umma_bf16_pair(d_tmem, adesc + a_step * kk, bdesc + b_step * kk, idesc,
+                                    (kb0 + u > 0 || kk > 0) ? 1u : 0u);
+            }
             ptx::umma_commit_pair(ptx::smem_u32(&sh->empty[stage]), 0x3);
           }
           __syncwarp();
