@@ -701,11 +701,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // The FFN GEMMs on pairs of SMs (clusters of two CTAs, tcgen05 cta_group::2).
 // A pair tile is 256 rows x 256 columns: CTA r of the pair holds rows
 // [128 r, 128 r + 128) of A and the r-th 128-row half of the B tile (gate rows
-// then up rows for the SwiGLU tile), so a stage is 32 KB per SM instead of
-// 48 KB and six stages fit.  The even (leader) CTA issues M=256 x N=256 MMAs
-// that read both CTAs' shared memory and write each CTA's own TMEM rows; each
+// then up rows for the SwiGLU tile), so a 64-deep K block is 32 KB per SM instead
+// of 48 KB.  A ring stage holds two K blocks (three stages of 64 KB): the MMA
+// issuer's barrier wait and commit, which cost the tensor pipe far more than an
+// MMA's issue, come once per 8 MMAs.  The even (leader) CTA issues M=256 x N=256
+// MMAs that read both CTAs' shared memory and write each CTA's own TMEM rows; each
 // CTA runs its own epilogue exactly as the single-CTA kernel does.
-//   full[s]       leader only; both CTAs' TMA loads complete on it (64 KB)
+//   full[s]       leader only; both CTAs' TMA loads complete on it (128 KB)
 //   empty[s]      both CTAs; the leader's MMA commit arrives on both
 //   tmem_full[a]  both CTAs; the leader's commit arrives on both
 //   tmem_empty[a] leader only; 4 epilogue warps of each CTA arrive (8)
