@@ -49,8 +49,9 @@ __device__ __forceinline__ void cp_async_wait_all() {
 }
 
 // Per dispatched row: fp32 norm and a 64-bit content hash (a filter for identical rows,
-// which are then compared element by element); resets the row's earliest-similar-row entry.  One warp per row; a lane's vectors are
-// loaded kStatBatch at a time, so their loads are in flight together.
+// which are then compared element by element); resets the row's earliest-similar-row
+// entry.  One warp per row; a lane's vectors are loaded kStatBatch at a time, so their
+// loads are in flight together.
 constexpr int kStatBatch = 4;
 __global__ void __launch_bounds__(256)
     row_stats_kernel(const __nv_bfloat16* __restrict__ rows, const int32_t* __restrict__ offsets,
