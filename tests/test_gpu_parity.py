@@ -583,6 +583,27 @@ def test_condense_tau_above_one_is_identity(moe):
     assert torch.equal(base, same)
 
 
+def test_condensed_layer_matches_the_step_by_step_calls(moe):
+    """A condensing layer call has its dispatch form the slots' row norms and hashes (its
+    condensation then skips the row-statistics pass); the step-by-step calls run that pass.
+    The two must give the same representatives, so the same output bit for bit (full-size
+    Luffy workload, both thresholds)."""
+    cfg, inp, C, w, x, r = _setup(moe, "luffy_condense")
+    layer = moe.Layer(C, w, condense=True)
+    for tau in cfg.taus:
+        n_layer = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = layer(x, r, tau, n_condensed_out=n_layer)
+        _, idx, gate = moe.route(C, x, w.W_r, w.router_bias)
+        d = moe.dispatch(C, x, idx)
+        rep_of, _, n_steps = moe.condense(C, d["x_perm"], d["offsets"], tau)
+        y, so = moe.expert_ffn(C, w, d["x_perm"], d["offsets"], rep_of=rep_of, x=x)
+        ref = moe.combine(C, y, so, d["slot_of"], rep_of, gate, x=x, residual=r)
+        torch.cuda.synchronize()
+        assert int(n_layer.item()) == int(n_steps.item()) > 0
+        assert torch.equal(out, ref), tau
+    _status_ok(moe)
+
+
 def test_condensed_layer_small(moe):
     cfg = gen.CONFIGS["luffy_condense"]
     for tau in cfg.taus:
