@@ -104,6 +104,39 @@ __device__ __forceinline__ void store_vec_f32<__nv_bfloat16>(__nv_bfloat16* p, c
   *reinterpret_cast<uint4*>(p) = v;
 }
 
+// The same with streaming cache hints (data read or written once: evict first).
+template <typename T>
+__device__ __forceinline__ void load_vec_f32_cs(const T* p, float* out);
+template <>
+__device__ __forceinline__ void load_vec_f32_cs<float>(const float* p, float* out) {
+  const float4 v = __ldcs(reinterpret_cast<const float4*>(p));
+  out[0] = v.x; out[1] = v.y; out[2] = v.z; out[3] = v.w;
+}
+template <>
+__device__ __forceinline__ void load_vec_f32_cs<__nv_bfloat16>(const __nv_bfloat16* p, float* out) {
+  uint4 v = __ldcs(reinterpret_cast<const uint4*>(p));
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 f = __bfloat1622float2(h[i]);
+    out[2 * i] = f.x; out[2 * i + 1] = f.y;
+  }
+}
+template <typename T>
+__device__ __forceinline__ void store_vec_f32_cs(T* p, const float* in);
+template <>
+__device__ __forceinline__ void store_vec_f32_cs<float>(float* p, const float* in) {
+  __stcs(reinterpret_cast<float4*>(p), make_float4(in[0], in[1], in[2], in[3]));
+}
+template <>
+__device__ __forceinline__ void store_vec_f32_cs<__nv_bfloat16>(__nv_bfloat16* p, const float* in) {
+  uint4 v;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(in[2 * i], in[2 * i + 1]);
+  __stcs(reinterpret_cast<uint4*>(p), v);
+}
+
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // Programmatic dependent launch.  Kernels of the layer are launched with

@@ -426,12 +426,12 @@ __global__ void __launch_bounds__(1024)
   pdl_trigger();
   if (inputs_ready && act) {
     if (use_x) {
-      load_vec_f32<T>(x + rowoff, tmp);
+      load_vec_f32_cs<T>(x + rowoff, tmp);
 #pragma unroll
       for (int i = 0; i < V; ++i) acc[i] += tmp[i];
     }
     if (use_r) {
-      load_vec_f32<T>(residual + rowoff, tmp);
+      load_vec_f32_cs<T>(residual + rowoff, tmp);
 #pragma unroll
       for (int i = 0; i < V; ++i) acc[i] += tmp[i];
     }
@@ -439,19 +439,19 @@ __global__ void __launch_bounds__(1024)
   pdl_wait();
   if (!inputs_ready && act) {
     if (use_x) {
-      load_vec_f32<T>(x + rowoff, tmp);
+      load_vec_f32_cs<T>(x + rowoff, tmp);
 #pragma unroll
       for (int i = 0; i < V; ++i) acc[i] += tmp[i];
     }
     if (use_r) {
-      load_vec_f32<T>(residual + rowoff, tmp);
+      load_vec_f32_cs<T>(residual + rowoff, tmp);
 #pragma unroll
       for (int i = 0; i < V; ++i) acc[i] += tmp[i];
     }
   }
   // the shared output's load is in flight while the slots are fetched
   uint4 sh = make_uint4(0u, 0u, 0u, 0u);
-  if (shared_out && act) sh = *reinterpret_cast<const uint4*>(shared_out + rowoff);
+  if (shared_out && act) sh = __ldcs(reinterpret_cast<const uint4*>(shared_out + rowoff));
   if (threadIdx.x < k) {
     int s = slot_of[static_cast<long long>(t) * k + threadIdx.x];
     if (s >= 0 && s < P && rep_of) s = rep_of[s];
@@ -476,11 +476,11 @@ __global__ void __launch_bounds__(1024)
 #pragma unroll 4
   for (int j = 0; j < k; ++j) {
     const float g = s_g[j];
-    load_vec_f32<T>(y + s_row[j] * d + static_cast<long long>(v) * V, tmp);
+    load_vec_f32_cs<T>(y + s_row[j] * d + static_cast<long long>(v) * V, tmp);
 #pragma unroll
     for (int i = 0; i < V; ++i) acc[i] = fmaf(g, tmp[i], acc[i]);
   }
-  store_vec_f32<T>(out + rowoff, acc);
+  store_vec_f32_cs<T>(out + rowoff, acc);
 }
 
 __global__ void __launch_bounds__(256)
