@@ -111,8 +111,10 @@ __global__ void __launch_bounds__(kLocalPairs)
                           unsigned* status) {
   extern __shared__ int wh_flat[];  // [kLocalPairs / 32][E]
   auto wh = [&](int w, int x) -> int& { return wh_flat[w * E + x]; };
-  pdl_trigger();
+  // The trigger follows the wait: the scatter after this kernel reads x before its own
+  // wait, and x is complete once this kernel's wait has returned.
   pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < (kLocalPairs / 32) * E; i += blockDim.x) wh_flat[i] = 0;
   __syncthreads();
@@ -259,22 +261,25 @@ __global__ void __launch_bounds__(256)
   extern __shared__ int tab[];
   __shared__ int wsum[33];
   pdl_trigger();
-  pdl_wait();
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int lane = threadIdx.x & 31;
   int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  // The first token's row chunk and its routing are loaded before the table scan, so
-  // their latency overlaps it; each later token's are loaded at the end of the previous
-  // token's iteration.
+  // The first token's row chunk is loaded before the programmatic-launch wait (x is
+  // complete when this kernel starts: dispatch_local_kernel, the kernel before it, triggers
+  // only after its own wait) and its routing right after, both before the table scan, so
+  // their latency overlaps the previous kernel's tail and the scan; each later token's are
+  // loaded at the end of the previous token's iteration.
   uint4 r[kRowChunk];
   int e = -1, lr = -1;
-  auto load_token = [&](int tok) {
+  auto load_row = [&](int tok) {
     const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<long long>(tok) * d);
 #pragma unroll
     for (int u = 0; u < kRowChunk; ++u) {
       const int v = u * 32 + lane;
       if (v < nv) r[u] = src[v];
     }
+  };
+  auto load_routing = [&](int tok) {
     e = -1;
     lr = -1;
     if (lane < k) {
@@ -283,7 +288,13 @@ __global__ void __launch_bounds__(256)
       lr = local_rank[p];
     }
   };
-  if (t < T_tok) load_token(t);
+  auto load_token = [&](int tok) {
+    load_row(tok);
+    load_routing(tok);
+  };
+  if (t < T_tok) load_row(t);
+  pdl_wait();
+  if (t < T_tok) load_routing(t);
   if (SCAN) {
     const int N = E * n_blk;
     for (int i = threadIdx.x; i < N; i += blockDim.x) tab[pad32(i)] = blk[i];
