@@ -9,20 +9,24 @@
 // condensed onto the earliest r in R with cos(x_j, x_r) >= tau, else it joins R.
 //
 // Work split:
-//   1. row_stats:   per dispatched row, fp32 L2 norm and a 64-bit content hash.
-//   2. tile list:   per bucket, the lower-triangle tiles (128 rows x 256 columns)
-//                   of its Gram matrix.
-//   3. sim tiles:   tcgen05 GEMM of the bucket against itself; the epilogue writes
-//                   bits A[i][j] = (cos >= tau) for j < i (identical rows count as
-//                   cos = 1; a zero row is otherwise dissimilar).
-//   4. greedy scan: one CTA per bucket walks the rows in order with R as a bitset;
-//                   j's candidates are A[j] & R, its representative the lowest.
-//                   Rows go 32 at a time, one per lane: a row's lowest candidate
-//                   among the representatives chosen before its group is its
-//                   answer (they all precede the group's own); only rows with none
-//                   are resolved in order against the group's new representatives,
-//                   on one 32-bit word.  Fifteen warps search a group's older words
-//                   while the group before it is being resolved.
+//   1. row_stats:   per dispatched row, fp32 L2 norm and a 64-bit content hash (inside a
+//                   condensing layer the dispatch forms them instead).
+//   2. tile list:   per bucket, the lower-triangle tiles (256 rows x 256 columns, a
+//                   pair of the bucket's m-tiles) of its Gram matrix.
+//   3. sim tiles:   tcgen05 GEMM of the bucket against itself on CTA pairs; the
+//                   epilogue writes bits A[i][j] = (cos >= tau) for j < i (identical
+//                   rows count as cos = 1; a zero row is otherwise dissimilar) and
+//                   lowers each row's earliest similar row.
+//   4. resolve:     rows with no similar row, or whose earliest similar row has none
+//                   before it, are decided at once (a warp per 32 rows, all buckets).
+//   5. greedy scan: one CTA per bucket that still has undecided rows walks the rows in
+//                   order with R as a bitset; j's candidates are A[j] & R, its
+//                   representative the lowest.  Rows go 32 at a time, one per lane: a
+//                   row's lowest candidate among the representatives chosen before its
+//                   group is its answer (they all precede the group's own); only rows
+//                   with none are resolved in order against the group's new
+//                   representatives, on one 32-bit word.  Fifteen warps search a
+//                   group's older words while the group before it is being resolved.
 // The decision cos >= tau is taken in fp32.
 #include "common.cuh"
 #include "kernels.h"
