@@ -4,11 +4,13 @@
 //
 //   D[m, n] = sum_k A[row0 + m, k] * B[slice, n0 + n, k]     (both operands K-major)
 //
-// One CTA per SM.  Warp 0 issues TMA loads into a 4-stage shared-memory ring,
-// warp 1 allocates TMEM and has one thread issue tcgen05.mma (M=128, N=256,
-// K=16) into one of two 256-column fp32 accumulators, warps 2-5 drain the
-// other accumulator through tcgen05.ld and run the epilogue, so the epilogue of
-// tile i overlaps the main loop of tile i+1.
+// One CTA per SM.  Warp 0 issues TMA loads into a shared-memory ring, warp 1
+// allocates TMEM and has one thread issue tcgen05.mma into one of two 256-column
+// fp32 accumulators, warps 2-5 drain the other accumulator through tcgen05.ld and
+// run the epilogue, so the epilogue of tile i overlaps the main loop of tile i+1.
+// The expert FFN (kSwiGLU, kStore) and the similarity tiles (kSimBits) run on CTA
+// pairs (cta_group::2, M=256 x N=256, below); the router logits (kRouter) on single
+// CTAs (M=128, a 4-stage ring).
 //
 // Epilogues:
 //   kSwiGLU  B rows are loaded as 128 gate rows then 128 up rows of the same
@@ -26,10 +28,10 @@
 //
 // Tiles.  Rows are grouped (one group per expert / bucket); a group's rows are
 // cut into 128-row m-tiles (the last one ragged; rows past the group are
-// computed but never stored).  For kSwiGLU/kStore, the linear tile index walks
-// groups in order; inside a group it walks blocks of up to 16 m-tiles, and
-// inside a block the N tiles with the m-tiles fastest, so CTAs running at the
-// same time share B tiles (weights) and A tiles (tokens) through L2.
+// computed but never stored).  For kSwiGLU/kStore the tile walk goes through the
+// groups in order and, inside a group, through blocks of units (pairs of m-tiles)
+// with the N tiles outside the units, so CTAs running at the same time share B
+// tiles (weights) and A tiles (tokens) through L2 (the pair kernel's tile_info).
 // kSimBits reads an explicit list of (pair of m-tiles, column tile).
 //
 // Every wait is bounded; on timeout the CTA records MOE_ERR_TIMEOUT, stops
