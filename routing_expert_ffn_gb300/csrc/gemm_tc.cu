@@ -103,7 +103,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Shared* 
 struct TileInfo {
   int slice;  // B slice (expert) of the m-tile
   int row0;   // first A row
-  int nrows;  // valid rows (<= 128)
+  int nrows;  // valid rows (<= 128; a tail tile's up to kMaxTailRows)
   int gbase;  // first row of the group (bucket offset)
   int nt;     // N tile (or column tile for kSimBits)
   int tail = 0;  // CTA-pair kernel: 1 for a tail tile (weights as M, the m-tile's rows as N)
@@ -283,7 +283,7 @@ __device__ __forceinline__ void ffn_epilogue_tma(const TcGemmArgs& args, const T
 
 // Tail tile of the CTA-pair kernel: the accumulator is transposed, TMEM lane =
 // weight row of this CTA's 128-row half of the N tile, column = token of the
-// tail (t.nrows <= 128 of them).  Warp quarter q holds lanes [32q, 32q + 32).
+// tail (t.nrows <= kMaxTailRows of them).  Warp quarter q holds lanes [32q, 32q + 32).
 //   kSwiGLU  lanes 32q + j (j < 16) are gate rows and lanes 32q + 16 + j the up
 //            rows of hidden unit 64 rank + 16 q + j of the tile, so a lane and
 //            its partner 16 apart swap half of each 32-token chunk: the low lane
@@ -713,14 +713,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 //   empty[s]      both CTAs; the leader's MMA commit arrives on both
 //   tmem_full[a]  both CTAs; the leader's commit arrives on both
 //   tmem_empty[a] leader only; 4 epilogue warps of each CTA arrive (8)
-// A pair tile is two consecutive m-tiles of one group.  When a group ends in a
-// single m-tile (1 to 128 rows left after its pairs), that m-tile runs as a
-// tail tile with the roles of the operands swapped: A is the 256 weight rows
-// of the N tile (128 per CTA), B is the left-over rows (N = their count
-// rounded up to 16, half in each CTA), so D is transposed in TMEM.  An MMA
-// issue costs about the same for any N, so the tail saves no tensor time; it
-// saves the load of the pair's second 128 token rows (its tokens come in one
-// 64-row box per CTA), which in a pair would be rows past the group's end.
+// A pair tile is two consecutive m-tiles of one group.  When a group's rows after its
+// full pairs are at most kMaxTailRows (192), they run as a tail tile with the roles of
+// the operands swapped: A is the 256 weight rows of the N tile (128 per CTA), B is the
+// left-over rows (N = their count rounded up to 16, half in each CTA, one 64- or
+// 128-row box), so D is transposed in TMEM.  The tail's MMAs cost in proportion to
+// its rows, where a partial pair's cost a full 256; and it loads no token rows past
+// the group's end.  More rows left than that run as one more (partial) pair.
 //   kSwiGLU tail A rows, per CTA: for q = 0..3, 16 gate rows then 16 up rows
 //           of hidden units 64 rank + 16 q + [0, 16) of the tile (tail_epilogue),
 //           one TMA box of a 5-D view of the gate/up weights.
@@ -747,9 +746,17 @@ static_assert((STAGES * STAGE_BYTES + SHARED_BYTES) % 1024 == 0, "output boxes 1
 // read 1.84x the DRAM bytes.
 constexpr int kUnitGroup = 8;
 constexpr int TAIL_ROWS = BM / 2;  // token rows a CTA loads for a tail tile (box height)
+// Rows left after a group's full pairs that run as a tail tile (weights as M, the rows as N,
+// so its MMAs cost in proportion to the rows) rather than as a partial pair: up to 192;
+// a tail of more than 128 rows loads its half of them with the 128-row box.
+constexpr int kMaxTailRows = 192;
 constexpr int TAIL_W_ROWS = 16;    // hidden units per gate (or up) run of a kSwiGLU tail
 constexpr int TAIL_TX = 2 * (A_BYTES + TAIL_ROWS * BK * 2);  // both CTAs, one K block
+constexpr int TAIL_TX_BIG = 2 * (A_BYTES + BM * BK * 2);      // the same with the 128-row box
 static_assert(TAIL_ROWS * BK * 2 <= B_BYTES, "tail tokens fit the B region");
+static_assert(kMaxTailRows <= 2 * BM && BM * BK * 2 <= B_BYTES, "a big tail's half fits the B region");
+// Token rows each CTA of the pair provides for a tail tile of n rows (N = n rounded up to 16).
+__host__ __device__ constexpr int tail_half(int n) { return ((n + 15) & ~15) >> 1; }
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 
 struct Shared {
@@ -763,7 +770,7 @@ struct Shared {
   int goff[257];   // first row of each group
   int grows[256];  // rows of each group
   int gub[257];    // first unit (pair or tail) of each group
-  int gpt[256];    // pairs of each group | rows of its tail (0..128) << 16
+  int gpt[256];    // pairs of each group | rows of its tail (0..kMaxTailRows) << 16
 };
 static_assert(sizeof(Shared) <= SHARED_BYTES, "pair kernel barriers and tables");
 
@@ -869,8 +876,9 @@ __device__ __forceinline__ void issue_kblock(const TcGemmArgs& args, const CUten
   const int nslice = t.nt / args.nt_per_slice;
   const int z = t.slice + nslice + kslice;
   if (t.tail) {
-    const int half = ((t.nrows + 15) & ~15) >> 1;
-    ptx::tma_load_2d_pair(sb, tmA64, full, kb * BK, t.row0 + static_cast<int>(rank) * half);
+    const int half = tail_half(t.nrows);
+    ptx::tma_load_2d_pair(sb, half <= TAIL_ROWS ? tmA64 : tmA, full, kb * BK,
+                          t.row0 + static_cast<int>(rank) * half);
   } else {
     ptx::tma_load_2d_pair(sa, tmA, full, kb * BK, t.row0);
   }
@@ -956,9 +964,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         rows = (e - b - 1) * BM + args.mt_info[e - 1].z;
       }
     }
-    const int m = (rows + BM - 1) / BM;
-    const int np = m >> 1;
-    const int tail_rows = (m & 1) ? rows - np * 2 * BM : 0;
+    // full pairs, then the rows left: up to kMaxTailRows run as a tail tile (its MMA's N is
+    // their count), more as one more (partial) pair
+    const int full = rows / (2 * BM);
+    const int left = rows - full * 2 * BM;
+    const bool as_tail = left > 0 && left <= pr::kMaxTailRows;
+    const int np = full + (left > 0 && !as_tail ? 1 : 0);
+    const int tail_rows = as_tail ? left : 0;
     sh->goff[g] = off;
     sh->grows[g] = rows;
     sh->gpt[g] = np | (tail_rows << 16);
@@ -1014,7 +1026,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t full = ptx::smem_u32(&sh->full[stage]) & ptx::kLeaderMask;
           const uint32_t sbase = smem0 + stage * pr::STAGE_BYTES;
           if (rank == 0)
-            ptx::mbar_arrive_expect_tx(full, nsub * (t.tail ? pr::TAIL_TX : 2 * pr::SUB_BYTES));
+            ptx::mbar_arrive_expect_tx(
+                full, nsub * (!t.tail                           ? 2 * pr::SUB_BYTES
+                              : pr::tail_half(t.nrows) <= pr::TAIL_ROWS ? pr::TAIL_TX
+                                                                        : pr::TAIL_TX_BIG));
           if (!fault_drop_loads())
             for (int u = 0; u < nsub; ++u) {
               const uint32_t sa = sbase + u * pr::SUB_BYTES;
