@@ -150,9 +150,9 @@ def work(cfg, n_condensed: int = 0, active_experts: int | None = None) -> dict:
 
 
 def launches_per_step(cfg, condense: bool) -> int:
-    # router: bf16 layers above 256 tokens split W_r into bf16 terms, run the tensor-core
-    # logits and the top-k; fp32 layers and small batches run FMA logits and the top-k
-    n = 3 if cfg.dtype == "bf16" and cfg.T > 256 else 2
+    # router: bf16 layers split W_r into bf16 terms, run the tensor-core logits and the
+    # top-k; fp32 layers run FMA logits and the top-k
+    n = 3 if cfg.dtype == "bf16" else 2
     # dispatch: block ranks and row scatter; the (expert, 1024-pair block) count table is
     # scanned inside the scatter up to 2048 entries, by a launch of its own above that
     n += 2 + (cfg.E * -(-(cfg.T * cfg.k) // 1024) > 2048)

@@ -20,14 +20,6 @@ size_t router_scratch_bytes(int T, int d, int E, int num_sms);
 cudaError_t launch_router_tc(const void* x, const float* W_r, int T, int d, int E, int num_sms,
                              void* scratch, const float** part, int* n_split, int* ld,
                              unsigned* status, cudaStream_t stream);
-// Few tokens (T <= kRouterSmallT): fp32 FMA split over d/64 K ranges instead
-// (the tensor-core path's fixed cost -- splitting W_r, a GEMM of a single
-// m-tile -- dominates there).  Partials [n_split][T][E] in scratch.
-constexpr int kRouterSmallT = 256;
-bool router_small_t(int T);
-cudaError_t launch_router_simt_split(const void* x, const float* W_r, int T, int d, int E,
-                                     void* scratch, const float** part, int* n_split, int* ld,
-                                     cudaStream_t stream);
 // logits[t,e] = sum_s part[s][t][e] (s in order) + bias[e]; then top-k and gates.
 // logits_out may be NULL (or equal to part when n_split == 1 and bias == NULL).
 cudaError_t launch_router_topk(const float* part, int n_split, int ld, const float* bias,

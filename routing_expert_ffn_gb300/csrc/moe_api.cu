@@ -280,12 +280,9 @@ moe_status run_router(const moe_config* c, const void* x, const float* W_r, cons
   if (c->act_dtype == MOE_BF16) {
     const float* part = nullptr;
     int n_split = 0, ld = 0;
-    if (router_small_t(c->T))
-      MOE_CUDA(launch_router_simt_split(x, W_r, c->T, c->d, c->E, ws, &part, &n_split, &ld, st));
-    else
-      MOE_CUDA(launch_router_tc(x, W_r, c->T, c->d, c->E,
-                                di->num_sms < kMaxSmsForSizing ? di->num_sms : kMaxSmsForSizing,
-                                ws, &part, &n_split, &ld, di->status, st));
+    MOE_CUDA(launch_router_tc(x, W_r, c->T, c->d, c->E,
+                              di->num_sms < kMaxSmsForSizing ? di->num_sms : kMaxSmsForSizing,
+                              ws, &part, &n_split, &ld, di->status, st));
     MOE_CUDA(launch_router_topk(part, n_split, ld, bias, logits, idx, gate, c->T, c->E, c->k,
                                 c->gating, st));
   } else {

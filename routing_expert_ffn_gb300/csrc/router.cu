@@ -262,22 +262,6 @@ cudaError_t launch_router_logits(int act_dtype, const void* x, const float* W_r,
                          stream);
 }
 
-bool router_small_t(int T) { return T <= kRouterSmallT; }
-
-int router_simt_splits(int d) { return d % 64 == 0 ? d / 64 : 1; }
-
-cudaError_t launch_router_simt_split(const void* x, const float* W_r, int T, int d, int E,
-                                     void* scratch, const float** part_out, int* n_split,
-                                     int* ld, cudaStream_t stream) {
-  const int splits = router_simt_splits(d);
-  float* part = static_cast<float*>(scratch);
-  *part_out = part;
-  *n_split = splits;
-  *ld = E;
-  return logits_dispatch(static_cast<const __nv_bfloat16*>(x), W_r, nullptr, part, T, d, E,
-                         splits, stream);
-}
-
 cudaError_t launch_router_topk(const float* part, int n_split, int ld, const float* bias,
                                float* logits_out, int32_t* topk_idx, float* topk_gate, int T,
                                int E, int k, int gating, cudaStream_t stream) {
@@ -294,11 +278,13 @@ int router_n_pad(int E) { return ceil_div(E, 32) * 32; }
 static bool router_stacked(int E) { return 3 * router_n_pad(E) <= 256; }
 
 // K splits: the largest divisor of the K blocks (d/64 with the terms side by side, else
-// 3d/64) that keeps the tile count (m-tiles x splits) within one wave of CTAs.
+// 3d/64) that keeps the tile count (m-tiles x splits) within one wave of CTAs, and at most
+// 8, so that the top-k kernel adds few partials (a batch of a few m-tiles would otherwise
+// take one split per K block).
 int router_splits(int T, int d, int E, int num_sms) {
   const int kb = (router_stacked(E) ? 1 : 3) * (d / kTcTileK);
   const int mtiles = ceil_div(T, kMTile);
-  const int target = max(1, num_sms / max(1, mtiles));
+  const int target = max(1, min(8, num_sms / max(1, mtiles)));
   int best = 1;
   for (int s = 1; s <= min(kb, target); ++s)
     if (kb % s == 0) best = s;
@@ -306,8 +292,6 @@ int router_splits(int T, int d, int E, int num_sms) {
 }
 
 size_t router_scratch_bytes(int T, int d, int E, int num_sms) {
-  if (router_small_t(T))
-    return static_cast<size_t>(router_simt_splits(d)) * T * E * sizeof(float);
   const size_t n_pad = router_n_pad(E);
   const size_t w3 = (3 * n_pad * d * sizeof(__nv_bfloat16) + 255) & ~size_t(255);
   const size_t part =
