@@ -753,15 +753,27 @@ constexpr int kMaxTailRows = 192;
 constexpr int TAIL_W_ROWS = 16;    // hidden units per gate (or up) run of a kSwiGLU tail
 constexpr int TAIL_TX = 2 * (A_BYTES + TAIL_ROWS * BK * 2);  // both CTAs, one K block
 constexpr int TAIL_TX_BIG = 2 * (A_BYTES + BM * BK * 2);      // the same with the 128-row box
+// Launches whose every group is a tail of at most 128 rows (batches of at most 128 tokens):
+// a K block needs only the weights and a 64-row token box, 24 KB, so four stages of two K
+// blocks fit where three of the general layout do.
+constexpr int TAIL_SUB_BYTES = A_BYTES + TAIL_ROWS * BK * 2;
+constexpr int STAGES_TAILS = 4;
+static_assert(STAGES_TAILS * KSUB * TAIL_SUB_BYTES == STAGES * STAGE_BYTES, "one layout size");
+static_assert(TAIL_SUB_BYTES % 1024 == 0, "1024-byte aligned K blocks");
+template <bool TAILS> __host__ __device__ constexpr int sub_bytes() { return TAILS ? TAIL_SUB_BYTES : SUB_BYTES; }
+template <bool TAILS> __host__ __device__ constexpr int n_stages() { return TAILS ? STAGES_TAILS : STAGES; }
 static_assert(TAIL_ROWS * BK * 2 <= B_BYTES, "tail tokens fit the B region");
+static_assert(TAIL_ROWS == kTailOnlyRows, "tails-only launches hold tails of 2 x TAIL_ROWS rows");
 static_assert(kMaxTailRows <= 2 * BM && BM * BK * 2 <= B_BYTES, "a big tail's half fits the B region");
 // Token rows each CTA of the pair provides for a tail tile of n rows (N = n rounded up to 16).
 __host__ __device__ constexpr int tail_half(int n) { return ((n + 15) & ~15) >> 1; }
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 
+constexpr int MAX_STAGES = STAGES_TAILS > STAGES ? STAGES_TAILS : STAGES;
+
 struct Shared {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint64_t drain;
@@ -899,7 +911,7 @@ __device__ __forceinline__ void issue_kblock(const TcGemmArgs& args, const CUten
 }
 }  // namespace pr
 
-template <int MODE>
+template <int MODE, bool TAILS>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                              const __grid_constant__ CUtensorMap tmB,
@@ -909,14 +921,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  pr::Shared* sh = reinterpret_cast<pr::Shared*>(smem + pr::STAGES * pr::STAGE_BYTES);
+  constexpr int NS = pr::n_stages<TAILS>();
+  constexpr int SUBB = pr::sub_bytes<TAILS>();
+  constexpr int SB = pr::KSUB * SUBB;
+  pr::Shared* sh = reinterpret_cast<pr::Shared*>(smem + NS * SB);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();
   const uint32_t smem0 = ptx::smem_u32(smem);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < pr::STAGES; ++s) {
+    for (int s = 0; s < NS; ++s) {
       ptx::mbar_init(ptx::smem_u32(&sh->full[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&sh->empty[s]), 1);
     }
@@ -973,6 +988,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int tail_rows = as_tail ? left : 0;
     sh->goff[g] = off;
     sh->grows[g] = rows;
+    // a tails-only launch takes no pair and no tail of more than 128 rows (the host picks it
+    // for batches of at most 128 tokens; any other offsets are refused below)
+    if (TAILS && (np > 0 || tail_rows > 2 * pr::TAIL_ROWS)) sh->abort_flag = 1;
     sh->gpt[g] = np | (tail_rows << 16);
     sh->gub[g] = np + (tail_rows > 0 ? 1 : 0);  // units, turned into offsets below
   }
@@ -1003,7 +1021,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   __syncthreads();
   const uint32_t tmem_base = sh->tmem_base;
-  const int n_tiles = MODE == kSimBits ? *args.n_list : sh->gub[args.n_groups] * args.n_ntiles;
+  int n_tiles = MODE == kSimBits ? *args.n_list : sh->gub[args.n_groups] * args.n_ntiles;
+  if (TAILS && sh->abort_flag) {
+    // offsets this layout cannot take: no tile runs, the status word says why
+    if (threadIdx.x == 0) record_status(args.status, MOE_ERR_DEVICE_INDEX);
+    n_tiles = 0;
+  }
   const int cluster = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
   auto tile_of = [&](int tile, uint32_t r) {
     return MODE == kSimBits ? pr::sim_tile_info(args, tile, r) : pr::tile_info(args, sh, tile, r);
@@ -1024,7 +1047,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (lane == 0) {
           const uint32_t full = ptx::smem_u32(&sh->full[stage]) & ptx::kLeaderMask;
-          const uint32_t sbase = smem0 + stage * pr::STAGE_BYTES;
+          const uint32_t sbase = smem0 + stage * SB;
           if (rank == 0)
             ptx::mbar_arrive_expect_tx(
                 full, nsub * (!t.tail                           ? 2 * pr::SUB_BYTES
@@ -1032,13 +1055,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                                                         : pr::TAIL_TX_BIG));
           if (!fault_drop_loads())
             for (int u = 0; u < nsub; ++u) {
-              const uint32_t sa = sbase + u * pr::SUB_BYTES;
+              const uint32_t sa = sbase + u * SUBB;
               pr::issue_kblock<MODE>(args, &tmA, &tmB, &tmA64, &tmW5, t, kb0 + u, rank, full, sa,
                                      sa + pr::A_BYTES);
             }
         }
         __syncwarp();
-        if (++stage == pr::STAGES) stage = 0, phase ^= 1u;
+        if (++stage == NS) stage = 0, phase ^= 1u;
       }
     }
     if (!ok) {
@@ -1076,7 +1099,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ptx::tc_fence_after();
           if (lane == 0) {
             for (int u = 0; u < nsub; ++u) {
-              const uint32_t sa = smem0 + stage * pr::STAGE_BYTES + u * pr::SUB_BYTES;
+              const uint32_t sa = smem0 + stage * SB + u * SUBB;
               const uint64_t adesc = ptx::sw128_kmajor_desc(sa);
               const uint64_t bdesc = ptx::sw128_kmajor_desc(sa + pr::A_BYTES);
 #pragma unroll
@@ -1087,7 +1110,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::umma_commit_pair(ptx::smem_u32(&sh->empty[stage]), 0x3);
           }
           __syncwarp();
-          if (++stage == pr::STAGES) stage = 0, phase ^= 1u;
+          if (++stage == NS) stage = 0, phase ^= 1u;
         }
         if (!ok) break;
         if (lane == 0) ptx::umma_commit_pair(ptx::smem_u32(&sh->tmem_full[acc]), 0x3);
@@ -1108,7 +1131,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int r = q * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     // full quarters store through TMA boxes, except a down projection with remapped rows
-    uint8_t* out_stage = smem + pr::STAGES * pr::STAGE_BYTES + pr::SHARED_BYTES +
+    uint8_t* out_stage = smem + NS * SB + pr::SHARED_BYTES +
                          (warp - 2) * 2 * pr::OUT_BOX_BYTES;
     const bool tma_out = MODE == kSwiGLU || args.out_rowmap == nullptr;
     uint32_t nstore = 0;
@@ -1214,7 +1237,7 @@ static bool make_out_map(CUtensorMap* m, const void* base, uint64_t inner, uint6
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE>
+template <int MODE, bool TAILS>
 static cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& a64,
                                const CUtensorMap& w5, const CUtensorMap& o, const TcGemmArgs& args,
                                int num_sms,
@@ -1225,7 +1248,7 @@ static cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const
   cudaGetDevice(&dev);
   cudaLaunchConfig_t cfg = {};
   const cudaError_t set_up = once.run(dev, [&]() -> cudaError_t {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<MODE>,
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<MODE, TAILS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          pr::SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -1241,7 +1264,8 @@ static cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const
     cfg.attrs = &ca;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<MODE>, &cfg) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<MODE, TAILS>, &cfg) !=
+            cudaSuccess ||
         n <= 0)
       n = num_sms / 2;
     if (dev < 64) max_clusters[dev] = n;
@@ -1264,7 +1288,7 @@ static cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<MODE>, a, b, a64, w5, o, args);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<MODE, TAILS>, a, b, a64, w5, o, args);
 }
 
 template <int MODE>
@@ -1319,11 +1343,15 @@ cudaError_t tc_gemm(int mode, const void* A, long long a_rows, int K, const void
     return cudaErrorInvalidValue;
   switch (mode) {
     case tc::kSwiGLU:
-      return tc::launch_pair<tc::kSwiGLU>(ma, mb, ma64, mw5, mo, args, grid, stream);
+      return args.tails_only
+                 ? tc::launch_pair<tc::kSwiGLU, true>(ma, mb, ma64, mw5, mo, args, grid, stream)
+                 : tc::launch_pair<tc::kSwiGLU, false>(ma, mb, ma64, mw5, mo, args, grid, stream);
     case tc::kStore:
-      return tc::launch_pair<tc::kStore>(ma, mb, ma64, mw5, mo, args, grid, stream);
+      return args.tails_only
+                 ? tc::launch_pair<tc::kStore, true>(ma, mb, ma64, mw5, mo, args, grid, stream)
+                 : tc::launch_pair<tc::kStore, false>(ma, mb, ma64, mw5, mo, args, grid, stream);
     case tc::kSimBits:
-      return tc::launch_pair<tc::kSimBits>(ma, mb, ma64, mw5, mo, args, grid, stream);
+      return tc::launch_pair<tc::kSimBits, false>(ma, mb, ma64, mw5, mo, args, grid, stream);
     case tc::kRouter: return tc::launch<tc::kRouter>(ma, mb, args, grid, stream);
   }
   return cudaErrorInvalidValue;

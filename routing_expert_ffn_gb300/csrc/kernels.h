@@ -98,6 +98,10 @@ struct TcGemmArgs {
   // pair kernel: units (pair or tail tiles) per block of the tile walk; a block sweeps every
   // N tile with its units fastest (0 = the default, 8)
   int unit_group;
+  // pair kernel (kSwiGLU, kStore): every group is a tail of at most 128 rows (a batch of at
+  // most 128 tokens), so the ring takes the tails-only layout (four stages); offsets that
+  // break this are refused (MOE_ERR_DEVICE_INDEX, no tile runs)
+  int tails_only;
   int kb_per_slice;  // K blocks per B slice (the shared down projection spans slices along K)
   int nt_per_slice;  // N tiles per B slice (the shared gate/up projection spans slices along N)
   int b_up_offset;   // kSwiGLU: row of the first up-projection row inside a B slice (= H)
@@ -137,6 +141,8 @@ enum TcMode { kTcSwiGLU = 0, kTcStore = 1, kTcSimBits = 2, kTcRouter = 3 };
 cudaError_t tc_gemm(int mode, const void* A, long long a_rows, int K, const void* B, int b_slices,
                     int b_rows, int b_cols, const TcGemmArgs& args, int grid, cudaStream_t stream);
 constexpr int kTcTileN = 256;
+// half the largest tail a tails-only pair launch takes (tails of at most 128 rows)
+constexpr int kTailOnlyRows = 64;
 constexpr int kTcTileK = 64;
 
 // ------------------------------------------------------------------ backward GEMMs (gemm_bwd.cu)

@@ -170,6 +170,8 @@ moe_status run_routed_ffn(const moe_config* c, const moe_weights* w, const void*
     a.group_mt_begin = s.gmb_routed;
     a.group_off = rep_of ? nullptr : offsets;
     a.n_groups = E;
+    // a bucket holds each token at most once: with at most 128 tokens every group is a tail
+    a.tails_only = T <= 2 * kTailOnlyRows ? 1 : 0;
     a.n_ntiles = H / 128;
     a.nt_per_slice = H / 128;
     a.n_kblocks = d / kTcTileK;
@@ -214,6 +216,7 @@ moe_status run_shared_ffn(const moe_config* c, const moe_weights* w, const void*
     b.status = di->status;
     b.fixed_rows = T;  // one group of all T tokens
     b.n_groups = 1;
+    b.tails_only = T <= 2 * kTailOnlyRows ? 1 : 0;
     b.n_ntiles = S * Hs / 128;
     b.nt_per_slice = Hs / 128;
     b.n_kblocks = d / kTcTileK;

@@ -295,7 +295,7 @@ def test_layer_max_experts_and_k(moe, E, k):
     _status_ok(moe)
 
 
-@pytest.mark.parametrize("T", [1, 2, 127, 129, 777])
+@pytest.mark.parametrize("T", [1, 2, 127, 128, 129, 777])
 def test_layer_ragged_token_counts(moe, T):
     _layer_check(moe, "dsv2_lite", T=T)
     _layer_check(moe, "tiny_fp32", T=min(T, 256))
