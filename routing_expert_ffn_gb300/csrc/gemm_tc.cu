@@ -1078,6 +1078,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
+      // the next ring stage's full barrier, tested before this stage's MMAs are issued: a
+      // blocking wait on a barrier that has already completed holds the issuer about 200
+      // cycles, during which the tensor pipe runs dry
+      uint32_t next_ready = 0;
       for (int tile = cluster; tile < n_tiles && ok; tile += n_clusters, ++local) {
         const TileInfo t = tile_of(tile, 0);
         const uint32_t idesc =
@@ -1092,11 +1096,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kb0 = 0; kb0 < args.n_kblocks; kb0 += pr::KSUB) {
           const int nsub = min(pr::KSUB, args.n_kblocks - kb0);
-          if (!pr::wait_bar(ptx::smem_u32(&sh->full[stage]), phase, sh, args.status)) {
+          if (!next_ready &&
+              !pr::wait_bar(ptx::smem_u32(&sh->full[stage]), phase, sh, args.status)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
+          {
+            const int ns = stage + 1 == NS ? 0 : stage + 1;
+            next_ready = ptx::mbar_test_wait(ptx::smem_u32(&sh->full[ns]), ns ? phase : phase ^ 1u);
+          }
           if (lane == 0) {
             for (int u = 0; u < nsub; ++u) {
               const uint32_t sa = smem0 + stage * SB + u * SUBB;
