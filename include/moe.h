@@ -243,7 +243,11 @@ moe_status moe_condense_hist(const moe_config* cfg, const void* x_perm, const in
  * fp32 layers run fp32 FMA.  With rep_of non-NULL only representative slots
  * are computed and y is written at those slots only (a condensed slot reads
  * its representative's row).  With n_shared > 0 the shared experts run on all
- * T rows of x and shared_out[t] = sum over shared experts.
+ * T rows of x and shared_out[t] = sum over shared experts.  offsets are as
+ * moe_dispatch writes them: non-decreasing from 0 to T*k, each bucket holding
+ * a token at most once (at most T rows).  A bf16 batch of at most 128 tokens
+ * checks the last on the device: a larger bucket makes the routed GEMM compute
+ * nothing and set MOE_ERR_DEVICE_INDEX.
  *   x_perm [T*k, d] act (in)  offsets [E+1] (in)  rep_of [T*k] or NULL (in)
  *   x [T, d] act (in, used when n_shared > 0)
  *   y_perm [T*k, d] act (out)  shared_out [T, d] act (out, NULL when n_shared == 0) */

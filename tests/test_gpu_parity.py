@@ -159,13 +159,15 @@ def test_expert_ffn_full_size(moe, name):
 
 
 # Group sizes around every tile boundary of the expert GEMMs: empty, one row, and one short of,
-# at and one past 16, 128, 256, 384 and 512 rows, so that every way a group splits into
-# 256-row pair tiles and tail tiles of at most 128 rows (N rounded up to 16) occurs.
-GROUP_SIZES = [0, 1, 15, 16, 17, 127, 128, 129, 255, 256, 257, 383, 384, 385, 511, 512, 513, 200]
+# at and one past 16, 128, 192, 256, 384, 448 and 512 rows, so that every way a group splits
+# into 256-row pair tiles and tail tiles of at most 192 rows (N rounded up to 16; a tail of more
+# than 128 rows loads its halves with the 128-row box) occurs.
+GROUP_SIZES = [0, 1, 15, 16, 17, 127, 128, 129, 191, 192, 193, 255, 256, 257, 383, 384, 385,
+               447, 448, 449, 511, 512, 513, 200]
 
 
 def test_expert_ffn_group_sizes_every_row(moe):
-    T = 700
+    T = 1100
     cfg, inp, C, w, x, r = _setup(moe, "dsv2_lite", T=T)
     P = cfg.P
     sizes = GROUP_SIZES + [0] * (cfg.E - len(GROUP_SIZES))
@@ -186,6 +188,60 @@ def test_expert_ffn_group_sizes_every_row(moe):
         ref = orc.swiglu_expert(rows[sl], inp["W_gu"][e], inp["W_down"][e])
         err = harness.max_rel_err(yg[sl], ref)
         assert err <= harness.tolerance(cfg), (e, n, err)
+    _status_ok(moe)
+
+
+def test_expert_ffn_tails_only_batch_every_row(moe):
+    """A batch of at most 128 tokens: every group (and the shared experts' one group of T rows)
+    is a single tail tile, which the GEMM runs with its tails-only ring layout.  Group sizes
+    around the 16-row N steps and the 64-row token box, up to T; every slot and every shared
+    row against the oracle."""
+    T = 128
+    cfg, inp, C, w, x, r = _setup(moe, "dsv2_lite", T=T)
+    P = cfg.P
+    head = [0, 1, 15, 16, 17, 63, 64, 65, 127, 128, 31, 33, 0, 96, 112]
+    sizes = head + [0] * (cfg.E - len(head))
+    rest = P - sum(head)
+    for e in range(len(head), cfg.E):  # the remaining rows in groups of at most T
+        sizes[e] = min(T, rest)
+        rest -= sizes[e]
+    assert rest == 0 and max(sizes) <= T
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    _, rows_inp = harness.workload("dsv2_lite", P)
+    rows = rows_inp["x"]
+    x_perm = torch.from_numpy(rows).to(device=x.device, dtype=C.torch_dtype)
+    off_d = torch.from_numpy(offsets).to(x.device)
+    y, so = moe.expert_ffn(C, w, x_perm, off_d, None, x)
+    torch.cuda.synchronize()
+    yg = _np(y)
+    for e, n in enumerate(sizes):
+        if n == 0:
+            continue
+        sl = slice(int(offsets[e]), int(offsets[e + 1]))
+        ref = orc.swiglu_expert(rows[sl], inp["W_gu"][e], inp["W_down"][e])
+        err = harness.max_rel_err(yg[sl], ref)
+        assert err <= harness.tolerance(cfg), (e, n, err)
+    ref_s = orc.shared_experts(inp["x"], inp["Ws_gu"], inp["Ws_down"])
+    assert harness.max_rel_err(_np(so), ref_s) <= harness.tolerance(cfg)
+    _status_ok(moe)
+
+
+def test_expert_ffn_small_batch_refuses_oversized_bucket(moe):
+    """Offsets that no dispatch writes (a bucket of more rows than the batch has tokens) on a
+    batch of at most 128 tokens: the routed GEMM refuses them on the device, computes no tile
+    and reports MOE_ERR_DEVICE_INDEX; the next valid call is unaffected."""
+    T = 100
+    cfg, inp, C, w, x, r = _setup(moe, "dsv2_lite", T=T)
+    P = cfg.P
+    sizes = [200, P - 200] + [0] * (cfg.E - 2)
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    _, rows_inp = harness.workload("dsv2_lite", P)
+    x_perm = torch.from_numpy(rows_inp["x"]).to(device=x.device, dtype=C.torch_dtype)
+    y, _ = moe.expert_ffn(C, w, x_perm, torch.from_numpy(offsets).to(x.device), None, x)
+    torch.cuda.synchronize()
+    assert moe.get_device_status() == 6  # MOE_ERR_DEVICE_INDEX
+    assert not torch.any(y != 0).item()  # no routed tile ran
+    _layer_check(moe, "dsv2_lite", T=T)
     _status_ok(moe)
 
 
