@@ -11,6 +11,7 @@ the kernels are deterministic, so the same inputs give the same error on every r
 """
 from __future__ import annotations
 
+import math
 from dataclasses import replace
 
 import numpy as np
@@ -164,3 +165,32 @@ def test_backward_deterministic(moe):
     torch.cuda.synchronize()
     for key in ("d_x", "dW_r", "dW_gu", "dW_down", "dWs_gu", "dWs_down"):
         assert torch.equal(a[key], b[key]), key
+
+
+@pytest.mark.parametrize("condense", [False, True])
+def test_backward_poisoned_workspace(moe, condense):
+    """Every byte of the backward's scratch set to 0xFF before the call (NaN in every float, -1
+    in every index) gives the same gradient bits as a zeroed workspace, and every gradient
+    element is written (the gradient buffers start as NaN)."""
+    if condense:
+        cfg = replace(gen.CONFIGS["luffy_condense"], name="bwd_poison_condense", T=600, d=512,
+                      E=4, k=2, H=256, n_centroids=16, copy_fraction=0.4, noise_rel=0.02)
+        tau = 0.95
+    else:
+        cfg, tau = SMALL["softmax_shared"], math.nan
+    inp, C, w, x, d_out, _ = _case(moe, cfg)
+    bwd = moe.Backward(C, w, condense=condense)
+    runs = []
+    for fill in (0, 255):
+        bwd.ws.fill_(fill)
+        for v in bwd.grads.values():
+            if v is not None:
+                v.fill_(float("nan"))
+        g = bwd(x, d_out, tau)
+        runs.append({k: v.clone() for k, v in g.items() if v is not None})
+    torch.cuda.synchronize()
+    a, b = runs
+    for key in a:
+        assert not torch.isnan(a[key]).any().item(), key
+        assert torch.equal(a[key], b[key]), key
+    assert moe.get_device_status() == 0

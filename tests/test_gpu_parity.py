@@ -386,6 +386,54 @@ def test_layer_deterministic(moe):
     assert torch.equal(a, b)
 
 
+# Workspace poisoning: every byte of the layer's scratch set to 0xFF before the call (NaN in
+# every float, -1 in every index) must give the same output bits as a zeroed workspace, and
+# every output element must be written (the output starts as NaN).  This would catch a kernel
+# that reads scratch the same call has not written (a table, a counter, a padding row).
+POISON_CASES = [("dsv2_lite", 600, math.nan), ("qwen3_30b_a3b", 700, math.nan),
+                ("luffy_condense", 1024, 0.95), ("dsv2_lite_decode", None, math.nan),
+                ("tiny_fp32", 256, math.nan)]
+
+
+@pytest.mark.parametrize("name,T,tau", POISON_CASES)
+def test_layer_poisoned_workspace(moe, name, T, tau):
+    cfg, inp, C, w, x, r = _setup(moe, name, T=T)
+    lay = moe.Layer(C, w, condense=tau <= 1.0)
+    outs = []
+    for fill in (0, 255):
+        lay.ws.fill_(fill)
+        out = torch.full((C.T, C.d), float("nan"), dtype=C.torch_dtype, device=x.device)
+        idx = torch.full((C.T, C.k), -7, dtype=torch.int32, device=x.device)
+        lay(x, r, tau, out=out, topk_idx_out=idx)
+        outs.append((out, idx))
+    torch.cuda.synchronize()
+    (a, ia), (b, ib) = outs
+    assert not torch.isnan(a).any().item()
+    assert torch.equal(a, b)
+    assert torch.equal(ia, ib)
+    _status_ok(moe)
+
+
+def test_layer_ex_poisoned_workspace(moe):
+    """The same for moe_layer_forward_ex: shared experts on a second stream and the partial
+    activation written beside the output."""
+    cfg, inp, C, w, x, r = _setup(moe, "dsv2_lite", T=600)
+    lay = moe.Layer(C, w)
+    aux = torch.cuda.Stream()
+    outs = []
+    for fill in (0, 255):
+        lay.ws.fill_(fill)
+        out = torch.full((C.T, C.d), float("nan"), dtype=C.torch_dtype, device=x.device)
+        part = torch.full_like(out, float("nan"))
+        lay(x, r, out=out, partial_out=part, aux_stream=aux)
+        outs.append((out, part))
+    torch.cuda.synchronize()
+    (a, pa), (b, pb) = outs
+    assert not torch.isnan(a).any().item() and not torch.isnan(pa).any().item()
+    assert torch.equal(a, b) and torch.equal(pa, pb)
+    _status_ok(moe)
+
+
 # ------------------------------------------------------------------ decode-shaped layer
 def test_decode_layer_every_token(moe):
     """One decode step (64 tokens) through the full DeepSeek-V2-Lite weights: routing bit for
