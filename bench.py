@@ -42,8 +42,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of the grouped-GEMM launches of one moe_expert_ffn call, from
 # one-pass ncu captures (dram__bytes_read.sum + dram__bytes_write.sum) of the pair kernel at
 # the workload's full size; workloads without a capture report null.
-GEMM_DRAM_BYTES = {"dsv2_lite": 1495.6e6, "llama4_scout_farskip": 6288.6e6,
-                   "qwen3_30b_a3b": 1889.4e6, "luffy_condense": 807.4e6}
+GEMM_DRAM_BYTES = {"dsv2_lite": 1496.8e6, "llama4_scout_farskip": 6316.9e6,
+                   "qwen3_30b_a3b": 1888.8e6, "luffy_condense": 808.1e6}
 
 
 def load_peaks() -> tuple[dict, str]:
