@@ -161,13 +161,14 @@ def test_expert_ffn_full_size(moe, name):
 # Group sizes around every tile boundary of the expert GEMMs: empty, one row, and one short of,
 # at and one past 16, 128, 192, 256, 384, 448 and 512 rows, so that every way a group splits
 # into 256-row pair tiles and tail tiles of at most 192 rows (N rounded up to 16; a tail of more
-# than 128 rows loads its halves with the 128-row box) occurs.
+# than 128 rows loads its halves with the 128-row box) occurs; and 14, 32 and 33 rows past one
+# pair and 32 past two (small tails, N = 16 or 32, beside the pairs of the same group).
 GROUP_SIZES = [0, 1, 15, 16, 17, 127, 128, 129, 191, 192, 193, 255, 256, 257, 383, 384, 385,
-               447, 448, 449, 511, 512, 513, 200]
+               447, 448, 449, 511, 512, 513, 200, 270, 288, 289, 544]
 
 
 def test_expert_ffn_group_sizes_every_row(moe):
-    T = 1100
+    T = 1300
     cfg, inp, C, w, x, r = _setup(moe, "dsv2_lite", T=T)
     P = cfg.P
     sizes = GROUP_SIZES + [0] * (cfg.E - len(GROUP_SIZES))
