@@ -132,8 +132,31 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// One warp per token: logits = ordered sum of the split partials (+ bias), then
-// k rounds of warp argmax (ties -> lower expert), then gates.
+// Order-preserving 32-bit key of a logit: a larger logit has a larger key (-0 reads as +0 and
+// NaN as -inf), and the key of any logit is above 0, the key of an empty slot.
+__device__ __forceinline__ uint32_t logit_key(float v) {
+  if (v != v) v = -INFINITY;
+  if (v == 0.f) v = 0.f;
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+// compare-exchange for a descending sort of 64-bit keys
+__device__ __forceinline__ void cas_desc(uint64_t& a, uint64_t& b) {
+  const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
+  a = hi;
+  b = lo;
+}
+
+// One warp per token: logits = ordered sum of the split partials (+ bias), then the top k
+// (ties -> lower expert), then gates.  Lane l holds experts l + 32 i, i < NV.  Each candidate
+// is one 64-bit key, {logit key, 0xffff - expert}, so that the larger key is the better
+// expert under the selection order; a lane sorts its NV keys, and each of the k rounds takes
+// the warp's largest head (two warp max reductions: logit key, then expert among the equal
+// logits) and pops it from its lane.
+template <int NV>
 __global__ void __launch_bounds__(256)
     router_topk_kernel(const float* __restrict__ part, int n_split, int ld,
                        const float* __restrict__ bias, float* __restrict__ logits_out,
@@ -145,20 +168,20 @@ __global__ void __launch_bounds__(256)
   pdl_wait();
   if (warp >= T) return;
   // logits: the split partials added in split order.  Loads are issued kChunk
-  // splits x 8 expert slots at a time, so their latencies overlap.
+  // splits x NV expert slots at a time, so their latencies overlap.
   constexpr int kChunk = 4;
-  float v[8];
+  float v[NV];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < NV; ++i) {
     const int e = lane + 32 * i;
     v[i] = e < E ? part[static_cast<long long>(warp) * ld + e] : 0.f;
   }
   for (int s0 = 1; s0 < n_split; s0 += kChunk) {
-    float q[kChunk][8];
+    float q[kChunk][NV];
 #pragma unroll
     for (int u = 0; u < kChunk; ++u)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < NV; ++i) {
         const int e = lane + 32 * i;
         q[u][i] = (e < E && s0 + u < n_split)
                       ? part[(static_cast<long long>(s0 + u) * T + warp) * ld + e]
@@ -167,49 +190,60 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int u = 0; u < kChunk; ++u)
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < NV; ++i)
         if (s0 + u < n_split) v[i] += q[u][i];
   }
+  uint64_t key[NV];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < NV; ++i) {
     const int e = lane + 32 * i;
     if (e < E) {
       if (bias) v[i] += bias[e];
       if (logits_out) logits_out[static_cast<long long>(warp) * E + e] = v[i];
+      key[i] = (static_cast<uint64_t>(logit_key(v[i])) << 32) | static_cast<uint32_t>(0xffff - e);
     } else {
       v[i] = -INFINITY;
+      key[i] = 0;
     }
   }
+  // this lane's keys in descending order (sorting networks; e rises with i, so equal logits
+  // keep the lower expert first)
+  if (NV == 2) {
+    cas_desc(key[0], key[1 % NV]);
+  } else if (NV == 4) {
+    cas_desc(key[0], key[1 % NV]); cas_desc(key[2 % NV], key[3 % NV]);
+    cas_desc(key[0], key[2 % NV]); cas_desc(key[1 % NV], key[3 % NV]);
+    cas_desc(key[1 % NV], key[2 % NV]);
+  } else if (NV == 8) {
+    cas_desc(key[0], key[1 % NV]); cas_desc(key[2 % NV], key[3 % NV]);
+    cas_desc(key[4 % NV], key[5 % NV]); cas_desc(key[6 % NV], key[7 % NV]);
+    cas_desc(key[0], key[2 % NV]); cas_desc(key[1 % NV], key[3 % NV]);
+    cas_desc(key[4 % NV], key[6 % NV]); cas_desc(key[5 % NV], key[7 % NV]);
+    cas_desc(key[1 % NV], key[2 % NV]); cas_desc(key[5 % NV], key[6 % NV]);
+    cas_desc(key[0], key[4 % NV]); cas_desc(key[1 % NV], key[5 % NV]);
+    cas_desc(key[2 % NV], key[6 % NV]); cas_desc(key[3 % NV], key[7 % NV]);
+    cas_desc(key[2 % NV], key[4 % NV]); cas_desc(key[3 % NV], key[5 % NV]);
+    cas_desc(key[1 % NV], key[2 % NV]); cas_desc(key[3 % NV], key[4 % NV]);
+    cas_desc(key[5 % NV], key[6 % NV]);
+  }
   // lane j < k keeps the j-th selection in registers
-  unsigned taken = 0;
   float my_v = -INFINITY;
   int my_i = 0;
 #pragma unroll 1
   for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
+    const uint32_t hh = static_cast<uint32_t>(key[0] >> 32);
+    const uint32_t hl = static_cast<uint32_t>(key[0]);
+    const uint32_t mh = __reduce_max_sync(0xffffffffu, hh);
+    const uint32_t ml = __reduce_max_sync(0xffffffffu, hh == mh ? hl : 0u);
+    if (hh == mh && hl == ml) {  // the lane holding the winner moves to its next key
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
-        bv = v[i];
-        bi = e;
-      }
+      for (int i = 0; i + 1 < NV; ++i) key[i] = key[i + 1];
+      key[NV - 1] = 0;
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      if (ov > bv || (ov == bv && oi < bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if (bi >= E) bi = 0;  // only reachable with NaN logits
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
     if (lane == j) {
-      my_v = bv;
-      my_i = bi;
+      my_v = key_logit(mh);
+      my_i = 0xffff - static_cast<int>(ml);
+      if (mh == 0 || my_i < 0 || my_i >= E) my_i = 0;  // fewer than k experts: not reachable
     }
   }
   float g;
@@ -220,7 +254,7 @@ __global__ void __launch_bounds__(256)
     float z = 0.f;
     if (gating == MOE_GATE_SOFTMAX_TOPK) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) z += (lane + 32 * i < E) ? expf(v[i] - m) : 0.f;
+      for (int i = 0; i < NV; ++i) z += (lane + 32 * i < E) ? expf(v[i] - m) : 0.f;
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
     } else {
@@ -267,9 +301,18 @@ cudaError_t launch_router_topk(const float* part, int n_split, int ld, const flo
                                int E, int k, int gating, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   const int warps_per_block = 8;
-  return launch_pdl(router_topk_kernel, dim3(ceil_div(T, warps_per_block)),
-                    dim3(32 * warps_per_block), 0, stream, part, n_split, ld, bias, logits_out,
-                    topk_idx, topk_gate, T, E, k, gating);
+  const dim3 grid(ceil_div(T, warps_per_block)), block(32 * warps_per_block);
+  if (E <= 32)
+    return launch_pdl(router_topk_kernel<1>, grid, block, 0, stream, part, n_split, ld, bias,
+                      logits_out, topk_idx, topk_gate, T, E, k, gating);
+  if (E <= 64)
+    return launch_pdl(router_topk_kernel<2>, grid, block, 0, stream, part, n_split, ld, bias,
+                      logits_out, topk_idx, topk_gate, T, E, k, gating);
+  if (E <= 128)
+    return launch_pdl(router_topk_kernel<4>, grid, block, 0, stream, part, n_split, ld, bias,
+                      logits_out, topk_idx, topk_gate, T, E, k, gating);
+  return launch_pdl(router_topk_kernel<8>, grid, block, 0, stream, part, n_split, ld, bias,
+                    logits_out, topk_idx, topk_gate, T, E, k, gating);
 }
 
 int router_n_pad(int E) { return ceil_div(E, 32) * 32; }

@@ -73,6 +73,37 @@ def test_router_full_size(moe, name):
     _status_ok(moe)
 
 
+@pytest.mark.parametrize("E,k,gating", [(16, 1, "sigmoid_topk"), (64, 6, "softmax_topk"),
+                                         (128, 8, "softmax_topk_renorm"), (200, 8, "softmax_topk"),
+                                         (256, 32, "softmax_topk_renorm")])
+def test_router_exact_ties(moe, E, k, gating):
+    """Small-integer tokens, router weights and bias: every logit is an integer that the
+    tensor-core path (exact bf16 terms, fp32 accumulation) and the fp64 oracle both compute
+    exactly, and logits tie often (a fifth of the experts copy another one's weights), so the
+    selection must follow the tie rule -- the lower expert index first -- bit for bit."""
+    rng = np.random.default_rng(1000 + E + k)
+    T, d = 777, 256
+    x = rng.integers(-2, 3, size=(T, d)).astype(np.float32)
+    W_r = rng.integers(-3, 4, size=(d, E)).astype(np.float32)
+    W_r[:, 1::5] = W_r[:, 0::5][:, : W_r[:, 1::5].shape[1]]
+    bias = rng.integers(-2, 3, size=E).astype(np.float32) if gating == "softmax_topk_renorm" else None
+    if bias is not None:
+        bias[1::5] = bias[0::5][: bias[1::5].shape[0]]
+    C = moe.Config(T=T, d=d, E=E, k=k, H=128, n_shared=0, H_shared=0, dtype="bf16",
+                   gating=gating, residual="none")
+    xd = torch.from_numpy(x).to(device="cuda", dtype=torch.bfloat16)
+    logits, idx, gate = moe.route(C, xd, torch.from_numpy(W_r).cuda(),
+                                  torch.from_numpy(bias).cuda() if bias is not None else None)
+    torch.cuda.synchronize()
+    l_ref, idx_ref, g_ref = orc.route(x, W_r, bias, k, gating)
+    np.testing.assert_array_equal(_np(logits), l_ref.astype(np.float32))  # integers, exact
+    srt = -np.sort(-l_ref, axis=1)
+    assert np.mean(srt[:, : k] == srt[:, 1 : k + 1]) > 0.05  # ties inside the top k + 1
+    np.testing.assert_array_equal(_np(idx), idx_ref)
+    np.testing.assert_allclose(_np(gate), g_ref, rtol=2e-5, atol=1e-7)
+    _status_ok(moe)
+
+
 @pytest.mark.parametrize("E", [8, 33, 64, 65, 96])
 def test_router_terms_side_by_side_boundary(moe, E):
     """Up to E = 64 the tensor-core router puts the three bf16 terms of W_r side by side
