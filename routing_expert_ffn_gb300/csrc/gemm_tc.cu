@@ -68,6 +68,11 @@ constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 512;
 constexpr int M_GROUP = 16;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align slack*/ + 2048 /*barriers, tables*/;
+// the router's wide layout (65..128 experts): x's 16 KB and three 128-row terms per stage
+constexpr int WIDE_STAGE_BYTES = A_BYTES + 3 * 128 * BK * 2;
+constexpr int WIDE_STAGES = STAGES * STAGE_BYTES / WIDE_STAGE_BYTES;
+static_assert(WIDE_STAGES * WIDE_STAGE_BYTES == STAGES * STAGE_BYTES, "one ring size");
+static_assert(WIDE_STAGES <= STAGES && WIDE_STAGE_BYTES % 1024 == 0, "wide router stages");
 
 enum Mode { kSwiGLU = 0, kStore = 1, kSimBits = 2, kRouter = 3 };
 
@@ -519,6 +524,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = sh->tmem_base;
   const int n_tiles = total_tiles<MODE>(args);
+  // Router with 65..128 experts: the three terms (up to 128 rows each) side by side need 64 KB
+  // stages (three of them in the same ring), two MMAs per K step (terms 1 and 2, then term 3)
+  // and a 384-column accumulator, so a single TMEM buffer.
+  const bool wide = MODE == kRouter && args.router_stacked && 3 * args.router_n > BN;
+  const int sbytes = wide ? WIDE_STAGE_BYTES : STAGE_BYTES;
+  const int nst = wide ? WIDE_STAGES : STAGES;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -537,7 +548,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (lane == 0) {
           const uint32_t full = ptx::smem_u32(&sh->full[stage]);
-          const uint32_t sa = smem0 + stage * STAGE_BYTES;
+          const uint32_t sa = smem0 + stage * sbytes;
           const uint32_t sb = sa + A_BYTES;
           const int kslice = kb / args.kb_per_slice;
           const int kin = (kb - kslice * args.kb_per_slice) * BK;
@@ -576,12 +587,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
         issued[stage] = 1;
         issued_phase[stage] = phase;
-        if (++stage == STAGES) stage = 0, phase ^= 1u;
+        if (++stage == nst) stage = 0, phase ^= 1u;
       }
     }
     if (!ok) {
       // Let the loads already in flight land before the CTA exits.
-      for (int s = 0; s < STAGES; ++s) {
+      for (int s = 0; s < nst; ++s) {
         if (!issued[s]) continue;
         uint64_t t0 = globaltimer_ns();
         while (!ptx::mbar_try_wait(ptx::smem_u32(&sh->full[s]), issued_phase[s]) &&
@@ -592,14 +603,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t idesc = ptx::idesc_bf16_f32(
-        BM, MODE == kRouter ? (args.router_stacked ? 3 : 1) * args.router_n : BN);
+        BM, MODE == kRouter ? (wide ? 2 : args.router_stacked ? 3 : 1) * args.router_n : BN);
+    const uint32_t idesc_term3 = ptx::idesc_bf16_f32(BM, MODE == kRouter ? args.router_n : BN);
     int stage = 0;
     uint32_t phase = 0;
     int local = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++local) {
-      const int acc = local & 1;
-      const uint32_t acc_phase = (local >> 1) & 1;
+      // one buffer when wide: its phase flips every tile
+      const int acc = wide ? 0 : local & 1;
+      const uint32_t acc_phase = wide ? local & 1 : (local >> 1) & 1;
       if (!wait_bar(ptx::smem_u32(&sh->tmem_empty[acc]), acc_phase ^ 1u, sh, args.status)) {
         ok = false;
         break;
@@ -613,7 +626,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         ptx::tc_fence_after();
         if (lane == 0) {
-          const uint32_t sa = smem0 + stage * STAGE_BYTES;
+          const uint32_t sa = smem0 + stage * sbytes;
           const uint32_t sb = sa + A_BYTES;
           const uint64_t adesc = ptx::sw128_kmajor_desc(sa);
           const uint64_t bdesc = ptx::sw128_kmajor_desc(sb);
@@ -623,10 +636,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc,
                            (kb > 0 || kk > 0) ? 1u : 0u);
           }
+          if (wide) {
+            // the third term's rows, into the columns after the first two terms'
+            const uint64_t bdesc3 = ptx::sw128_kmajor_desc(sb + 2 * args.router_n * BK * 2);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              ptx::umma_bf16(d_tmem + 2 * args.router_n, adesc + 2 * kk, bdesc3 + 2 * kk,
+                             idesc_term3, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
           ptx::umma_commit(ptx::smem_u32(&sh->empty[stage]));
         }
         __syncwarp();
-        if (++stage == STAGES) stage = 0, phase ^= 1u;
+        if (++stage == nst) stage = 0, phase ^= 1u;
       }
       if (!ok) break;
       if (lane == 0) ptx::umma_commit(ptx::smem_u32(&sh->tmem_full[acc]));
@@ -648,8 +669,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     int local = 0;
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++local) {
-      const int acc = local & 1;
-      const uint32_t acc_phase = (local >> 1) & 1;
+      const int acc = wide ? 0 : local & 1;
+      const uint32_t acc_phase = wide ? local & 1 : (local >> 1) & 1;
       if (!wait_bar(ptx::smem_u32(&sh->tmem_full[acc]), acc_phase, sh, args.status)) break;
       ptx::tc_fence_after();
       const TileInfo t = tile_info<MODE>(args, sh->gmb, tile);

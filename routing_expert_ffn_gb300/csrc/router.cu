@@ -317,8 +317,9 @@ cudaError_t launch_router_topk(const float* part, int n_split, int ld, const flo
 
 int router_n_pad(int E) { return ceil_div(E, 32) * 32; }
 
-// The three terms fit side by side in one MMA (N = 3 x E rounded up to 32, at most 256).
-static bool router_stacked(int E) { return 3 * router_n_pad(E) <= 256; }
+// The three terms sit side by side along N: in one MMA up to 64 experts (N = 3 x E rounded up
+// to 32, at most 256), in two (terms 1 and 2, then term 3) up to 128.
+static bool router_stacked(int E) { return 3 * router_n_pad(E) <= 384; }
 
 // K splits: the largest divisor of the K blocks (d/64 with the terms side by side, else
 // 3d/64) that keeps the tile count (m-tiles x splits) within one wave of CTAs, and at most

@@ -104,12 +104,13 @@ def test_router_exact_ties(moe, E, k, gating):
     _status_ok(moe)
 
 
-@pytest.mark.parametrize("E", [8, 33, 64, 65, 96])
+@pytest.mark.parametrize("E", [8, 33, 64, 65, 96, 128, 129])
 def test_router_terms_side_by_side_boundary(moe, E):
-    """Up to E = 64 the tensor-core router puts the three bf16 terms of W_r side by side
-    along N (N = 3 x E rounded up to 32, at most 256) and splits K over d; above that the
-    terms follow one another along K.  Both sides of the boundary, 1000 tokens (a ragged
-    last m-tile), every token against the oracle."""
+    """Up to E = 128 the tensor-core router puts the three bf16 terms of W_r side by side
+    along N and splits K over d: in one MMA up to E = 64 (N = 3 x E rounded up to 32, at
+    most 256), in two (terms 1 and 2, then term 3) above; past 128 the terms follow one
+    another along K.  Both sides of both boundaries, 1000 tokens (a ragged last m-tile),
+    every token against the oracle."""
     from dataclasses import replace
     cfg = replace(gen.CONFIGS["qwen3_30b_a3b"], name=f"router{E}", T=1000, d=512, E=E, k=2, H=128,
                   n_shared=1, H_shared=128, router_bias="none")
