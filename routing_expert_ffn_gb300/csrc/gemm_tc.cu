@@ -20,11 +20,12 @@
 //   kSimBits condensation (CTA pairs): D is a 256 x 256 tile of the bucket's Gram matrix;
 //            the epilogue turns cos(x_i, x_j) >= tau, j < i, into bits.
 //   kRouter  router logits: B is the fp32 router weight split exactly into
-//            three bf16 terms.  With E up to 64 the terms sit side by side along N
-//            (N = 3 x E rounded up to 32): the K loop runs over d, split across CTAs,
-//            and the epilogue adds the three accumulators; otherwise the K loop runs
-//            over the three terms in turn (N = E rounded up to 32).  The epilogue
-//            writes fp32 partial sums.
+//            three bf16 terms.  With E up to 128 the terms sit side by side along N
+//            (each E rounded up to 32 rows; one MMA up to 64 experts, two above -- terms
+//            1 and 2, then term 3 -- into a 384-column accumulator): the K loop runs
+//            over d, split across CTAs, and the epilogue adds the three accumulators;
+//            otherwise the K loop runs over the three terms in turn (N = E rounded up
+//            to 32).  The epilogue writes fp32 partial sums.
 //
 // Tiles.  Rows are grouped (one group per expert / bucket); a group's rows are
 // cut into 128-row m-tiles (the last one ragged; rows past the group are
