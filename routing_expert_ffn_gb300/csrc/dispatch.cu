@@ -254,16 +254,22 @@ __global__ void __launch_bounds__(256)
                         int n_blk, int E, int T_tok, int k, int d, T* __restrict__ x_perm,
                         int32_t* __restrict__ perm, int32_t* __restrict__ slot_of,
                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-                        RowStatsOut stats, unsigned* status) {
+                        RowStatsOut stats, int split, unsigned* status) {
   constexpr int V = Act<T>::kVec;
   const int nv = d / V;
   const int P = T_tok * k;
   extern __shared__ int tab[];
   __shared__ int wsum[33];
   pdl_trigger();
-  const int warps = (gridDim.x * blockDim.x) >> 5;
+  // `split` warps share a token (1 with STATS), each moving one slice of its row to all of
+  // its slots, so that small batches still have enough rows in flight
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int sub = gw % split;
+  const int warps = ((gridDim.x * blockDim.x) >> 5) / split;
+  const int nvs = (nv + split - 1) / split;
+  const int vbeg = sub * nvs, vend = min(nv, vbeg + nvs);
   const int lane = threadIdx.x & 31;
-  int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  int t = gw / split;
   // The first token's row chunk is loaded before the programmatic-launch wait (x is
   // complete when this kernel starts: dispatch_local_kernel, the kernel before it, triggers
   // only after its own wait) and its routing right after, both before the table scan, so
@@ -275,8 +281,8 @@ __global__ void __launch_bounds__(256)
     const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<long long>(tok) * d);
 #pragma unroll
     for (int u = 0; u < kRowChunk; ++u) {
-      const int v = u * 32 + lane;
-      if (v < nv) r[u] = src[v];
+      const int v = vbeg + u * 32 + lane;
+      if (v < vend) r[u] = src[v];
     }
   };
   auto load_routing = [&](int tok) {
@@ -322,17 +328,19 @@ __global__ void __launch_bounds__(256)
           slot = -1;
         }
       }
-      slot_of[p] = slot;
-      if (slot >= 0) perm[slot] = t;
+      if (sub == 0) {
+        slot_of[p] = slot;
+        if (slot >= 0) perm[slot] = t;
+      }
     }
     float ss = 0.f;
     unsigned long long h = 0x9E3779B97F4A7C15ull * (lane + 1);
-    for (int v0 = 0; v0 < nv; v0 += 32 * kRowChunk) {
-      if (v0 > 0) {
+    for (int v0 = vbeg; v0 < vend; v0 += 32 * kRowChunk) {
+      if (v0 > vbeg) {
 #pragma unroll
         for (int u = 0; u < kRowChunk; ++u) {
           const int v = v0 + u * 32 + lane;
-          if (v < nv) r[u] = src[v];
+          if (v < vend) r[u] = src[v];
         }
       }
       if (STATS) {
@@ -357,7 +365,7 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
         for (int u = 0; u < kRowChunk; ++u) {
           const int v = v0 + u * 32 + lane;
-          if (v < nv) dst[v] = r[u];
+          if (v < vend) dst[v] = r[u];
         }
       }
     }
@@ -631,7 +639,16 @@ cudaError_t launch_dispatch_auto(int act_dtype, const void* x, const int32_t* to
                      static_cast<const int32_t*>(blk), blk, E, n_blk, counts, offsets);
     if (err != cudaSuccess) return err;
   }
-  const long long want = (static_cast<long long>(T) + 7) / 8;  // one warp per token
+  // warps per token: small batches (fewer than 16 tokens per SM) share each row among up to
+  // 8 warps, each slice at least two 16-byte vectors per lane (the row statistics need whole
+  // rows).  Measured: the 64-token decode scatter 12.1 -> 10.0 us; two warps per token on the
+  // 4096-token DeepSeek-V2-Lite layer changed nothing (its stores are bandwidth-bound).
+  const int nv = d / (act_dtype == MOE_F32 ? 4 : 8);
+  int split = 1;
+  while (stats == nullptr && split < 8 && static_cast<long long>(T) * split < 16ll * num_sms &&
+         nv >= 64 * split)
+    split *= 2;
+  const long long want = (static_cast<long long>(T) * split + 7) / 8;  // 8 warps per block
   const int blocks = static_cast<int>(want < 8ll * num_sms ? want : 8ll * num_sms);
   const size_t smem = scan_in_smem ? sizeof(int) * (table + table / 32 + 1) : 0;
   if (act_dtype == MOE_F32) {
@@ -640,11 +657,11 @@ cudaError_t launch_dispatch_auto(int act_dtype, const void* x, const int32_t* to
     err = scan_in_smem ? launch_pdl(scatter_rows_kernel<float, true, false>, dim3(blocks),
                                     dim3(256), smem, stream, xf, topk_idx, local_rank, blk, n_blk,
                                     E, T, k, d, xp, perm, slot_of, counts, offsets, RowStatsOut{},
-                                    status)
+                                    split, status)
                        : launch_pdl(scatter_rows_kernel<float, false, false>, dim3(blocks),
                                     dim3(256), 0, stream, xf, topk_idx, local_rank, blk, n_blk, E,
                                     T, k, d, xp, perm, slot_of, counts, offsets, RowStatsOut{},
-                                    status);
+                                    split, status);
   } else {
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
     __nv_bfloat16* xp = static_cast<__nv_bfloat16*>(x_perm);
@@ -655,7 +672,7 @@ cudaError_t launch_dispatch_auto(int act_dtype, const void* x, const int32_t* to
                                    : scatter_rows_kernel<__nv_bfloat16, false, false>);
     err = launch_pdl(kern, dim3(blocks), dim3(256), scan_in_smem ? smem : 0, stream, xb, topk_idx,
                      local_rank, blk, n_blk, E, T, k, d, xp, perm, slot_of, counts, offsets,
-                     st ? *stats : RowStatsOut{}, status);
+                     st ? *stats : RowStatsOut{}, split, status);
   }
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
