@@ -132,8 +132,9 @@ moe_status moe_get_device_status(moe_stream_t stream);
  * fp32 accuracy (no TF32): fp32 layers on the FMA pipe; bf16 layers on tcgen05
  * tensor cores with W_r split exactly into three bf16 terms (x is exactly
  * bf16, so every product is exact and the sums are fp32).  Then the k experts
- * with the largest logits, largest first, a tie going to the lower index;
- * gates per cfg->gating from the fp32 logits.
+ * with the largest logits, largest first, a tie going to the lower index (a
+ * NaN logit ranks as -inf, -0 as +0); gates per cfg->gating from the fp32
+ * logits.
  *   x        [T, d] act           (in)
  *   W_r      [d, E] fp32          (in)
  *   bias     [E] fp32 or NULL     (in)
