@@ -425,7 +425,7 @@ def test_layer_deterministic(moe):
 # that reads scratch the same call has not written (a table, a counter, a padding row).
 POISON_CASES = [("dsv2_lite", 600, math.nan), ("qwen3_30b_a3b", 700, math.nan),
                 ("luffy_condense", 1024, 0.95), ("dsv2_lite_decode", None, math.nan),
-                ("tiny_fp32", 256, math.nan)]
+                ("tiny_fp32", 256, math.nan), ("llama4_scout_farskip", 300, math.nan)]
 
 
 @pytest.mark.parametrize("name,T,tau", POISON_CASES)
@@ -447,10 +447,11 @@ def test_layer_poisoned_workspace(moe, name, T, tau):
     _status_ok(moe)
 
 
-def test_layer_ex_poisoned_workspace(moe):
+@pytest.mark.parametrize("name", ["dsv2_lite", "llama4_scout_farskip"])
+def test_layer_ex_poisoned_workspace(moe, name):
     """The same for moe_layer_forward_ex: shared experts on a second stream and the partial
     activation written beside the output."""
-    cfg, inp, C, w, x, r = _setup(moe, "dsv2_lite", T=600)
+    cfg, inp, C, w, x, r = _setup(moe, name, T=600)
     lay = moe.Layer(C, w)
     aux = torch.cuda.Stream()
     outs = []
@@ -464,6 +465,42 @@ def test_layer_ex_poisoned_workspace(moe):
     (a, pa), (b, pb) = outs
     assert not torch.isnan(a).any().item() and not torch.isnan(pa).any().item()
     assert torch.equal(a, b) and torch.equal(pa, pb)
+    _status_ok(moe)
+
+
+@pytest.mark.parametrize("residual,n_shared,T", [("external", 1, 300), ("input_plus_external", 0, 300),
+                                                 ("input", 2, 100), ("none", 1, 129)])
+def test_layer_matches_step_by_step_one_expert_per_token(moe, residual, n_shared, T):
+    """One routed expert per token (the Llama-4-Scout shape, narrowed): the layer's output and
+    partial activation equal, bit for bit, what the step-by-step calls (route, dispatch,
+    expert FFN, combine) give, through both layer entry points, for every residual mode, with
+    and without shared experts, and on a small batch (tail tiles only)."""
+    from dataclasses import replace
+    cfg = replace(gen.CONFIGS["llama4_scout_farskip"], name=f"k1_{residual}_{n_shared}",
+                  T=T, d=512, E=4, k=1, H=256, n_shared=n_shared, H_shared=256,
+                  residual=residual)
+    inp = harness.condition(cfg, gen.make_inputs(cfg))
+    C = moe.Config.from_workload(cfg)
+    w, x, r = moe.upload(C, inp)
+    lay = moe.Layer(C, w)
+    out = lay(x, r)
+    part = torch.empty_like(out)
+    out_ex = lay(x, r, partial_out=part, aux_stream=torch.cuda.Stream())
+    _, idx, gate = moe.route(C, x, w.W_r, w.router_bias)
+    dsp = moe.dispatch(C, x, idx)
+    y, so = moe.expert_ffn(C, w, dsp["x_perm"], dsp["offsets"], None, x)
+    ref = moe.combine(C, y, so, dsp["slot_of"], None, gate, x, r)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    assert torch.equal(out_ex, ref)
+    base = torch.zeros(out.shape, dtype=torch.float32, device=out.device)
+    if residual in ("input", "input_plus_external"):
+        base = base + x.float()
+    if residual in ("external", "input_plus_external"):
+        base = base + r.float()
+    if n_shared:
+        base = base + so.float()
+    assert torch.equal(part, base.to(torch.bfloat16))
     _status_ok(moe)
 
 
